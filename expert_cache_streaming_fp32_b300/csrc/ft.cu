@@ -1,0 +1,442 @@
+// libft: the exported C ABI (include/ft.h).  Single translation unit: the
+// kernels live in the included .cuh files.
+#include "common.cuh"
+#include "route.cuh"
+#include "expert.cuh"
+#include "cache.cuh"
+#include "stream.cuh"
+
+#include <new>
+
+using namespace ft;
+
+#define FT_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+int sms() { return dev_info().sms; }
+
+template <typename K>
+int occupancy_grid(K kernel, int threads, size_t smem) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  return per_sm * sms();
+}
+
+template <typename K>
+int set_smem(K kernel, size_t smem) {
+  if (smem > 48 * 1024)
+    FT_CHECK_CUDA(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  return FT_OK;
+}
+
+}  // namespace
+
+FT_API const char* ft_status_str(int status) {
+  switch (status) {
+    case FT_OK: return "ok";
+    case FT_EINVAL: return "invalid argument";
+    case FT_ENOMEM: return "out of device memory";
+    case FT_ECUDA: return "CUDA error";
+    case FT_ETIMEOUT: return "timed out";
+    case FT_ESTATE: return "call not allowed in this state";
+    case FT_EUNSUPPORTED: return "unsupported configuration";
+    case FT_EDEVICE: return "device-side index error";
+    default: return "unknown status";
+  }
+}
+
+FT_API int ft_version(void) { return 1; }
+
+FT_API int ft_last_cuda_error(void) { return g_last_cuda_error; }
+
+FT_API int ft_get_device_error(int* code) {
+  FT_REQUIRE(code);
+  int v = 0, zero = 0;
+  FT_CHECK_CUDA(cudaDeviceSynchronize());
+  FT_CHECK_CUDA(cudaMemcpyFromSymbol(&v, g_derr, sizeof(int)));
+  FT_CHECK_CUDA(cudaMemcpyToSymbol(g_derr, &zero, sizeof(int)));
+  *code = v;
+  return v ? FT_EDEVICE : FT_OK;
+}
+
+FT_API int ft_expert_layout_get(int wtype, int hidden, int inter, ft_expert_layout* out) {
+  FT_REQUIRE(out);
+  return expert_layout(wtype, hidden, inter, out);
+}
+
+FT_API int ft_qsplit(int m, double bw_fill, double bw_host) {
+  if (m <= 0) return 0;
+  if (!(bw_host > bw_fill)) return m;
+  return qsplit_ratio(m, bw_fill / bw_host);
+}
+
+// ------------------------------------------------------------------ pinned pool
+FT_API int ft_host_alloc(uint64_t bytes, void** out) {
+  FT_REQUIRE(out && bytes > 0);
+  *out = nullptr;
+  void* p = nullptr;
+  cudaError_t e = cudaHostAlloc(&p, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    g_last_cuda_error = (int)e;
+    return FT_ENOMEM;
+  }
+  *out = p;
+  return FT_OK;
+}
+
+FT_API int ft_host_free(void* p) {
+  if (!p) return FT_OK;
+  FT_CHECK_CUDA(cudaFreeHost(p));
+  return FT_OK;
+}
+
+// ------------------------------------------------------------------ router logits
+FT_API int ft_router_logits(const void* x, int x_type, const void* w_router, const float* bias, int T, int H, int E,
+                            float* logits, ft_cuda_stream s) {
+  FT_REQUIRE(T >= 0 && H > 0 && H % 256 == 0 && E >= 1 && E <= 1024);
+  FT_REQUIRE(x_type == FT_X_F32 || x_type == FT_X_BF16);
+  if (T == 0) return FT_OK;
+  FT_REQUIRE(x && w_router && logits);
+  const size_t smem = (size_t)RL_RT * H * sizeof(float);
+  dim3 grid(ceil_div(T, RL_RT));
+  if (x_type == FT_X_BF16) {
+    auto k = router_logits_kernel<__nv_bfloat16>;
+    if (int st = set_smem(k, smem)) return st;
+    k<<<grid, RL_WARPS * 32, smem, (cudaStream_t)s>>>((const __nv_bfloat16*)x, (const __nv_bfloat16*)w_router, bias,
+                                                      T, H, E, logits);
+  } else {
+    auto k = router_logits_kernel<float>;
+    if (int st = set_smem(k, smem)) return st;
+    k<<<grid, RL_WARPS * 32, smem, (cudaStream_t)s>>>((const float*)x, (const float*)w_router, bias, T, H, E, logits);
+  }
+  FT_CHECK_LAUNCH();
+  return FT_OK;
+}
+
+// ------------------------------------------------------------------ route
+FT_API int ft_route(const float* logits, int T, int E, int k, int32_t* topk_idx, float* topk_w, ft_cuda_stream s) {
+  FT_REQUIRE(T >= 0 && E >= 1 && E <= RT_MAXE && k >= 1 && k <= RT_MAXK && k <= E);
+  if (T == 0) return FT_OK;
+  FT_REQUIRE(logits && topk_idx && topk_w);
+  const int warps = 8;
+  dim3 grid(ceil_div(T, warps));
+  cudaStream_t st = (cudaStream_t)s;
+  const int per = ceil_div(E, 32);
+  if (per <= 1) route_kernel<1><<<grid, warps * 32, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
+  else if (per <= 2) route_kernel<2><<<grid, warps * 32, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
+  else if (per <= 4) route_kernel<4><<<grid, warps * 32, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
+  else if (per <= 8) route_kernel<8><<<grid, warps * 32, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
+  else if (per <= 16) route_kernel<16><<<grid, warps * 32, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
+  else route_kernel<32><<<grid, warps * 32, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
+  FT_CHECK_LAUNCH();
+  return FT_OK;
+}
+
+// ------------------------------------------------------------------ permute
+FT_API int ft_permute(const int32_t* topk_idx, int T, int k, int E, int32_t* counts, int32_t* offsets, int32_t* perm,
+                      int32_t* inv, ft_cuda_stream s) {
+  FT_REQUIRE(T >= 0 && k >= 1 && E >= 1 && E <= PM_MAXE);
+  FT_REQUIRE(counts && offsets);
+  const long long n = (long long)T * k;
+  FT_REQUIRE(n < (1ll << 30));
+  FT_REQUIRE(n == 0 || (topk_idx && perm && inv));
+  const size_t smem = (size_t)(2 * E + PM_WARPS * E) * sizeof(int32_t);
+  if (int st = set_smem(permute_kernel, smem)) return st;
+  permute_kernel<<<1, PM_THREADS, smem, (cudaStream_t)s>>>(topk_idx, (int)n, E, counts, offsets, perm, inv);
+  FT_CHECK_LAUNCH();
+  return FT_OK;
+}
+
+// ------------------------------------------------------------------ combine
+FT_API int ft_combine(const float* y, const int32_t* inv, const int32_t* topk_idx, const float* topk_w,
+                      const int32_t* ext_flags, const float* ext_partial, int T, int k, int H, int E, float* out,
+                      ft_cuda_stream s) {
+  FT_REQUIRE(T >= 0 && k >= 1 && H > 0 && H % 4 == 0 && E >= 1);
+  if (T == 0) return FT_OK;
+  FT_REQUIRE(y && inv && topk_idx && topk_w && out);
+  FT_REQUIRE(T <= 65535);
+  dim3 grid(ceil_div(H / 4, 256), T);
+  combine_kernel<<<grid, 256, 0, (cudaStream_t)s>>>(y, inv, topk_idx, topk_w, ext_flags, ext_partial, T, k, H, E, out);
+  FT_CHECK_LAUNCH();
+  return FT_OK;
+}
+
+// ------------------------------------------------------------------ expert grouped
+FT_API size_t ft_expert_grouped_workspace(int T, int k, int hidden, int inter) {
+  (void)hidden;
+  if (T <= 0 || k <= 0 || inter <= 0) return 256;
+  return ((size_t)T * k * inter * sizeof(float) + 255) / 256 * 256;
+}
+
+namespace {
+
+template <int WT>
+int launch_expert(const ExpertArgs& a, cudaStream_t st) {
+  constexpr int EPL = WFmt<WT>::EPL;
+  const size_t head = ((size_t)(2 * a.E + 1) * 4 + 15) / 16 * 16;
+  const size_t smem_gu = head + (size_t)EX_MR * staged_stride<EPL>(a.H) * sizeof(float);
+  const size_t smem_dn = head + (size_t)EX_MR * staged_stride<EPL>(a.I) * sizeof(float);
+  if (smem_gu > 227 * 1024 || smem_dn > 227 * 1024) return FT_EUNSUPPORTED;
+  if (a.x_type == FT_X_BF16) {
+    auto kg = gateup_kernel<WT, __nv_bfloat16>;
+    if (int s = set_smem(kg, smem_gu)) return s;
+    kg<<<occupancy_grid(kg, EX_THREADS, smem_gu), EX_THREADS, smem_gu, st>>>(a);
+  } else {
+    auto kg = gateup_kernel<WT, float>;
+    if (int s = set_smem(kg, smem_gu)) return s;
+    kg<<<occupancy_grid(kg, EX_THREADS, smem_gu), EX_THREADS, smem_gu, st>>>(a);
+  }
+  FT_CHECK_LAUNCH();
+  auto kd = down_kernel<WT>;
+  if (int s = set_smem(kd, smem_dn)) return s;
+  kd<<<occupancy_grid(kd, EX_THREADS, smem_dn), EX_THREADS, smem_dn, st>>>(a);
+  FT_CHECK_LAUNCH();
+  return FT_OK;
+}
+
+}  // namespace
+
+FT_API int ft_expert_grouped(const void* x, int x_type, int T, int k, int hidden, int inter, int E, int wtype,
+                             const int32_t* perm, const int32_t* offsets, const int32_t* slot_of,
+                             const void* slot_pool, uint64_t slot_bytes, int pool_slots, float* y, void* workspace,
+                             size_t workspace_bytes, ft_cuda_stream s) {
+  FT_REQUIRE(T >= 0 && k >= 1 && E >= 1 && E <= 1024 && pool_slots >= 1);
+  FT_REQUIRE(x_type == FT_X_F32 || x_type == FT_X_BF16);
+  ft_expert_layout L;
+  if (expert_layout(wtype, hidden, inter, &L) != FT_OK) return FT_EINVAL;
+  FT_REQUIRE(slot_bytes >= L.bytes && slot_bytes % 256 == 0);
+  if (T == 0) return FT_OK;
+  FT_REQUIRE(x && perm && offsets && slot_of && slot_pool && y && workspace);
+  FT_REQUIRE(workspace_bytes >= ft_expert_grouped_workspace(T, k, hidden, inter));
+  FT_REQUIRE(((uintptr_t)workspace & 255) == 0 && ((uintptr_t)slot_pool & 255) == 0);
+  ExpertArgs a;
+  a.x = x; a.x_type = x_type; a.T = T; a.k = k; a.H = hidden; a.I = inter; a.E = E; a.pool_slots = pool_slots;
+  a.perm = perm; a.offsets = offsets; a.slot_of = slot_of; a.pool = (const uint8_t*)slot_pool; a.S = slot_bytes;
+  for (int m = 0; m < 3; ++m) { a.off_val[m] = L.off_val[m]; a.off_scale[m] = L.off_scale[m]; }
+  a.off_gscale = L.off_gscale;
+  a.A = (float*)workspace;
+  a.y = y;
+  cudaStream_t st = (cudaStream_t)s;
+  switch (wtype) {
+    case FT_W_F32: return launch_expert<FT_W_F32>(a, st);
+    case FT_W_BF16: return launch_expert<FT_W_BF16>(a, st);
+    case FT_W_FP8E4M3: return launch_expert<FT_W_FP8E4M3>(a, st);
+    case FT_W_NVFP4: return launch_expert<FT_W_NVFP4>(a, st);
+    case FT_W_MXFP4: return launch_expert<FT_W_MXFP4>(a, st);
+  }
+  return FT_EINVAL;
+}
+
+// ------------------------------------------------------------------ cache
+FT_API int ft_cache_create(const ft_cache_config* cfg, ft_cache** out) {
+  FT_REQUIRE(cfg && out);
+  *out = nullptr;
+  FT_REQUIRE(cfg->n_layers >= 1 && cfg->n_experts >= 1 && cfg->n_experts <= CACHE_MAX_E);
+  FT_REQUIRE(cfg->n_phys_layers >= 1 && cfg->n_phys_layers <= cfg->n_layers);
+  FT_REQUIRE(cfg->max_slots >= 1 && cfg->max_slots <= CACHE_MAX_SLOTS);
+  FT_REQUIRE(cfg->n_slots >= 1 && cfg->n_slots <= cfg->max_slots);
+  FT_REQUIRE(cfg->slot_bytes > 0 && cfg->slot_bytes % 256 == 0);
+  FT_REQUIRE(cfg->host_pool && cfg->slot_pool);
+  FT_REQUIRE((long long)cfg->n_layers * cfg->n_experts < (1ll << 30));
+  void* hd = nullptr;
+  cudaError_t e = cudaHostGetDevicePointer(&hd, const_cast<void*>(cfg->host_pool), 0);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FT_EINVAL;  // not mapped pinned memory
+  }
+  ft_cache* c = new (std::nothrow) ft_cache();
+  if (!c) return FT_ENOMEM;
+  c->L = cfg->n_layers; c->E = cfg->n_experts; c->Lp = cfg->n_phys_layers; c->N = cfg->n_slots;
+  c->max_slots = cfg->max_slots; c->S = cfg->slot_bytes;
+  c->host = (const uint8_t*)cfg->host_pool; c->host_dev = (const uint8_t*)hd; c->pool = (uint8_t*)cfg->slot_pool;
+  cudaGetDevice(&c->dev);
+  const size_t nk = (size_t)c->L * c->E;
+  bool ok = cudaMalloc(&c->slot_of_key, nk * 4) == cudaSuccess &&
+            cudaMalloc(&c->key_of_slot, (size_t)c->max_slots * 4) == cudaSuccess &&
+            cudaMalloc(&c->stamp, (size_t)c->max_slots * 4) == cudaSuccess &&
+            cudaMalloc(&c->order, (size_t)c->max_slots * 4) == cudaSuccess &&
+            cudaMalloc(&c->clock, 4) == cudaSuccess && cudaMalloc(&c->stats, 5 * 8) == cudaSuccess &&
+            cudaMalloc(&c->fill_src, (size_t)c->E * 4) == cudaSuccess &&
+            cudaMalloc(&c->fill_dst, (size_t)c->E * 4) == cudaSuccess && cudaMalloc(&c->n_fill, 4) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    ft_cache_destroy(c);
+    return FT_ENOMEM;
+  }
+  int st = FT_OK;
+  if (cudaMemset(c->stats, 0, 5 * 8) != cudaSuccess || cudaMemset(c->n_fill, 0, 4) != cudaSuccess) st = FT_ECUDA;
+  HostTables t;
+  t.key.assign(c->N, -1);
+  t.stamp.assign(c->N, 0);
+  t.clock = 0;
+  if (!st) st = upload_tables(c, t);
+  if (!st) st = set_smem(cache_control_kernel, cache_control_smem(c->max_slots, c->E));
+  if (!st && cudaDeviceSynchronize() != cudaSuccess) st = FT_ECUDA;
+  if (st) {
+    ft_cache_destroy(c);
+    return st;
+  }
+  c->fill_grid = 2 * sms();
+  *out = c;
+  return FT_OK;
+}
+
+FT_API int ft_cache_destroy(ft_cache* c) {
+  if (!c) return FT_OK;
+  cudaFree(c->slot_of_key); cudaFree(c->key_of_slot); cudaFree(c->stamp); cudaFree(c->order);
+  cudaFree(c->clock); cudaFree(c->stats); cudaFree(c->fill_src); cudaFree(c->fill_dst); cudaFree(c->n_fill);
+  delete c;
+  return FT_OK;
+}
+
+FT_API int ft_cache_n_waves(const ft_cache* c) {
+  if (!c) return 0;
+  return ceil_div(c->E, c->N);
+}
+
+FT_API int ft_cache_step(ft_cache* c, int layer, const int32_t* counts, double fill_ratio, int wave, int32_t* slot_of,
+                         int32_t* ext_flags, int32_t* step_counts, ft_cuda_stream s) {
+  FT_REQUIRE(c && counts && slot_of);
+  FT_REQUIRE(layer >= 0 && layer < c->L && wave >= 0 && wave < ceil_div(c->E, c->N));
+  FT_REQUIRE(fill_ratio > 0.0);
+  if (c->streaming) return FT_ESTATE;
+  cudaStream_t st = (cudaStream_t)s;
+  const size_t smem = cache_control_smem(c->N, c->E);
+  cache_control_kernel<<<1, CC_THREADS, smem, st>>>(cache_dev(c), layer, counts, fill_ratio, wave, slot_of, ext_flags,
+                                                     step_counts);
+  FT_CHECK_LAUNCH();
+  cache_fill_kernel<<<c->fill_grid, FILL_THREADS, 0, st>>>(c->host_dev, c->pool, c->S, c->Lp * c->E, c->max_slots,
+                                                           c->fill_src, c->fill_dst, c->n_fill);
+  FT_CHECK_LAUNCH();
+  return FT_OK;
+}
+
+FT_API int ft_cache_resize(ft_cache* c, int n_slots) {
+  FT_REQUIRE(c && n_slots >= 1 && n_slots <= c->max_slots);
+  if (c->streaming) return FT_ESTATE;
+  return cache_resize_impl(c, n_slots);
+}
+
+FT_API int ft_cache_stats(ft_cache* c, ft_cache_stats_t* out) {
+  FT_REQUIRE(c && out);
+  unsigned long long v[5];
+  FT_CHECK_CUDA(cudaDeviceSynchronize());
+  FT_CHECK_CUDA(cudaMemcpy(v, c->stats, sizeof(v), cudaMemcpyDeviceToHost));
+  out->steps = v[0]; out->hits = v[1]; out->fills = v[2]; out->externals = v[3]; out->bytes_h2d = v[4];
+  return FT_OK;
+}
+
+FT_API int ft_cache_export(ft_cache* c, int32_t* key_of_slot, uint32_t* stamp, int* n_slots, uint32_t* clock) {
+  FT_REQUIRE(c && key_of_slot && stamp && n_slots && clock);
+  HostTables t;
+  if (int s = download_tables(c, t)) return s;
+  for (int i = 0; i < c->N; ++i) { key_of_slot[i] = t.key[i]; stamp[i] = t.stamp[i]; }
+  *n_slots = c->N;
+  *clock = t.clock;
+  return FT_OK;
+}
+
+// ------------------------------------------------------------------ stream
+FT_API int ft_stream_create(ft_cache* c, int serialized, ft_stream** out) {
+  FT_REQUIRE(c && out);
+  *out = nullptr;
+  if (c->streaming) return FT_ESTATE;
+  if (c->N < 2 * c->E) return FT_EUNSUPPORTED;
+  ft_stream* st = new (std::nothrow) ft_stream();
+  if (!st) return FT_ENOMEM;
+  const int n_full = c->N;
+  int s = cache_resize_impl(c, n_full - 2 * c->E);
+  if (s) { delete st; return s; }
+  c->n_full = n_full;
+  c->streaming = 1;
+  st->c = c;
+  st->serialized = serialized ? 1 : 0;
+  st->base = n_full - 2 * c->E;
+  st->buf_layer[0] = st->buf_layer[1] = -1;
+  st->freed_rec[0] = st->freed_rec[1] = false;
+  st->next_buf = 0;
+  st->pending_layer = -1;
+  st->bytes = 0;
+  st->n_hist = 0;
+  cudaError_t e = cudaStreamCreateWithFlags(&st->copy, cudaStreamNonBlocking);
+  for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+    e = cudaEventCreateWithFlags(&st->ready[b], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st->freed[b], cudaEventDisableTiming);
+  }
+  if (e != cudaSuccess) {
+    c->streaming = 0;
+    c->N = n_full;
+    delete st;
+    return cuda_status(e);
+  }
+  *out = st;
+  return FT_OK;
+}
+
+FT_API int ft_stream_layer(ft_stream* st, int layer, int next_layer, int32_t* slot_of, ft_cuda_stream compute) {
+  FT_REQUIRE(st && slot_of);
+  ft_cache* c = st->c;
+  FT_REQUIRE(layer >= 0 && layer < c->L && next_layer >= -1 && next_layer < c->L);
+  cudaStream_t cs = (cudaStream_t)compute;
+  int b = buffer_of(st, layer);
+  if (b < 0) {
+    b = st->next_buf;
+    if (int s = stream_issue_copy(st, layer, b, nullptr)) return s;
+    st->next_buf = b ^ 1;
+  }
+  FT_CHECK_CUDA(cudaStreamWaitEvent(cs, st->ready[b], 0));
+  set_buffer_slots_kernel<<<ceil_div(c->E, 256), 256, 0, cs>>>(slot_of, c->E, st->base + b * c->E);
+  FT_CHECK_LAUNCH();
+  st->pending_layer = -1;
+  if (next_layer >= 0 && buffer_of(st, next_layer) < 0) {
+    const int nb = b ^ 1;
+    if (!st->serialized) {
+      if (int s = stream_issue_copy(st, next_layer, nb, nullptr)) return s;
+      st->next_buf = b;
+    } else {
+      st->pending_layer = next_layer;
+      st->pending_buf = nb;
+    }
+  }
+  return FT_OK;
+}
+
+FT_API int ft_stream_layer_done(ft_stream* st, int layer, ft_cuda_stream compute) {
+  FT_REQUIRE(st);
+  const int b = buffer_of(st, layer);
+  FT_REQUIRE(b >= 0);
+  cudaStream_t cs = (cudaStream_t)compute;
+  FT_CHECK_CUDA(cudaEventRecord(st->freed[b], cs));
+  st->freed_rec[b] = true;
+  if (st->serialized && st->pending_layer >= 0) {
+    const int nb = st->pending_buf;
+    if (int s = stream_issue_copy(st, st->pending_layer, nb, st->freed[b])) return s;
+    st->next_buf = b;
+    st->pending_layer = -1;
+  }
+  return FT_OK;
+}
+
+FT_API int ft_stream_bytes(const ft_stream* st, uint64_t* bytes) {
+  FT_REQUIRE(st && bytes);
+  *bytes = st->bytes;
+  return FT_OK;
+}
+
+FT_API int ft_stream_destroy(ft_stream* st) {
+  if (!st) return FT_OK;
+  ft_cache* c = st->c;
+  cudaStreamSynchronize(st->copy);
+  int s = stream_adopt(st);
+  c->streaming = 0;
+  cudaStreamDestroy(st->copy);
+  for (int b = 0; b < 2; ++b) {
+    cudaEventDestroy(st->ready[b]);
+    cudaEventDestroy(st->freed[b]);
+  }
+  delete st;
+  return s;
+}

@@ -1,0 +1,277 @@
+// Router logits, top-k gating, permutation by expert, and the weighted combine.
+#pragma once
+#include "common.cuh"
+
+namespace ft {
+
+// ====================================================================== router logits
+// z[t][e] = sum_h x[t][h] W_r[e][h] + b[e].  A CTA stages RT token rows of x
+// in shared memory (fp32) and its warps sweep the experts: a warp reads one
+// router row with 16-byte loads and dots it with every staged row; lane
+// partials are reduced with one reduce-scatter per expert.
+constexpr int RL_RT = 8;        // token rows per CTA
+constexpr int RL_WARPS = 8;
+
+template <typename XT>
+__device__ __forceinline__ void load8(const XT* p, float (&o)[8]);
+
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&o)[8]) {
+  uint4 u = *reinterpret_cast<const uint4*>(p);
+  o[0] = bf16lo(u.x); o[1] = bf16hi(u.x); o[2] = bf16lo(u.y); o[3] = bf16hi(u.y);
+  o[4] = bf16lo(u.z); o[5] = bf16hi(u.z); o[6] = bf16lo(u.w); o[7] = bf16hi(u.w);
+}
+
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float (&o)[8]) {
+  float4 a = *reinterpret_cast<const float4*>(p);
+  float4 b = *reinterpret_cast<const float4*>(p + 4);
+  o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+
+template <typename XT>
+__global__ void __launch_bounds__(RL_WARPS * 32)
+router_logits_kernel(const XT* __restrict__ x, const XT* __restrict__ wr, const float* __restrict__ bias,
+                     int T, int H, int E, float* __restrict__ z) {
+  extern __shared__ float xs[];  // [RL_RT][H]
+  const int t0 = blockIdx.x * RL_RT;
+  const int nrows = min(RL_RT, T - t0);
+  for (int i = threadIdx.x; i < RL_RT * H; i += blockDim.x) {
+    int r = i / H, h = i - r * H;
+    xs[i] = r < nrows ? (float)x[(size_t)(t0 + r) * H + h] : 0.0f;
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int e = warp; e < E; e += RL_WARPS) {
+    float acc[RL_RT];
+#pragma unroll
+    for (int r = 0; r < RL_RT; ++r) acc[r] = 0.0f;
+    const XT* w = wr + (size_t)e * H;
+    for (int k = lane * 8; k < H; k += 256) {
+      float wv[8];
+      load8<XT>(w + k, wv);
+#pragma unroll
+      for (int r = 0; r < RL_RT; ++r) {
+        const float* xr = xs + r * H + k;
+        float4 a = *reinterpret_cast<const float4*>(xr);
+        float4 b = *reinterpret_cast<const float4*>(xr + 4);
+        acc[r] += wv[0] * a.x + wv[1] * a.y + wv[2] * a.z + wv[3] * a.w +
+                  wv[4] * b.x + wv[5] * b.y + wv[6] * b.z + wv[7] * b.w;
+      }
+    }
+    warp_reduce_scatter<RL_RT>(acc, lane);
+    const int r = lane / (32 / RL_RT);
+    if ((lane % (32 / RL_RT)) == 0 && r < nrows)
+      z[(size_t)(t0 + r) * E + e] = acc[0] + (bias ? bias[e] : 0.0f);
+  }
+}
+
+// ====================================================================== top-k gating
+// One warp per token.  Lane l holds logits e = l, l+32, ...  Each of the k
+// rounds takes the warp-wide maximum of (value, -index) among the experts not
+// yet chosen.  Weights are a softmax over the chosen logits.
+constexpr int RT_MAXK = 16;
+constexpr int RT_MAXE = 1024;
+
+__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+template <int PER_LANE>
+__global__ void __launch_bounds__(256)
+route_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ idx_out,
+             float* __restrict__ w_out) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float* z = logits + (size_t)t * E;
+  float v[PER_LANE];
+  unsigned taken = 0;
+#pragma unroll
+  for (int i = 0; i < PER_LANE; ++i) {
+    int e = lane + 32 * i;
+    v[i] = e < E ? z[e] : -INFINITY;
+    if (e >= E) taken |= 1u << i;
+  }
+  float sel_v[RT_MAXK];
+  int sel_i[RT_MAXK];
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i) {
+      int e = lane + 32 * i;
+      if (!(taken >> i & 1u) && better(v[i], e, bv, bi)) { bv = v[i]; bi = e; }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      float ov = __shfl_xor_sync(FT_FULL_MASK, bv, o);
+      int oi = __shfl_xor_sync(FT_FULL_MASK, bi, o);
+      if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+    }
+    // NaN logits or all -inf: fall back to the lowest untaken index so the id stays in range
+    if (bi >= E) {
+      int cand = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < PER_LANE; ++i) {
+        int e = lane + 32 * i;
+        if (!(taken >> i & 1u) && e < cand) cand = e;
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) cand = min(cand, __shfl_xor_sync(FT_FULL_MASK, cand, o));
+      bi = cand;
+      bv = z[bi];
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    sel_v[j] = bv;
+    sel_i[j] = bi;
+  }
+  if (lane == 0) {
+    const float m = sel_v[0];
+    float s = 0.0f;
+    float ex[RT_MAXK];
+#pragma unroll 1
+    for (int j = 0; j < k; ++j) { ex[j] = expf(sel_v[j] - m); s += ex[j]; }
+    const float inv = 1.0f / s;
+#pragma unroll 1
+    for (int j = 0; j < k; ++j) {
+      idx_out[(size_t)t * k + j] = sel_i[j];
+      w_out[(size_t)t * k + j] = ex[j] * inv;
+    }
+  }
+}
+
+// ====================================================================== permutation
+// One CTA.  Pass 1: per-expert counts with shared-memory atomics, exclusive
+// scan into offsets.  Pass 2: assignments in tiles of blockDim; inside a warp,
+// __match_any_sync groups equal experts and the rank is the number of equal
+// lanes below; across warps a per-(warp, expert) count table is scanned in warp
+// order, continuing from the previous tiles.  Positions therefore follow the
+// assignment order a = t*k + j within each expert (stable).
+constexpr int PM_THREADS = 1024;
+constexpr int PM_WARPS = PM_THREADS / 32;
+constexpr int PM_MAXE = 512;
+
+__global__ void __launch_bounds__(PM_THREADS)
+permute_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __restrict__ counts,
+               int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+  extern __shared__ int32_t pm_smem[];
+  int32_t* cnt = pm_smem;                    // [E]
+  int32_t* base = cnt + E;                // [E] running position per expert (absolute)
+  int32_t* wc = base + E;                 // [PM_WARPS][E]
+  __shared__ int32_t warp_tot[PM_WARPS];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < E; e += PM_THREADS) cnt[e] = 0;
+  for (int i = tid; i < PM_WARPS * E; i += PM_THREADS) wc[i] = 0;
+  __syncthreads();
+  for (int a = tid; a < n; a += PM_THREADS) {
+    int e = idx[a];
+    if ((unsigned)e < (unsigned)E) atomicAdd(&cnt[e], 1);
+    else record_error(FT_DERR_EXPERT_INDEX);
+  }
+  __syncthreads();
+  // exclusive scan of cnt (E <= 512): each thread sums a strided chunk, then warp scans
+  {
+    const int per = ceil_div(E, PM_THREADS);
+    int local = 0;
+    for (int i = 0; i < per; ++i) {
+      int e = tid * per + i;
+      if (e < E) local += cnt[e];
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(FT_FULL_MASK, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_tot[lane];
+      int wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(FT_FULL_MASK, wi, o);
+        if (lane >= o) wi += y;
+      }
+      warp_tot[lane] = wi - w;
+    }
+    __syncthreads();
+    int run = warp_tot[warp] + incl - local;
+    for (int i = 0; i < per; ++i) {
+      int e = tid * per + i;
+      if (e < E) {
+        base[e] = run;
+        offsets[e] = run;
+        counts[e] = cnt[e];
+        run += cnt[e];
+      }
+    }
+    if (tid == 0) offsets[E] = n;
+  }
+  __syncthreads();
+  for (int t0 = 0; t0 < n; t0 += PM_THREADS) {
+    const int a = t0 + tid;
+    int e = a < n ? idx[a] : -1;
+    if ((unsigned)e >= (unsigned)E) e = -1;
+    const unsigned peers = __match_any_sync(FT_FULL_MASK, e);
+    const int rank = __popc(peers & ((1u << lane) - 1));
+    const int leader = __ffs(peers) - 1;
+    if (e >= 0 && lane == leader) wc[warp * E + e] = __popc(peers);
+    __syncthreads();
+    for (int ex = tid; ex < E; ex += PM_THREADS) {
+      int run = base[ex];
+#pragma unroll 4
+      for (int w = 0; w < PM_WARPS; ++w) {
+        int c = wc[w * E + ex];
+        wc[w * E + ex] = run;
+        run += c;
+      }
+      base[ex] = run;
+    }
+    __syncthreads();
+    if (e >= 0) {
+      const int pos = wc[warp * E + e] + rank;
+      perm[pos] = a;
+      inv[a] = pos;
+    }
+    __syncthreads();
+    // the scan above wrote every (w, ex) entry: reset the whole table for the next tile
+    for (int i = tid; i < PM_WARPS * E; i += PM_THREADS) wc[i] = 0;
+    __syncthreads();
+  }
+}
+
+// ====================================================================== combine
+// out[t][h] = sum_j w[t][j] y[inv[t*k+j]][h] (+ P[t][h]); assignments of
+// experts flagged external are skipped.  One CTA row-block per token, float4
+// per thread; the sum order is fixed (j ascending, then P).
+__global__ void __launch_bounds__(256)
+combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv, const int32_t* __restrict__ idx,
+               const float* __restrict__ w, const int32_t* __restrict__ ext, const float* __restrict__ P,
+               int T, int k, int H, int E, float* __restrict__ out) {
+  const int t = blockIdx.y;
+  const int h4 = blockIdx.x * blockDim.x + threadIdx.x;
+  if (h4 * 4 >= H) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int nrows = T * k;
+  for (int j = 0; j < k; ++j) {
+    const int a = t * k + j;
+    const int e = idx[a];
+    if ((unsigned)e >= (unsigned)E) { record_error(FT_DERR_EXPERT_INDEX); continue; }
+    if (ext && ext[e]) continue;
+    const int row = inv[a];
+    if ((unsigned)row >= (unsigned)nrows) { record_error(FT_DERR_ROW_INDEX); continue; }
+    const float wj = w[a];
+    float4 v = reinterpret_cast<const float4*>(y + (size_t)row * H)[h4];
+    acc.x += wj * v.x; acc.y += wj * v.y; acc.z += wj * v.z; acc.w += wj * v.w;
+  }
+  if (P) {
+    float4 p = reinterpret_cast<const float4*>(P + (size_t)t * H)[h4];
+    acc.x += p.x; acc.y += p.y; acc.z += p.z; acc.w += p.w;
+  }
+  reinterpret_cast<float4*>(out + (size_t)t * H)[h4] = acc;
+}
+
+}  // namespace ft

@@ -1,0 +1,134 @@
+"""Expert pool setup and the per-layer call sequence over libft.
+
+``ExpertPool`` owns the pinned host pool (all experts of ``n_phys_layers``
+layers as records, row l*E + e) and writes synthetic weights into it.
+``MoELayer`` owns the per-step device buffers and issues the libft calls of
+one MoE layer step in order:
+
+    ft_router_logits -> ft_route -> ft_permute -> [ft_cache_step per wave ->
+    ft_expert_grouped] -> ft_combine
+
+Nothing here computes: it allocates buffers and sequences the C calls.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import (FT_W_BF16, FT_W_F32, FT_W_FP8E4M3, FT_W_MXFP4, FT_W_NVFP4, Cache, PinnedBuffer, ft_combine,
+               ft_expert_grouped, ft_expert_grouped_workspace, ft_expert_layout_get, ft_permute, ft_route,
+               ft_router_logits)
+
+
+def pack_expert(comps: dict, wtype: int, layout, out: torch.Tensor) -> None:
+    """Writes one expert's stored components into a record (uint8 tensor of S bytes)."""
+    out.zero_()
+    for m, name in enumerate(("gate", "up", "down")):
+        c = comps[name]
+        vals = c["w"] if wtype in (FT_W_F32, FT_W_BF16) else c["codes"]
+        vb = vals.contiguous().view(torch.uint8).reshape(-1)
+        o = layout.off_val[m]
+        out[o:o + vb.numel()].copy_(vb)
+        if wtype in (FT_W_FP8E4M3, FT_W_NVFP4, FT_W_MXFP4):
+            sb = c["scales"].contiguous().view(torch.uint8).reshape(-1)
+            o = layout.off_scale[m]
+            out[o:o + sb.numel()].copy_(sb)
+    if wtype == FT_W_NVFP4:
+        g = torch.tensor([comps[n]["gscale"] for n in ("gate", "up", "down")], dtype=torch.float32)
+        o = layout.off_gscale
+        out[o:o + 12].copy_(g.view(torch.uint8).to(out.device))
+
+
+class ExpertPool:
+    """Pinned host pool of expert records for ``n_phys_layers`` layers of a config."""
+
+    def __init__(self, cfg, n_phys_layers: int):
+        self.cfg = cfg
+        self.n_phys = n_phys_layers
+        self.layout = ft_expert_layout_get(cfg.wtype, cfg.hidden, cfg.inter)
+        self.S = int(self.layout.bytes)
+        self.E = cfg.n_experts
+        self.buf = PinnedBuffer(self.n_phys * self.E * self.S)
+        self.host = self.buf.tensor
+
+    @property
+    def ptr(self) -> int:
+        return self.buf.ptr
+
+    def row(self, phys_layer: int, expert: int) -> torch.Tensor:
+        o = (phys_layer * self.E + expert) * self.S
+        return self.host[o:o + self.S]
+
+    def fill(self, device="cuda", layers=None) -> None:
+        """Generates every expert with ``synth`` on ``device`` and copies each layer into the pool."""
+        import synth
+        staging = torch.empty(self.E * self.S, dtype=torch.uint8, device=device)
+        for l in (range(self.n_phys) if layers is None else layers):
+            for e in range(self.E):
+                rec = staging[e * self.S:(e + 1) * self.S]
+                pack_expert(synth.expert_weights(self.cfg, l, e, device), self.cfg.wtype, self.layout, rec)
+            o = l * self.E * self.S
+            self.host[o:o + self.E * self.S].copy_(staging, non_blocking=False)
+        del staging
+
+    def free(self):
+        self.buf.free()
+
+
+class MoELayer:
+    """Per-step device buffers for batches of up to ``T_max`` tokens, and the call sequence."""
+
+    def __init__(self, cfg, T_max: int, device="cuda"):
+        self.cfg = cfg
+        E, k, H, I = cfg.n_experts, cfg.top_k, cfg.hidden, cfg.inter
+        self.T_max = T_max
+        i32 = dict(dtype=torch.int32, device=device)
+        f32 = dict(dtype=torch.float32, device=device)
+        self.logits = torch.empty(T_max, E, **f32)
+        self.idx = torch.empty(T_max, k, **i32)
+        self.w = torch.empty(T_max, k, **f32)
+        self.counts = torch.empty(E, **i32)
+        self.offsets = torch.empty(E + 1, **i32)
+        self.perm = torch.empty(T_max * k, **i32)
+        self.inv = torch.empty(T_max * k, **i32)
+        self.slot_of = torch.empty(E, **i32)
+        self.ext = torch.zeros(E, **i32)
+        self.step_counts = torch.zeros(4, **i32)
+        self.y = torch.empty(T_max * k, H, **f32)
+        self.out = torch.empty(T_max, H, **f32)
+        ws = ft_expert_grouped_workspace(T_max, k, H, I)
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=device)
+
+    def route(self, x, w_router, bias, stream=None):
+        T = x.shape[0]
+        ft_router_logits(x, w_router, bias, self.logits[:T], stream)
+        ft_route(self.logits[:T], self.cfg.top_k, self.idx[:T], self.w[:T], stream)
+        ft_permute(self.idx[:T], self.cfg.n_experts, self.counts, self.offsets, self.perm, self.inv, stream)
+
+    def experts(self, x, slot_of, slot_pool, slot_bytes, pool_slots, stream=None):
+        ft_expert_grouped(x, self.cfg.top_k, self.cfg.inter, self.cfg.n_experts, self.cfg.wtype, self.perm,
+                          self.offsets, slot_of, slot_pool, slot_bytes, pool_slots,
+                          self.y[: x.shape[0] * self.cfg.top_k], self.workspace, stream)
+
+    def combine(self, T, ext_flags=None, ext_partial=None, stream=None):
+        ft_combine(self.y[: T * self.cfg.top_k], self.inv, self.idx[:T], self.w[:T], ext_flags, ext_partial,
+                   self.cfg.n_experts, self.out[:T], stream)
+        return self.out[:T]
+
+    def forward_cached(self, x, w_router, bias, layer: int, cache: Cache, slot_bytes: int,
+                       fill_ratio: float = 1.0, ext_partial: Optional[torch.Tensor] = None, stream=None):
+        """One layer step over the LRU cache (all waves), returning out [T, H] fp32."""
+        T = x.shape[0]
+        self.route(x, w_router, bias, stream)
+        for wv in range(cache.n_waves()):
+            cache.step(layer, self.counts, fill_ratio, wv, self.slot_of, self.ext, self.step_counts, stream)
+            self.experts(x, self.slot_of, cache.slot_pool, slot_bytes, cache.max_slots, stream)
+        return self.combine(T, self.ext, ext_partial, stream)
+
+    def forward_slots(self, x, w_router, bias, slot_of, slot_pool, slot_bytes, pool_slots, stream=None):
+        """One layer step with every expert already resident at slot_of[e] (streaming, fused mode)."""
+        T = x.shape[0]
+        self.route(x, w_router, bias, stream)
+        self.experts(x, slot_of, slot_pool, slot_bytes, pool_slots, stream)
+        return self.combine(T, None, None, stream)

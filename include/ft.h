@@ -1,0 +1,337 @@
+/*
+ * ft.h -- C ABI of the expert-cache MoE layer library (libft.so, sm_103a).
+ *
+ * One routed-expert MoE layer evaluated over a slot-pool expert cache:
+ * router logits -> top-k gating -> permutation by expert -> cache control and
+ * miss fill -> grouped SwiGLU expert FFN over cache slots -> weighted combine
+ * (+ an optional external partial output), plus whole-layer double-buffered
+ * prefill streaming of the expert pool and the q* miss-split rule.
+ *
+ * Sources (page title, section):
+ *   [Review]   "论文综述：FreeToken 让个人电脑跑起前沿 MoE 大模型的边缘原生服务系统"
+ *              (paper.oopus.info), §2 opening, §2.2, §2.4, §2.5, §2.6, §2.7, Table 1.
+ *   [Overview] "FreeToken – 边缘原生的 MoE（混合专家）模型推理服务系统"
+ *              (shshi.cn), "FreeToken技术原理" items 1, 2, 4.
+ *
+ * Conventions for every call:
+ *   - The caller owns every device and pinned-host buffer and keeps it alive
+ *     until the work that uses it has finished on the stream.  The library
+ *     owns only the opaque handles (ft_cache, ft_stream) and their small
+ *     device tables.
+ *   - "dev" pointers are CUDA device pointers on the current device; "host"
+ *     pointers are ordinary host memory; "pinned" means page-locked host
+ *     memory mapped into the device address space (cudaHostAlloc, or
+ *     cudaHostRegister with the mapped flag).
+ *   - Hot-path calls are asynchronous on the given stream (a cudaStream_t;
+ *     NULL = the legacy default stream) and never synchronise the host.  The
+ *     calls that synchronise say so.
+ *   - Sizes are checked before any launch: a bad size or a NULL where one is
+ *     not allowed returns FT_EINVAL and launches nothing.  A CUDA error returns
+ *     FT_ECUDA (ft_last_cuda_error() gives the cudaError_t).
+ *   - Kernels check every index they read from memory (expert ids, slots,
+ *     rows).  An out-of-range index skips the access and records an error
+ *     code in a device error word, read and cleared by ft_get_device_error().
+ *   - Not thread-safe per handle: use one handle from one host thread.
+ */
+#ifndef FT_H
+#define FT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* ft_cuda_stream; /* a cudaStream_t */
+
+typedef enum {
+  FT_OK = 0,
+  FT_EINVAL = 1,        /* bad argument or size */
+  FT_ENOMEM = 2,        /* device allocation for a handle's tables failed */
+  FT_ECUDA = 3,         /* a CUDA runtime call failed */
+  FT_ETIMEOUT = 4,      /* a bounded wait ran out */
+  FT_ESTATE = 5,        /* call not allowed in the handle's current state */
+  FT_EUNSUPPORTED = 6,  /* configuration the library does not handle */
+  FT_EDEVICE = 7        /* a kernel recorded an index error (see ft_get_device_error) */
+} ft_status;
+
+/* Stored expert-weight formats ([Overview] feature table: MXFP4, NVFP4, FP8, BF16). */
+typedef enum {
+  FT_W_F32 = 0,      /* fp32 */
+  FT_W_BF16 = 1,     /* bf16 */
+  FT_W_FP8E4M3 = 2,  /* e4m3 values, one fp32 scale per 128 consecutive K elements */
+  FT_W_NVFP4 = 3,    /* e2m1 values, one e4m3 scale per 16 K elements, one fp32 scale per matrix */
+  FT_W_MXFP4 = 4     /* e2m1 values, one E8M0 scale per 32 K elements */
+} ft_wtype;
+
+/* Activation (x) formats. */
+typedef enum { FT_X_F32 = 0, FT_X_BF16 = 1 } ft_xtype;
+
+/* Device error codes recorded by kernels. */
+enum {
+  FT_DERR_NONE = 0,
+  FT_DERR_EXPERT_INDEX = 1,  /* an expert id outside [0, E) */
+  FT_DERR_SLOT_INDEX = 2,    /* a slot outside the pool */
+  FT_DERR_ROW_INDEX = 3,     /* a permutation row outside [0, T*k) */
+  FT_DERR_TABLE = 4          /* cache tables inconsistent */
+};
+
+const char* ft_status_str(int status);
+int ft_version(void);
+int ft_last_cuda_error(void);
+
+/* Reads and clears the device error word of the current device (synchronises
+ * the device).  *code receives one of FT_DERR_*; returns FT_EDEVICE when it was
+ * non-zero, FT_OK otherwise. */
+int ft_get_device_error(int* code);
+
+/* ------------------------------------------------------------------------
+ * Expert record layout.
+ *
+ * One cache slot holds every tensor of one (layer, expert) ([Review] §2
+ * opening: a slot holds all tensors needed to evaluate one layer-expert pair).
+ * The host pool and the device slot pool are arrays of such records; host row
+ * l*E + e is expert e of physical layer l ([Review] §2.7, expert banks with the
+ * flattened first dimension lE+e; here all banks of one expert are one record,
+ * so one copy moves one expert and one copy moves one whole layer).
+ *
+ * Inside a record, K-major matrices (contraction index contiguous), each
+ * section starting on a 256-byte boundary, in this order:
+ *   gate values [I][H], up values [I][H], down values [H][I],
+ *   then (formats with scales) gate scales, up scales, down scales,
+ *   then (NVFP4) 3 fp32 matrix scales {gate, up, down}.
+ * Values: f32 4 bytes, bf16 2 bytes, e4m3 1 byte, e2m1 4 bits with element 2i
+ * in the low nibble of byte i.  Scales per row: fp8 [rows][K/128] fp32,
+ * NVFP4 [rows][K/16] e4m3 bytes, MXFP4 [rows][K/32] E8M0 bytes.
+ * The record size S is rounded up to a multiple of 256 bytes.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  uint64_t bytes;           /* S: bytes per record (slot stride) */
+  uint64_t payload_bytes;   /* bytes of weights and scales, without padding */
+  uint64_t off_val[3];      /* gate, up, down values */
+  uint64_t off_scale[3];    /* gate, up, down block scales (0 when the format has none) */
+  uint64_t off_gscale;      /* NVFP4: 3 fp32 matrix scales (0 otherwise) */
+} ft_expert_layout;
+
+/* Fills *out for a format and shape.  H and I must be multiples of 256. */
+int ft_expert_layout_get(int wtype, int hidden, int inter, ft_expert_layout* out);
+
+/* ------------------------------------------------------------------------
+ * Pinned host pool.  The full expert pool lives in page-locked host memory,
+ * mapped into the device address space, so that copies and kernels can read
+ * it over the host link ([Review] §2 opening: the host pool is the source of
+ * truth; §2.7: the pool must be pinned for DMA).  A failed pin returns
+ * FT_ENOMEM (there is no unpinned fallback).
+ * ---------------------------------------------------------------------- */
+int ft_host_alloc(uint64_t bytes, void** out);  /* *out = pinned, mapped, 4 KiB aligned */
+int ft_host_free(void* p);
+
+/* ------------------------------------------------------------------------
+ * Router logits: z[t][e] = sum_h x[t][h] * W_r[h][e] + bias[e] (fp32 accumulate).
+ * The gating network that picks each token's experts ([Review] §1, MoE
+ * routing; the pages do not spell out the gate).
+ *   x        dev [T][H], x_type
+ *   w_router dev [E][H] (K-major), same type as x
+ *   bias     dev [E] fp32, or NULL
+ *   logits   dev [T][E] fp32 (written)
+ * T >= 0, H a multiple of 256, 1 <= E <= 1024.
+ * ---------------------------------------------------------------------- */
+int ft_router_logits(const void* x, int x_type, const void* w_router, const float* bias,
+                     int T, int H, int E, float* logits, ft_cuda_stream s);
+
+/* ------------------------------------------------------------------------
+ * ft_route: softmax over all E experts, top-k, renormalise over the k chosen.
+ * Experts are ranked by descending logit (softmax is increasing in the logit);
+ * equal logits go to the lower index.  Output j = 0..k-1 in rank order.
+ * topk_w[t][j] = exp(z_j - z_0) / sum_{i<k} exp(z_i - z_0), which equals the
+ * full softmax renormalised over the chosen k.
+ *   logits   dev [T][E] fp32
+ *   topk_idx dev [T][k] int32 (written)
+ *   topk_w   dev [T][k] fp32 (written)
+ * 1 <= k <= min(E, 16), 1 <= E <= 1024.  NaN logits give unspecified (but
+ * in-range) choices.
+ * ---------------------------------------------------------------------- */
+int ft_route(const float* logits, int T, int E, int k, int32_t* topk_idx, float* topk_w,
+             ft_cuda_stream s);
+
+/* ------------------------------------------------------------------------
+ * ft_permute: groups the T*k assignments a = t*k + j by expert for grouped
+ * evaluation ([Review] §2.5: the GPU evaluates its expert set grouped by expert).
+ *   topk_idx dev [T*k] int32 in [0, E)
+ *   counts   dev [E]    (written) assignments per expert
+ *   offsets  dev [E+1]  (written) exclusive prefix sum, offsets[E] = T*k
+ *   perm     dev [T*k]  (written) perm[offsets[e] + r] = the r-th assignment
+ *                       routed to e, in ascending a (stable)
+ *   inv      dev [T*k]  (written) inv[perm[p]] = p
+ * 1 <= E <= 512.  Deterministic.
+ * ---------------------------------------------------------------------- */
+int ft_permute(const int32_t* topk_idx, int T, int k, int E, int32_t* counts, int32_t* offsets,
+               int32_t* perm, int32_t* inv, ft_cuda_stream s);
+
+/* ------------------------------------------------------------------------
+ * ft_cache: one LRU cache of expert records shared by all MoE layers, keyed by
+ * the logical (layer, expert) ([Review] §2 opening, §2.4).  The full expert
+ * pool stays in pinned host memory; GPU memory changes only speed, never the
+ * result ([Review] §2 opening).
+ *
+ * Per layer step, one kernel de-duplicates the routed experts, classifies hits
+ * and misses against the residency table, takes q from the bandwidth ratio,
+ * picks victims in one pass over the recency order and rewrites every routed
+ * expert to a slot or to the "evaluate elsewhere" marker ([Review] §2.6,
+ * device-side cache control and one-pass victim selection); a second
+ * fixed-shape launch copies the q filled experts from the pinned pool into
+ * their slots, driven by a device-resident (source, destination) table and a
+ * device valid count ([Review] §2.6, one fused transfer).
+ *
+ * Rules where the pages are silent: routed experts in ascending id; the q
+ * filled misses are the first q misses in ascending id; a step with more
+ * unique experts than slots runs in waves of at most N experts, each wave
+ * with its own recency stamp; victims are empty slots first (ascending slot),
+ * then untouched slots by (stamp, slot).
+ * ---------------------------------------------------------------------- */
+typedef struct ft_cache ft_cache;
+
+typedef struct {
+  int n_layers;            /* logical layers L (keys are layer*E + expert) */
+  int n_experts;           /* E per layer, 1..1024 */
+  int n_phys_layers;       /* layers stored in the host pool; logical l reads physical l % n_phys_layers */
+  int n_slots;             /* initial capacity N, 1..max_slots */
+  int max_slots;           /* records the device slot pool can hold, <= 16384 */
+  uint64_t slot_bytes;     /* S, from ft_expert_layout_get */
+  const void* host_pool;   /* pinned [n_phys_layers*E][S]; caller-owned */
+  void* slot_pool;         /* dev [max_slots][S]; caller-owned */
+} ft_cache_config;
+
+typedef struct {
+  uint64_t steps, hits, fills, externals, bytes_h2d;
+} ft_cache_stats_t;
+
+/* Creates the handle and its device tables (all slots empty).  Synchronises. */
+int ft_cache_create(const ft_cache_config* cfg, ft_cache** out);
+int ft_cache_destroy(ft_cache* c);
+
+/* Waves a layer step may need: ceil(E / N). */
+int ft_cache_n_waves(const ft_cache* c);
+
+/* One wave of one layer step (asynchronous on s).
+ *   layer       logical layer, 0 <= layer < n_layers
+ *   counts      dev [E] int32, assignments per expert (> 0 = routed)
+ *   fill_ratio  B_P / B_H; q = clamp(floor(m*ratio + 0.5), 1, m) for m >= 1
+ *               misses; ratio >= 1 fills every miss ([Review] §2.5)
+ *   wave        0 .. ft_cache_n_waves()-1; wave w holds routed experts of
+ *               rank [w*N, (w+1)*N) in ascending id; an empty wave is a no-op
+ *   slot_of     dev [E] int32 (written): slot (>= 0) for this wave's experts
+ *               evaluated on the GPU, -2 for this wave's experts left to the
+ *               external path, -1 for every other expert
+ *   ext_flags   dev [E] int32 or NULL: wave 0 clears it, every wave sets 1 for
+ *               its external experts (the skip mask of ft_combine)
+ *   step_counts dev [4] int32 or NULL (written): {experts in wave, hits,
+ *               fills (q), externals (m - q)}
+ * The fill copies are ordered on s before any later work on s. */
+int ft_cache_step(ft_cache* c, int layer, const int32_t* counts, double fill_ratio, int wave,
+                  int32_t* slot_of, int32_t* ext_flags, int32_t* step_counts, ft_cuda_stream s);
+
+/* Safe-point rebuild for a new slot budget without touching the host pool
+ * ([Review] §2.7, runtime cache reconfiguration).  Keeps the min(used, N')
+ * most recent entries (largest (stamp, -slot)); kept entries below N' stay,
+ * kept entries at or above N' move (ascending old slot) into the lowest free
+ * slots below N'.  Synchronises the device.  FT_ESTATE while a stream handle
+ * holds the pool's buffers. */
+int ft_cache_resize(ft_cache* c, int n_slots);
+
+/* Counters since creation.  Synchronises. */
+int ft_cache_stats(ft_cache* c, ft_cache_stats_t* out);
+
+/* Copies the residency state to host arrays of at least max_slots entries:
+ * key_of_slot (-1 empty, else layer*E + expert) and stamp (0 for empty);
+ * *n_slots = current N, *clock = last stamp issued.  Synchronises. */
+int ft_cache_export(ft_cache* c, int32_t* key_of_slot, uint32_t* stamp, int* n_slots, uint32_t* clock);
+
+/* ------------------------------------------------------------------------
+ * ft_expert_grouped: per expert e with rows and slot_of[e] >= 0,
+ *   Y_e = (silu(X_e W_g[e]) * (X_e W_u[e])) W_d[e]
+ * with the weights read from the expert's slot and dequantised in the kernel
+ * ([Review] §2.5: grouped evaluation of the GPU expert set from cache slots).
+ *   x           dev [T][H], x_type
+ *   perm,offsets from ft_permute (row p of Y is assignment perm[p], token perm[p]/k)
+ *   slot_of     dev [E] int32; experts with slot_of < 0 are skipped and their
+ *               rows of y are left untouched
+ *   slot_pool   dev [pool_slots][S] expert records of format wtype (256-aligned);
+ *               a slot_of value >= pool_slots is a device error
+ *   y           dev [T*k][H] fp32 (written for evaluated experts), permuted order
+ *   workspace   dev, >= ft_expert_grouped_workspace(T, k, H, I) bytes, 256-aligned
+ * Accumulation is fp32; the intermediate silu(G)*U is kept in fp32.  Each
+ * output element is reduced in a fixed order, so results do not depend on
+ * which other experts are evaluated in the same call or on the slot used.
+ * ---------------------------------------------------------------------- */
+size_t ft_expert_grouped_workspace(int T, int k, int hidden, int inter);
+int ft_expert_grouped(const void* x, int x_type, int T, int k, int hidden, int inter, int E,
+                      int wtype, const int32_t* perm, const int32_t* offsets, const int32_t* slot_of,
+                      const void* slot_pool, uint64_t slot_bytes, int pool_slots, float* y,
+                      void* workspace, size_t workspace_bytes, ft_cuda_stream s);
+
+/* ------------------------------------------------------------------------
+ * ft_combine: out[t] = sum_j topk_w[t][j] * y[inv[t*k+j]] + ext_partial[t],
+ * skipping assignments whose expert has ext_flags != 0.  GPU and external
+ * partial sums are added, keeping the MoE output exact ([Review] §2.5, the
+ * exact merge).  Sum order: j = 0..k-1, then the partial.
+ *   y           dev [T*k][H] fp32 (from ft_expert_grouped)
+ *   inv, topk_idx, topk_w  from ft_permute / ft_route
+ *   ext_flags   dev [E] int32 or NULL (no assignment skipped)
+ *   ext_partial dev [T][H] fp32 or NULL
+ *   out         dev [T][H] fp32 (written)
+ * H a multiple of 4.
+ * ---------------------------------------------------------------------- */
+int ft_combine(const float* y, const int32_t* inv, const int32_t* topk_idx, const float* topk_w,
+               const int32_t* ext_flags, const float* ext_partial, int T, int k, int H, int E,
+               float* out, ft_cuda_stream s);
+
+/* ------------------------------------------------------------------------
+ * ft_stream: whole-layer double-buffered prefill streaming ([Review] §2.2;
+ * [Overview] "FreeToken技术原理" item 2).  Two whole-layer buffers (2E slots)
+ * are carved from the end of the cache's slot pool (a resize to N - 2E).
+ * While layer l is computed from one buffer, a transfer stream copies all of
+ * layer l+1 into the other with one cudaMemcpyAsync from the pinned pool,
+ * before l+1's routing is known.  Events order the copy after the compute that
+ * last read the buffer, and the compute after its copy.  In serialized mode
+ * the copy of l+1 starts only after layer l's compute (the ablation without the
+ * second buffer's overlap).
+ * ---------------------------------------------------------------------- */
+typedef struct ft_stream ft_stream;
+
+/* Carves the buffers (synchronises).  FT_EUNSUPPORTED when N < 2E: the caller
+ * then runs prefill through ft_cache_step (on-demand waves). */
+int ft_stream_create(ft_cache* c, int serialized, ft_stream** out);
+
+/* Makes `compute` wait until `layer` is resident (issuing its copy first if it
+ * was not prefetched), writes slot_of[e] = its buffer slot for every e (dev
+ * [E] int32), and, unless serialized, issues the copy of next_layer (-1: none)
+ * into the other buffer. */
+int ft_stream_layer(ft_stream* st, int layer, int next_layer, int32_t* slot_of, ft_cuda_stream compute);
+
+/* Marks the end of `layer`'s compute on `compute` (its buffer may be refilled
+ * after this point); in serialized mode issues the pending next copy here. */
+int ft_stream_layer_done(ft_stream* st, int layer, ft_cuda_stream compute);
+
+/* Bytes copied host->device by this handle so far. */
+int ft_stream_bytes(const ft_stream* st, uint64_t* bytes);
+
+/* Waits for the transfer stream, gives the 2E slots back and adopts the
+ * experts of the last two streamed layers into the LRU table (older layer
+ * first, one stamp per layer, experts in ascending id; a key already resident
+ * is refreshed and its buffer slot left empty): entries that survive prefill
+ * warm decode ([Review] §2.2).  Synchronises. */
+int ft_stream_destroy(ft_stream* st);
+
+/* ------------------------------------------------------------------------
+ * ft_qsplit (host only, pure): q* = m B_P / B_H, rounded half up, at least 1,
+ * at most m; m when B_H <= B_P; 0 when m <= 0 ([Review] §2.5, balance equation
+ * and the rounding rule after it).
+ * ---------------------------------------------------------------------- */
+int ft_qsplit(int m, double bw_fill, double bw_host);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FT_H */

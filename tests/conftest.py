@@ -20,3 +20,40 @@ def read_golden(name):
             if line and not line.startswith("#"):
                 rows.append(line.split())
     return rows
+
+
+import pytest  # noqa: E402
+
+
+@pytest.fixture(scope="session")
+def ftlib():
+    """The built libft binding (builds the library in-tree when it is missing or stale)."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "_ft_build", os.path.join(ROOT, "expert_cache_streaming_fp32_b300", "build.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    b.build()
+    import expert_cache_streaming_fp32_b300 as ft
+    return ft
+
+
+def rel_fro(a, b):
+    import numpy as np
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def assert_close_layer(got, ref, fro=5e-3, maxrel=2e-2):
+    """The floating-point bar: relative Frobenius error and max |err| against max |ref|."""
+    import numpy as np
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape
+    rf = rel_fro(got, ref)
+    mx = float(np.abs(got - ref).max()) if got.size else 0.0
+    scale = float(np.abs(ref).max()) if ref.size else 0.0
+    assert rf <= fro, f"relative Frobenius error {rf:.3e} > {fro}"
+    assert mx <= maxrel * scale + 1e-30, f"max |err| {mx:.3e} > {maxrel} * max|ref| ({scale:.3e})"
+    return rf, mx

@@ -1,0 +1,296 @@
+"""Layer-level parity: routing, cache decisions, streaming and layer outputs against the oracle and the LRU simulator."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from conftest import assert_close_layer
+from oracle import formats, moe
+from oracle.lru import LRUSim
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def ft(ftlib):
+    assert torch.cuda.is_available()
+    return ftlib
+
+
+def make_cache(ft, cfg, n_phys, N, max_slots):
+    pool = ft.ExpertPool(cfg, n_phys)
+    pool.fill(DEV)
+    sp = torch.empty(max_slots * pool.S, dtype=torch.uint8, device=DEV)
+    cache = ft.Cache(cfg.n_layers, cfg.n_experts, n_phys, N, max_slots, pool.S, pool.ptr, sp)
+    return pool, sp, cache
+
+
+class OracleLayer:
+    """fp64 experts of a config, decoded once per (physical layer, expert)."""
+
+    def __init__(self, cfg, n_phys):
+        self.cfg, self.n_phys, self.src = cfg, n_phys, {}
+
+    def experts(self, layer):
+        p = layer % self.n_phys
+        if p not in self.src:
+            self.src[p] = moe.ExpertSource(lambda e, p=p: synth.expert_weights(self.cfg, p, e, DEV), self.cfg.wtype)
+        return self.src[p]
+
+
+def run_waves(ft, layer_obj, cache, layer, x, ratio, sim=None, events=None):
+    """All waves of one cached layer step, checking slot_of against the simulator after each wave."""
+    idx = layer_obj.idx[: x.shape[0]].cpu().numpy()
+    if sim is not None:
+        ev, sim_slot_of = sim.step(layer, idx.reshape(-1), ratio)
+        if events is not None:
+            events.extend(ev)
+    for w in range(cache.n_waves()):
+        cache.step(layer, layer_obj.counts, ratio, w, layer_obj.slot_of, layer_obj.ext, layer_obj.step_counts)
+        if sim is not None:
+            got = layer_obj.slot_of.cpu().numpy()
+            exp = sim_slot_of[w] if w < len(sim_slot_of) else [-1] * cache.E
+            assert got.tolist() == list(exp), f"layer {layer} wave {w}"
+        layer_obj.experts(x, layer_obj.slot_of, cache.slot_pool, layer_obj_S(cache), cache.max_slots)
+
+
+def layer_obj_S(cache):
+    return cache.slot_pool.numel() // cache.max_slots
+
+
+# ---------------------------------------------------------------- the tiny fp32 layer
+
+def test_tiny_fp32_layer_one_step_and_sequential(ft):
+    cfg = synth.TINY_F32
+    pool, sp, cache = make_cache(ft, cfg, 1, 6, 6)
+    L = ft.MoELayer(cfg, 64)
+    wr, b = synth.router_weights(cfg, 0, DEV)
+    x = synth.activations(cfg, 64, device=DEV)
+    ol = OracleLayer(cfg, 1)
+    x64, wr64 = formats.to_f64(x), formats.to_f64(wr)
+    sim = LRUSim(6, 16)
+
+    # (i) one step of 64 tokens: about 16 unique experts over 6 slots -> 3 waves
+    L.route(x, wr, b)
+    z = L.logits[:64].cpu().numpy()
+    idx = L.idx[:64].cpu().numpy()
+    ri, rw = moe.route(z.astype(np.float64), 2)
+    assert np.array_equal(idx, ri)
+    assert cache.n_waves() == 3
+    run_waves(ft, L, cache, 0, x, 1.0, sim)
+    out = L.combine(64, L.ext, None).cpu().numpy()
+    z_ref = moe.router_logits(x64, wr64)
+    assert np.abs(z - z_ref).max() < 1e-5
+    ri2, rw2 = moe.route(z_ref, 2)
+    tie = moe.near_ties(z_ref, 2)
+    assert not tie.any()
+    assert np.array_equal(idx, ri2)
+    ref = moe.moe_layer(x64, ri2, rw2, ol.experts(0))
+    assert_close_layer(out, ref)
+
+    # (ii) 64 sequential single-token steps over the same cache
+    for t in range(64):
+        xt = x[t:t + 1]
+        L.route(xt, wr, b)
+        run_waves(ft, L, cache, 0, xt, 1.0, sim)
+        o = L.combine(1, L.ext, None).cpu().numpy()
+        assert_close_layer(o, ref[t:t + 1])
+    key, stamp, clock = cache.export()
+    sk, ss = sim.state()
+    assert key.tolist() == sk.tolist() and stamp.tolist() == ss.tolist() and clock == sim.clock
+    st = cache.stats()
+    assert (st.hits, st.fills, st.externals) == (sim.hits, sim.fills, sim.externals)
+    assert ft.ft_get_device_error() == 0
+
+
+# ---------------------------------------------------------------- a cache trace with resizes and splits
+
+def test_cache_trace_resize_split_matches_simulator(ft):
+    cfg = synth.MoEConfig("trace", 256, 64, 4, 256, 4, synth.W_BF16, "bf16", seed=5, zipf_s=1.1)
+    pool, sp, cache = make_cache(ft, cfg, 4, 40, 60)
+    big_pool_sp = torch.empty(256 * pool.S, dtype=torch.uint8, device=DEV)
+    big = ft.Cache(cfg.n_layers, cfg.n_experts, 4, 256, 256, pool.S, pool.ptr, big_pool_sp)
+    L = ft.MoELayer(cfg, 16)
+    Lb = ft.MoELayer(cfg, 16)
+    sim = LRUSim(40, 64)
+    ol = OracleLayer(cfg, 4)
+    routers = [synth.router_weights(cfg, l, DEV) for l in range(4)]
+    traces = {T: synth.AR1Trace(cfg, T, DEV, tag=T) for T in (1, 4, 16)}
+    for step in range(45):
+        T = (1, 4, 16)[step % 3]
+        x = traces[T].next()
+        ratio = 1.0 if step < 15 else 0.6
+        if step == 25:
+            cache.resize(25)
+            sim.resize(25)
+        if step == 35:
+            cache.resize(55)
+            sim.resize(55)
+        for l in range(4):
+            wr, b = routers[l]
+            L.route(x, wr, b)
+            run_waves(ft, L, cache, l, x, ratio, sim)
+            # the external experts' partial output, as the host branch would supply it (fp64 -> fp32)
+            idx = L.idx[:T].cpu().numpy()
+            z = L.logits[:T].cpu().numpy().astype(np.float64)
+            ri, rw = moe.route(z, cfg.top_k)
+            assert np.array_equal(idx, ri)
+            ext = L.ext.cpu().numpy()
+            C = [e for e in range(64) if ext[e]]
+            P = None
+            if C:
+                P = torch.from_numpy(moe.moe_layer(formats.to_f64(x), ri, rw, ol.experts(l), only=C)
+                                     .astype(np.float32)).to(DEV)
+            out = L.combine(T, L.ext, P).cpu().numpy()
+            # the same step with every expert resident: bitwise equal when nothing went external
+            Lb.route(x, wr, b)
+            for w in range(big.n_waves()):
+                big.step(l, Lb.counts, 1.0, w, Lb.slot_of, Lb.ext, Lb.step_counts)
+                Lb.experts(x, Lb.slot_of, big.slot_pool, pool.S, 256)
+            out_b = Lb.combine(T, Lb.ext, None).cpu().numpy()
+            if not C:
+                assert np.array_equal(out, out_b), f"step {step} layer {l}: output depends on the cache"
+            if step % 5 == 0 or C:
+                ref = moe.moe_layer(formats.to_f64(x), ri, rw, ol.experts(l))
+                assert_close_layer(out, ref)
+    key, stamp, clock = cache.export()
+    sk, ss = sim.state()
+    assert key.tolist() == sk.tolist() and stamp.tolist() == ss.tolist() and clock == sim.clock
+    st = cache.stats()
+    assert (st.hits, st.fills, st.externals) == (sim.hits, sim.fills, sim.externals)
+    assert st.externals > 0 and st.fills > 0
+    # every resident slot holds the bytes of its key's host record
+    for s, kk in enumerate(key.tolist()):
+        if kk >= 0:
+            l, e = divmod(kk, 64)
+            host = pool.row(l % 4, e).to(DEV)
+            assert torch.equal(sp[s * pool.S:(s + 1) * pool.S], host), f"slot {s}"
+    assert ft.ft_get_device_error() == 0
+
+
+# ---------------------------------------------------------------- prefill streaming
+
+def test_stream_double_buffered_and_serialized(ft):
+    cfg = synth.MoEConfig("stream", 512, 32, 4, 256, 6, synth.W_BF16, "bf16", seed=6)
+    n_phys = 3
+    pool, sp, cache = make_cache(ft, cfg, n_phys, 80, 80)
+    L = ft.MoELayer(cfg, 300)
+    sim = LRUSim(80, 32)
+    routers = [synth.router_weights(cfg, l, DEV) for l in range(6)]
+    # warm the cache with a few decode steps
+    tr = synth.AR1Trace(cfg, 2, DEV)
+    for step in range(3):
+        x = tr.next()
+        for l in range(6):
+            L.route(x, *routers[l])
+            run_waves(ft, L, cache, l, x, 1.0, sim)
+    # reference: every record resident in a fused pool, slot = phys_layer * E + e
+    fused = pool.host.to(DEV)
+    xp = synth.activations(cfg, 300, tag=9, device=DEV)
+    ref_out = []
+    for l in range(6):
+        so = torch.arange(32, dtype=torch.int32, device=DEV) + (l % n_phys) * 32
+        ref_out.append(L.forward_slots(xp, *routers[l], so, fused, pool.S, n_phys * 32).clone())
+    slot_of = torch.empty(32, dtype=torch.int32, device=DEV)
+    for serialized in (False, True):
+        st = ft.Stream(cache, serialized)
+        base, _ = sim.stream_begin()
+        for l in range(6):
+            st.layer(l, l + 1 if l < 5 else -1, slot_of)
+            out = L.forward_slots(xp, *routers[l], slot_of, sp, pool.S, 80)
+            st.layer_done(l)
+            assert torch.equal(out, ref_out[l]), f"layer {l} serialized={serialized}"
+        assert st.bytes() == 6 * 32 * pool.S
+        st.destroy()
+        sim.stream_end([(4, 0), (5, 1)])
+        key, stamp, clock = cache.export()
+        sk, ss = sim.state()
+        assert key.tolist() == sk.tolist() and stamp.tolist() == ss.tolist() and clock == sim.clock
+        # decode after prefill: the adopted layers hit
+        x = tr.next()
+        L.route(x, *routers[5])
+        run_waves(ft, L, cache, 5, x, 1.0, sim)
+        assert int(L.step_counts[2]) == 0          # no fills: layer 5 is resident
+    # one streamed layer against the oracle on sampled tokens
+    rows = np.arange(0, 300, 37)
+    ol = OracleLayer(cfg, n_phys)
+    z = moe.router_logits(formats.to_f64(xp[rows]), formats.to_f64(routers[2][0]), formats.to_f64(routers[2][1]))
+    ri, rw = moe.route(z, 4)
+    assert not moe.near_ties(z, 4).any()
+    ref = moe.moe_layer(formats.to_f64(xp[rows]), ri, rw, ol.experts(2))
+    assert_close_layer(ref_out[2].cpu().numpy()[rows], ref)
+    assert ft.ft_get_device_error() == 0
+
+
+def test_stream_needs_two_layers_of_slots(ft):
+    cfg = synth.MoEConfig("small", 256, 32, 2, 256, 2, synth.W_BF16, "bf16", seed=8)
+    pool, sp, cache = make_cache(ft, cfg, 2, 40, 64)
+    with pytest.raises(ft.FTError) as ei:
+        ft.Stream(cache)
+    assert ei.value.status == ft.FT_EUNSUPPORTED
+    cache.resize(64)
+    st = ft.Stream(cache)
+    with pytest.raises(ft.FTError) as ei:
+        cache.resize(30)                         # not a safe point: buffers are held
+    assert ei.value.status == ft.FT_ESTATE
+    st.destroy()
+
+
+# ---------------------------------------------------------------- full-size decode and prefill shapes
+
+def test_decode_full_size_sampled(ft):
+    """H=2048, E=256, k=8, I=512, 40 logical layers over 2 physical layers, 4096 slots, T=64."""
+    cfg = synth.DECODE_BF16
+    n_phys = 2
+    pool, sp, cache = make_cache(ft, cfg, n_phys, 4096, 4096)
+    L = ft.MoELayer(cfg, 64)
+    sim = LRUSim(4096, 256)
+    ol = OracleLayer(cfg, n_phys)
+    routers = [synth.router_weights(cfg, l, DEV) for l in range(cfg.n_layers)]
+    tr = synth.AR1Trace(cfg, 64, DEV)
+    sample = [0, 9, 33, 63]
+    for step in range(3):
+        x = tr.next()
+        for l in range(cfg.n_layers):
+            L.route(x, *routers[l])
+            z = L.logits[:64].cpu().numpy().astype(np.float64)
+            ri, rw = moe.route(z, 8)
+            assert np.array_equal(L.idx[:64].cpu().numpy(), ri)
+            run_waves(ft, L, cache, l, x, 1.0, sim)
+            out = L.combine(64, L.ext, None)
+            if (step, l) in ((0, 0), (0, 21), (2, 39), (2, 7)):
+                xs = formats.to_f64(x[sample])
+                zr = moe.router_logits(xs, formats.to_f64(routers[l][0]), formats.to_f64(routers[l][1]))
+                r2, w2 = moe.route(zr, 8)
+                ok = ~moe.near_ties(zr, 8)
+                assert np.array_equal(r2[ok], ri[sample][ok])
+                ref = moe.moe_layer(xs, ri[sample], rw[sample], ol.experts(l))
+                assert_close_layer(out.cpu().numpy()[sample], ref)
+    st = cache.stats()
+    assert (st.hits, st.fills) == (sim.hits, sim.fills)
+    assert ft.ft_get_device_error() == 0
+
+
+def test_prefill_chunk_full_size_sampled(ft):
+    """8192 tokens through one H=2048, E=256, k=8, I=512 layer with every expert resident."""
+    cfg = synth.PREFILL_BF16
+    L_ = ft.ft_expert_layout_get(cfg.wtype, cfg.hidden, cfg.inter)
+    S = int(L_.bytes)
+    fused = torch.empty(256 * S, dtype=torch.uint8, device=DEV)
+    for e in range(256):
+        ft.pack_expert(synth.expert_weights(cfg, 0, e, DEV), cfg.wtype, L_, fused[e * S:(e + 1) * S])
+    L = ft.MoELayer(cfg, 8192)
+    wr, b = synth.router_weights(cfg, 0, DEV)
+    x = synth.activations(cfg, 8192, tag=1, device=DEV)
+    so = torch.arange(256, dtype=torch.int32, device=DEV)
+    out = L.forward_slots(x, wr, b, so, fused, S, 256).cpu().numpy()
+    counts = L.counts.cpu().numpy()
+    assert counts.sum() == 8192 * 8 and (counts > 0).sum() >= 250    # near-uniform routing touches ~all experts
+    z = L.logits.cpu().numpy().astype(np.float64)
+    ri, rw = moe.route(z, 8)
+    assert np.array_equal(L.idx.cpu().numpy(), ri)
+    rows = np.random.default_rng(0).choice(8192, 24, replace=False)
+    ol = OracleLayer(cfg, 1)
+    ref = moe.moe_layer(formats.to_f64(x[rows]), ri[rows], rw[rows], ol.experts(0))
+    assert_close_layer(out[rows], ref)
