@@ -486,9 +486,10 @@ down_kernel(ExpertArgs a) {
 // ------------------------------------------------------------------ layout
 static int expert_layout(int wt, int H, int I, ft_expert_layout* L) {
   if (wt < FT_W_F32 || wt > FT_W_MXFP4) return FT_EINVAL;
-  // K a multiple of 256 keeps every value row 16-byte aligned and every scale
-  // row aligned for its element size, in all formats
-  if (H <= 0 || I <= 0 || H % 256 || I % 256) return FT_EINVAL;
+  // K a multiple of 128 keeps every value row 16-byte aligned, covers whole
+  // scale blocks (128 for fp8, 16/32 for fp4) and keeps scale rows aligned for
+  // their element size, in all formats
+  if (H <= 0 || I <= 0 || H % 128 || I % 128) return FT_EINVAL;
   auto al = [](uint64_t v) { return (v + 255) / 256 * 256; };
   const uint64_t HI = (uint64_t)H * I;
   const uint64_t vb = HI * fmt_bits(wt) / 8;

@@ -96,7 +96,7 @@ FT_API int ft_host_free(void* p) {
 // ------------------------------------------------------------------ router logits
 FT_API int ft_router_logits(const void* x, int x_type, const void* w_router, const float* bias, int T, int H, int E,
                             float* logits, ft_cuda_stream s) {
-  FT_REQUIRE(T >= 0 && H > 0 && H % 256 == 0 && E >= 1 && E <= 1024);
+  FT_REQUIRE(T >= 0 && H > 0 && H % 8 == 0 && E >= 1 && E <= 1024);
   FT_REQUIRE(x_type == FT_X_F32 || x_type == FT_X_BF16);
   if (T == 0) return FT_OK;
   FT_REQUIRE(x && w_router && logits);

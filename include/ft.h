@@ -114,7 +114,7 @@ typedef struct {
   uint64_t off_gscale;      /* NVFP4: 3 fp32 matrix scales (0 otherwise) */
 } ft_expert_layout;
 
-/* Fills *out for a format and shape.  H and I must be multiples of 256. */
+/* Fills *out for a format and shape.  H and I must be multiples of 128. */
 int ft_expert_layout_get(int wtype, int hidden, int inter, ft_expert_layout* out);
 
 /* ------------------------------------------------------------------------
@@ -135,7 +135,7 @@ int ft_host_free(void* p);
  *   w_router dev [E][H] (K-major), same type as x
  *   bias     dev [E] fp32, or NULL
  *   logits   dev [T][E] fp32 (written)
- * T >= 0, H a multiple of 256, 1 <= E <= 1024.
+ * T >= 0, H a multiple of 8, 1 <= E <= 1024.
  * ---------------------------------------------------------------------- */
 int ft_router_logits(const void* x, int x_type, const void* w_router, const float* bias,
                      int T, int H, int E, float* logits, ft_cuda_stream s);

@@ -58,7 +58,7 @@ def test_route_empty_batch(ft):
 def test_permute_bit_exact(ft, T, k, E, seed, distinct):
     rng = np.random.default_rng(seed)
     if distinct:
-        idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32).reshape(T, k)
+        idx = np.array([rng.permutation(E)[:k] for _ in range(T)], dtype=np.int32).reshape(T, k)
     else:
         idx = rng.integers(0, E, size=(T, k)).astype(np.int32)
     d = torch.from_numpy(idx).to(DEV)
