@@ -35,7 +35,9 @@ EXPORTED = [
     "ft_cache_destroy", "ft_cache_n_waves", "ft_cache_step", "ft_cache_resize", "ft_cache_stats",
     "ft_cache_export", "ft_expert_grouped_workspace", "ft_expert_grouped", "ft_combine", "ft_stream_create",
     "ft_stream_layer", "ft_stream_layer_done", "ft_stream_bytes", "ft_stream_destroy", "ft_qsplit",
+    "ft_expert_grouped_noalloc",
 ]
+FT_NOALLOC_MAX_ELEMS = 1 << 20
 
 
 class FTError(RuntimeError):
@@ -93,6 +95,7 @@ _sigs = {
     "ft_stream_bytes": (_I, [_P, ctypes.POINTER(ctypes.c_uint64)]),
     "ft_stream_destroy": (_I, [_P]),
     "ft_qsplit": (_I, [_I, ctypes.c_double, ctypes.c_double]),
+    "ft_expert_grouped_noalloc": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, ctypes.c_uint64, _I, _P, _P]),
 }
 for _name, (_res, _args) in _sigs.items():
     _f = getattr(_lib, _name)
@@ -184,6 +187,19 @@ def ft_expert_grouped(x, k, inter, E, wtype, perm, offsets, slot_of, slot_pool, 
         _ptr(x), _xtype(x), T, k, H, inter, E, wtype, _ptr(perm), _ptr(offsets), _ptr(slot_of), _ptr(slot_pool),
         slot_bytes, pool_slots, _ptr(y), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+
+
+def ft_expert_grouped_noalloc(x, k, inter, E, wtype, perm, offsets, slot_of, slot_pool, slot_bytes, pool_slots, y,
+                              stream=None):
+    """ft_expert_grouped without a workspace, for callers that cannot allocate device memory.
+
+    The intermediate uses a fixed 4 MiB array inside libft (T*k*inter must not
+    exceed FT_NOALLOC_MAX_ELEMS); calls that overlap on the GPU race on it.
+    """
+    T, H = x.shape
+    _check("ft_expert_grouped_noalloc", _lib.ft_expert_grouped_noalloc(
+        _ptr(x), _xtype(x), T, k, H, inter, E, wtype, _ptr(perm), _ptr(offsets), _ptr(slot_of), _ptr(slot_pool),
+        slot_bytes, pool_slots, _ptr(y), _stream(stream)))
 
 
 def ft_combine(y, inv, topk_idx, topk_w, ext_flags, ext_partial, E, out, stream=None):

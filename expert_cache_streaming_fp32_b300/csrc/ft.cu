@@ -440,3 +440,72 @@ FT_API int ft_stream_destroy(ft_stream* st) {
   delete st;
   return s;
 }
+
+// ------------------------------------------------------------------ expert grouped without allocation
+// A variant of ft_expert_grouped for callers that cannot allocate device
+// memory.  The fp32 intermediate silu(G)*U lives in the fixed array below
+// instead of a caller-supplied workspace.  Host code must not hand the array's
+// name to a kernel (in host code it is a host-side stand-in); its device
+// address is looked up once per device with cudaGetSymbolAddress.
+
+#include <mutex>
+
+static constexpr size_t kNoAllocMaxElems = (size_t)1 << 20;  // fp32 elements: 4 MiB per device
+static __device__ __align__(256) float ft_noalloc_scratch[kNoAllocMaxElems];
+
+static constexpr int kNoAllocMaxDevices = 64;
+static void* g_noalloc_addr[kNoAllocMaxDevices];  // device address of the array, per device
+static std::mutex g_noalloc_mu;
+
+// Device address of the scratch array on the current device (set up on first use).
+static int noalloc_scratch_address(void** out) {
+  int d = 0;
+  FT_CHECK_CUDA(cudaGetDevice(&d));
+  if (d < 0 || d >= kNoAllocMaxDevices) return FT_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[d]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress((void**)&p, ft_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return cuda_status(e == cudaSuccess ? cudaErrorInvalidSymbol : e);
+    }
+    g_noalloc_addr[d] = p;
+  }
+  *out = g_noalloc_addr[d];
+  return FT_OK;
+}
+
+FT_API int ft_expert_grouped_noalloc(const void* x, int x_type, int T, int k, int hidden, int inter, int E, int wtype,
+                                     const int32_t* perm, const int32_t* offsets, const int32_t* slot_of,
+                                     const void* slot_pool, uint64_t slot_bytes, int pool_slots, float* y,
+                                     ft_cuda_stream s) {
+  FT_REQUIRE(T >= 0 && k >= 1 && E >= 1 && E <= 1024 && pool_slots >= 1);
+  FT_REQUIRE(x_type == FT_X_F32 || x_type == FT_X_BF16);
+  ft_expert_layout L;
+  if (expert_layout(wtype, hidden, inter, &L) != FT_OK) return FT_EINVAL;
+  FT_REQUIRE(slot_bytes >= L.bytes && slot_bytes % 256 == 0);
+  // the intermediate needs T*k*inter fp32 elements; larger calls are refused
+  if ((size_t)T * (size_t)k * (size_t)inter > kNoAllocMaxElems) return FT_EINVAL;
+  if (T == 0) return FT_OK;
+  FT_REQUIRE(x && perm && offsets && slot_of && slot_pool && y);
+  FT_REQUIRE(((uintptr_t)slot_pool & 255) == 0);
+  void* scratch = nullptr;
+  if (int st = noalloc_scratch_address(&scratch)) return st;
+  ExpertArgs a;
+  a.x = x; a.x_type = x_type; a.T = T; a.k = k; a.H = hidden; a.I = inter; a.E = E; a.pool_slots = pool_slots;
+  a.perm = perm; a.offsets = offsets; a.slot_of = slot_of; a.pool = (const uint8_t*)slot_pool; a.S = slot_bytes;
+  for (int m = 0; m < 3; ++m) { a.off_val[m] = L.off_val[m]; a.off_scale[m] = L.off_scale[m]; }
+  a.off_gscale = L.off_gscale;
+  a.A = (float*)scratch;  // every element the down pass reads is written by the gate/up pass of this call
+  a.y = y;
+  cudaStream_t st = (cudaStream_t)s;
+  switch (wtype) {
+    case FT_W_F32: return launch_expert<FT_W_F32>(a, st);
+    case FT_W_BF16: return launch_expert<FT_W_BF16>(a, st);
+    case FT_W_FP8E4M3: return launch_expert<FT_W_FP8E4M3>(a, st);
+    case FT_W_NVFP4: return launch_expert<FT_W_NVFP4>(a, st);
+    case FT_W_MXFP4: return launch_expert<FT_W_MXFP4>(a, st);
+  }
+  return FT_EINVAL;
+}

@@ -272,6 +272,32 @@ int ft_expert_grouped(const void* x, int x_type, int T, int k, int hidden, int i
                       void* workspace, size_t workspace_bytes, ft_cuda_stream s);
 
 /* ------------------------------------------------------------------------
+ * ft_expert_grouped_noalloc: the same computation and arguments as
+ * ft_expert_grouped, without the workspace.  The pages have no counterpart:
+ * this entry point exists for callers that cannot call cudaMalloc -- a host
+ * application that owns every device allocation through its own allocator or
+ * fixed budget, or a latency-critical path where cudaMalloc's implicit device
+ * synchronisation is not acceptable.  The library allocates nothing here.
+ *
+ * The fp32 intermediate lives in one fixed device array inside the library,
+ * FT_NOALLOC_MAX_ELEMS floats (4 MiB), which every GPU that loads the library
+ * holds until the process exits.  Calls with T*k*inter > FT_NOALLOC_MAX_ELEMS
+ * return FT_EINVAL and launch nothing.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls share the one array and it keeps the
+ * last call's contents (nothing needs clearing: each call writes every element
+ * it reads before reading it).  Calls that overlap on the GPU -- on different
+ * streams, or from different host threads -- race on the array: order them.
+ * ---------------------------------------------------------------------- */
+#define FT_NOALLOC_MAX_ELEMS (1u << 20)
+int ft_expert_grouped_noalloc(const void* x, int x_type, int T, int k, int hidden, int inter, int E,
+                              int wtype, const int32_t* perm, const int32_t* offsets,
+                              const int32_t* slot_of, const void* slot_pool, uint64_t slot_bytes,
+                              int pool_slots, float* y, ft_cuda_stream s);
+
+/* ------------------------------------------------------------------------
  * ft_combine: out[t] = sum_j topk_w[t][j] * y[inv[t*k+j]] + ext_partial[t],
  * skipping assignments whose expert has ext_flags != 0.  GPU and external
  * partial sums are added, keeping the MoE output exact ([Review] §2.5, the
