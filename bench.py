@@ -48,6 +48,9 @@ def parse():
     p.add_argument("--no-prefill", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--kernel-case", default="", choices=["", "experts_decode", "experts_prefill"],
+                   help="time one expert-kernel case on a small resident pool (profiling aid; prints its own line)")
+    p.add_argument("--reps", type=int, default=5)
     return p.parse_args()
 
 
@@ -390,6 +393,52 @@ def reference_main(args, world, rank):
     }))
 
 
+# ---------------------------------------------------------------- single expert-kernel cases (profiling)
+
+def kernel_case(args):
+    """One layer's experts resident in a 256-record slot pool (1.6 GB); ft_expert_grouped timed alone.
+
+    experts_decode: T = --batches[0] tokens routed with the Zipf prior of the decode trace.
+    experts_prefill: T = 8192 tokens, near-uniform routing (tensor-core path).
+    Small enough on the device (< 3 GB) for a multi-pass ncu capture of one launch.
+    """
+    import expert_cache_streaming_fp32_b300 as ft
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    cfg = synth.DECODE_BF16 if args.kernel_case == "experts_decode" else synth.PREFILL_BF16
+    T = int(args.batches.split(",")[0]) if args.kernel_case == "experts_decode" else 8192
+    E, k, H, I = cfg.n_experts, cfg.top_k, cfg.hidden, cfg.inter
+    lay = ft.ft_expert_layout_get(cfg.wtype, H, I)
+    S = int(lay.bytes)
+    pool = torch.empty(E * S, dtype=torch.uint8, device=dev)
+    for e in range(E):
+        ft.pack_expert(synth.expert_weights(cfg, 0, e, dev), cfg.wtype, lay, pool[e * S:(e + 1) * S])
+    L = ft.MoELayer(cfg, T, dev)
+    wr, b = synth.router_weights(cfg, 0, dev)
+    x = synth.AR1Trace(cfg, T, dev, tag=7).next() if args.kernel_case == "experts_decode" else \
+        synth.activations(cfg, T, tag=1, device=dev)
+    L.route(x, wr, b)
+    so = torch.arange(E, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        L.experts(x, so, pool, S, E)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.reps):
+        L.experts(x, so, pool, S, E)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.reps
+    U = int((L.counts > 0).sum())
+    wbytes = U * int(lay.payload_bytes)
+    flops = 2.0 * T * k * 3 * H * I
+    peaks = load_peaks()
+    print(json.dumps({"kernel_case": args.kernel_case, "T": T, "unique_experts": U, "ms": ms,
+                      "weight_gbs": wbytes / (ms * 1e-3) / 1e9, "hbm_frac": wbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                      "tflops": flops / (ms * 1e-3) / 1e12, "bf16_frac": flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                      "device_error": ft.ft_get_device_error()}))
+
+
 # ---------------------------------------------------------------- main
 
 def main():
@@ -397,6 +446,9 @@ def main():
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         reference_main(args, world, rank)
+        return
+    if args.kernel_case:
+        kernel_case(args)
         return
     import expert_cache_streaming_fp32_b300 as ft
     dev = f"cuda:{local}"

@@ -1,0 +1,380 @@
+// Grouped SwiGLU expert FFN on the tcgen05 tensor cores (large batches).
+//
+// The gate/up and down products of every evaluated expert are dense
+// contractions once an expert has tens of rows or more (prefill), so this path
+// runs them as grouped GEMMs: 128-row tiles of one expert's permuted rows
+// against that expert's weights, read straight from its cache slot.
+//
+//   gather:  Xp[p][:] = bf16(x[perm[p] / k][:])                 (rows in permuted order)
+//   gate/up: Aint[p][n] = bf16(silu(Xp[p] . Wg[n]) * (Xp[p] . Wu[n]))
+//   down:    Y[p][h] = Aint[p] . Wd[h]                           (fp32)
+//
+// One persistent kernel per product, one CTA per SM, warp-specialised:
+//   warp 0      TMA producer: A tile (128 x 64 bf16) and B tile (256 x 64 bf16)
+//               per stage, 128-byte swizzle, 4 stages
+//   warp 1      tensor-memory owner and MMA issuer (one thread): 4 x
+//               tcgen05.mma kind::f16 (M=128, N=256, K=16) per stage into one
+//               of two 256-column fp32 accumulators
+//   warps 2..5  epilogue: tcgen05.ld of the finished accumulator while the
+//               next tile accumulates into the other one
+// For gate/up the 256 B rows are 128 gate rows then the same 128 up rows, so
+// one accumulator holds G and U for the same 128 outputs and the SwiGLU is
+// applied in registers.  Weights come through 3-D tensor maps over the whole
+// slot pool (K, row, slot), so the slot is just a TMA coordinate.
+//
+// Rows of a tile past the end of its expert belong to the next expert (or lie
+// past the last row and read as zero): their results are computed and dropped.
+// Each output element is one fixed-order K reduction in the tensor core, so the
+// result does not depend on the other experts of the call or on the slot.
+#pragma once
+#include "sm100.cuh"
+
+namespace ft {
+namespace tc {
+
+constexpr int BM = 128;                    // rows per tile (UMMA M)
+constexpr int BN = 256;                    // UMMA N
+constexpr int BK = 64;                     // K per stage: 128 bytes of bf16
+constexpr int UK = 16;                     // K per tcgen05.mma (kind::f16)
+constexpr int STAGES = 4;
+constexpr int THREADS = 192;
+constexpr int WARPS = THREADS / 32;
+constexpr int A_BYTES = BM * BK * 2;       // 16 KiB
+constexpr int B_BYTES = BN * BK * 2;       // 32 KiB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int ACC_COLS = BN;               // fp32 columns per accumulator
+constexpr int TMEM_COLS = 2 * ACC_COLS;    // double-buffered accumulators
+constexpr int MAX_E = 1024;
+
+enum Mode { GATEUP = 0, DOWN = 1 };
+
+// Bytes of dynamic shared memory: 1 KiB alignment slack, the stages, then the
+// barriers and the expert list.
+__host__ __device__ constexpr size_t smem_bytes(int E) {
+  return 1024 + (size_t)STAGES * STAGE_BYTES + 256 + (size_t)(2 * E + 2) * 4;
+}
+
+struct Args {
+  int T, k, H, I, E, pool_slots;
+  const int32_t* offsets;
+  const int32_t* slot_of;
+  const float* gscale_base;  // NVFP4: record base for the fp32 matrix scales (unused for bf16)
+  uint64_t S;
+  __nv_bfloat16* Aint;       // [T*k][I]
+  float* y;                  // [T*k][H]
+};
+
+// ------------------------------------------------------------------ expert list
+// act_e[i] = i-th evaluated expert (rows > 0, valid slot) in ascending id;
+// act_pref[i] = its first tile index; act_pref[n_act] = total tiles.
+__device__ __forceinline__ int block_scan6(int v, int* buf, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(FT_FULL_MASK, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) buf[warp] = incl;
+  __syncthreads();
+  int before = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < WARPS; ++w) {
+    const int b = buf[w];
+    before += w < warp ? b : 0;
+    tot += b;
+  }
+  __syncthreads();
+  total = tot;
+  return before + incl - v;
+}
+
+__device__ int build_tiles(const Args& a, int n_tiles_n, int* act_e, int* act_pref, int* buf, int& n_act) {
+  const int per = ceil_div(a.E, THREADS);
+  const int e0 = threadIdx.x * per;
+  int my_act = 0, my_tiles = 0;
+  for (int i = 0; i < per; ++i) {
+    const int e = e0 + i;
+    if (e < a.E) {
+      const int cnt = a.offsets[e + 1] - a.offsets[e];
+      const int s = a.slot_of[e];
+      if (cnt > 0 && s >= 0) {
+        if (s >= a.pool_slots) {
+          record_error(FT_DERR_SLOT_INDEX);
+          continue;
+        }
+        my_act += 1;
+        my_tiles += n_tiles_n * ceil_div(cnt, BM);
+      }
+    }
+  }
+  int total;
+  int pos = block_scan6(my_act, buf, n_act);
+  int tpos = block_scan6(my_tiles, buf, total);
+  for (int i = 0; i < per; ++i) {
+    const int e = e0 + i;
+    if (e < a.E) {
+      const int cnt = a.offsets[e + 1] - a.offsets[e];
+      const int s = a.slot_of[e];
+      if (cnt > 0 && s >= 0 && s < a.pool_slots) {
+        act_e[pos] = e;
+        act_pref[pos] = tpos;
+        pos += 1;
+        tpos += n_tiles_n * ceil_div(cnt, BM);
+      }
+    }
+  }
+  if (threadIdx.x == 0) act_pref[n_act] = total;
+  __syncthreads();
+  return total;
+}
+
+struct Tile {
+  int e, nt, mt, row0, cnt, slot;
+};
+
+// Tiles of one expert are ordered n-tile major, m-tile minor, so CTAs that run
+// at the same time share the same weight tile through L2.
+__device__ __forceinline__ Tile decode_tile(const Args& a, const int* act_e, const int* act_pref, int n_act,
+                                            int item) {
+  int lo = 0, hi = n_act - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (act_pref[mid] <= item) lo = mid; else hi = mid - 1;
+  }
+  Tile t;
+  t.e = act_e[lo];
+  const int local = item - act_pref[lo];
+  const int off = a.offsets[t.e];
+  t.cnt = a.offsets[t.e + 1] - off;
+  const int n_mt = ceil_div(t.cnt, BM);
+  t.nt = local / n_mt;
+  t.mt = local - t.nt * n_mt;
+  t.row0 = off + t.mt * BM;
+  t.slot = a.slot_of[t.e];
+  return t;
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
+                    const __grid_constant__ CUtensorMap map_b1, Args a) {
+  using namespace sm100;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // 1 KiB-aligned stage buffers (the 128-byte swizzle pattern repeats every 1 KiB)
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t pad = (1024 - (raw_addr & 1023)) & 1023;
+  unsigned char* smem = smem_raw + pad;
+  const uint32_t sbase = raw_addr + pad;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)STAGES * STAGE_BYTES);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* scan_buf = const_cast<int*>(reinterpret_cast<volatile int*>(tmem_holder + 2));  // [WARPS]
+  int* act_e = reinterpret_cast<int*>(smem + (size_t)STAGES * STAGE_BYTES + 256);
+  int* act_pref = act_e + a.E;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto full_bar = [&](int s) { return smem_u32(bars + s); };
+  auto empty_bar = [&](int s) { return smem_u32(bars + STAGES + s); };
+  auto tfull_bar = [&](int b) { return smem_u32(bars + 2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return smem_u32(bars + 2 * STAGES + 2 + b); };
+  const uint32_t drain_bar = smem_u32(bars + 2 * STAGES + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 4 * 32);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&map_a);
+    tma_prefetch_desc(&map_b0);
+    if (MODE == GATEUP) tma_prefetch_desc(&map_b1);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
+    tmem_relinquish();
+  }
+  const int n_tiles_n = MODE == GATEUP ? a.I / (BN / 2) : ceil_div(a.H, BN);
+  const int K = MODE == GATEUP ? a.H : a.I;
+  const int nk = K / BK;
+  int n_act = 0;
+  const int total = build_tiles(a, n_tiles_n, act_e, act_pref, scan_buf, n_act);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (elect_one()) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, last_par = 0;  // per stage: a load was issued / parity of its phase
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+        const Tile t = decode_tile(a, act_e, act_pref, n_act, item);
+        for (int ks = 0; ks < nk; ++ks) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag)) { ok = false; break; }
+          const uint32_t sa = sbase + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
+          tma_load_2d(sa, &map_a, full_bar(stage), ks * BK, t.row0);
+          if (MODE == GATEUP) {
+            tma_load_3d(sb, &map_b0, full_bar(stage), ks * BK, t.nt * (BN / 2), t.slot);
+            tma_load_3d(sb + B_BYTES / 2, &map_b1, full_bar(stage), ks * BK, t.nt * (BN / 2), t.slot);
+          } else {
+            tma_load_3d(sb, &map_b0, full_bar(stage), ks * BK, t.nt * BN, t.slot);
+          }
+          issued |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok) {
+        // wind down: let every load already issued land before the CTA exits
+        for (int s = 0; s < STAGES; ++s)
+          if (issued & (1u << s)) mbar_drain(full_bar(s), (last_par >> s) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (elect_one()) {
+      constexpr uint32_t idesc = idesc_bf16(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true, any = false;
+      for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * ACC_COLS;
+        for (int ks = 0; ks < nk; ++ks) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = sbase + stage * STAGE_BYTES;
+          const uint64_t da = sdesc_k_sw128(sa);
+          const uint64_t db = sdesc_k_sw128(sa + A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / UK; ++kk)
+            mma_bf16(d, da + (uint64_t)(kk * UK * 2 / 16), db + (uint64_t)(kk * UK * 2 / 16), idesc,
+                     (ks | kk) != 0 ? 1u : 0u);
+          any = true;
+          mma_commit(empty_bar(stage));
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        mma_commit(tfull_bar(acc));
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      }
+      if (!ok && any) {
+        // wind down: wait until every MMA issued so far has finished with TMEM and smem
+        mma_commit(drain_bar);
+        mbar_drain(drain_bar, 0);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (warps 2..5)
+    const int q = warp & 3;          // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;     // tile row = TMEM lane
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int item = blockIdx.x; item < total; item += gridDim.x) {
+      const Tile t = decode_tile(a, act_e, act_pref, n_act, item);
+      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) break;
+      tc_fence_after();
+      const bool valid = t.mt * BM + r < t.cnt;
+      const size_t p = (size_t)t.row0 + r;
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * ACC_COLS;
+      if (MODE == GATEUP) {
+#pragma unroll 1
+        for (int c = 0; c < (BN / 2) / 32; ++c) {
+          uint32_t g[32], u[32];
+          tmem_ld32(taddr + c * 32, g);
+          tmem_ld32(taddr + BN / 2 + c * 32, u);
+          tmem_ld_wait();
+          if (valid) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float a0 = silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
+              const float a1 = silu(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
+              packed[j] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(a.Aint + p * a.I + t.nt * (BN / 2) + c * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(taddr + c * 32, v);
+          tmem_ld_wait();
+          const int col = t.nt * BN + c * 32;
+          if (valid && col < a.H) {
+            float4* dst = reinterpret_cast<float4*>(a.y + p * a.H + col);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                   __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty_bar(acc));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ gather
+// Xp[p][:] = bf16(x[perm[p] / k][:]); 16 bytes of output per thread step.
+template <typename XT>
+__global__ void __launch_bounds__(256)
+gather_rows_kernel(const XT* __restrict__ x, const int32_t* __restrict__ perm, int T, int k, int H, int n_rows,
+                   __nv_bfloat16* __restrict__ xp) {
+  const int vpr = H / 8;  // 16-byte output vectors per row
+  const long long n = (long long)n_rows * vpr;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const int p = (int)(i / vpr), v = (int)(i - (long long)p * vpr);
+    const int t = perm[p] / k;
+    uint4 o = make_uint4(0, 0, 0, 0);
+    if ((unsigned)t < (unsigned)T) {
+      if constexpr (sizeof(XT) == 2) {
+        o = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H) + v);
+      } else {
+        const float4* s = reinterpret_cast<const float4*>(x + (size_t)t * H) + 2 * v;
+        const float4 f0 = __ldg(s), f1 = __ldg(s + 1);
+        __nv_bfloat162 b0 = __floats2bfloat162_rn(f0.x, f0.y), b1 = __floats2bfloat162_rn(f0.z, f0.w);
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(f1.x, f1.y), b3 = __floats2bfloat162_rn(f1.z, f1.w);
+        o = make_uint4(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1),
+                       *reinterpret_cast<uint32_t*>(&b2), *reinterpret_cast<uint32_t*>(&b3));
+      }
+    } else {
+      record_error(FT_DERR_ROW_INDEX);
+    }
+    reinterpret_cast<uint4*>(xp + (size_t)p * H)[v] = o;
+  }
+}
+
+}  // namespace tc
+}  // namespace ft

@@ -3,9 +3,13 @@
 #include "common.cuh"
 #include "route.cuh"
 #include "expert.cuh"
+#include "expert_tc.cuh"
 #include "cache.cuh"
 #include "stream.cuh"
 
+#include <cudaTypedefs.h>
+
+#include <mutex>
 #include <new>
 
 using namespace ft;
@@ -101,7 +105,10 @@ FT_API int ft_router_logits(const void* x, int x_type, const void* w_router, con
   if (T == 0) return FT_OK;
   FT_REQUIRE(x && w_router && logits);
   const size_t smem = (size_t)RL_RT * H * sizeof(float);
-  dim3 grid(ceil_div(T, RL_RT));
+  if (smem > 227 * 1024 || ceil_div(T, RL_RT) > 65535) return FT_EUNSUPPORTED;
+  const int chunks = ceil_div(T, RL_RT);
+  const int groups = std::max(1, std::min(ceil_div(E, RL_WARPS), ceil_div(2 * sms(), chunks)));
+  dim3 grid(groups, chunks);
   if (x_type == FT_X_BF16) {
     auto k = router_logits_kernel<__nv_bfloat16>;
     if (int st = set_smem(k, smem)) return st;
@@ -165,10 +172,21 @@ FT_API int ft_combine(const float* y, const int32_t* inv, const int32_t* topk_id
 }
 
 // ------------------------------------------------------------------ expert grouped
+static size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+// Workspace of the CUDA-core path: the fp32 intermediate [T*k][I].
+static size_t ws_cuda_core(long long Tk, int inter) { return align256((size_t)Tk * inter * sizeof(float)); }
+// Workspace of the tensor-core path: gathered bf16 rows [T*k][H], then the bf16 intermediate [T*k][I].
+static size_t ws_tensor_core(long long Tk, int hidden, int inter) {
+  return align256((size_t)Tk * hidden * 2) + align256((size_t)Tk * inter * 2);
+}
+
 FT_API size_t ft_expert_grouped_workspace(int T, int k, int hidden, int inter) {
-  (void)hidden;
-  if (T <= 0 || k <= 0 || inter <= 0) return 256;
-  return ((size_t)T * k * inter * sizeof(float) + 255) / 256 * 256;
+  if (T <= 0 || k <= 0 || inter <= 0 || hidden <= 0) return 256;
+  const long long Tk = (long long)T * k;
+  size_t ws = ws_cuda_core(Tk, inter);
+  if (Tk >= FT_TC_MIN_ASSIGNMENTS) ws = std::max(ws, ws_tensor_core(Tk, hidden, inter));
+  return std::max(ws, (size_t)256);
 }
 
 namespace {
@@ -197,6 +215,92 @@ int launch_expert(const ExpertArgs& a, cudaStream_t st) {
   return FT_OK;
 }
 
+// ------------------------------------------------------------------ tensor-core path
+using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// bf16 tensor map, 128-byte swizzle, box {64, rows(, 1)}; dims[0] innermost.
+int make_map_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                  uint32_t box_rows) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return FT_EUNSUPPORTED;
+  cuuint64_t gd[3], gs[2];
+  cuuint32_t bd[3] = {(cuuint32_t)tc::BK, box_rows, 1}, es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) gd[i] = dims[i];
+  for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), gd, gs, bd, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FT_OK : FT_EINVAL;
+}
+
+// The tensor-core path takes bf16 weights at batches of FT_TC_MIN_ASSIGNMENTS
+// assignments or more, for shapes whose tiles divide evenly.
+bool tc_path_applies(int wtype, int T, int k, int H, int I, int E) {
+  return wtype == FT_W_BF16 && (long long)T * k >= FT_TC_MIN_ASSIGNMENTS && H % tc::BN == 0 &&
+         I % (tc::BN / 2) == 0 && E <= tc::MAX_E && (long long)T * k < (1ll << 31) / 8;
+}
+
+int launch_expert_tc(const ExpertArgs& ea, const ft_expert_layout& L, void* workspace, cudaStream_t st) {
+  const long long Tk = (long long)ea.T * ea.k;
+  const int H = ea.H, I = ea.I;
+  __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(workspace);
+  __nv_bfloat16* aint = reinterpret_cast<__nv_bfloat16*>((uint8_t*)workspace + align256((size_t)Tk * H * 2));
+  // gather the permuted rows (bf16)
+  {
+    const long long vecs = Tk * (H / 8);
+    const int grid = (int)std::min<long long>(ceil_div((int)std::min<long long>(vecs, 1ll << 30), 256), 8 * sms());
+    if (ea.x_type == FT_X_BF16)
+      tc::gather_rows_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)ea.x, ea.perm, ea.T, ea.k, H,
+                                                                  (int)Tk, xp);
+    else
+      tc::gather_rows_kernel<float><<<grid, 256, 0, st>>>((const float*)ea.x, ea.perm, ea.T, ea.k, H, (int)Tk, xp);
+    FT_CHECK_LAUNCH();
+  }
+  CUtensorMap mx, mg, mu, ma, md;
+  const uint8_t* pool = ea.pool;
+  {
+    const uint64_t dx[2] = {(uint64_t)H, (uint64_t)Tk}, sx[1] = {(uint64_t)H * 2};
+    const uint64_t dw[3] = {(uint64_t)H, (uint64_t)I, (uint64_t)ea.pool_slots}, sw[2] = {(uint64_t)H * 2, ea.S};
+    const uint64_t da[2] = {(uint64_t)I, (uint64_t)Tk}, sa[1] = {(uint64_t)I * 2};
+    const uint64_t dd[3] = {(uint64_t)I, (uint64_t)H, (uint64_t)ea.pool_slots}, sd[2] = {(uint64_t)I * 2, ea.S};
+    int r = make_map_bf16(&mx, xp, 2, dx, sx, tc::BM);
+    if (!r) r = make_map_bf16(&mg, pool + L.off_val[0], 3, dw, sw, tc::BN / 2);
+    if (!r) r = make_map_bf16(&mu, pool + L.off_val[1], 3, dw, sw, tc::BN / 2);
+    if (!r) r = make_map_bf16(&ma, aint, 2, da, sa, tc::BM);
+    if (!r) r = make_map_bf16(&md, pool + L.off_val[2], 3, dd, sd, tc::BN);
+    if (r) return r;
+  }
+  tc::Args a;
+  a.T = ea.T; a.k = ea.k; a.H = H; a.I = I; a.E = ea.E; a.pool_slots = ea.pool_slots;
+  a.offsets = ea.offsets; a.slot_of = ea.slot_of; a.gscale_base = nullptr; a.S = ea.S;
+  a.Aint = aint; a.y = ea.y;
+  const size_t smem = tc::smem_bytes(ea.E);
+  auto kg = tc::grouped_gemm_kernel<tc::GATEUP>;
+  auto kd = tc::grouped_gemm_kernel<tc::DOWN>;
+  if (int s = set_smem(kg, smem)) return s;
+  if (int s = set_smem(kd, smem)) return s;
+  kg<<<sms(), tc::THREADS, smem, st>>>(mx, mg, mu, a);
+  FT_CHECK_LAUNCH();
+  kd<<<sms(), tc::THREADS, smem, st>>>(ma, md, md, a);
+  FT_CHECK_LAUNCH();
+  return FT_OK;
+}
+
 }  // namespace
 
 FT_API int ft_expert_grouped(const void* x, int x_type, int T, int k, int hidden, int inter, int E, int wtype,
@@ -220,6 +324,7 @@ FT_API int ft_expert_grouped(const void* x, int x_type, int T, int k, int hidden
   a.A = (float*)workspace;
   a.y = y;
   cudaStream_t st = (cudaStream_t)s;
+  if (tc_path_applies(wtype, T, k, hidden, inter, E)) return launch_expert_tc(a, L, workspace, st);
   switch (wtype) {
     case FT_W_F32: return launch_expert<FT_W_F32>(a, st);
     case FT_W_BF16: return launch_expert<FT_W_BF16>(a, st);
@@ -447,8 +552,6 @@ FT_API int ft_stream_destroy(ft_stream* st) {
 // instead of a caller-supplied workspace.  Host code must not hand the array's
 // name to a kernel (in host code it is a host-side stand-in); its device
 // address is looked up once per device with cudaGetSymbolAddress.
-
-#include <mutex>
 
 static constexpr size_t kNoAllocMaxElems = (size_t)1 << 20;  // fp32 elements: 4 MiB per device
 static __device__ __align__(256) float ft_noalloc_scratch[kNoAllocMaxElems];

@@ -5,10 +5,13 @@
 namespace ft {
 
 // ====================================================================== router logits
-// z[t][e] = sum_h x[t][h] W_r[e][h] + b[e].  A CTA stages RT token rows of x
-// in shared memory (fp32) and its warps sweep the experts: a warp reads one
+// z[t][e] = sum_h x[t][h] W_r[e][h] + b[e].  The grid is (expert groups,
+// row chunks of RL_RT): a CTA stages its RL_RT token rows of x in shared
+// memory (fp32) and its warps sweep the experts of its group: a warp reads one
 // router row with 16-byte loads and dots it with every staged row; lane
-// partials are reduced with one reduce-scatter per expert.
+// partials are reduced with one reduce-scatter.  Few row chunks (decode) get
+// many expert groups, so the router matrix is read in parallel even for one
+// token; many row chunks (prefill) get few groups, so x is staged few times.
 constexpr int RL_RT = 8;        // token rows per CTA
 constexpr int RL_WARPS = 8;
 
@@ -34,7 +37,7 @@ __global__ void __launch_bounds__(RL_WARPS * 32)
 router_logits_kernel(const XT* __restrict__ x, const XT* __restrict__ wr, const float* __restrict__ bias,
                      int T, int H, int E, float* __restrict__ z) {
   extern __shared__ float xs[];  // [RL_RT][H]
-  const int t0 = blockIdx.x * RL_RT;
+  const int t0 = blockIdx.y * RL_RT;
   const int nrows = min(RL_RT, T - t0);
   for (int i = threadIdx.x; i < RL_RT * H; i += blockDim.x) {
     int r = i / H, h = i - r * H;
@@ -42,7 +45,7 @@ router_logits_kernel(const XT* __restrict__ x, const XT* __restrict__ wr, const 
   }
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int e = warp; e < E; e += RL_WARPS) {
+  for (int e = blockIdx.x * RL_WARPS + warp; e < E; e += gridDim.x * RL_WARPS) {
     float acc[RL_RT];
 #pragma unroll
     for (int r = 0; r < RL_RT; ++r) acc[r] = 0.0f;

@@ -74,7 +74,9 @@ enum {
   FT_DERR_EXPERT_INDEX = 1,  /* an expert id outside [0, E) */
   FT_DERR_SLOT_INDEX = 2,    /* a slot outside the pool */
   FT_DERR_ROW_INDEX = 3,     /* a permutation row outside [0, T*k) */
-  FT_DERR_TABLE = 4          /* cache tables inconsistent */
+  FT_DERR_TABLE = 4,         /* cache tables inconsistent */
+  FT_DERR_TIMEOUT = 5        /* a kernel's bounded wait on an on-chip barrier ran out; the kernel
+                                stopped early and its outputs are incomplete */
 };
 
 const char* ft_status_str(int status);
@@ -261,10 +263,22 @@ int ft_cache_export(ft_cache* c, int32_t* key_of_slot, uint32_t* stamp, int* n_s
  *               a slot_of value >= pool_slots is a device error
  *   y           dev [T*k][H] fp32 (written for evaluated experts), permuted order
  *   workspace   dev, >= ft_expert_grouped_workspace(T, k, H, I) bytes, 256-aligned
- * Accumulation is fp32; the intermediate silu(G)*U is kept in fp32.  Each
- * output element is reduced in a fixed order, so results do not depend on
- * which other experts are evaluated in the same call or on the slot used.
+ * Accumulation is fp32.  Each output element is reduced in a fixed order, so
+ * results do not depend on which other experts are evaluated in the same call
+ * or on the slot used.
+ *
+ * Two execution paths, chosen from the arguments alone:
+ *   - T*k < FT_TC_MIN_ASSIGNMENTS (decode), or a shape or format the
+ *     tensor-core path does not take: CUDA cores, weights streamed once per
+ *     8-row chunk of an expert's rows, x and the intermediate silu(G)*U kept
+ *     in fp32.
+ *   - T*k >= FT_TC_MIN_ASSIGNMENTS with bf16 weights, H a multiple of 256 and
+ *     I a multiple of 128 (prefill): tcgen05 tensor cores, 128-row tiles of
+ *     each expert's rows.  x is rounded to bf16 (round to nearest even) for
+ *     the products, and the intermediate silu(G)*U is rounded to bf16 before
+ *     the down product; products accumulate in fp32.
  * ---------------------------------------------------------------------- */
+#define FT_TC_MIN_ASSIGNMENTS 2048
 size_t ft_expert_grouped_workspace(int T, int k, int hidden, int inter);
 int ft_expert_grouped(const void* x, int x_type, int T, int k, int hidden, int inter, int E,
                       int wtype, const int32_t* perm, const int32_t* offsets, const int32_t* slot_of,

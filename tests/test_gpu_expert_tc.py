@@ -1,0 +1,147 @@
+"""Parity of the tensor-core (tcgen05) grouped expert path against the fp64 oracle, through the C ABI.
+
+Batches of FT_TC_MIN_ASSIGNMENTS assignments or more with bf16 weights run on
+the tensor cores: x is rounded to bf16 and the intermediate silu(G)*U is
+rounded to bf16 before the down product.  The oracle applies the same two
+roundings (x is already bf16 here; the intermediate goes through
+formats.round_to_bf16), and the bar is the tensor-core one: relative Frobenius
+error <= 1e-2, max |err| <= 2e-2 * max |ref|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from conftest import assert_close_layer, rel_fro
+from oracle import formats, moe
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TC_MIN = 2048  # FT_TC_MIN_ASSIGNMENTS in include/ft.h
+
+
+@pytest.fixture(scope="module")
+def ft(ftlib):
+    assert torch.cuda.is_available()
+    return ftlib
+
+
+def _setup(ft, H, I, E, k, T, seed, skewed=False):
+    cfg = synth.MoEConfig(f"tc_{H}_{I}_{E}", H, E, k, I, 1, synth.W_BF16, "bf16", seed=seed)
+    L = ft.ft_expert_layout_get(synth.W_BF16, H, I)
+    S = int(L.bytes)
+    n_slots = E + 5
+    pool = torch.zeros(n_slots * S, dtype=torch.uint8, device=DEV)
+    rng = np.random.default_rng(seed)
+    slot_perm = rng.permutation(n_slots)[:E]
+    comps = {}
+    for e in range(E):
+        comps[e] = synth.expert_weights(cfg, 0, e, DEV)
+        ft.pack_expert(comps[e], synth.W_BF16, L, pool[slot_perm[e] * S:(slot_perm[e] + 1) * S])
+    x = synth.activations(cfg, T, tag=5, device=DEV)
+    if skewed:
+        # a few heavy experts (several 128-row tiles) and a tail of light ones
+        p = 1.0 / np.arange(1, E + 1) ** 1.2
+        p /= p.sum()
+        idx = np.stack([rng.choice(E, k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    else:
+        idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    return cfg, L, S, n_slots, pool, slot_perm, comps, x, idx
+
+
+def _run(ft, x, k, I, E, perm, offsets, slot_of, pool, S, n_slots):
+    T, H = x.shape
+    y = torch.full((T * k, H), float("nan"), dtype=torch.float32, device=DEV)
+    ws = torch.empty(ft.ft_expert_grouped_workspace(T, k, H, I), dtype=torch.uint8, device=DEV)
+    ft.ft_expert_grouped(x, k, I, E, synth.W_BF16, torch.from_numpy(perm).to(DEV),
+                         torch.from_numpy(offsets).to(DEV), torch.from_numpy(slot_of).to(DEV), pool, S, n_slots, y, ws)
+    torch.cuda.synchronize()
+    assert ft.ft_get_device_error() == 0
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("H,I,E,k,T,seed,skewed", [
+    (256, 128, 8, 8, 300, 0, False),      # 300 rows per expert: 3 row tiles, ragged tail; one n-tile
+    (512, 256, 4, 2, 1100, 1, False),     # ~550 rows per expert, 5 row tiles
+    (2048, 512, 32, 8, 512, 2, False),    # the decode/prefill expert shape, ~128 rows per expert
+    (1024, 384, 16, 4, 700, 3, True),     # skewed counts: heavy and light experts, I = 3 x 128
+    (768, 256, 64, 8, 256, 4, False),     # exactly 2048 assignments; ~32 rows per expert (mostly-empty tiles)
+])
+def test_tc_expert_grouped_parity(ft, H, I, E, k, T, seed, skewed):
+    assert T * k >= TC_MIN
+    cfg, L, S, n_slots, pool, slot_perm, comps, x, idx = _setup(ft, H, I, E, k, T, seed, skewed)
+    counts, offsets, perm, inv = moe.permute(idx, E)
+    slot_of = slot_perm.astype(np.int32).copy()
+    skipped = {E - 1, 1}
+    slot_of[E - 1] = -1                      # not evaluated
+    slot_of[1] = -2                          # evaluated elsewhere
+    Y = _run(ft, x, k, I, E, perm, offsets, slot_of, pool, S, n_slots)
+    xs = formats.to_f64(x)
+    got, ref = [], []
+    for e in range(E):
+        rows = np.arange(offsets[e], offsets[e + 1])
+        if e in skipped:
+            assert np.isnan(Y[rows]).all(), "rows of skipped experts must be left untouched"
+            continue
+        g, u, d = (formats.dequant(comps[e][m], synth.W_BF16) for m in ("gate", "up", "down"))
+        ref.append(moe.expert_ffn(xs[perm[rows] // k], g, u, d, act_round=formats.round_to_bf16))
+        got.append(Y[rows])
+    got, ref = np.concatenate(got), np.concatenate(ref)
+    assert np.isfinite(got).all()
+    assert_close_layer(got, ref, fro=1e-2)
+    # both sides round the same intermediate to bf16: they differ only where the
+    # fp32 and fp64 values fall on different sides of a bf16 rounding boundary
+    assert rel_fro(got, ref) < 2e-3
+
+
+def test_tc_threshold_selects_the_path(ft):
+    """T*k one below the threshold keeps the fp32 intermediate; at the threshold it is rounded to bf16."""
+    H, I, E, k = 512, 256, 8, 8
+    T_cc, T_tc = TC_MIN // k - 1, TC_MIN // k
+    cfg, L, S, n_slots, pool, slot_perm, comps, x, idx = _setup(ft, H, I, E, k, T_tc, 9)
+    experts = {e: tuple(formats.dequant(comps[e][m], synth.W_BF16) for m in ("gate", "up", "down")) for e in range(E)}
+    slot_of = slot_perm.astype(np.int32)
+    for T, tight in ((T_cc, True), (T_tc, False)):
+        counts, offsets, perm, inv = moe.permute(idx[:T], E)
+        Y = _run(ft, x[:T], k, I, E, perm, offsets, slot_of, pool, S, n_slots)
+        xs = formats.to_f64(x[:T])
+        ref_f32 = np.concatenate([moe.expert_ffn(xs[perm[offsets[e]:offsets[e + 1]] // k], *experts[e])
+                                  for e in range(E)])
+        err = rel_fro(Y, ref_f32)
+        if tight:
+            assert err < 2e-5, err            # fp32 intermediate
+        else:
+            assert 1e-5 < err < 1e-2, err     # bf16 intermediate: visibly rounded, within the bar
+
+
+def test_tc_independent_of_slot_and_other_experts(ft):
+    """Same expert, same rows: bitwise equal output whatever the slot or the other experts in the call."""
+    H, I, E, k, T = 512, 256, 6, 4, 600
+    cfg, L, S, n_slots, pool, slot_perm, comps, x, idx = _setup(ft, H, I, E, k, T, 11)
+    # second copy of expert 2 in a spare slot
+    spare = int(np.setdiff1d(np.arange(n_slots), slot_perm)[0])
+    ft.pack_expert(comps[2], synth.W_BF16, L, pool[spare * S:(spare + 1) * S])
+    counts, offsets, perm, inv = moe.permute(idx, E)
+    all_on = slot_perm.astype(np.int32)
+    only2 = np.full(E, -1, dtype=np.int32)
+    only2[2] = spare
+    Y1 = _run(ft, x, k, I, E, perm, offsets, all_on, pool, S, n_slots)
+    Y2 = _run(ft, x, k, I, E, perm, offsets, only2, pool, S, n_slots)
+    r = slice(int(offsets[2]), int(offsets[3]))
+    assert np.array_equal(Y1[r], Y2[r])
+
+
+def test_tc_empty_experts_and_all_rows_on_one_expert(ft):
+    """Every assignment routed to experts 0..k-1 (the rest empty): k experts of T rows each."""
+    H, I, E, k, T = 256, 128, 16, 8, 260
+    cfg, L, S, n_slots, pool, slot_perm, comps, x, _ = _setup(ft, H, I, E, k, T, 13)
+    idx = np.tile(np.arange(k, dtype=np.int32), (T, 1))
+    counts, offsets, perm, inv = moe.permute(idx, E)
+    assert (counts[k:] == 0).all()
+    Y = _run(ft, x, k, I, E, perm, offsets, slot_perm.astype(np.int32), pool, S, n_slots)
+    xs = formats.to_f64(x)
+    ref = np.concatenate([moe.expert_ffn(xs[perm[offsets[e]:offsets[e + 1]] // k],
+                                         *(formats.dequant(comps[e][m], synth.W_BF16) for m in ("gate", "up", "down")),
+                                         act_round=formats.round_to_bf16) for e in range(k)])
+    assert_close_layer(Y, ref, fro=1e-2)
+    assert rel_fro(Y, ref) < 2e-3

@@ -292,5 +292,6 @@ def test_prefill_chunk_full_size_sampled(ft):
     assert np.array_equal(L.idx.cpu().numpy(), ri)
     rows = np.random.default_rng(0).choice(8192, 24, replace=False)
     ol = OracleLayer(cfg, 1)
-    ref = moe.moe_layer(formats.to_f64(x[rows]), ri[rows], rw[rows], ol.experts(0))
-    assert_close_layer(out[rows], ref)
+    # 8192 x 8 assignments run on the tensor cores: the intermediate is rounded to bf16 on both sides
+    ref = moe.moe_layer(formats.to_f64(x[rows]), ri[rows], rw[rows], ol.experts(0), act_round=formats.round_to_bf16)
+    assert_close_layer(out[rows], ref, fro=1e-2)
