@@ -10,15 +10,19 @@
 //   down:    Y[p][h] = Aint[p] . Wd[h]                           (fp32)
 //
 // One persistent kernel per product, one CTA per SM, warp-specialised:
-//   warp 0      TMA producer: A tile (128 x 64 bf16) and B tile (256 x 64 bf16)
-//               per stage, 128-byte swizzle, 4 stages
+//   warp 0      TMA producer: A tile (128 x 64 bf16) and B tile (BN x 64 bf16)
+//               per stage, 128-byte swizzle, as many stages as fit in 192 KiB
 //   warp 1      tensor-memory owner and MMA issuer (one thread): 4 x
-//               tcgen05.mma kind::f16 (M=128, N=256, K=16) per stage into one
-//               of two 256-column fp32 accumulators
+//               tcgen05.mma kind::f16 (M=128, N=BN, K=16) per stage into one
+//               of two BN-column fp32 accumulators
 //   warps 2..5  epilogue: tcgen05.ld of the finished accumulator while the
-//               next tile accumulates into the other one
-// For gate/up the 256 B rows are 128 gate rows then the same 128 up rows, so
-// one accumulator holds G and U for the same 128 outputs and the SwiGLU is
+//               next tile accumulates into the other one; results go through
+//               a per-warp shared-memory transpose so that global stores are
+//               whole 128-byte row segments
+// BN = 256 for large batches; BN = 128 for small ones (decode), which doubles
+// the number of tiles so that a handful of experts still spreads over the SMs.
+// For gate/up the BN B rows are BN/2 gate rows then the same BN/2 up rows, so
+// one accumulator holds G and U for the same BN/2 outputs and the SwiGLU is
 // applied in registers.  Weights come through 3-D tensor maps over the whole
 // slot pool (K, row, slot), so the slot is just a TMA coordinate.
 //
@@ -33,25 +37,34 @@ namespace ft {
 namespace tc {
 
 constexpr int BM = 128;                    // rows per tile (UMMA M)
-constexpr int BN = 256;                    // UMMA N
 constexpr int BK = 64;                     // K per stage: 128 bytes of bf16
 constexpr int UK = 16;                     // K per tcgen05.mma (kind::f16)
-constexpr int STAGES = 4;
 constexpr int THREADS = 192;
 constexpr int WARPS = THREADS / 32;
+constexpr int EPI_WARPS = 4;
 constexpr int A_BYTES = BM * BK * 2;       // 16 KiB
-constexpr int B_BYTES = BN * BK * 2;       // 32 KiB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int ACC_COLS = BN;               // fp32 columns per accumulator
-constexpr int TMEM_COLS = 2 * ACC_COLS;    // double-buffered accumulators
+constexpr int STAGE_BUDGET = 192 * 1024;   // shared memory for the operand stages
+constexpr int EPI_STRIDE = 36;             // 32-bit words per staged epilogue row (32 + 4 pad)
+constexpr int EPI_BYTES = EPI_WARPS * 32 * EPI_STRIDE * 4;
 constexpr int MAX_E = 1024;
 
 enum Mode { GATEUP = 0, DOWN = 1 };
 
-// Bytes of dynamic shared memory: 1 KiB alignment slack, the stages, then the
-// barriers and the expert list.
+template <int BN>
+struct Cfg {
+  static_assert(BN == 128 || BN == 256, "UMMA N");
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = STAGE_BUDGET / STAGE_BYTES;  // 4 (BN 256) or 6 (BN 128)
+  static constexpr int ACC_COLS = BN;                        // fp32 columns per accumulator
+  static constexpr int TMEM_COLS = 2 * ACC_COLS;             // double-buffered accumulators
+};
+
+// Bytes of dynamic shared memory: 1 KiB alignment slack, the stages, the
+// barriers, the epilogue transpose buffers, then the expert list.
+template <int BN>
 __host__ __device__ constexpr size_t smem_bytes(int E) {
-  return 1024 + (size_t)STAGES * STAGE_BYTES + 256 + (size_t)(2 * E + 2) * 4;
+  return 1024 + (size_t)Cfg<BN>::STAGES * Cfg<BN>::STAGE_BYTES + 256 + EPI_BYTES + (size_t)(2 * E + 2) * 4;
 }
 
 struct Args {
@@ -156,11 +169,16 @@ __device__ __forceinline__ Tile decode_tile(const Args& a, const int* act_e, con
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int MODE>
+template <int MODE, int BN>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                     const __grid_constant__ CUtensorMap map_b1, Args a) {
   using namespace sm100;
+  constexpr int STAGES = Cfg<BN>::STAGES;
+  constexpr int STAGE_BYTES = Cfg<BN>::STAGE_BYTES;
+  constexpr int B_BYTES = Cfg<BN>::B_BYTES;
+  constexpr int ACC_COLS = Cfg<BN>::ACC_COLS;
+  constexpr int TMEM_COLS = Cfg<BN>::TMEM_COLS;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1 KiB-aligned stage buffers (the 128-byte swizzle pattern repeats every 1 KiB)
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -172,7 +190,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* scan_buf = const_cast<int*>(reinterpret_cast<volatile int*>(tmem_holder + 2));  // [WARPS]
-  int* act_e = reinterpret_cast<int*>(smem + (size_t)STAGES * STAGE_BYTES + 256);
+  uint32_t* epi_buf = reinterpret_cast<uint32_t*>(smem + (size_t)STAGES * STAGE_BYTES + 256);
+  int* act_e = reinterpret_cast<int*>(smem + (size_t)STAGES * STAGE_BYTES + 256 + EPI_BYTES);
   int* act_pref = act_e + a.E;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -284,52 +303,69 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
   } else {
     // ---------------------------------------------------------------- epilogue (warps 2..5)
     const int q = warp & 3;          // TMEM lane quarter this warp may access
-    const int r = q * 32 + lane;     // tile row = TMEM lane
+    uint32_t* buf = epi_buf + (warp - 2) * 32 * EPI_STRIDE;  // this warp's 32 x 32 transpose buffer
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int item = blockIdx.x; item < total; item += gridDim.x) {
       const Tile t = decode_tile(a, act_e, act_pref, n_act, item);
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) break;
       tc_fence_after();
-      const bool valid = t.mt * BM + r < t.cnt;
-      const size_t p = (size_t)t.row0 + r;
+      const int rbase = t.mt * BM + q * 32;   // expert-local row of this warp's first lane
+      const size_t pbase = (size_t)t.row0 + q * 32;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * ACC_COLS;
       if (MODE == GATEUP) {
+        // lane = row: 32 outputs silu(g) * u as bf16 (64 bytes), staged, then
+        // written as 16-byte pieces, 4 lanes per row, 8 rows per instruction
 #pragma unroll 1
         for (int c = 0; c < (BN / 2) / 32; ++c) {
           uint32_t g[32], u[32];
           tmem_ld32(taddr + c * 32, g);
           tmem_ld32(taddr + BN / 2 + c * 32, u);
           tmem_ld_wait();
-          if (valid) {
-            uint32_t packed[16];
+          uint32_t* row = buf + lane * EPI_STRIDE;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float a0 = silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
-              const float a1 = silu(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
-              packed[j] = *reinterpret_cast<uint32_t*>(&h2);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(a.Aint + p * a.I + t.nt * (BN / 2) + c * 32);
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+          for (int j = 0; j < 16; ++j) {
+            const float a0 = silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
+            const float a1 = silu(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
+            row[j] = *reinterpret_cast<uint32_t*>(&h2);
           }
+          __syncwarp();
+          const int col = t.nt * (BN / 2) + c * 32;
+#pragma unroll
+          for (int it = 0; it < 4; ++it) {
+            const int r = it * 8 + (lane >> 2), piece = lane & 3;
+            if (rbase + r < t.cnt) {
+              const uint4 v = *reinterpret_cast<const uint4*>(buf + r * EPI_STRIDE + piece * 4);
+              *reinterpret_cast<uint4*>(a.Aint + (pbase + r) * a.I + col + piece * 8) = v;
+            }
+          }
+          __syncwarp();
         }
       } else {
+        // lane = row: 32 fp32 outputs (128 bytes), staged, then written as
+        // 16-byte pieces, 8 lanes per row, 4 rows per instruction
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(taddr + c * 32, v);
           tmem_ld_wait();
-          const int col = t.nt * BN + c * 32;
-          if (valid && col < a.H) {
-            float4* dst = reinterpret_cast<float4*>(a.y + p * a.H + col);
+          uint4* row = reinterpret_cast<uint4*>(buf + lane * EPI_STRIDE);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                   __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          for (int j = 0; j < 8; ++j) row[j] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          __syncwarp();
+          const int col = t.nt * BN + c * 32;
+          if (col < a.H) {
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+              const int r = it * 4 + (lane >> 3), piece = lane & 7;
+              if (rbase + r < t.cnt) {
+                const uint4 w = *reinterpret_cast<const uint4*>(buf + r * EPI_STRIDE + piece * 4);
+                *reinterpret_cast<uint4*>(a.y + (pbase + r) * a.H + col + piece * 4) = w;
+              }
+            }
           }
+          __syncwarp();
         }
       }
       tc_fence_before();

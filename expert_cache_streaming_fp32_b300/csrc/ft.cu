@@ -181,12 +181,11 @@ static size_t ws_tensor_core(long long Tk, int hidden, int inter) {
   return align256((size_t)Tk * hidden * 2) + align256((size_t)Tk * inter * 2);
 }
 
+// Enough for either path (the weight format, which picks the path, is not an argument here).
 FT_API size_t ft_expert_grouped_workspace(int T, int k, int hidden, int inter) {
   if (T <= 0 || k <= 0 || inter <= 0 || hidden <= 0) return 256;
   const long long Tk = (long long)T * k;
-  size_t ws = ws_cuda_core(Tk, inter);
-  if (Tk >= FT_TC_MIN_ASSIGNMENTS) ws = std::max(ws, ws_tensor_core(Tk, hidden, inter));
-  return std::max(ws, (size_t)256);
+  return std::max({ws_cuda_core(Tk, inter), ws_tensor_core(Tk, hidden, inter), (size_t)256});
 }
 
 namespace {
@@ -248,11 +247,27 @@ int make_map_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* di
   return r == CUDA_SUCCESS ? FT_OK : FT_EINVAL;
 }
 
-// The tensor-core path takes bf16 weights at batches of FT_TC_MIN_ASSIGNMENTS
-// assignments or more, for shapes whose tiles divide evenly.
+// The tensor-core path takes bf16 weights (H and I multiples of 128, which the
+// record layout already requires).
 bool tc_path_applies(int wtype, int T, int k, int H, int I, int E) {
-  return wtype == FT_W_BF16 && (long long)T * k >= FT_TC_MIN_ASSIGNMENTS && H % tc::BN == 0 &&
-         I % (tc::BN / 2) == 0 && E <= tc::MAX_E && (long long)T * k < (1ll << 31) / 8;
+  return wtype == FT_W_BF16 && H % 128 == 0 && I % 128 == 0 && E <= tc::MAX_E && (long long)T * k < (1ll << 28);
+}
+
+// Tile width: 256 columns from FT_TC_WIDE_ASSIGNMENTS assignments up (fewer,
+// larger tiles), 128 below (twice the tiles, so a few experts still cover the SMs).
+template <int BN>
+int launch_tc_gemms(const CUtensorMap& mx, const CUtensorMap& mg, const CUtensorMap& mu, const CUtensorMap& ma,
+                    const CUtensorMap& md, const tc::Args& a, cudaStream_t st) {
+  const size_t smem = tc::smem_bytes<BN>(a.E);
+  auto kg = tc::grouped_gemm_kernel<tc::GATEUP, BN>;
+  auto kd = tc::grouped_gemm_kernel<tc::DOWN, BN>;
+  if (int s = set_smem(kg, smem)) return s;
+  if (int s = set_smem(kd, smem)) return s;
+  kg<<<sms(), tc::THREADS, smem, st>>>(mx, mg, mu, a);
+  FT_CHECK_LAUNCH();
+  kd<<<sms(), tc::THREADS, smem, st>>>(ma, md, md, a);
+  FT_CHECK_LAUNCH();
+  return FT_OK;
 }
 
 int launch_expert_tc(const ExpertArgs& ea, const ft_expert_layout& L, void* workspace, cudaStream_t st) {
@@ -273,32 +288,24 @@ int launch_expert_tc(const ExpertArgs& ea, const ft_expert_layout& L, void* work
   }
   CUtensorMap mx, mg, mu, ma, md;
   const uint8_t* pool = ea.pool;
+  const int BN = (Tk >= FT_TC_WIDE_ASSIGNMENTS && H % 256 == 0) ? 256 : 128;
   {
     const uint64_t dx[2] = {(uint64_t)H, (uint64_t)Tk}, sx[1] = {(uint64_t)H * 2};
     const uint64_t dw[3] = {(uint64_t)H, (uint64_t)I, (uint64_t)ea.pool_slots}, sw[2] = {(uint64_t)H * 2, ea.S};
     const uint64_t da[2] = {(uint64_t)I, (uint64_t)Tk}, sa[1] = {(uint64_t)I * 2};
     const uint64_t dd[3] = {(uint64_t)I, (uint64_t)H, (uint64_t)ea.pool_slots}, sd[2] = {(uint64_t)I * 2, ea.S};
     int r = make_map_bf16(&mx, xp, 2, dx, sx, tc::BM);
-    if (!r) r = make_map_bf16(&mg, pool + L.off_val[0], 3, dw, sw, tc::BN / 2);
-    if (!r) r = make_map_bf16(&mu, pool + L.off_val[1], 3, dw, sw, tc::BN / 2);
+    if (!r) r = make_map_bf16(&mg, pool + L.off_val[0], 3, dw, sw, BN / 2);
+    if (!r) r = make_map_bf16(&mu, pool + L.off_val[1], 3, dw, sw, BN / 2);
     if (!r) r = make_map_bf16(&ma, aint, 2, da, sa, tc::BM);
-    if (!r) r = make_map_bf16(&md, pool + L.off_val[2], 3, dd, sd, tc::BN);
+    if (!r) r = make_map_bf16(&md, pool + L.off_val[2], 3, dd, sd, BN);
     if (r) return r;
   }
   tc::Args a;
   a.T = ea.T; a.k = ea.k; a.H = H; a.I = I; a.E = ea.E; a.pool_slots = ea.pool_slots;
   a.offsets = ea.offsets; a.slot_of = ea.slot_of; a.gscale_base = nullptr; a.S = ea.S;
   a.Aint = aint; a.y = ea.y;
-  const size_t smem = tc::smem_bytes(ea.E);
-  auto kg = tc::grouped_gemm_kernel<tc::GATEUP>;
-  auto kd = tc::grouped_gemm_kernel<tc::DOWN>;
-  if (int s = set_smem(kg, smem)) return s;
-  if (int s = set_smem(kd, smem)) return s;
-  kg<<<sms(), tc::THREADS, smem, st>>>(mx, mg, mu, a);
-  FT_CHECK_LAUNCH();
-  kd<<<sms(), tc::THREADS, smem, st>>>(ma, md, md, a);
-  FT_CHECK_LAUNCH();
-  return FT_OK;
+  return BN == 256 ? launch_tc_gemms<256>(mx, mg, mu, ma, md, a, st) : launch_tc_gemms<128>(mx, mg, mu, ma, md, a, st);
 }
 
 }  // namespace

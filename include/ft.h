@@ -267,18 +267,18 @@ int ft_cache_export(ft_cache* c, int32_t* key_of_slot, uint32_t* stamp, int* n_s
  * results do not depend on which other experts are evaluated in the same call
  * or on the slot used.
  *
- * Two execution paths, chosen from the arguments alone:
- *   - T*k < FT_TC_MIN_ASSIGNMENTS (decode), or a shape or format the
- *     tensor-core path does not take: CUDA cores, weights streamed once per
- *     8-row chunk of an expert's rows, x and the intermediate silu(G)*U kept
- *     in fp32.
- *   - T*k >= FT_TC_MIN_ASSIGNMENTS with bf16 weights, H a multiple of 256 and
- *     I a multiple of 128 (prefill): tcgen05 tensor cores, 128-row tiles of
- *     each expert's rows.  x is rounded to bf16 (round to nearest even) for
- *     the products, and the intermediate silu(G)*U is rounded to bf16 before
- *     the down product; products accumulate in fp32.
+ * Two execution paths, chosen by the weight format:
+ *   - bf16 weights: tcgen05 tensor cores at every batch size, 128-row tiles
+ *     of each expert's rows against 128 or 256 weight rows (256 from
+ *     FT_TC_WIDE_ASSIGNMENTS assignments T*k up, when H is a multiple of 256).
+ *     x is rounded to bf16 (round to nearest even) for the products, and the
+ *     intermediate silu(G)*U is rounded to bf16 before the down product;
+ *     products accumulate in fp32.
+ *   - other formats: CUDA cores, weights streamed once per 8-row chunk of an
+ *     expert's rows and dequantised in registers; x and the intermediate
+ *     silu(G)*U stay in fp32.
  * ---------------------------------------------------------------------- */
-#define FT_TC_MIN_ASSIGNMENTS 2048
+#define FT_TC_WIDE_ASSIGNMENTS 2048
 size_t ft_expert_grouped_workspace(int T, int k, int hidden, int inter);
 int ft_expert_grouped(const void* x, int x_type, int T, int k, int hidden, int inter, int E,
                       int wtype, const int32_t* perm, const int32_t* offsets, const int32_t* slot_of,

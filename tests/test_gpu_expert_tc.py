@@ -1,11 +1,12 @@
 """Parity of the tensor-core (tcgen05) grouped expert path against the fp64 oracle, through the C ABI.
 
-Batches of FT_TC_MIN_ASSIGNMENTS assignments or more with bf16 weights run on
-the tensor cores: x is rounded to bf16 and the intermediate silu(G)*U is
-rounded to bf16 before the down product.  The oracle applies the same two
-roundings (x is already bf16 here; the intermediate goes through
-formats.round_to_bf16), and the bar is the tensor-core one: relative Frobenius
-error <= 1e-2, max |err| <= 2e-2 * max |ref|.
+bf16 weights run on the tensor cores at every batch size: x is rounded to
+bf16 and the intermediate silu(G)*U is rounded to bf16 before the down
+product.  The oracle applies the same two roundings (x is already bf16 here;
+the intermediate goes through formats.round_to_bf16), and the bar is the
+tensor-core one: relative Frobenius error <= 1e-2, max |err| <= 2e-2 * max |ref|.
+Batches below FT_TC_WIDE_ASSIGNMENTS use 128-column weight tiles, larger ones
+256-column tiles; both are covered.
 """
 import numpy as np
 import pytest
@@ -17,7 +18,7 @@ from oracle import formats, moe
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-TC_MIN = 2048  # FT_TC_MIN_ASSIGNMENTS in include/ft.h
+TC_WIDE = 2048  # FT_TC_WIDE_ASSIGNMENTS in include/ft.h
 
 
 @pytest.fixture(scope="module")
@@ -66,9 +67,12 @@ def _run(ft, x, k, I, E, perm, offsets, slot_of, pool, S, n_slots):
     (2048, 512, 32, 8, 512, 2, False),    # the decode/prefill expert shape, ~128 rows per expert
     (1024, 384, 16, 4, 700, 3, True),     # skewed counts: heavy and light experts, I = 3 x 128
     (768, 256, 64, 8, 256, 4, False),     # exactly 2048 assignments; ~32 rows per expert (mostly-empty tiles)
+    (2048, 512, 32, 8, 1, 5, False),      # one decode token: 8 experts of one row, 128-column tiles
+    (2048, 512, 64, 8, 16, 6, True),      # decode batch of 16, skewed
+    (256, 128, 8, 2, 3, 7, False),        # tiny: H = 256, I = 128
+    (4096, 256, 16, 6, 40, 8, False),     # wide hidden, narrow intermediate
 ])
 def test_tc_expert_grouped_parity(ft, H, I, E, k, T, seed, skewed):
-    assert T * k >= TC_MIN
     cfg, L, S, n_slots, pool, slot_perm, comps, x, idx = _setup(ft, H, I, E, k, T, seed, skewed)
     counts, offsets, perm, inv = moe.permute(idx, E)
     slot_of = slot_perm.astype(np.int32).copy()
@@ -94,24 +98,24 @@ def test_tc_expert_grouped_parity(ft, H, I, E, k, T, seed, skewed):
     assert rel_fro(got, ref) < 2e-3
 
 
-def test_tc_threshold_selects_the_path(ft):
-    """T*k one below the threshold keeps the fp32 intermediate; at the threshold it is rounded to bf16."""
+def test_tc_both_tile_widths(ft):
+    """T*k just below FT_TC_WIDE_ASSIGNMENTS (128-column tiles) and at it (256-column tiles)."""
     H, I, E, k = 512, 256, 8, 8
-    T_cc, T_tc = TC_MIN // k - 1, TC_MIN // k
-    cfg, L, S, n_slots, pool, slot_perm, comps, x, idx = _setup(ft, H, I, E, k, T_tc, 9)
+    T_narrow, T_wide = TC_WIDE // k - 1, TC_WIDE // k
+    cfg, L, S, n_slots, pool, slot_perm, comps, x, idx = _setup(ft, H, I, E, k, T_wide, 9)
     experts = {e: tuple(formats.dequant(comps[e][m], synth.W_BF16) for m in ("gate", "up", "down")) for e in range(E)}
     slot_of = slot_perm.astype(np.int32)
-    for T, tight in ((T_cc, True), (T_tc, False)):
+    xs = formats.to_f64(x)
+    for T in (T_narrow, T_wide):
         counts, offsets, perm, inv = moe.permute(idx[:T], E)
         Y = _run(ft, x[:T], k, I, E, perm, offsets, slot_of, pool, S, n_slots)
-        xs = formats.to_f64(x[:T])
-        ref_f32 = np.concatenate([moe.expert_ffn(xs[perm[offsets[e]:offsets[e + 1]] // k], *experts[e])
-                                  for e in range(E)])
-        err = rel_fro(Y, ref_f32)
-        if tight:
-            assert err < 2e-5, err            # fp32 intermediate
-        else:
-            assert 1e-5 < err < 1e-2, err     # bf16 intermediate: visibly rounded, within the bar
+        ref = np.concatenate([moe.expert_ffn(xs[perm[offsets[e]:offsets[e + 1]] // k], *experts[e],
+                                             act_round=formats.round_to_bf16) for e in range(E)])
+        assert_close_layer(Y, ref, fro=1e-2)
+        assert rel_fro(Y, ref) < 2e-3
+        ref32 = np.concatenate([moe.expert_ffn(xs[perm[offsets[e]:offsets[e + 1]] // k], *experts[e])
+                                for e in range(E)])
+        assert rel_fro(Y, ref32) > 1e-5       # the intermediate is visibly rounded to bf16
 
 
 def test_tc_independent_of_slot_and_other_experts(ft):

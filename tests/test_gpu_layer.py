@@ -10,6 +10,9 @@ from oracle.lru import LRUSim
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
+# bf16 expert weights run on the tensor cores, which round the intermediate
+# silu(G)*U to bf16: the oracle applies the same rounding, and the bar is 1e-2
+TC_ROUND = formats.round_to_bf16
 
 
 @pytest.fixture(scope="module")
@@ -152,8 +155,8 @@ def test_cache_trace_resize_split_matches_simulator(ft):
             if not C:
                 assert np.array_equal(out, out_b), f"step {step} layer {l}: output depends on the cache"
             if step % 5 == 0 or C:
-                ref = moe.moe_layer(formats.to_f64(x), ri, rw, ol.experts(l))
-                assert_close_layer(out, ref)
+                ref = moe.moe_layer(formats.to_f64(x), ri, rw, ol.experts(l), act_round=TC_ROUND)
+                assert_close_layer(out, ref, fro=1e-2)
     key, stamp, clock = cache.export()
     sk, ss = sim.state()
     assert key.tolist() == sk.tolist() and stamp.tolist() == ss.tolist() and clock == sim.clock
@@ -218,8 +221,8 @@ def test_stream_double_buffered_and_serialized(ft):
     z = moe.router_logits(formats.to_f64(xp[rows]), formats.to_f64(routers[2][0]), formats.to_f64(routers[2][1]))
     ri, rw = moe.route(z, 4)
     assert not moe.near_ties(z, 4).any()
-    ref = moe.moe_layer(formats.to_f64(xp[rows]), ri, rw, ol.experts(2))
-    assert_close_layer(ref_out[2].cpu().numpy()[rows], ref)
+    ref = moe.moe_layer(formats.to_f64(xp[rows]), ri, rw, ol.experts(2), act_round=TC_ROUND)
+    assert_close_layer(ref_out[2].cpu().numpy()[rows], ref, fro=1e-2)
     assert ft.ft_get_device_error() == 0
 
 
@@ -265,8 +268,8 @@ def test_decode_full_size_sampled(ft):
                 r2, w2 = moe.route(zr, 8)
                 ok = ~moe.near_ties(zr, 8)
                 assert np.array_equal(r2[ok], ri[sample][ok])
-                ref = moe.moe_layer(xs, ri[sample], rw[sample], ol.experts(l))
-                assert_close_layer(out.cpu().numpy()[sample], ref)
+                ref = moe.moe_layer(xs, ri[sample], rw[sample], ol.experts(l), act_round=TC_ROUND)
+                assert_close_layer(out.cpu().numpy()[sample], ref, fro=1e-2)
     st = cache.stats()
     assert (st.hits, st.fills) == (sim.hits, sim.fills)
     assert ft.ft_get_device_error() == 0
@@ -292,6 +295,5 @@ def test_prefill_chunk_full_size_sampled(ft):
     assert np.array_equal(L.idx.cpu().numpy(), ri)
     rows = np.random.default_rng(0).choice(8192, 24, replace=False)
     ol = OracleLayer(cfg, 1)
-    # 8192 x 8 assignments run on the tensor cores: the intermediate is rounded to bf16 on both sides
-    ref = moe.moe_layer(formats.to_f64(x[rows]), ri[rows], rw[rows], ol.experts(0), act_round=formats.round_to_bf16)
+    ref = moe.moe_layer(formats.to_f64(x[rows]), ri[rows], rw[rows], ol.experts(0), act_round=TC_ROUND)
     assert_close_layer(out[rows], ref, fro=1e-2)
