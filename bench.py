@@ -48,10 +48,17 @@ def parse():
     p.add_argument("--no-prefill", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-graphs", action="store_true", help="issue the decode steps eagerly instead of as CUDA graphs")
     p.add_argument("--kernel-case", default="", choices=["", "experts_decode", "experts_prefill"],
                    help="time one expert-kernel case on a small resident pool (profiling aid; prints its own line)")
     p.add_argument("--reps", type=int, default=5)
     return p.parse_args()
+
+
+def log(msg: str) -> None:
+    """Phase marker on stderr (the JSON line goes to stdout)."""
+    sys.stderr.write(f"[bench {time.strftime('%H:%M:%S')}] {msg}\n")
+    sys.stderr.flush()
 
 
 # ---------------------------------------------------------------- distributed plumbing
@@ -197,19 +204,31 @@ class DecodeTrace:
             self.x_host = torch.empty(n_steps, T, cfg.hidden, dtype=torch.bfloat16).pin_memory()
             self.x_host.copy_(self.xs.cpu())
             self.x_dev = torch.empty(T, cfg.hidden, dtype=torch.bfloat16, device=dev)
+            self.outs = torch.empty(L, T, cfg.hidden, dtype=torch.float32, device=dev)
             self.out_host = torch.empty(L, T, cfg.hidden, dtype=torch.float32).pin_memory()
 
     def launches_per_step(self) -> int:
-        # router_logits, route, permute, (control, fill, gate/up, down) per wave, combine
-        return self.cfg.n_layers * (3 + 4 * self.n_waves + 1)
+        # router_logits, route, permute, (control, fill, expert kernels) per wave, combine;
+        # bf16 experts run gather + gate/up + down on the tensor cores, other formats gate/up + down
+        n_exp = 3 if self.cfg.wtype == synth.W_BF16 else 2
+        return self.cfg.n_layers * (3 + (2 + n_exp) * self.n_waves + 1)
+
+    def capture(self, t, e2e=False, timed=True):
+        """One CUDA graph of decode step t (all layers).
+
+        With ``timed`` the graph also records timing events (event-record nodes);
+        the returned EventLog owns them and must outlive every replay of the graph."""
+        g = torch.cuda.CUDAGraph()
+        ev = EventLog(external=True) if timed else None
+        with torch.cuda.graph(g):
+            self.step(t, ev, e2e)
+        return g, ev
 
     def step(self, t, ev=None, e2e=False):
+        """One decode step of every layer.  With ``e2e`` the input is read from the device
+        staging buffer ``x_dev`` and every layer's output is kept in ``outs`` for the host."""
         lay, cache, L = self.layer, self.cache, self.cfg.n_layers
-        if e2e:
-            self.x_dev.copy_(self.x_host[t], non_blocking=True)
-            x = self.x_dev
-        else:
-            x = self.xs[t]
+        x = self.x_dev if e2e else self.xs[t]
         for l in range(L):
             wr, b = self.routers[l]
             lay.route(x, wr, b)
@@ -224,17 +243,30 @@ class DecodeTrace:
                     ev.rec("expert_end")
             out = lay.combine(self.T, lay.ext, None)
             if e2e:
-                self.out_host[l].copy_(out, non_blocking=True)
+                self.outs[l].copy_(out, non_blocking=True)
+
+    def e2e_step(self, t, graph=None):
+        """Host input -> device, the step (graph replay or eager), every layer's output -> host."""
+        self.x_dev.copy_(self.x_host[t], non_blocking=True)
+        if graph is not None:
+            graph.replay()
+        else:
+            self.step(t, None, e2e=True)
+        self.out_host.copy_(self.outs, non_blocking=True)
 
 
 class EventLog:
-    """CUDA events recorded on the launching (current) stream, in order."""
+    """CUDA events recorded on the launching (current) stream, in order.
 
-    def __init__(self):
+    With ``external`` the events become event-record nodes when recorded under
+    graph capture, so each replay of the graph records them again."""
+
+    def __init__(self, external=False):
         self.ev = []
+        self.external = external
 
     def rec(self, tag):
-        e = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True, external=self.external)
         e.record()
         self.ev.append((tag, e))
 
@@ -472,14 +504,26 @@ def main():
     traces = [DecodeTrace(ft, cfg, T, pool, routers, n_steps, dev, not args.no_e2e) for T in batches]
     tokens_per_step = sum(batches)
 
+    log(f"pool of {n_phys} layers filled in {t_fill:.1f} s; link {link:.1f} GB/s")
     # warm-up (cold caches fill here, as they would in service)
     for t in range(args.warmup):
         for tr in traces:
             tr.step(t)
     torch.cuda.synchronize()
 
+    # each timed step is one CUDA graph per batch size (captured now, replayed once in the timed
+    # region); the graphs hold the same library calls as the eager warm-up steps
+    graphs = {}
+    log("warm-up done")
+    if not args.no_graphs:
+        for k in range(args.steps):
+            for tr in traces:
+                graphs[(tr.T, args.warmup + k)] = tr.capture(args.warmup + k)
+        torch.cuda.synchronize()
+
+    log(f"{len(graphs)} step graphs captured")
     # timed region
-    ev = EventLog()
+    logs = []
     tb = []
     barrier(world)
     torch.cuda.synchronize()
@@ -492,7 +536,13 @@ def main():
             e = torch.cuda.Event(enable_timing=True)
             e.record()
             tb.append((tr.T, e))
-            tr.step(t, ev)
+            if graphs:
+                g, ev = graphs[(tr.T, t)]
+                g.replay()
+            else:
+                ev = EventLog()
+                tr.step(t, ev)
+            logs.append(ev)
     e_end.record()
     torch.cuda.synchronize()
     barrier(world)
@@ -502,18 +552,20 @@ def main():
     tokens = sum_over_ranks(world, tokens_per_step * args.steps)
     value = tokens / (ms_max * 1e-3)
 
+    log(f"timed region: {ms:.1f} ms")
     # per-batch breakdown
     per_T = {T: 0.0 for T in batches}
     marks = tb + [(None, e_end)]
     for i in range(len(tb)):
         per_T[marks[i][0]] += marks[i][1].elapsed_time(marks[i + 1][1])
     # kernel spans
-    cache_ms = ev.spans("cache", "cache_end")
-    expert_ms = ev.spans("cache_end", "expert_end")
+    cache_ms = [v for ev in logs for v in ev.spans("cache", "cache_end")]
+    expert_ms = [v for ev in logs for v in ev.spans("cache_end", "expert_end")]
 
     # roofline over the timed layer steps
     roof_s, roof_detail = 0.0, {"hbm_bytes": 0.0, "link_bytes": 0.0, "flops": 0.0}
     per_T_roof = {}
+    hit_rate = {}
     fills_total, unique_total = 0, 0
     for tr in traces:
         h = tr.hist[args.warmup:args.warmup + args.steps].cpu().numpy()
@@ -524,6 +576,7 @@ def main():
             roof_detail[kk] += d[kk]
         fills_total += int(h[..., 2].sum())
         unique_total += int(h[..., 0].sum())
+        hit_rate[tr.T] = float(h[..., 1].sum() / max(h[..., 0].sum(), 1))
     layer_roofline_frac = roof_s / (ms * 1e-3)
 
     n_ls = len(cache_ms)
@@ -537,7 +590,7 @@ def main():
                  "algorithmic_bytes_per_launch": fill_bytes / max(n_ls, 1),
                  "avg_launch_ms": sum(cache_ms) / max(n_ls, 1),
                  "peak_source": "cudaMemcpyAsync pinned->device, measured in this run"}
-    roof_exp = {"kernel": "ft_expert_grouped (gate/up + down launches)", "bound": "hbm",
+    roof_exp = {"kernel": "ft_expert_grouped (row gather + tcgen05 gate/up + down launches)", "bound": "hbm",
                 "achieved": expert_hbm / expert_total_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": expert_hbm / expert_total_s / 1e9 / peaks["hbm_gbs"], "traffic": None,
                 "algorithmic_bytes_per_launch": expert_hbm / max(n_ls, 1),
@@ -545,17 +598,25 @@ def main():
                 "peak_source": f"MEASURED_PEAKS hbm_gbs ({peaks['source']})"}
     dominant = roof_fill if cache_total_s >= expert_total_s else roof_exp
 
-    # end to end through the public API with host buffers
+    # end to end through the public API with host buffers: every step copies its
+    # inputs from pinned host memory, runs (as a graph of device work only), and
+    # copies every layer's output back to pinned host memory
     e2e = None
     if not args.no_e2e:
+        egraphs = {}
+        if not args.no_graphs:
+            for k in range(args.steps):
+                for tr in traces:
+                    egraphs[(tr.T, k)] = tr.capture(args.warmup + args.steps + k, e2e=True, timed=False)[0]
         torch.cuda.synchronize()
+        log(f"{len(egraphs)} end-to-end step graphs captured")
         barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for k in range(args.steps):
             t = args.warmup + args.steps + k
             for tr in traces:
-                tr.step(t, None, e2e=True)
+                tr.e2e_step(t, egraphs.get((tr.T, k)))
         e1.record()
         torch.cuda.synchronize()
         barrier(world)
@@ -564,6 +625,12 @@ def main():
         d2h = sum(L * T * cfg.hidden * 4 for T in batches)
         e2e = {"value": tokens / (ms_e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
+    # the graphs reference the traces' buffers: release them before the traces go
+    del graphs, logs
+    if not args.no_e2e:
+        del egraphs
+    torch.cuda.synchronize()
+    log("decode legs done")
     derr = ft.ft_get_device_error()
     stats = {T: tr.cache.stats() for T, tr in zip(batches, traces)}
     launches = sum(tr.launches_per_step() for tr in traces) * args.steps
@@ -574,10 +641,12 @@ def main():
             tr.cache.destroy()
         del tr, traces
         torch.cuda.empty_cache()
+        log("prefill leg")
         prefill = prefill_leg(ft, cfg, pool, routers, dev, args.prefill_chunks, link, peaks)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        log("cpu baseline")
         layers = list(range(cfg.n_layers))
         rcpu = [tuple(t.cpu() for t in r) for r in routers]
         x1 = synth.AR1Trace(cfg, 1, dev, tag=1).next().cpu()
@@ -603,7 +672,7 @@ def main():
             "per_batch": {str(T): {"tokens_per_s": T * args.steps / (per_T[T] * 1e-3),
                                    "ms_per_step": per_T[T] / args.steps,
                                    "layer_roofline_frac": per_T_roof[T] / (per_T[T] * 1e-3),
-                                   "hit_rate": stats[T].hits / max(stats[T].hits + stats[T].fills, 1)}
+                                   "hit_rate": hit_rate[T]}
                           for T in batches},
             "roofline": dominant,
             "roofline_experts": roof_exp,
@@ -613,12 +682,13 @@ def main():
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,
+            "cuda_graphs": not args.no_graphs,
             "clocks": clocks,
             "prefill_8192": prefill,
             "device_error": derr,
             "pool_fill_s": t_fill,
         }
-        print(json.dumps(line))
+        print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

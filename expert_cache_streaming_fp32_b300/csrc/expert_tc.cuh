@@ -384,13 +384,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
 
 // ------------------------------------------------------------------ gather
 // Xp[p][:] = bf16(x[perm[p] / k][:]); 16 bytes of output per thread step.
+// Also clears the split counters of the decode kernels that follow it.
 template <typename XT>
 __global__ void __launch_bounds__(256)
 gather_rows_kernel(const XT* __restrict__ x, const int32_t* __restrict__ perm, int T, int k, int H, int n_rows,
-                   __nv_bfloat16* __restrict__ xp) {
+                   __nv_bfloat16* __restrict__ xp, int32_t* __restrict__ zero, int n_zero) {
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  for (long long i = tid; i < n_zero; i += (long long)gridDim.x * blockDim.x) zero[i] = 0;
   const int vpr = H / 8;  // 16-byte output vectors per row
   const long long n = (long long)n_rows * vpr;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+  for (long long i = tid; i < n; i += (long long)gridDim.x * blockDim.x) {
     const int p = (int)(i / vpr), v = (int)(i - (long long)p * vpr);
     const int t = perm[p] / k;
     uint4 o = make_uint4(0, 0, 0, 0);

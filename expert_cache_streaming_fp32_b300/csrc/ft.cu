@@ -4,13 +4,16 @@
 #include "route.cuh"
 #include "expert.cuh"
 #include "expert_tc.cuh"
+#include "expert_tc_decode.cuh"
 #include "cache.cuh"
 #include "stream.cuh"
 
 #include <cudaTypedefs.h>
 
+#include <map>
 #include <mutex>
 #include <new>
+#include <utility>
 
 using namespace ft;
 
@@ -28,10 +31,22 @@ int occupancy_grid(K kernel, int threads, size_t smem) {
   return per_sm * sms();
 }
 
+// Raises a kernel's dynamic shared-memory limit once per (device, kernel,
+// size), so that steady-state calls -- and calls under stream capture -- make
+// no attribute calls.
 template <typename K>
 int set_smem(K kernel, size_t smem) {
-  if (smem > 48 * 1024)
+  if (smem <= 48 * 1024) return FT_OK;
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, size_t> done;
+  int dev = 0;
+  FT_CHECK_CUDA(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lock(mu);
+  size_t& cur = done[{dev, reinterpret_cast<const void*>(kernel)}];
+  if (smem > cur) {
     FT_CHECK_CUDA(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    cur = smem;
+  }
   return FT_OK;
 }
 
@@ -104,23 +119,37 @@ FT_API int ft_router_logits(const void* x, int x_type, const void* w_router, con
   FT_REQUIRE(x_type == FT_X_F32 || x_type == FT_X_BF16);
   if (T == 0) return FT_OK;
   FT_REQUIRE(x && w_router && logits);
-  const size_t smem = (size_t)RL_RT * H * sizeof(float);
-  if (smem > 227 * 1024 || ceil_div(T, RL_RT) > 65535) return FT_EUNSUPPORTED;
-  const int chunks = ceil_div(T, RL_RT);
+  const int RT = T >= 8 ? 8 : T >= 4 ? 4 : T >= 2 ? 2 : 1;  // rows staged per CTA
+  const size_t smem = (size_t)RT * H * sizeof(float);
+  if (smem > 227 * 1024 || ceil_div(T, RT) > 65535) return FT_EUNSUPPORTED;
+  const int chunks = ceil_div(T, RT);
   const int groups = std::max(1, std::min(ceil_div(E, RL_WARPS), ceil_div(2 * sms(), chunks)));
   dim3 grid(groups, chunks);
+  cudaStream_t st = (cudaStream_t)s;
+  auto go = [&](auto kernel, const auto* xx, const auto* ww) -> int {
+    if (int r = set_smem(kernel, smem)) return r;
+    kernel<<<grid, RL_WARPS * 32, smem, st>>>(xx, ww, bias, T, H, E, logits);
+    FT_CHECK_LAUNCH();
+    return FT_OK;
+  };
   if (x_type == FT_X_BF16) {
-    auto k = router_logits_kernel<__nv_bfloat16>;
-    if (int st = set_smem(k, smem)) return st;
-    k<<<grid, RL_WARPS * 32, smem, (cudaStream_t)s>>>((const __nv_bfloat16*)x, (const __nv_bfloat16*)w_router, bias,
-                                                      T, H, E, logits);
-  } else {
-    auto k = router_logits_kernel<float>;
-    if (int st = set_smem(k, smem)) return st;
-    k<<<grid, RL_WARPS * 32, smem, (cudaStream_t)s>>>((const float*)x, (const float*)w_router, bias, T, H, E, logits);
+    const auto* xx = (const __nv_bfloat16*)x;
+    const auto* ww = (const __nv_bfloat16*)w_router;
+    switch (RT) {
+      case 1: return go(router_logits_kernel<__nv_bfloat16, 1>, xx, ww);
+      case 2: return go(router_logits_kernel<__nv_bfloat16, 2>, xx, ww);
+      case 4: return go(router_logits_kernel<__nv_bfloat16, 4>, xx, ww);
+      default: return go(router_logits_kernel<__nv_bfloat16, 8>, xx, ww);
+    }
   }
-  FT_CHECK_LAUNCH();
-  return FT_OK;
+  const auto* xx = (const float*)x;
+  const auto* ww = (const float*)w_router;
+  switch (RT) {
+    case 1: return go(router_logits_kernel<float, 1>, xx, ww);
+    case 2: return go(router_logits_kernel<float, 2>, xx, ww);
+    case 4: return go(router_logits_kernel<float, 4>, xx, ww);
+    default: return go(router_logits_kernel<float, 8>, xx, ww);
+  }
 }
 
 // ------------------------------------------------------------------ route
@@ -164,9 +193,10 @@ FT_API int ft_combine(const float* y, const int32_t* inv, const int32_t* topk_id
   FT_REQUIRE(T >= 0 && k >= 1 && H > 0 && H % 4 == 0 && E >= 1);
   if (T == 0) return FT_OK;
   FT_REQUIRE(y && inv && topk_idx && topk_w && out);
-  FT_REQUIRE(T <= 65535);
-  dim3 grid(ceil_div(H / 4, 256), T);
-  combine_kernel<<<grid, 256, 0, (cudaStream_t)s>>>(y, inv, topk_idx, topk_w, ext_flags, ext_partial, T, k, H, E, out);
+  FT_REQUIRE(T <= 65535 && k <= RT_MAXK);
+  dim3 grid(ceil_div(H / 4, CB_THREADS), T);
+  combine_kernel<<<grid, CB_THREADS, 0, (cudaStream_t)s>>>(y, inv, topk_idx, topk_w, ext_flags, ext_partial, T, k, H, E,
+                                                            out);
   FT_CHECK_LAUNCH();
   return FT_OK;
 }
@@ -176,10 +206,55 @@ static size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 // Workspace of the CUDA-core path: the fp32 intermediate [T*k][I].
 static size_t ws_cuda_core(long long Tk, int inter) { return align256((size_t)Tk * inter * sizeof(float)); }
-// Workspace of the tensor-core path: gathered bf16 rows [T*k][H], then the bf16 intermediate [T*k][I].
-static size_t ws_tensor_core(long long Tk, int hidden, int inter) {
-  return align256((size_t)Tk * hidden * 2) + align256((size_t)Tk * inter * 2);
+// Small-batch tensor-core tiling: K splits so that about one wave of tiles
+// covers the SMs when a step has few experts (U <= T*k experts are routed).
+static constexpr int kSplitTargetTiles = 148;
+static int sk_splits(long long Tk, int n_mt, int K) {
+  const long long est = std::min<long long>(Tk, 256) * n_mt;
+  int ks = 1;
+  while (ks < tc::SK_MAX_SPLITS && est * ks * 2 <= kSplitTargetTiles && (K / (ks * 2)) % tc::BK == 0 &&
+         K / (ks * 2) >= 4 * tc::BK)
+    ks *= 2;
+  return ks;
 }
+// Upper bound of the tile groups (weight-row tile x token chunk) of one launch.
+static long long sk_groups(long long Tk, int n_mt) { return (long long)n_mt * (Tk + Tk / tc::SK_NB + 1); }
+
+// Workspace of the tensor-core path: gathered bf16 rows [T*k][H], the bf16
+// intermediate [T*k][I], the split counters and the split partials of the
+// small-batch kernels.  Every region grows (or stays) with T*k, so a
+// workspace sized for a batch also serves every smaller batch.
+struct TcWorkspace {
+  size_t off_aint, off_counters, off_part, bytes;
+  int ks_gu, ks_dn;
+  long long g_gu, g_dn;
+};
+static TcWorkspace tc_workspace(long long Tk, int hidden, int inter) {
+  TcWorkspace w{};
+  const int mt_gu = tc::sk_m_tiles(tc::GATEUP, hidden, inter), mt_dn = tc::sk_m_tiles(tc::DOWN, hidden, inter);
+  w.off_aint = align256((size_t)Tk * hidden * 2);
+  size_t o = w.off_aint + align256((size_t)Tk * inter * 2);
+  const long long Tk_small = std::min<long long>(Tk, FT_TC_WIDE_ASSIGNMENTS - 1);
+  w.ks_gu = Tk < FT_TC_WIDE_ASSIGNMENTS ? sk_splits(Tk, mt_gu, hidden) : 1;
+  w.ks_dn = Tk < FT_TC_WIDE_ASSIGNMENTS ? sk_splits(Tk, mt_dn, inter) : 1;
+  w.g_gu = sk_groups(Tk_small, mt_gu);
+  w.g_dn = sk_groups(Tk_small, mt_dn);
+  w.off_counters = o;
+  o += align256((size_t)(w.g_gu + w.g_dn) * 4);
+  w.off_part = o;
+  // splits happen only while an estimated wave of tiles is short, i.e. for
+  // T*k up to kSplitTargetTiles: size the partials for the largest need there
+  long long pg = 0;
+  for (long long t = 1; t <= std::min<long long>(Tk, kSplitTargetTiles); ++t) {
+    const int kg = sk_splits(t, mt_gu, hidden), kd = sk_splits(t, mt_dn, inter);
+    if (kg > 1) pg = std::max(pg, sk_groups(t, mt_gu) * kg);
+    if (kd > 1) pg = std::max(pg, sk_groups(t, mt_dn) * kd);
+  }
+  o += align256((size_t)pg * tc::SK_MR * tc::SK_NB * 4);
+  w.bytes = o;
+  return w;
+}
+static size_t ws_tensor_core(long long Tk, int hidden, int inter) { return tc_workspace(Tk, hidden, inter).bytes; }
 
 // Enough for either path (the weight format, which picks the path, is not an argument here).
 FT_API size_t ft_expert_grouped_workspace(int T, int k, int hidden, int inter) {
@@ -270,22 +345,74 @@ int launch_tc_gemms(const CUtensorMap& mx, const CUtensorMap& mg, const CUtensor
   return FT_OK;
 }
 
+// Small batches: weights on the MMA's M side, token rows on N, K split when few experts are routed.
+int launch_expert_skinny(const ExpertArgs& ea, const ft_expert_layout& L, const TcWorkspace& w, uint8_t* ws,
+                         cudaStream_t st) {
+  const long long Tk = (long long)ea.T * ea.k;
+  const int H = ea.H, I = ea.I;
+  __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(ws);
+  __nv_bfloat16* aint = reinterpret_cast<__nv_bfloat16*>(ws + w.off_aint);
+  const int nb_box = (int)std::min<long long>(tc::SK_NB, (Tk + 15) / 16 * 16);
+  CUtensorMap mg, mu, md, mx, ma;
+  {
+    const uint8_t* pool = ea.pool;
+    const uint64_t dw[3] = {(uint64_t)H, (uint64_t)I, (uint64_t)ea.pool_slots}, sw[2] = {(uint64_t)H * 2, ea.S};
+    const uint64_t dd[3] = {(uint64_t)I, (uint64_t)H, (uint64_t)ea.pool_slots}, sd[2] = {(uint64_t)I * 2, ea.S};
+    const uint64_t dx[2] = {(uint64_t)H, (uint64_t)Tk}, sx[1] = {(uint64_t)H * 2};
+    const uint64_t da[2] = {(uint64_t)I, (uint64_t)Tk}, sa[1] = {(uint64_t)I * 2};
+    int r = make_map_bf16(&mg, pool + L.off_val[0], 3, dw, sw, 64);
+    if (!r) r = make_map_bf16(&mu, pool + L.off_val[1], 3, dw, sw, 64);
+    if (!r) r = make_map_bf16(&md, pool + L.off_val[2], 3, dd, sd, tc::SK_MR);
+    if (!r) r = make_map_bf16(&mx, xp, 2, dx, sx, nb_box);
+    if (!r) r = make_map_bf16(&ma, aint, 2, da, sa, nb_box);
+    if (r) return r;
+  }
+  tc::SkArgs a;
+  a.T = ea.T; a.k = ea.k; a.H = H; a.I = I; a.E = ea.E; a.pool_slots = ea.pool_slots;
+  a.nb_box = nb_box;
+  a.offsets = ea.offsets; a.slot_of = ea.slot_of;
+  a.Aint = aint; a.y = ea.y;
+  a.part = reinterpret_cast<float*>(ws + w.off_part);
+  int32_t* counters = reinterpret_cast<int32_t*>(ws + w.off_counters);
+  const size_t smem = tc::sk_smem_bytes(ea.E);
+  auto kg = tc::skinny_gemm_kernel<tc::GATEUP>;
+  auto kd = tc::skinny_gemm_kernel<tc::DOWN>;
+  if (int s = set_smem(kg, smem)) return s;
+  if (int s = set_smem(kd, smem)) return s;
+  a.KS = w.ks_gu;
+  a.counters = counters;
+  kg<<<sms(), tc::THREADS, smem, st>>>(mg, mu, mx, a);
+  FT_CHECK_LAUNCH();
+  a.KS = w.ks_dn;
+  a.counters = counters + w.g_gu;
+  kd<<<sms(), tc::THREADS, smem, st>>>(md, md, ma, a);
+  FT_CHECK_LAUNCH();
+  return FT_OK;
+}
+
 int launch_expert_tc(const ExpertArgs& ea, const ft_expert_layout& L, void* workspace, cudaStream_t st) {
   const long long Tk = (long long)ea.T * ea.k;
   const int H = ea.H, I = ea.I;
-  __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(workspace);
-  __nv_bfloat16* aint = reinterpret_cast<__nv_bfloat16*>((uint8_t*)workspace + align256((size_t)Tk * H * 2));
-  // gather the permuted rows (bf16)
+  const TcWorkspace w = tc_workspace(Tk, H, I);
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(ws);
+  __nv_bfloat16* aint = reinterpret_cast<__nv_bfloat16*>(ws + w.off_aint);
+  const bool skinny = Tk < FT_TC_WIDE_ASSIGNMENTS;
+  // gather the permuted rows (bf16); clear the split counters of the small-batch kernels
   {
     const long long vecs = Tk * (H / 8);
     const int grid = (int)std::min<long long>(ceil_div((int)std::min<long long>(vecs, 1ll << 30), 256), 8 * sms());
+    int32_t* zero = skinny ? reinterpret_cast<int32_t*>(ws + w.off_counters) : nullptr;
+    const int n_zero = skinny ? (int)(w.g_gu + w.g_dn) : 0;
     if (ea.x_type == FT_X_BF16)
       tc::gather_rows_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)ea.x, ea.perm, ea.T, ea.k, H,
-                                                                  (int)Tk, xp);
+                                                                  (int)Tk, xp, zero, n_zero);
     else
-      tc::gather_rows_kernel<float><<<grid, 256, 0, st>>>((const float*)ea.x, ea.perm, ea.T, ea.k, H, (int)Tk, xp);
+      tc::gather_rows_kernel<float><<<grid, 256, 0, st>>>((const float*)ea.x, ea.perm, ea.T, ea.k, H, (int)Tk, xp,
+                                                          zero, n_zero);
     FT_CHECK_LAUNCH();
   }
+  if (skinny) return launch_expert_skinny(ea, L, w, ws, st);
   CUtensorMap mx, mg, mu, ma, md;
   const uint8_t* pool = ea.pool;
   const int BN = (Tk >= FT_TC_WIDE_ASSIGNMENTS && H % 256 == 0) ? 256 : 128;

@@ -12,7 +12,7 @@ namespace ft {
 // partials are reduced with one reduce-scatter.  Few row chunks (decode) get
 // many expert groups, so the router matrix is read in parallel even for one
 // token; many row chunks (prefill) get few groups, so x is staged few times.
-constexpr int RL_RT = 8;        // token rows per CTA
+constexpr int RL_RT = 8;        // token rows per CTA (at most)
 constexpr int RL_WARPS = 8;
 
 template <typename XT>
@@ -32,39 +32,55 @@ __device__ __forceinline__ void load8<float>(const float* p, float (&o)[8]) {
   o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
 }
 
-template <typename XT>
+template <typename XT, int RT>
 __global__ void __launch_bounds__(RL_WARPS * 32)
 router_logits_kernel(const XT* __restrict__ x, const XT* __restrict__ wr, const float* __restrict__ bias,
                      int T, int H, int E, float* __restrict__ z) {
-  extern __shared__ float xs[];  // [RL_RT][H]
-  const int t0 = blockIdx.y * RL_RT;
-  const int nrows = min(RL_RT, T - t0);
-  for (int i = threadIdx.x; i < RL_RT * H; i += blockDim.x) {
+  extern __shared__ float xs[];  // [RT][H]
+  const int t0 = blockIdx.y * RT;
+  const int nrows = min(RT, T - t0);
+  for (int i = threadIdx.x; i < RT * H; i += blockDim.x) {
     int r = i / H, h = i - r * H;
     xs[i] = r < nrows ? (float)x[(size_t)(t0 + r) * H + h] : 0.0f;
   }
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int U = 8;  // 256-element chunks whose weight loads are in flight together
   for (int e = blockIdx.x * RL_WARPS + warp; e < E; e += gridDim.x * RL_WARPS) {
-    float acc[RL_RT];
+    float acc[RT];
 #pragma unroll
-    for (int r = 0; r < RL_RT; ++r) acc[r] = 0.0f;
+    for (int r = 0; r < RT; ++r) acc[r] = 0.0f;
     const XT* w = wr + (size_t)e * H;
-    for (int k = lane * 8; k < H; k += 256) {
-      float wv[8];
-      load8<XT>(w + k, wv);
+    for (int k0 = 0; k0 < H; k0 += 256 * U) {
+      float wv[U][8];
 #pragma unroll
-      for (int r = 0; r < RL_RT; ++r) {
-        const float* xr = xs + r * H + k;
-        float4 a = *reinterpret_cast<const float4*>(xr);
-        float4 b = *reinterpret_cast<const float4*>(xr + 4);
-        acc[r] += wv[0] * a.x + wv[1] * a.y + wv[2] * a.z + wv[3] * a.w +
-                  wv[4] * b.x + wv[5] * b.y + wv[6] * b.z + wv[7] * b.w;
+      for (int u = 0; u < U; ++u) {
+        const int k = k0 + u * 256 + lane * 8;
+        if (k < H) {
+          load8<XT>(w + k, wv[u]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) wv[u][i] = 0.0f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int k = k0 + u * 256 + lane * 8;
+        if (k < H) {
+#pragma unroll
+          for (int r = 0; r < RT; ++r) {
+            const float* xr = xs + r * H + k;
+            float4 a = *reinterpret_cast<const float4*>(xr);
+            float4 b = *reinterpret_cast<const float4*>(xr + 4);
+            acc[r] += wv[u][0] * a.x + wv[u][1] * a.y + wv[u][2] * a.z + wv[u][3] * a.w +
+                      wv[u][4] * b.x + wv[u][5] * b.y + wv[u][6] * b.z + wv[u][7] * b.w;
+          }
+        }
       }
     }
-    warp_reduce_scatter<RL_RT>(acc, lane);
-    const int r = lane / (32 / RL_RT);
-    if ((lane % (32 / RL_RT)) == 0 && r < nrows)
+    warp_reduce_scatter<RT>(acc, lane);
+    const int r = lane / (32 / RT);
+    if ((lane % (32 / RT)) == 0 && r < nrows)
       z[(size_t)(t0 + r) * E + e] = acc[0] + (bias ? bias[e] : 0.0f);
   }
 }
@@ -248,27 +264,48 @@ permute_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __restric
 
 // ====================================================================== combine
 // out[t][h] = sum_j w[t][j] y[inv[t*k+j]][h] (+ P[t][h]); assignments of
-// experts flagged external are skipped.  One CTA row-block per token, float4
-// per thread; the sum order is fixed (j ascending, then P).
-__global__ void __launch_bounds__(256)
+// experts flagged external are skipped.  CB threads per CTA cover CB float4
+// columns of one token; every assignment's index loads are issued before the
+// row loads, so a token costs two dependent memory round trips.  The sum order
+// is fixed (j ascending, then P).
+constexpr int CB_THREADS = 64;
+
+__global__ void __launch_bounds__(CB_THREADS)
 combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv, const int32_t* __restrict__ idx,
                const float* __restrict__ w, const int32_t* __restrict__ ext, const float* __restrict__ P,
                int T, int k, int H, int E, float* __restrict__ out) {
   const int t = blockIdx.y;
   const int h4 = blockIdx.x * blockDim.x + threadIdx.x;
   if (h4 * 4 >= H) return;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   const int nrows = T * k;
-  for (int j = 0; j < k; ++j) {
-    const int a = t * k + j;
-    const int e = idx[a];
-    if ((unsigned)e >= (unsigned)E) { record_error(FT_DERR_EXPERT_INDEX); continue; }
-    if (ext && ext[e]) continue;
-    const int row = inv[a];
-    if ((unsigned)row >= (unsigned)nrows) { record_error(FT_DERR_ROW_INDEX); continue; }
-    const float wj = w[a];
-    float4 v = reinterpret_cast<const float4*>(y + (size_t)row * H)[h4];
-    acc.x += wj * v.x; acc.y += wj * v.y; acc.z += wj * v.z; acc.w += wj * v.w;
+  int row[RT_MAXK];
+  float wj[RT_MAXK];
+#pragma unroll
+  for (int j = 0; j < RT_MAXK; ++j) {
+    row[j] = -1;
+    wj[j] = 0.0f;
+    if (j < k) {
+      const int a = t * k + j;
+      const int e = idx[a];
+      const int rr = inv[a];
+      if ((unsigned)e >= (unsigned)E) {
+        record_error(FT_DERR_EXPERT_INDEX);
+      } else if (!(ext && ext[e])) {
+        if ((unsigned)rr >= (unsigned)nrows) record_error(FT_DERR_ROW_INDEX);
+        else { row[j] = rr; wj[j] = w[a]; }
+      }
+    }
+  }
+  float4 v[RT_MAXK];
+#pragma unroll
+  for (int j = 0; j < RT_MAXK; ++j)
+    if (row[j] >= 0) v[j] = reinterpret_cast<const float4*>(y + (size_t)row[j] * H)[h4];
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < RT_MAXK; ++j) {
+    if (row[j] >= 0) {
+      acc.x += wj[j] * v[j].x; acc.y += wj[j] * v[j].y; acc.z += wj[j] * v[j].z; acc.w += wj[j] * v[j].w;
+    }
   }
   if (P) {
     float4 p = reinterpret_cast<const float4*>(P + (size_t)t * H)[h4];

@@ -321,7 +321,7 @@ int ft_expert_grouped_noalloc(const void* x, int x_type, int T, int k, int hidde
  *   ext_flags   dev [E] int32 or NULL (no assignment skipped)
  *   ext_partial dev [T][H] fp32 or NULL
  *   out         dev [T][H] fp32 (written)
- * H a multiple of 4.
+ * H a multiple of 4, 1 <= k <= 16.
  * ---------------------------------------------------------------------- */
 int ft_combine(const float* y, const int32_t* inv, const int32_t* topk_idx, const float* topk_w,
                const int32_t* ext_flags, const float* ext_partial, int T, int k, int H, int E,

@@ -5,8 +5,10 @@ bf16 and the intermediate silu(G)*U is rounded to bf16 before the down
 product.  The oracle applies the same two roundings (x is already bf16 here;
 the intermediate goes through formats.round_to_bf16), and the bar is the
 tensor-core one: relative Frobenius error <= 1e-2, max |err| <= 2e-2 * max |ref|.
-Batches below FT_TC_WIDE_ASSIGNMENTS use 128-column weight tiles, larger ones
-256-column tiles; both are covered.
+Batches below FT_TC_WIDE_ASSIGNMENTS use the small-batch tiling (weights on
+the MMA's M side, up to 64 token rows on N, K split when few experts are
+routed), larger ones 256-column weight tiles against 128-row token tiles; both
+are covered, including split and multi-chunk cases.
 """
 import numpy as np
 import pytest
@@ -71,6 +73,9 @@ def _run(ft, x, k, I, E, perm, offsets, slot_of, pool, S, n_slots):
     (2048, 512, 64, 8, 16, 6, True),      # decode batch of 16, skewed
     (256, 128, 8, 2, 3, 7, False),        # tiny: H = 256, I = 128
     (4096, 256, 16, 6, 40, 8, False),     # wide hidden, narrow intermediate
+    (4096, 512, 16, 4, 1, 10, False),     # one token, 4 experts: gate/up K split 4 ways
+    (256, 2048, 8, 2, 1, 11, False),      # one token, 2 experts: down K split 4 ways
+    (512, 256, 2, 2, 100, 12, False),     # 100 rows per expert: two token chunks on the small-batch tiling
 ])
 def test_tc_expert_grouped_parity(ft, H, I, E, k, T, seed, skewed):
     cfg, L, S, n_slots, pool, slot_perm, comps, x, idx = _setup(ft, H, I, E, k, T, seed, skewed)
@@ -98,8 +103,8 @@ def test_tc_expert_grouped_parity(ft, H, I, E, k, T, seed, skewed):
     assert rel_fro(got, ref) < 2e-3
 
 
-def test_tc_both_tile_widths(ft):
-    """T*k just below FT_TC_WIDE_ASSIGNMENTS (128-column tiles) and at it (256-column tiles)."""
+def test_tc_both_tilings(ft):
+    """T*k just below FT_TC_WIDE_ASSIGNMENTS (small-batch tiling) and at it (large-batch tiling)."""
     H, I, E, k = 512, 256, 8, 8
     T_narrow, T_wide = TC_WIDE // k - 1, TC_WIDE // k
     cfg, L, S, n_slots, pool, slot_perm, comps, x, idx = _setup(ft, H, I, E, k, T_wide, 9)
@@ -149,3 +154,13 @@ def test_tc_empty_experts_and_all_rows_on_one_expert(ft):
                                          act_round=formats.round_to_bf16) for e in range(k)])
     assert_close_layer(Y, ref, fro=1e-2)
     assert rel_fro(Y, ref) < 2e-3
+
+
+def test_tc_split_k_is_deterministic(ft):
+    """A one-token step whose K is split: repeated calls give bitwise equal outputs."""
+    H, I, E, k, T = 4096, 512, 16, 4, 1
+    cfg, L, S, n_slots, pool, slot_perm, comps, x, idx = _setup(ft, H, I, E, k, T, 14)
+    counts, offsets, perm, inv = moe.permute(idx, E)
+    so = slot_perm.astype(np.int32)
+    Y = [_run(ft, x, k, I, E, perm, offsets, so, pool, S, n_slots) for _ in range(3)]
+    assert np.array_equal(Y[0], Y[1]) and np.array_equal(Y[0], Y[2])

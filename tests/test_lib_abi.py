@@ -76,3 +76,15 @@ def test_invalid_arguments_rejected_before_launch(ftlib):
     assert lib.ft_expert_grouped(None, 1, 4, 2, 2048, 512, 16, 7, None, None, None, None, 0, 1, None, None, 0, s) \
         == ftlib.FT_EINVAL
     assert ftlib.ft_status_str(ftlib.FT_ESTATE) == "call not allowed in this state"
+
+
+def test_expert_workspace_grows_with_the_batch(ftlib):
+    """A workspace sized for a batch also serves every smaller batch (one buffer per layer object)."""
+    lib = ftlib.lib()
+    for H, I, k in ((2048, 512, 8), (512, 256, 4), (4096, 2048, 6), (6144, 2048, 8), (256, 128, 2)):
+        prev = 0
+        for T in list(range(1, 300)) + [511, 512, 1024, 2047, 2048, 4096, 8192]:
+            w = lib.ft_expert_grouped_workspace(T, k, H, I)
+            assert w >= prev, (H, I, k, T)
+            assert w % 256 == 0
+            prev = w
