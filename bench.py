@@ -52,6 +52,7 @@ def parse():
     p.add_argument("--kernel-case", default="", choices=["", "experts_decode", "experts_prefill"],
                    help="time one expert-kernel case on a small resident pool (profiling aid; prints its own line)")
     p.add_argument("--reps", type=int, default=5)
+    p.add_argument("--case-config", default="", help="workload of --kernel-case (a synth config name)")
     return p.parse_args()
 
 
@@ -438,6 +439,8 @@ def kernel_case(args):
     dev = "cuda:0"
     torch.cuda.set_device(0)
     cfg = synth.DECODE_BF16 if args.kernel_case == "experts_decode" else synth.PREFILL_BF16
+    if args.case_config:
+        cfg = synth.CONFIGS[args.case_config]
     T = int(args.batches.split(",")[0]) if args.kernel_case == "experts_decode" else 8192
     E, k, H, I = cfg.n_experts, cfg.top_k, cfg.hidden, cfg.inter
     lay = ft.ft_expert_layout_get(cfg.wtype, H, I)
@@ -465,7 +468,7 @@ def kernel_case(args):
     wbytes = U * int(lay.payload_bytes)
     flops = 2.0 * T * k * 3 * H * I
     peaks = load_peaks()
-    print(json.dumps({"kernel_case": args.kernel_case, "T": T, "unique_experts": U, "ms": ms,
+    print(json.dumps({"kernel_case": args.kernel_case, "config": cfg.name, "T": T, "unique_experts": U, "ms": ms,
                       "weight_gbs": wbytes / (ms * 1e-3) / 1e9, "hbm_frac": wbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                       "tflops": flops / (ms * 1e-3) / 1e12, "bf16_frac": flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
                       "device_error": ft.ft_get_device_error()}))

@@ -50,28 +50,118 @@ constexpr int MAX_E = 1024;
 
 enum Mode { GATEUP = 0, DOWN = 1 };
 
-template <int BN>
+constexpr int LUT_BYTES = 256 * 4 + 256 * 2;  // e2m1 byte -> bf16x2, e4m3 byte -> bf16
+
+__host__ __device__ constexpr bool is_fp4(int wt) { return wt == FT_W_NVFP4 || wt == FT_W_MXFP4; }
+
+// Threads that expand FP4 rows: two per 128-row tile row (32 elements each).
+constexpr int CVT_THREADS = 256;
+// Stages of block scales a converter thread keeps in flight ahead of use.
+constexpr int SCALE_AHEAD = 8;
+
+// bf16 weights: TMA writes the swizzled B tile.  NVFP4 / MXFP4: TMA stages
+// the packed rows (32 bytes per row per stage) and eight more warps expand them.
+template <int BN, int WT = FT_W_BF16>
 struct Cfg {
   static_assert(BN == 128 || BN == 256, "UMMA N");
+  static constexpr bool FP4 = is_fp4(WT);
+  static_assert(!FP4 || BN == 128, "FP4 expansion covers 128-row weight tiles");
+  static constexpr int THREADS = FP4 ? 192 + CVT_THREADS : 192;
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = STAGE_BUDGET / STAGE_BYTES;  // 4 (BN 256) or 6 (BN 128)
+  static constexpr int RAW_BYTES = FP4 ? BN * BK / 2 : 0;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + RAW_BYTES;
+  static constexpr int STAGES = STAGE_BUDGET / STAGE_BYTES;  // bf16: 4 (BN 256) or 6 (BN 128); fp4 BN 128: 5
   static constexpr int ACC_COLS = BN;                        // fp32 columns per accumulator
   static constexpr int TMEM_COLS = 2 * ACC_COLS;             // double-buffered accumulators
 };
 
 // Bytes of dynamic shared memory: 1 KiB alignment slack, the stages, the
-// barriers, the epilogue transpose buffers, then the expert list.
-template <int BN>
+// barriers, the epilogue transpose buffers, the FP4 tables, then the expert list.
+template <int BN, int WT = FT_W_BF16>
 __host__ __device__ constexpr size_t smem_bytes(int E) {
-  return 1024 + (size_t)Cfg<BN>::STAGES * Cfg<BN>::STAGE_BYTES + 256 + EPI_BYTES + (size_t)(2 * E + 2) * 4;
+  return 1024 + (size_t)Cfg<BN, WT>::STAGES * Cfg<BN, WT>::STAGE_BYTES + 256 + EPI_BYTES + LUT_BYTES +
+         (size_t)(2 * E + 2) * 4;
 }
+
+// ------------------------------------------------------------------ FP4 expansion
+// bf16 bits of an E8M0 scale 2^(b - 127) (b = 0 is the bf16 subnormal 2^-127).
+__device__ __forceinline__ uint32_t e8m0_bf16_bits(uint32_t b) { return b ? (b << 7) : 0x0040u; }
+
+// Tables: byte of two e2m1 codes (first element in the low nibble) -> bf16x2;
+// e4m3 byte -> bf16.  Every entry is exact.
+__device__ __forceinline__ void fill_fp4_tables(uint32_t* lut_e2m1, uint16_t* lut_e4m3, int nthreads) {
+  for (int i = threadIdx.x; i < 256; i += nthreads) {
+    const float2 f = e2m1x2_to_float2((uint8_t)i);
+    __nv_bfloat162 h = __floats2bfloat162_rn(f.x, f.y);
+    lut_e2m1[i] = *reinterpret_cast<uint32_t*>(&h);
+    __nv_bfloat16 b = __float2bfloat16_rn(e4m3_to_float((uint8_t)i));
+    lut_e4m3[i] = *reinterpret_cast<uint16_t*>(&b);
+  }
+}
+
+// Block scales of half a row's 64 elements at K offset kc (half = 0: elements
+// 0..31, 1: 32..63): 2 e4m3 bytes (NVFP4, blocks of 16) or 1 E8M0 byte (MXFP4,
+// blocks of 32).
+template <int WT>
+__device__ __forceinline__ uint32_t load_fp4_scales(const uint8_t* scale_row, int kc, int half) {
+  if (WT == FT_W_NVFP4) return __ldg(reinterpret_cast<const uint16_t*>(scale_row + kc / 16 + 2 * half));
+  return __ldg(scale_row + kc / 32 + half);
+}
+
+// Half a row (32 elements): 16 packed bytes -> 32 bf16 (value x block scale,
+// exact) written as 4 16-byte chunks into a 128-byte-swizzled row.
+template <int WT>
+__device__ __forceinline__ void expand_fp4_half(const unsigned char* raw_row, int half, uint32_t sc,
+                                                const uint32_t* lut_e2m1, const uint16_t* lut_e4m3,
+                                                unsigned char* dst_row, int row) {
+  const uint4 p = reinterpret_cast<const uint4*>(raw_row)[half];
+  const uint32_t packed[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {  // 8 elements (one 16-byte chunk) per step
+    const int j = half * 4 + jj;
+    uint32_t sbits;
+    if (WT == FT_W_NVFP4) sbits = lut_e4m3[(sc >> (8 * (jj >> 1))) & 0xff];
+    else sbits = e8m0_bf16_bits(sc & 0xff);
+    const uint32_t s2 = sbits | (sbits << 16);
+    const __nv_bfloat162 sv = *reinterpret_cast<const __nv_bfloat162*>(&s2);
+    uint32_t o[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t v = lut_e2m1[(packed[jj] >> (8 * b)) & 0xff];
+      __nv_bfloat162 w = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&v), sv);
+      o[b] = *reinterpret_cast<uint32_t*>(&w);
+    }
+    *reinterpret_cast<uint4*>(dst_row + ((j ^ (row & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Ring of block scales loaded SCALE_AHEAD stages before they are needed, so
+// their memory latency stays off the per-stage critical path.
+template <int WT>
+struct ScaleRing {
+  uint32_t v[SCALE_AHEAD];
+  __device__ __forceinline__ void start(const uint8_t* row, int kbase, int nk, int half) {
+#pragma unroll
+    for (int i = 0; i < SCALE_AHEAD; ++i) v[i] = i < nk ? load_fp4_scales<WT>(row, kbase + i * BK, half) : 0u;
+  }
+  // scales of stage ks; loads those of stage ks + SCALE_AHEAD
+  __device__ __forceinline__ uint32_t next(const uint8_t* row, int kbase, int nk, int ks, int half) {
+    const uint32_t cur = v[0];
+#pragma unroll
+    for (int i = 0; i < SCALE_AHEAD - 1; ++i) v[i] = v[i + 1];
+    const int kn = ks + SCALE_AHEAD;
+    v[SCALE_AHEAD - 1] = kn < nk ? load_fp4_scales<WT>(row, kbase + kn * BK, half) : 0u;
+    return cur;
+  }
+};
 
 struct Args {
   int T, k, H, I, E, pool_slots;
   const int32_t* offsets;
   const int32_t* slot_of;
-  const float* gscale_base;  // NVFP4: record base for the fp32 matrix scales (unused for bf16)
+  const uint8_t* pool;       // slot pool (block and matrix scales of the FP4 formats)
+  uint64_t off_scale[3];
+  uint64_t off_gscale;
   uint64_t S;
   __nv_bfloat16* Aint;       // [T*k][I]
   float* y;                  // [T*k][H]
@@ -80,6 +170,8 @@ struct Args {
 // ------------------------------------------------------------------ expert list
 // act_e[i] = i-th evaluated expert (rows > 0, valid slot) in ascending id;
 // act_pref[i] = its first tile index; act_pref[n_act] = total tiles.
+// Exclusive scan over the NW warps of the block; buf holds NW ints.
+template <int NW = WARPS>
 __device__ __forceinline__ int block_scan6(int v, int* buf, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = v;
@@ -92,7 +184,7 @@ __device__ __forceinline__ int block_scan6(int v, int* buf, int& total) {
   __syncthreads();
   int before = 0, tot = 0;
 #pragma unroll
-  for (int w = 0; w < WARPS; ++w) {
+  for (int w = 0; w < NW; ++w) {
     const int b = buf[w];
     before += w < warp ? b : 0;
     tot += b;
@@ -102,8 +194,9 @@ __device__ __forceinline__ int block_scan6(int v, int* buf, int& total) {
   return before + incl - v;
 }
 
+template <int NTHREADS>
 __device__ int build_tiles(const Args& a, int n_tiles_n, int* act_e, int* act_pref, int* buf, int& n_act) {
-  const int per = ceil_div(a.E, THREADS);
+  const int per = ceil_div(a.E, NTHREADS);
   const int e0 = threadIdx.x * per;
   int my_act = 0, my_tiles = 0;
   for (int i = 0; i < per; ++i) {
@@ -122,8 +215,8 @@ __device__ int build_tiles(const Args& a, int n_tiles_n, int* act_e, int* act_pr
     }
   }
   int total;
-  int pos = block_scan6(my_act, buf, n_act);
-  int tpos = block_scan6(my_tiles, buf, total);
+  int pos = block_scan6<NTHREADS / 32>(my_act, buf, n_act);
+  int tpos = block_scan6<NTHREADS / 32>(my_tiles, buf, total);
   for (int i = 0; i < per; ++i) {
     const int e = e0 + i;
     if (e < a.E) {
@@ -169,29 +262,35 @@ __device__ __forceinline__ Tile decode_tile(const Args& a, const int* act_e, con
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int MODE, int BN>
-__global__ void __launch_bounds__(THREADS, 1)
+template <int MODE, int BN, int WT>
+__global__ void __launch_bounds__(Cfg<BN, WT>::THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                     const __grid_constant__ CUtensorMap map_b1, Args a) {
   using namespace sm100;
-  constexpr int STAGES = Cfg<BN>::STAGES;
-  constexpr int STAGE_BYTES = Cfg<BN>::STAGE_BYTES;
-  constexpr int B_BYTES = Cfg<BN>::B_BYTES;
-  constexpr int ACC_COLS = Cfg<BN>::ACC_COLS;
-  constexpr int TMEM_COLS = Cfg<BN>::TMEM_COLS;
+  using C = Cfg<BN, WT>;
+  constexpr bool FP4 = C::FP4;
+  constexpr int STAGES = C::STAGES;
+  constexpr int STAGE_BYTES = C::STAGE_BYTES;
+  constexpr int B_BYTES = C::B_BYTES;
+  constexpr int RAW_BYTES = C::RAW_BYTES;
+  constexpr int ACC_COLS = C::ACC_COLS;
+  constexpr int TMEM_COLS = C::TMEM_COLS;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1 KiB-aligned stage buffers (the 128-byte swizzle pattern repeats every 1 KiB)
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t pad = (1024 - (raw_addr & 1023)) & 1023;
   unsigned char* smem = smem_raw + pad;
   const uint32_t sbase = raw_addr + pad;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)STAGES * STAGE_BYTES);
-  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  unsigned char* tail = smem + (size_t)STAGES * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tail);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, cvt[STAGES]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  int* scan_buf = const_cast<int*>(reinterpret_cast<volatile int*>(tmem_holder + 2));  // [WARPS]
-  uint32_t* epi_buf = reinterpret_cast<uint32_t*>(smem + (size_t)STAGES * STAGE_BYTES + 256);
-  int* act_e = reinterpret_cast<int*>(smem + (size_t)STAGES * STAGE_BYTES + 256 + EPI_BYTES);
+  int* scan_buf = const_cast<int*>(reinterpret_cast<volatile int*>(tmem_holder + 2));  // [C::THREADS / 32]
+  uint32_t* epi_buf = reinterpret_cast<uint32_t*>(tail + 256);
+  uint32_t* lut_e2m1 = reinterpret_cast<uint32_t*>(tail + 256 + EPI_BYTES);
+  uint16_t* lut_e4m3 = reinterpret_cast<uint16_t*>(lut_e2m1 + 256);
+  int* act_e = reinterpret_cast<int*>(tail + 256 + EPI_BYTES + LUT_BYTES);
   int* act_pref = act_e + a.E;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -200,11 +299,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
   auto tfull_bar = [&](int b) { return smem_u32(bars + 2 * STAGES + b); };
   auto tempty_bar = [&](int b) { return smem_u32(bars + 2 * STAGES + 2 + b); };
   const uint32_t drain_bar = smem_u32(bars + 2 * STAGES + 4);
+  auto cvt_bar = [&](int s) { return smem_u32(bars + 2 * STAGES + 5 + s); };
+  // stage s: token rows (A) | bf16 weight rows (B) | packed e2m1 rows (FP4)
+  auto raw_off = [&](int s) { return (uint32_t)(s * STAGE_BYTES + A_BYTES + B_BYTES); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      mbar_init(cvt_bar(s), CVT_THREADS / 32);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -221,11 +324,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
     tmem_relinquish();
   }
+  if (FP4) fill_fp4_tables(lut_e2m1, lut_e4m3, C::THREADS);
   const int n_tiles_n = MODE == GATEUP ? a.I / (BN / 2) : ceil_div(a.H, BN);
   const int K = MODE == GATEUP ? a.H : a.I;
   const int nk = K / BK;
   int n_act = 0;
-  const int total = build_tiles(a, n_tiles_n, act_e, act_pref, scan_buf, n_act);
+  const int total = build_tiles<C::THREADS>(a, n_tiles_n, act_e, act_pref, scan_buf, n_act);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -243,14 +347,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
         for (int ks = 0; ks < nk; ++ks) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag)) { ok = false; break; }
           const uint32_t sa = sbase + stage * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
-          mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
+          // FP4: the packed rows go to the staging area, the map's unit is a byte of two elements
+          const uint32_t sb = FP4 ? sbase + raw_off(stage) : sa + A_BYTES;
+          const int kb = FP4 ? ks * BK / 2 : ks * BK;
+          const uint32_t half = FP4 ? RAW_BYTES / 2 : B_BYTES / 2;
+          mbar_arrive_expect_tx(full_bar(stage), A_BYTES + (FP4 ? RAW_BYTES : B_BYTES));
           tma_load_2d(sa, &map_a, full_bar(stage), ks * BK, t.row0);
           if (MODE == GATEUP) {
-            tma_load_3d(sb, &map_b0, full_bar(stage), ks * BK, t.nt * (BN / 2), t.slot);
-            tma_load_3d(sb + B_BYTES / 2, &map_b1, full_bar(stage), ks * BK, t.nt * (BN / 2), t.slot);
+            tma_load_3d(sb, &map_b0, full_bar(stage), kb, t.nt * (BN / 2), t.slot);
+            tma_load_3d(sb + half, &map_b1, full_bar(stage), kb, t.nt * (BN / 2), t.slot);
           } else {
-            tma_load_3d(sb, &map_b0, full_bar(stage), ks * BK, t.nt * BN, t.slot);
+            tma_load_3d(sb, &map_b0, full_bar(stage), kb, t.nt * BN, t.slot);
           }
           issued |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
@@ -277,7 +384,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
         tc_fence_after();
         const uint32_t d = tmem_base + acc * ACC_COLS;
         for (int ks = 0; ks < nk; ++ks) {
-          if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(FP4 ? cvt_bar(stage) : full_bar(stage), phase, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = sbase + stage * STAGE_BYTES;
           const uint64_t da = sdesc_k_sw128(sa);
@@ -300,6 +407,34 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
         mbar_drain(drain_bar, 0);
       }
     }
+  } else if (warp >= 6) {
+    // ---------------------------------------------------------------- FP4 expansion (warps 6..13)
+    const int c = threadIdx.x - 192;
+    const int row = c >> 1, half = c & 1;  // B-tile row and which 32 of its 64 elements
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    ScaleRing<WT> ring;
+    for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+      const Tile t = decode_tile(a, act_e, act_pref, n_act, item);
+      // matrix row of B-tile row `row`; selects, not a parameter-array index
+      const bool up = MODE == GATEUP && row >= BN / 2;
+      const int m = MODE == GATEUP ? t.nt * (BN / 2) + (row % (BN / 2)) : t.nt * BN + row;
+      const uint64_t off_s = MODE == GATEUP ? (up ? a.off_scale[1] : a.off_scale[0]) : a.off_scale[2];
+      const uint8_t* srow_p =
+          a.pool + (uint64_t)t.slot * a.S + off_s + (uint64_t)m * (uint64_t)(K / (WT == FT_W_NVFP4 ? 16 : 32));
+      ring.start(srow_p, 0, nk, half);
+      for (int ks = 0; ks < nk; ++ks) {
+        const uint32_t sc = ring.next(srow_p, 0, nk, ks, half);
+        if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
+        expand_fp4_half<WT>(smem + raw_off(stage) + row * 32, half, sc, lut_e2m1, lut_e4m3,
+                            smem + stage * STAGE_BYTES + A_BYTES + row * 128, row);
+        fence_proxy_async_smem();  // make the generic-proxy writes visible to the tensor core
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cvt_bar(stage));  // one arrival per converter warp
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+    }
   } else {
     // ---------------------------------------------------------------- epilogue (warps 2..5)
     const int q = warp & 3;          // TMEM lane quarter this warp may access
@@ -313,6 +448,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       const int rbase = t.mt * BM + q * 32;   // expert-local row of this warp's first lane
       const size_t pbase = (size_t)t.row0 + q * 32;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * ACC_COLS;
+      // NVFP4: the fp32 matrix scales multiply the finished dot products
+      float gs_g = 1.0f, gs_u = 1.0f, gs_d = 1.0f;
+      if (WT == FT_W_NVFP4) {
+        const float* gs = reinterpret_cast<const float*>(a.pool + (uint64_t)t.slot * a.S + a.off_gscale);
+        gs_g = gs[0]; gs_u = gs[1]; gs_d = gs[2];
+      }
       if (MODE == GATEUP) {
         // lane = row: 32 outputs silu(g) * u as bf16 (64 bytes), staged, then
         // written as 16-byte pieces, 4 lanes per row, 8 rows per instruction
@@ -325,8 +466,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
           uint32_t* row = buf + lane * EPI_STRIDE;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float a0 = silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
-            const float a1 = silu(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
+            const float a0 = silu(__uint_as_float(g[2 * j]) * gs_g) * (__uint_as_float(u[2 * j]) * gs_u);
+            const float a1 = silu(__uint_as_float(g[2 * j + 1]) * gs_g) * (__uint_as_float(u[2 * j + 1]) * gs_u);
             __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
             row[j] = *reinterpret_cast<uint32_t*>(&h2);
           }
@@ -351,6 +492,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
           tmem_ld32(taddr + c * 32, v);
           tmem_ld_wait();
           uint4* row = reinterpret_cast<uint4*>(buf + lane * EPI_STRIDE);
+          if (WT == FT_W_NVFP4) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * gs_d);
+          }
 #pragma unroll
           for (int j = 0; j < 8; ++j) row[j] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
           __syncwarp();

@@ -307,47 +307,65 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// bf16 tensor map, 128-byte swizzle, box {64, rows(, 1)}; dims[0] innermost.
-int make_map_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-                  uint32_t box_rows) {
+// Tensor map with box {box_inner, box_rows(, 1)}; dims[0] innermost.
+int make_map(CUtensorMap* m, CUtensorMapDataType dtype, const void* base, int rank, const uint64_t* dims,
+             const uint64_t* strides_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz) {
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return FT_EUNSUPPORTED;
   cuuint64_t gd[3], gs[2];
-  cuuint32_t bd[3] = {(cuuint32_t)tc::BK, box_rows, 1}, es[3] = {1, 1, 1};
+  cuuint32_t bd[3] = {box_inner, box_rows, 1}, es[3] = {1, 1, 1};
   for (int i = 0; i < rank; ++i) gd[i] = dims[i];
   for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), gd, gs, bd, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(m, dtype, (cuuint32_t)rank, const_cast<void*>(base), gd, gs, bd, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FT_OK : FT_EINVAL;
 }
 
-// The tensor-core path takes bf16 weights (H and I multiples of 128, which the
-// record layout already requires).
+// bf16 tensor map, 128-byte swizzle, box {64, rows(, 1)}.
+int make_map_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                  uint32_t box_rows) {
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides_bytes, tc::BK, box_rows,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Packed e2m1 values viewed as bytes (two K elements per byte), no swizzle,
+// box {32 bytes = 64 elements, rows, 1}: [K/2 bytes][rows][slot].
+int make_map_fp4(CUtensorMap* m, const void* base, int K, int rows, int slots, uint64_t S, uint32_t box_rows) {
+  const uint64_t d[3] = {(uint64_t)K / 2, (uint64_t)rows, (uint64_t)slots}, st[2] = {(uint64_t)K / 2, S};
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 3, d, st, tc::BK / 2, box_rows,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// The tensor-core path takes bf16, NVFP4 and MXFP4 weights (H and I multiples
+// of 128, which the record layout already requires).
 bool tc_path_applies(int wtype, int T, int k, int H, int I, int E) {
-  return wtype == FT_W_BF16 && H % 128 == 0 && I % 128 == 0 && E <= tc::MAX_E && (long long)T * k < (1ll << 28);
+  const long long Tk = (long long)T * k;
+  const bool fmt = wtype == FT_W_BF16 || tc::is_fp4(wtype);
+  return fmt && H % 128 == 0 && I % 128 == 0 && E <= tc::MAX_E && Tk < (1ll << 28);
 }
 
 // Tile width: 256 columns from FT_TC_WIDE_ASSIGNMENTS assignments up (fewer,
 // larger tiles), 128 below (twice the tiles, so a few experts still cover the SMs).
-template <int BN>
+template <int BN, int WT>
 int launch_tc_gemms(const CUtensorMap& mx, const CUtensorMap& mg, const CUtensorMap& mu, const CUtensorMap& ma,
                     const CUtensorMap& md, const tc::Args& a, cudaStream_t st) {
-  const size_t smem = tc::smem_bytes<BN>(a.E);
-  auto kg = tc::grouped_gemm_kernel<tc::GATEUP, BN>;
-  auto kd = tc::grouped_gemm_kernel<tc::DOWN, BN>;
+  const size_t smem = tc::smem_bytes<BN, WT>(a.E);
+  constexpr int NT = tc::Cfg<BN, WT>::THREADS;
+  auto kg = tc::grouped_gemm_kernel<tc::GATEUP, BN, WT>;
+  auto kd = tc::grouped_gemm_kernel<tc::DOWN, BN, WT>;
   if (int s = set_smem(kg, smem)) return s;
   if (int s = set_smem(kd, smem)) return s;
-  kg<<<sms(), tc::THREADS, smem, st>>>(mx, mg, mu, a);
+  kg<<<sms(), NT, smem, st>>>(mx, mg, mu, a);
   FT_CHECK_LAUNCH();
-  kd<<<sms(), tc::THREADS, smem, st>>>(ma, md, md, a);
+  kd<<<sms(), NT, smem, st>>>(ma, md, md, a);
   FT_CHECK_LAUNCH();
   return FT_OK;
 }
 
 // Small batches: weights on the MMA's M side, token rows on N, K split when few experts are routed.
-int launch_expert_skinny(const ExpertArgs& ea, const ft_expert_layout& L, const TcWorkspace& w, uint8_t* ws,
-                         cudaStream_t st) {
+template <int WT>
+int launch_skinny_wt(const ExpertArgs& ea, const ft_expert_layout& L, const TcWorkspace& w, uint8_t* ws,
+                     cudaStream_t st) {
   const long long Tk = (long long)ea.T * ea.k;
   const int H = ea.H, I = ea.I;
   __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(ws);
@@ -356,13 +374,20 @@ int launch_expert_skinny(const ExpertArgs& ea, const ft_expert_layout& L, const 
   CUtensorMap mg, mu, md, mx, ma;
   {
     const uint8_t* pool = ea.pool;
-    const uint64_t dw[3] = {(uint64_t)H, (uint64_t)I, (uint64_t)ea.pool_slots}, sw[2] = {(uint64_t)H * 2, ea.S};
-    const uint64_t dd[3] = {(uint64_t)I, (uint64_t)H, (uint64_t)ea.pool_slots}, sd[2] = {(uint64_t)I * 2, ea.S};
     const uint64_t dx[2] = {(uint64_t)H, (uint64_t)Tk}, sx[1] = {(uint64_t)H * 2};
     const uint64_t da[2] = {(uint64_t)I, (uint64_t)Tk}, sa[1] = {(uint64_t)I * 2};
-    int r = make_map_bf16(&mg, pool + L.off_val[0], 3, dw, sw, 64);
-    if (!r) r = make_map_bf16(&mu, pool + L.off_val[1], 3, dw, sw, 64);
-    if (!r) r = make_map_bf16(&md, pool + L.off_val[2], 3, dd, sd, tc::SK_MR);
+    int r;
+    if (tc::is_fp4(WT)) {
+      r = make_map_fp4(&mg, pool + L.off_val[0], H, I, ea.pool_slots, ea.S, 64);
+      if (!r) r = make_map_fp4(&mu, pool + L.off_val[1], H, I, ea.pool_slots, ea.S, 64);
+      if (!r) r = make_map_fp4(&md, pool + L.off_val[2], I, H, ea.pool_slots, ea.S, tc::SK_MR);
+    } else {
+      const uint64_t dw[3] = {(uint64_t)H, (uint64_t)I, (uint64_t)ea.pool_slots}, sw[2] = {(uint64_t)H * 2, ea.S};
+      const uint64_t dd[3] = {(uint64_t)I, (uint64_t)H, (uint64_t)ea.pool_slots}, sd[2] = {(uint64_t)I * 2, ea.S};
+      r = make_map_bf16(&mg, pool + L.off_val[0], 3, dw, sw, 64);
+      if (!r) r = make_map_bf16(&mu, pool + L.off_val[1], 3, dw, sw, 64);
+      if (!r) r = make_map_bf16(&md, pool + L.off_val[2], 3, dd, sd, tc::SK_MR);
+    }
     if (!r) r = make_map_bf16(&mx, xp, 2, dx, sx, nb_box);
     if (!r) r = make_map_bf16(&ma, aint, 2, da, sa, nb_box);
     if (r) return r;
@@ -371,26 +396,40 @@ int launch_expert_skinny(const ExpertArgs& ea, const ft_expert_layout& L, const 
   a.T = ea.T; a.k = ea.k; a.H = H; a.I = I; a.E = ea.E; a.pool_slots = ea.pool_slots;
   a.nb_box = nb_box;
   a.offsets = ea.offsets; a.slot_of = ea.slot_of;
+  a.pool = ea.pool; a.S = ea.S;
+  for (int m = 0; m < 3; ++m) a.off_scale[m] = L.off_scale[m];
+  a.off_gscale = L.off_gscale;
   a.Aint = aint; a.y = ea.y;
   a.part = reinterpret_cast<float*>(ws + w.off_part);
   int32_t* counters = reinterpret_cast<int32_t*>(ws + w.off_counters);
-  const size_t smem = tc::sk_smem_bytes(ea.E);
-  auto kg = tc::skinny_gemm_kernel<tc::GATEUP>;
-  auto kd = tc::skinny_gemm_kernel<tc::DOWN>;
+  const size_t smem = tc::sk_smem_bytes<WT>(ea.E);
+  constexpr int NT = tc::SkCfg<WT>::THREADS;
+  auto kg = tc::skinny_gemm_kernel<tc::GATEUP, WT>;
+  auto kd = tc::skinny_gemm_kernel<tc::DOWN, WT>;
   if (int s = set_smem(kg, smem)) return s;
   if (int s = set_smem(kd, smem)) return s;
   a.KS = w.ks_gu;
   a.counters = counters;
-  kg<<<sms(), tc::THREADS, smem, st>>>(mg, mu, mx, a);
+  kg<<<sms(), NT, smem, st>>>(mg, mu, mx, a);
   FT_CHECK_LAUNCH();
   a.KS = w.ks_dn;
   a.counters = counters + w.g_gu;
-  kd<<<sms(), tc::THREADS, smem, st>>>(md, md, ma, a);
+  kd<<<sms(), NT, smem, st>>>(md, md, ma, a);
   FT_CHECK_LAUNCH();
   return FT_OK;
 }
 
-int launch_expert_tc(const ExpertArgs& ea, const ft_expert_layout& L, void* workspace, cudaStream_t st) {
+int launch_expert_skinny(int wtype, const ExpertArgs& ea, const ft_expert_layout& L, const TcWorkspace& w,
+                         uint8_t* ws, cudaStream_t st) {
+  switch (wtype) {
+    case FT_W_BF16: return launch_skinny_wt<FT_W_BF16>(ea, L, w, ws, st);
+    case FT_W_NVFP4: return launch_skinny_wt<FT_W_NVFP4>(ea, L, w, ws, st);
+    case FT_W_MXFP4: return launch_skinny_wt<FT_W_MXFP4>(ea, L, w, ws, st);
+  }
+  return FT_EINVAL;
+}
+
+int launch_expert_tc(int wtype, const ExpertArgs& ea, const ft_expert_layout& L, void* workspace, cudaStream_t st) {
   const long long Tk = (long long)ea.T * ea.k;
   const int H = ea.H, I = ea.I;
   const TcWorkspace w = tc_workspace(Tk, H, I);
@@ -412,27 +451,44 @@ int launch_expert_tc(const ExpertArgs& ea, const ft_expert_layout& L, void* work
                                                           zero, n_zero);
     FT_CHECK_LAUNCH();
   }
-  if (skinny) return launch_expert_skinny(ea, L, w, ws, st);
+  if (skinny) return launch_expert_skinny(wtype, ea, L, w, ws, st);
   CUtensorMap mx, mg, mu, ma, md;
   const uint8_t* pool = ea.pool;
-  const int BN = (Tk >= FT_TC_WIDE_ASSIGNMENTS && H % 256 == 0) ? 256 : 128;
+  // bf16: 256-column weight tiles when H allows; FP4: 128 (deeper pipeline beside the staging buffers)
+  const int BN = (wtype == FT_W_BF16 && H % 256 == 0) ? 256 : 128;
   {
     const uint64_t dx[2] = {(uint64_t)H, (uint64_t)Tk}, sx[1] = {(uint64_t)H * 2};
-    const uint64_t dw[3] = {(uint64_t)H, (uint64_t)I, (uint64_t)ea.pool_slots}, sw[2] = {(uint64_t)H * 2, ea.S};
     const uint64_t da[2] = {(uint64_t)I, (uint64_t)Tk}, sa[1] = {(uint64_t)I * 2};
-    const uint64_t dd[3] = {(uint64_t)I, (uint64_t)H, (uint64_t)ea.pool_slots}, sd[2] = {(uint64_t)I * 2, ea.S};
     int r = make_map_bf16(&mx, xp, 2, dx, sx, tc::BM);
-    if (!r) r = make_map_bf16(&mg, pool + L.off_val[0], 3, dw, sw, BN / 2);
-    if (!r) r = make_map_bf16(&mu, pool + L.off_val[1], 3, dw, sw, BN / 2);
     if (!r) r = make_map_bf16(&ma, aint, 2, da, sa, tc::BM);
-    if (!r) r = make_map_bf16(&md, pool + L.off_val[2], 3, dd, sd, BN);
+    if (tc::is_fp4(wtype)) {
+      if (!r) r = make_map_fp4(&mg, pool + L.off_val[0], H, I, ea.pool_slots, ea.S, BN / 2);
+      if (!r) r = make_map_fp4(&mu, pool + L.off_val[1], H, I, ea.pool_slots, ea.S, BN / 2);
+      if (!r) r = make_map_fp4(&md, pool + L.off_val[2], I, H, ea.pool_slots, ea.S, BN);
+    } else {
+      const uint64_t dw[3] = {(uint64_t)H, (uint64_t)I, (uint64_t)ea.pool_slots}, sw[2] = {(uint64_t)H * 2, ea.S};
+      const uint64_t dd[3] = {(uint64_t)I, (uint64_t)H, (uint64_t)ea.pool_slots}, sd[2] = {(uint64_t)I * 2, ea.S};
+      if (!r) r = make_map_bf16(&mg, pool + L.off_val[0], 3, dw, sw, BN / 2);
+      if (!r) r = make_map_bf16(&mu, pool + L.off_val[1], 3, dw, sw, BN / 2);
+      if (!r) r = make_map_bf16(&md, pool + L.off_val[2], 3, dd, sd, BN);
+    }
     if (r) return r;
   }
   tc::Args a;
   a.T = ea.T; a.k = ea.k; a.H = H; a.I = I; a.E = ea.E; a.pool_slots = ea.pool_slots;
-  a.offsets = ea.offsets; a.slot_of = ea.slot_of; a.gscale_base = nullptr; a.S = ea.S;
+  a.offsets = ea.offsets; a.slot_of = ea.slot_of; a.S = ea.S;
+  a.pool = ea.pool;
+  for (int m = 0; m < 3; ++m) a.off_scale[m] = L.off_scale[m];
+  a.off_gscale = L.off_gscale;
   a.Aint = aint; a.y = ea.y;
-  return BN == 256 ? launch_tc_gemms<256>(mx, mg, mu, ma, md, a, st) : launch_tc_gemms<128>(mx, mg, mu, ma, md, a, st);
+  switch (wtype) {
+    case FT_W_BF16:
+      return BN == 256 ? launch_tc_gemms<256, FT_W_BF16>(mx, mg, mu, ma, md, a, st)
+                       : launch_tc_gemms<128, FT_W_BF16>(mx, mg, mu, ma, md, a, st);
+    case FT_W_NVFP4: return launch_tc_gemms<128, FT_W_NVFP4>(mx, mg, mu, ma, md, a, st);
+    case FT_W_MXFP4: return launch_tc_gemms<128, FT_W_MXFP4>(mx, mg, mu, ma, md, a, st);
+  }
+  return FT_EINVAL;
 }
 
 }  // namespace
@@ -458,7 +514,7 @@ FT_API int ft_expert_grouped(const void* x, int x_type, int T, int k, int hidden
   a.A = (float*)workspace;
   a.y = y;
   cudaStream_t st = (cudaStream_t)s;
-  if (tc_path_applies(wtype, T, k, hidden, inter, E)) return launch_expert_tc(a, L, workspace, st);
+  if (tc_path_applies(wtype, T, k, hidden, inter, E)) return launch_expert_tc(wtype, a, L, workspace, st);
   switch (wtype) {
     case FT_W_F32: return launch_expert<FT_W_F32>(a, st);
     case FT_W_BF16: return launch_expert<FT_W_BF16>(a, st);

@@ -29,9 +29,9 @@ def ft(ftlib):
     return ftlib
 
 
-def _setup(ft, H, I, E, k, T, seed, skewed=False):
-    cfg = synth.MoEConfig(f"tc_{H}_{I}_{E}", H, E, k, I, 1, synth.W_BF16, "bf16", seed=seed)
-    L = ft.ft_expert_layout_get(synth.W_BF16, H, I)
+def _setup(ft, H, I, E, k, T, seed, skewed=False, wtype=synth.W_BF16):
+    cfg = synth.MoEConfig(f"tc_{H}_{I}_{E}", H, E, k, I, 1, wtype, "bf16", seed=seed)
+    L = ft.ft_expert_layout_get(wtype, H, I)
     S = int(L.bytes)
     n_slots = E + 5
     pool = torch.zeros(n_slots * S, dtype=torch.uint8, device=DEV)
@@ -40,7 +40,7 @@ def _setup(ft, H, I, E, k, T, seed, skewed=False):
     comps = {}
     for e in range(E):
         comps[e] = synth.expert_weights(cfg, 0, e, DEV)
-        ft.pack_expert(comps[e], synth.W_BF16, L, pool[slot_perm[e] * S:(slot_perm[e] + 1) * S])
+        ft.pack_expert(comps[e], wtype, L, pool[slot_perm[e] * S:(slot_perm[e] + 1) * S])
     x = synth.activations(cfg, T, tag=5, device=DEV)
     if skewed:
         # a few heavy experts (several 128-row tiles) and a tail of light ones
@@ -52,11 +52,11 @@ def _setup(ft, H, I, E, k, T, seed, skewed=False):
     return cfg, L, S, n_slots, pool, slot_perm, comps, x, idx
 
 
-def _run(ft, x, k, I, E, perm, offsets, slot_of, pool, S, n_slots):
+def _run(ft, x, k, I, E, perm, offsets, slot_of, pool, S, n_slots, wtype=synth.W_BF16):
     T, H = x.shape
     y = torch.full((T * k, H), float("nan"), dtype=torch.float32, device=DEV)
     ws = torch.empty(ft.ft_expert_grouped_workspace(T, k, H, I), dtype=torch.uint8, device=DEV)
-    ft.ft_expert_grouped(x, k, I, E, synth.W_BF16, torch.from_numpy(perm).to(DEV),
+    ft.ft_expert_grouped(x, k, I, E, wtype, torch.from_numpy(perm).to(DEV),
                          torch.from_numpy(offsets).to(DEV), torch.from_numpy(slot_of).to(DEV), pool, S, n_slots, y, ws)
     torch.cuda.synchronize()
     assert ft.ft_get_device_error() == 0
@@ -164,3 +164,38 @@ def test_tc_split_k_is_deterministic(ft):
     so = slot_perm.astype(np.int32)
     Y = [_run(ft, x, k, I, E, perm, offsets, so, pool, S, n_slots) for _ in range(3)]
     assert np.array_equal(Y[0], Y[1]) and np.array_equal(Y[0], Y[2])
+
+
+@pytest.mark.parametrize("wtype,H,I,E,k,T,seed", [
+    (synth.W_NVFP4, 4096, 2048, 16, 6, 1, 20),    # the NVFP4 stack's shape, one decode token
+    (synth.W_NVFP4, 1024, 512, 8, 2, 1, 21),      # NVFP4 with the gate/up K split
+    (synth.W_NVFP4, 4096, 2048, 32, 6, 64, 22),   # NVFP4 decode batch of 64
+    (synth.W_MXFP4, 6144, 2048, 16, 8, 1, 23),    # the MXFP4 layer's shape, one decode token
+    (synth.W_MXFP4, 2048, 512, 32, 8, 16, 24),
+    (synth.W_MXFP4, 256, 128, 8, 2, 3, 25),       # tiny: one 64-element scale pair per row
+    (synth.W_NVFP4, 1024, 512, 16, 8, 300, 26),   # 2400 assignments: large-batch tiling with FP4 expansion
+    (synth.W_MXFP4, 2048, 1024, 8, 4, 600, 27),
+    (synth.W_NVFP4, 4096, 2048, 4, 2, 1100, 28),  # the NVFP4 stack's expert shape, ~550 rows per expert
+])
+def test_tc_fp4_expert_parity(ft, wtype, H, I, E, k, T, seed):
+    """NVFP4 / MXFP4 weights expanded to bf16 in shared memory (exact), then the same tensor-core path."""
+    cfg, L, S, n_slots, pool, slot_perm, comps, x, idx = _setup(ft, H, I, E, k, T, seed, wtype=wtype)
+    counts, offsets, perm, inv = moe.permute(idx, E)
+    slot_of = slot_perm.astype(np.int32).copy()
+    slot_of[E - 1] = -1
+    Y = _run(ft, x, k, I, E, perm, offsets, slot_of, pool, S, n_slots, wtype)
+    xs = formats.to_f64(x)
+    got, ref = [], []
+    for e in range(E - 1):
+        rows = np.arange(offsets[e], offsets[e + 1])
+        if rows.size == 0:
+            continue
+        g, u, d = (formats.dequant(comps[e][m], wtype) for m in ("gate", "up", "down"))
+        ref.append(moe.expert_ffn(xs[perm[rows] // k], g, u, d, act_round=formats.round_to_bf16))
+        got.append(Y[rows])
+    rows = np.arange(offsets[E - 1], offsets[E])
+    assert np.isnan(Y[rows]).all()
+    got, ref = np.concatenate(got), np.concatenate(ref)
+    assert np.isfinite(got).all()
+    assert_close_layer(got, ref, fro=1e-2)
+    assert rel_fro(got, ref) < 2e-3
