@@ -44,8 +44,11 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--phys-layers", type=int, default=0, help="host pool layers (0: all 40 when RAM allows)")
     p.add_argument("--batches", default=",".join(map(str, BATCHES)))
-    p.add_argument("--prefill-chunks", type=int, default=2)
+    p.add_argument("--prompts", default="4096,8192,16384", help="prefill prompt lengths (chunks of <= 8192)")
     p.add_argument("--no-prefill", action="store_true")
+    p.add_argument("--no-fp4", action="store_true", help="skip the NVFP4 stack and the MXFP4 mixed-trace legs")
+    p.add_argument("--fp4-steps", type=int, default=6, help="timed decode steps per batch size, NVFP4 stack")
+    p.add_argument("--mixed-decode-steps", type=int, default=512)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graphs", action="store_true", help="issue the decode steps eagerly instead of as CUDA graphs")
@@ -188,25 +191,38 @@ def host_ram_bytes() -> int:
 class DecodeTrace:
     """One batch size: its cache, per-step buffers, resident inputs and per-layer-step counters."""
 
-    def __init__(self, ft, cfg, T, pool, routers, n_steps, dev, e2e):
+    def __init__(self, ft, cfg, T, pool, routers, n_steps, dev, e2e, n_slots=None):
         self.ft, self.cfg, self.T = ft, cfg, T
         L, E = cfg.n_layers, cfg.n_experts
-        self.n_slots = int(round(CACHE_FRAC * L * E))
+        self.n_slots = n_slots or int(round(CACHE_FRAC * L * E))
         self.S = pool.S
         self.sp = torch.empty(self.n_slots * pool.S, dtype=torch.uint8, device=dev)
+        self.pool = pool
         self.cache = ft.Cache(L, E, pool.n_phys, self.n_slots, self.n_slots, pool.S, pool.ptr, self.sp)
         self.layer = ft.MoELayer(cfg, T, dev)
         tr = synth.AR1Trace(cfg, T, dev, tag=T)
         self.xs = torch.stack([tr.next() for _ in range(n_steps)])          # [steps, T, H] resident
-        self.hist = torch.zeros(n_steps, L, 4, dtype=torch.int32, device=dev)
-        self.routers = routers
         self.n_waves = self.cache.n_waves()
+        self.hist = torch.zeros(n_steps, L, self.n_waves, 4, dtype=torch.int32, device=dev)  # per wave
+        self.routers = routers
         if e2e:
             self.x_host = torch.empty(n_steps, T, cfg.hidden, dtype=torch.bfloat16).pin_memory()
             self.x_host.copy_(self.xs.cpu())
             self.x_dev = torch.empty(T, cfg.hidden, dtype=torch.bfloat16, device=dev)
             self.outs = torch.empty(L, T, cfg.hidden, dtype=torch.float32, device=dev)
             self.out_host = torch.empty(L, T, cfg.hidden, dtype=torch.float32).pin_memory()
+
+    def reset_cache(self):
+        """A new, empty cache on the same slot pool (the state the trace started from)."""
+        cfg, pool = self.cfg, self.pool
+        self.cache.destroy()
+        self.cache = self.ft.Cache(cfg.n_layers, cfg.n_experts, pool.n_phys, self.n_slots, self.n_slots, pool.S,
+                                   pool.ptr, self.sp)
+        self.hist.zero_()
+
+    def counts(self, t0, t1) -> np.ndarray:
+        """Per layer step {experts, hits, fills, externals} of steps t0..t1-1 (summed over waves)."""
+        return self.hist[t0:t1].sum(dim=2).cpu().numpy()
 
     def launches_per_step(self) -> int:
         # router_logits, route, permute, (control, fill, expert kernels) per wave, combine;
@@ -236,7 +252,7 @@ class DecodeTrace:
             for w in range(self.n_waves):
                 if ev is not None:
                     ev.rec("cache")
-                cache.step(l, lay.counts, 1.0, w, lay.slot_of, lay.ext, self.hist[t, l])
+                cache.step(l, lay.counts, 1.0, w, lay.slot_of, lay.ext, self.hist[t, l, w])
                 if ev is not None:
                     ev.rec("cache_end")
                 lay.experts(x, lay.slot_of, self.sp, self.S, self.n_slots)
@@ -302,35 +318,46 @@ def layer_roofline_seconds(hist: np.ndarray, T: int, cfg, S_payload: int, peaks,
 
 # ---------------------------------------------------------------- prefill streaming leg
 
-def prefill_leg(ft, cfg, pool, routers0, dev, chunks, link_gbs, peaks):
+def prefill_leg(ft, cfg, pool, routers0, dev, prompts, link_gbs, peaks, chunk=8192):
+    """Prompts of the given lengths streamed through ft_stream in chunks of at most ``chunk`` tokens.
+
+    For each prompt length: double-buffered and serialized runs; each chunk
+    streams every layer once (zero router bias: near-uniform routing)."""
     L, E = cfg.n_layers, cfg.n_experts
-    n_slots = int(round(CACHE_FRAC * L * E))
+    n_slots = 2 * E + 16                      # the two whole-layer buffers (+ a few LRU slots)
     sp = torch.empty(n_slots * pool.S, dtype=torch.uint8, device=dev)
     cache = ft.Cache(L, E, pool.n_phys, n_slots, n_slots, pool.S, pool.ptr, sp)
-    lay = ft.MoELayer(cfg, 8192, dev)
-    xcfg = synth.PREFILL_BF16
-    xs = [synth.activations(xcfg, 8192, tag=c, device=dev) for c in range(chunks)]
+    lay = ft.MoELayer(cfg, chunk, dev)
+    max_chunks = max((p + chunk - 1) // chunk for p in prompts)
+    xs = [synth.activations(cfg, chunk, tag=c, device=dev) for c in range(max_chunks)]
     zero = torch.zeros(E, dtype=torch.float32, device=dev)
     slot_of = torch.empty(E, dtype=torch.int32, device=dev)
-    res = {}
-    for mode in ("overlapped", "serialized"):
-        st = ft.Stream(cache, serialized=(mode == "serialized"))
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for c in range(chunks):
-            for l in range(L):
-                nxt = l + 1 if l + 1 < L else (0 if c + 1 < chunks else -1)
-                st.layer(l, nxt, slot_of)
-                lay.forward_slots(xs[c], routers0[l][0], zero, slot_of, sp, pool.S, n_slots)
-                st.layer_done(l)
-        e1.record()
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1)
-        nbytes = st.bytes()
-        st.destroy()
-        res[mode] = {"tokens_per_s": 8192 * chunks / (ms * 1e-3), "ms_per_chunk": ms / chunks,
-                     "h2d_gbs": nbytes / (ms * 1e-3) / 1e9, "link_frac": nbytes / (ms * 1e-3) / 1e9 / link_gbs}
+    res = {"prompts": {}}
+    for P in prompts:
+        sizes = [min(chunk, P - c0) for c0 in range(0, P, chunk)]
+        r = {}
+        for mode in ("overlapped", "serialized"):
+            st = ft.Stream(cache, serialized=(mode == "serialized"))
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for c, n in enumerate(sizes):
+                for l in range(L):
+                    nxt = l + 1 if l + 1 < L else (0 if c + 1 < len(sizes) else -1)
+                    st.layer(l, nxt, slot_of)
+                    lay.forward_slots(xs[c][:n], routers0[l][0], zero, slot_of, sp, pool.S, n_slots)
+                    st.layer_done(l)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            nbytes = st.bytes()
+            st.destroy()
+            r[mode] = {"tokens_per_s": P / (ms * 1e-3), "ms": ms, "h2d_gbs": nbytes / (ms * 1e-3) / 1e9,
+                       "link_frac": nbytes / (ms * 1e-3) / 1e9 / link_gbs}
+        r["loss_without_overlap"] = 1.0 - r["serialized"]["tokens_per_s"] / r["overlapped"]["tokens_per_s"]
+        res["prompts"][str(P)] = r
+    res["overlapped"] = res["prompts"][str(prompts[-1] if chunk not in prompts else chunk)]["overlapped"]
+    res["serialized"] = res["prompts"][str(prompts[-1] if chunk not in prompts else chunk)]["serialized"]
     # compute alone (weights resident in a buffer): one 8192-token layer through the grouped experts
     st = ft.Stream(cache)
     st.layer(0, -1, slot_of)
@@ -355,6 +382,175 @@ def prefill_leg(ft, cfg, pool, routers0, dev, chunks, link_gbs, peaks):
     del sp, lay
     torch.cuda.empty_cache()
     return res
+
+
+# ---------------------------------------------------------------- secondary workloads
+
+def decode_trace_leg(ft, cfg, T, pool, routers, n_slots, steps, warmup, dev, peaks, link, payload):
+    """One batch size on its own cache: eager warm-up, then ``steps`` graph-replayed decode steps."""
+    tr = DecodeTrace(ft, cfg, T, pool, routers, warmup + steps, dev, False, n_slots=n_slots)
+    for t in range(warmup):
+        tr.step(t)
+    graphs = [tr.capture(warmup + k) for k in range(steps)]
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for g, _ in graphs:
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    h = tr.counts(warmup, warmup + steps)
+    roof, _ = layer_roofline_seconds(h, T, cfg, payload, peaks, link)
+    cache_ms = sum(v for _, ev in graphs for v in ev.spans("cache", "cache_end"))
+    expert_ms = sum(v for _, ev in graphs for v in ev.spans("cache_end", "expert_end"))
+    out = {"tokens_per_s": T * steps / (ms * 1e-3), "ms_per_step": ms / steps,
+           "layer_roofline_frac": roof / (ms * 1e-3), "hit_rate": float(h[..., 1].sum() / max(h[..., 0].sum(), 1)),
+           "fill_gbs": float(h[..., 2].sum()) * payload / max(cache_ms * 1e-3, 1e-12) / 1e9,
+           "expert_weight_gbs": float(h[..., 0].sum()) * payload / max(expert_ms * 1e-3, 1e-12) / 1e9}
+    del graphs
+    tr.cache.destroy()
+    del tr
+    torch.cuda.empty_cache()
+    return out
+
+
+def nvfp4_leg(ft, dev, peaks, link, batches, steps, warmup):
+    """The 43-layer NVFP4 stack: decode at 40% cache per batch size, and 8192-token streamed prefill.
+
+    The host pool stores a cyclic window of 4 physical layers (logical layer l
+    reads physical l mod 4); cache keys and bytes moved stay logical."""
+    cfg = synth.NVFP4_43L
+    pool = ft.ExpertPool(cfg, 4)
+    pool.fill(dev)
+    payload = int(ft.ft_expert_layout_get(cfg.wtype, cfg.hidden, cfg.inter).payload_bytes)
+    routers = [synth.router_weights(cfg, l, dev) for l in range(cfg.n_layers)]
+    n_slots = int(round(CACHE_FRAC * cfg.n_layers * cfg.n_experts))
+    res = {"workload": "nvfp4_43L: H=4096 E=256 top-6 I=2048, NVFP4 weights, 43 layers over a 4-layer host window",
+           "cache_slots": n_slots, "decode": {}}
+    for T in batches:
+        log(f"nvfp4 decode T={T}")
+        res["decode"][str(T)] = decode_trace_leg(ft, cfg, T, pool, routers, n_slots, steps, warmup, dev, peaks, link,
+                                                 payload)
+    log("nvfp4 prefill")
+    pf = prefill_leg(ft, cfg, pool, routers, dev, [8192], link, peaks)
+    res["prefill_8192"] = pf
+    pool.free()
+    return res
+
+
+def mxfp4_mixed_leg(ft, dev, peaks, link, decode_steps=512, cycles=4):
+    """The MXFP4 agent-like trace on 4 layers: cycles of (8192-token prefill, T=1 decode run).
+
+    The cache is resized at the safe point before each cycle (57.8% -> 40% ->
+    20% -> 57.8% of the 1024 (layer, expert) slots); misses are split with
+    ratio 0.7, so 30% of them go to the external path, whose partial output is
+    supplied to the combine (a zero placeholder here: the host share is not
+    part of this build).  With fewer slots than two whole layers the prefill
+    runs on demand through the cache in waves; otherwise it streams.  Every
+    resize re-captures the decode graph, since the wave count can change."""
+    cfg = synth.MXFP4_MIXED
+    L, E, H = cfg.n_layers, cfg.n_experts, cfg.hidden
+    budgets = [592, 410, 205, 592][:cycles]
+    pool = ft.ExpertPool(cfg, L)
+    pool.fill(dev)
+    payload = int(ft.ft_expert_layout_get(cfg.wtype, cfg.hidden, cfg.inter).payload_bytes)
+    routers = [synth.router_weights(cfg, l, dev) for l in range(L)]
+    zero_b = torch.zeros(E, dtype=torch.float32, device=dev)
+    max_slots = max(budgets)
+    sp = torch.empty(max_slots * pool.S, dtype=torch.uint8, device=dev)
+    cache = ft.Cache(L, E, L, budgets[0], max_slots, pool.S, pool.ptr, sp)
+    lay_p = ft.MoELayer(cfg, 8192, dev)
+    lay_d = ft.MoELayer(cfg, 1, dev)
+    P_p = torch.zeros(8192, H, dtype=torch.float32, device=dev)
+    P_d = torch.zeros(1, H, dtype=torch.float32, device=dev)
+    x_d = torch.empty(1, H, dtype=torch.bfloat16, device=dev)
+    counts_d = torch.zeros(L, 8, 4, dtype=torch.int32, device=dev)   # per layer, per wave (<= 8 waves)
+    trace = synth.AR1Trace(cfg, 1, dev, tag=5)
+    slot_of = torch.empty(E, dtype=torch.int32, device=dev)
+    ratio = 0.7
+
+    def decode_layers():
+        for l in range(L):
+            lay_d.route(x_d, *routers[l])
+            for w in range(cache.n_waves()):
+                cache.step(l, lay_d.counts, ratio, w, lay_d.slot_of, lay_d.ext, counts_d[l, w])
+                lay_d.experts(x_d, lay_d.slot_of, sp, pool.S, max_slots)
+            lay_d.combine(1, lay_d.ext, P_d)
+
+    cyc = []
+    total_ms, total_tokens, roof_s = 0.0, 0, 0.0
+    for c, N in enumerate(budgets):
+        if c > 0:
+            cache.resize(N)                     # safe point: nothing in flight
+        xp = synth.activations(cfg, 8192, tag=100 + c, device=dev)
+        streamed = N >= 2 * E
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        if streamed:
+            st = ft.Stream(cache)
+            for l in range(L):
+                st.layer(l, l + 1 if l + 1 < L else -1, slot_of)
+                lay_p.forward_slots(xp, routers[l][0], zero_b, slot_of, sp, pool.S, max_slots)
+                st.layer_done(l)
+        else:
+            for l in range(L):
+                lay_p.forward_cached(xp, routers[l][0], zero_b, l, cache, pool.S, fill_ratio=ratio, ext_partial=P_p)
+        e1.record()
+        torch.cuda.synchronize()
+        p_ms = e0.elapsed_time(e1)
+        p_bytes = 0
+        if streamed:
+            p_bytes = st.bytes()
+            st.destroy()
+        stats0 = cache.stats()
+        # decode run: one graph of the 4 layers, re-captured for this cache size, replayed per step
+        for _ in range(3):
+            x_d.copy_(trace.next())
+            decode_layers()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            decode_layers()
+        hist = torch.zeros(decode_steps, L, 4, dtype=torch.int32, device=dev)
+        xs = torch.stack([trace.next() for _ in range(decode_steps)])
+        torch.cuda.synchronize()
+        e0.record()
+        counts_d.zero_()
+        for t in range(decode_steps):
+            x_d.copy_(xs[t])
+            g.replay()
+            torch.sum(counts_d, dim=1, out=hist[t])   # a step's counts: the sum over its waves
+        e1.record()
+        torch.cuda.synchronize()
+        d_ms = e0.elapsed_time(e1)
+        h = hist.cpu().numpy()
+        d_roof, _ = layer_roofline_seconds(h, 1, cfg, payload, peaks, link)
+        stats1 = cache.stats()
+        p_link = p_bytes if streamed else (stats0.bytes_h2d - (cyc[-1]["_bytes_after"] if cyc else 0))
+        p_flops = 2.0 * 8192 * cfg.top_k * 3 * cfg.hidden * cfg.inter * L
+        p_roof = max(p_link / (link * 1e9), p_flops / (peaks["bf16_tflops_sustained"] * 1e12))
+        cyc.append({"slots": N, "prefill_mode": "streamed" if streamed else "on-demand (waves, 30% external)",
+                    "prefill_ms": p_ms, "prefill_tokens_per_s": 8192 / (p_ms * 1e-3),
+                    "prefill_h2d_gbs": p_link / (p_ms * 1e-3) / 1e9, "prefill_roofline_frac": p_roof / (p_ms * 1e-3),
+                    "decode_tokens_per_s": decode_steps / (d_ms * 1e-3), "decode_ms_per_step": d_ms / decode_steps,
+                    "decode_layer_roofline_frac": d_roof / (d_ms * 1e-3),
+                    "decode_hits": int(h[..., 1].sum()), "decode_fills": int(h[..., 2].sum()),
+                    "decode_externals": int(h[..., 3].sum()), "_bytes_after": stats1.bytes_h2d})
+        total_ms += p_ms + d_ms
+        total_tokens += 8192 + decode_steps
+        roof_s += p_roof + d_roof
+        del g
+    for c in cyc:
+        c.pop("_bytes_after")
+    cache.destroy()
+    pool.free()
+    del sp
+    torch.cuda.empty_cache()
+    return {"workload": "mxfp4_mixed_4L: H=6144 E=256 top-8 I=2048, MXFP4 weights, 4 layers; "
+                        "4 x (8192-token prefill, 512 T=1 decode steps); cache 592/410/205/592 slots; 30% external",
+            "tokens_per_s": total_tokens / (total_ms * 1e-3), "layer_roofline_frac": roof_s / (total_ms * 1e-3),
+            "cycles": cyc}
 
 
 # ---------------------------------------------------------------- CPU oracle baseline
@@ -503,7 +699,7 @@ def main():
     t_fill = time.perf_counter() - t_fill
     routers = [synth.router_weights(cfg, l, dev) for l in range(L)]
     link = link_peak_gbs(pool.host, E * S, dev)
-    n_steps = args.warmup + args.steps * (1 if args.no_e2e else 2)
+    n_steps = args.warmup + args.steps
     traces = [DecodeTrace(ft, cfg, T, pool, routers, n_steps, dev, not args.no_e2e) for T in batches]
     tokens_per_step = sum(batches)
 
@@ -571,7 +767,7 @@ def main():
     hit_rate = {}
     fills_total, unique_total = 0, 0
     for tr in traces:
-        h = tr.hist[args.warmup:args.warmup + args.steps].cpu().numpy()
+        h = tr.counts(args.warmup, args.warmup + args.steps)
         s, d = layer_roofline_seconds(h, tr.T, cfg, int(lay_bytes.payload_bytes), peaks, link)
         per_T_roof[tr.T] = s
         roof_s += s
@@ -604,20 +800,30 @@ def main():
     # end to end through the public API with host buffers: every step copies its
     # inputs from pinned host memory, runs (as a graph of device work only), and
     # copies every layer's output back to pinned host memory
+    # (fresh caches, the same warm-up and the same trace steps as the device-resident run)
     e2e = None
     if not args.no_e2e:
-        egraphs = {}
+        del graphs, logs
+        for tr in traces:
+            tr.reset_cache()
+        for t in range(args.warmup):
+            for tr in traces:
+                tr.step(t)
+        # (the same timing events as the device-resident graphs, so both carry the same instrumentation)
+        egraphs, elogs = {}, []
         if not args.no_graphs:
             for k in range(args.steps):
                 for tr in traces:
-                    egraphs[(tr.T, k)] = tr.capture(args.warmup + args.steps + k, e2e=True, timed=False)[0]
+                    g, lg = tr.capture(args.warmup + k, e2e=True, timed=True)
+                    egraphs[(tr.T, k)] = g
+                    elogs.append(lg)
         torch.cuda.synchronize()
         log(f"{len(egraphs)} end-to-end step graphs captured")
         barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for k in range(args.steps):
-            t = args.warmup + args.steps + k
+            t = args.warmup + k
             for tr in traces:
                 tr.e2e_step(t, egraphs.get((tr.T, k)))
         e1.record()
@@ -629,9 +835,10 @@ def main():
         e2e = {"value": tokens / (ms_e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     # the graphs reference the traces' buffers: release them before the traces go
-    del graphs, logs
-    if not args.no_e2e:
-        del egraphs
+    if args.no_e2e:
+        del graphs, logs
+    else:
+        del egraphs, elogs
     torch.cuda.synchronize()
     log("decode legs done")
     derr = ft.ft_get_device_error()
@@ -645,7 +852,16 @@ def main():
         del tr, traces
         torch.cuda.empty_cache()
         log("prefill leg")
-        prefill = prefill_leg(ft, cfg, pool, routers, dev, args.prefill_chunks, link, peaks)
+        prefill = prefill_leg(ft, cfg, pool, routers, dev, [int(p) for p in args.prompts.split(",")], link, peaks)
+
+    nvfp4 = mixed = None
+    if not args.no_fp4 and world == 1:
+        pool.free()
+        torch.cuda.empty_cache()
+        log("nvfp4 stack")
+        nvfp4 = nvfp4_leg(ft, dev, peaks, link, batches, args.fp4_steps, args.warmup)
+        log("mxfp4 mixed trace")
+        mixed = mxfp4_mixed_leg(ft, dev, peaks, link, decode_steps=args.mixed_decode_steps)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -687,7 +903,9 @@ def main():
             "gpu_launches": launches,
             "cuda_graphs": not args.no_graphs,
             "clocks": clocks,
-            "prefill_8192": prefill,
+            "prefill_bf16": prefill,
+            "nvfp4_43L": nvfp4,
+            "mxfp4_mixed": mixed,
             "device_error": derr,
             "pool_fill_s": t_fill,
         }
