@@ -32,6 +32,14 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 BATCHES = (1, 4, 16, 64)
+
+# DRAM traffic per algorithmic byte, from one ncu capture of each kernel
+# (dram__bytes_read.sum + dram__bytes_write.sum over the algorithmic bytes of the
+# same launch; profiles/cache_fill_bf16_32experts.md, profiles/expert_tc_bf16_decode_T64.md).
+# The fill's reads come over the host link, so its DRAM traffic is the writes of
+# the filled experts that reached DRAM before the launch ended.
+TRAFFIC_PER_BYTE = {"fill": (0.133e6 + 140.343e6) / 201.327e6,
+                    "experts": (207.776e6 + 3.545e6 + 103.355e6 + 2.734e6) / (205.5e6 + 0.5e6 + 102.8e6)}
 CACHE_FRAC = 0.40
 METRIC = "MoE-layer tokens/s (decode T=1..64, prefill 8192) and % of layer roofline"
 
@@ -52,7 +60,7 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graphs", action="store_true", help="issue the decode steps eagerly instead of as CUDA graphs")
-    p.add_argument("--kernel-case", default="", choices=["", "experts_decode", "experts_prefill"],
+    p.add_argument("--kernel-case", default="", choices=["", "experts_decode", "experts_prefill", "fill"],
                    help="time one expert-kernel case on a small resident pool (profiling aid; prints its own line)")
     p.add_argument("--reps", type=int, default=5)
     p.add_argument("--case-config", default="", help="workload of --kernel-case (a synth config name)")
@@ -624,6 +632,42 @@ def reference_main(args, world, rank):
 
 # ---------------------------------------------------------------- single expert-kernel cases (profiling)
 
+def fill_case(args):
+    """Miss fill alone: a 1-layer BF16 pool (1.6 GB pinned), a fresh 64-slot cache, 32 routed experts.
+
+    Each repetition starts from an empty cache, so its one fill launch copies
+    all 32 experts (201 MB) over the host link."""
+    import expert_cache_streaming_fp32_b300 as ft
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    cfg = synth.DECODE_BF16
+    E = cfg.n_experts
+    pool = ft.ExpertPool(cfg, 1)
+    pool.fill(dev)
+    payload = int(ft.ft_expert_layout_get(cfg.wtype, cfg.hidden, cfg.inter).payload_bytes)
+    counts = torch.zeros(E, dtype=torch.int32, device=dev)
+    counts[torch.arange(0, E, E // 32)] = 1
+    slot_of = torch.empty(E, dtype=torch.int32, device=dev)
+    sc = torch.zeros(4, dtype=torch.int32, device=dev)
+    sp = torch.empty(64 * pool.S, dtype=torch.uint8, device=dev)
+    ms = []
+    for r in range(3 + args.reps):
+        cache = ft.Cache(1, E, 1, 64, 64, pool.S, pool.ptr, sp)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        cache.step(0, counts, 1.0, 0, slot_of, None, sc)
+        e1.record()
+        torch.cuda.synchronize()
+        if r >= 3:
+            ms.append(e0.elapsed_time(e1))
+        cache.destroy()
+    link = link_peak_gbs(pool.host, E * pool.S, dev)
+    t = float(np.median(ms))
+    print(json.dumps({"kernel_case": "fill", "experts": int(sc[2]), "ms": t,
+                      "link_gbs": int(sc[2]) * payload / (t * 1e-3) / 1e9, "link_peak_gbs": link,
+                      "device_error": ft.ft_get_device_error()}))
+
+
 def kernel_case(args):
     """One layer's experts resident in a 256-record slot pool (1.6 GB); ft_expert_grouped timed alone.
 
@@ -677,6 +721,9 @@ def main():
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         reference_main(args, world, rank)
+        return
+    if args.kernel_case == "fill":
+        fill_case(args)
         return
     if args.kernel_case:
         kernel_case(args)
@@ -785,13 +832,15 @@ def main():
     expert_hbm = unique_total * int(lay_bytes.payload_bytes)
     roof_fill = {"kernel": "ft_cache_step (control + fill launches)", "bound": "link",
                  "achieved": fill_bytes / cache_total_s / 1e9, "peak": link, "unit": "GB/s",
-                 "frac": fill_bytes / cache_total_s / 1e9 / link, "traffic": None,
+                 "frac": fill_bytes / cache_total_s / 1e9 / link,
+                 "traffic": TRAFFIC_PER_BYTE["fill"] * fill_bytes / max(n_ls, 1),
                  "algorithmic_bytes_per_launch": fill_bytes / max(n_ls, 1),
                  "avg_launch_ms": sum(cache_ms) / max(n_ls, 1),
                  "peak_source": "cudaMemcpyAsync pinned->device, measured in this run"}
     roof_exp = {"kernel": "ft_expert_grouped (row gather + tcgen05 gate/up + down launches)", "bound": "hbm",
                 "achieved": expert_hbm / expert_total_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": expert_hbm / expert_total_s / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                "frac": expert_hbm / expert_total_s / 1e9 / peaks["hbm_gbs"],
+                "traffic": TRAFFIC_PER_BYTE["experts"] * expert_hbm / max(n_ls, 1),
                 "algorithmic_bytes_per_launch": expert_hbm / max(n_ls, 1),
                 "avg_launch_ms": sum(expert_ms) / max(n_ls, 1),
                 "peak_source": f"MEASURED_PEAKS hbm_gbs ({peaks['source']})"}

@@ -85,6 +85,7 @@ cache_control_kernel(CacheDev d, int layer, const int32_t* __restrict__ counts, 
                      int32_t* __restrict__ slot_of, int32_t* __restrict__ ext_flags, int32_t* __restrict__ step_counts) {
   extern __shared__ __align__(16) unsigned char cc_smem[];
   __shared__ int buf[33];
+  pdl_begin();
   const int N = d.N, E = d.E;
   int32_t* s_order = reinterpret_cast<int32_t*>(cc_smem);          // [N]
   int32_t* s_victim = s_order + N;                            // [E]
@@ -219,6 +220,7 @@ constexpr uint64_t FILL_CHUNK = 64 * 1024;
 __global__ void __launch_bounds__(FILL_THREADS)
 cache_fill_kernel(const uint8_t* __restrict__ host, uint8_t* __restrict__ pool, uint64_t S, int n_rows_host, int n_slots,
                   const int32_t* __restrict__ src, const int32_t* __restrict__ dst, const int32_t* __restrict__ n_fill) {
+  pdl_begin();
   const int n = *n_fill;
   const uint64_t cpe = (S + FILL_CHUNK - 1) / FILL_CHUNK;
   const uint64_t items = (uint64_t)n * cpe;
@@ -253,6 +255,7 @@ cache_fill_kernel(const uint8_t* __restrict__ host, uint8_t* __restrict__ pool, 
 }
 
 __global__ void set_buffer_slots_kernel(int32_t* slot_of, int E, int base) {
+  pdl_begin();
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e < E) slot_of[e] = base + e;
 }

@@ -9,6 +9,8 @@
 #include <stdint.h>
 #include <stddef.h>
 
+#include <utility>
+
 #include "../../include/ft.h"
 
 #define FT_FULL_MASK 0xffffffffu
@@ -42,6 +44,36 @@ static inline int cuda_status(cudaError_t e) {
 __device__ int g_derr = 0;
 
 __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_derr, 0, code); }
+
+// ------------------------------------------------------------------ dependent launches
+// Every kernel of the library is launched with programmatic stream
+// serialization: it may start while the kernel before it on the stream is
+// still finishing, runs only set-up work that touches no global memory, and
+// then waits (griddepcontrol.wait) until that kernel has completed and its
+// memory is visible.  Right after the wait it lets the next kernel launch.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+static inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+#define FT_LAUNCH(kernel, grid, block, smem, stream, ...) \
+  FT_CHECK_CUDA(::ft::launch_pdl(kernel, dim3(grid), dim3(block), (size_t)(smem), (cudaStream_t)(stream), __VA_ARGS__))
 
 // ------------------------------------------------------------------ numeric helpers
 __device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }

@@ -330,6 +330,7 @@ __device__ __forceinline__ void gateup_rows(const ExpertArgs& a, const float* xs
 template <int WT, typename XT>
 __global__ void __launch_bounds__(EX_THREADS, 2)
 gateup_kernel(ExpertArgs a) {
+  pdl_begin();
   constexpr int EPL = WFmt<WT>::EPL;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ int warp_buf[EX_WARPS + 1];
@@ -446,6 +447,7 @@ __device__ __forceinline__ void down_rows(const ExpertArgs& a, const float* as, 
 template <int WT>
 __global__ void __launch_bounds__(EX_THREADS, 2)
 down_kernel(ExpertArgs a) {
+  pdl_begin();
   constexpr int EPL = WFmt<WT>::EPL;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ int warp_buf[EX_WARPS + 1];

@@ -50,7 +50,7 @@ constexpr int MAX_E = 1024;
 
 enum Mode { GATEUP = 0, DOWN = 1 };
 
-constexpr int LUT_BYTES = 256 * 4 + 256 * 2;  // e2m1 byte -> bf16x2, e4m3 byte -> bf16
+constexpr int LUT_BYTES = 256 * 2;  // e4m3 byte -> bf16
 
 __host__ __device__ constexpr bool is_fp4(int wt) { return wt == FT_W_NVFP4 || wt == FT_W_MXFP4; }
 
@@ -60,7 +60,8 @@ constexpr int CVT_THREADS = 256;
 constexpr int SCALE_AHEAD = 8;
 
 // bf16 weights: TMA writes the swizzled B tile.  NVFP4 / MXFP4: TMA stages
-// the packed rows (32 bytes per row per stage) and eight more warps expand them.
+// the packed rows (32 bytes per row per stage) and eight more warps expand them
+// (expand_fp4_half).
 template <int BN, int WT = FT_W_BF16>
 struct Cfg {
   static_assert(BN == 128 || BN == 256, "UMMA N");
@@ -87,13 +88,9 @@ __host__ __device__ constexpr size_t smem_bytes(int E) {
 // bf16 bits of an E8M0 scale 2^(b - 127) (b = 0 is the bf16 subnormal 2^-127).
 __device__ __forceinline__ uint32_t e8m0_bf16_bits(uint32_t b) { return b ? (b << 7) : 0x0040u; }
 
-// Tables: byte of two e2m1 codes (first element in the low nibble) -> bf16x2;
-// e4m3 byte -> bf16.  Every entry is exact.
-__device__ __forceinline__ void fill_fp4_tables(uint32_t* lut_e2m1, uint16_t* lut_e4m3, int nthreads) {
+// Table of e4m3 byte -> bf16 bits (exact: e4m3 has 3 mantissa bits).
+__device__ __forceinline__ void fill_fp4_tables(uint16_t* lut_e4m3, int nthreads) {
   for (int i = threadIdx.x; i < 256; i += nthreads) {
-    const float2 f = e2m1x2_to_float2((uint8_t)i);
-    __nv_bfloat162 h = __floats2bfloat162_rn(f.x, f.y);
-    lut_e2m1[i] = *reinterpret_cast<uint32_t*>(&h);
     __nv_bfloat16 b = __float2bfloat16_rn(e4m3_to_float((uint8_t)i));
     lut_e4m3[i] = *reinterpret_cast<uint16_t*>(&b);
   }
@@ -108,26 +105,47 @@ __device__ __forceinline__ uint32_t load_fp4_scales(const uint8_t* scale_row, in
   return __ldg(scale_row + kc / 32 + half);
 }
 
+// Two e2m1 codes (one byte, first element in the low nibble) -> f16x2, in hardware.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(r) : "r"(byte));
+  return r;
+}
+
+// bf16 bits of a block scale times 2^112 (see expand_fp4_half): e4m3 through
+// the table, E8M0 b as the exponent b + 112 (b <= 142, i.e. scales up to 2^15;
+// larger ones are recorded as FT_DERR_SCALE_RANGE).
+template <int WT>
+__device__ __forceinline__ uint32_t scale_bits_x2p112(uint32_t byte, const uint16_t* lut_e4m3) {
+  if (WT == FT_W_NVFP4) return lut_e4m3[byte] + (112u << 7);
+  if (byte > 142) record_error(FT_DERR_SCALE_RANGE);
+  return (byte + 112u) << 7;
+}
+
 // Half a row (32 elements): 16 packed bytes -> 32 bf16 (value x block scale,
-// exact) written as 4 16-byte chunks into a 128-byte-swizzled row.
+// exact) written as 4 16-byte chunks into a 128-byte-swizzled row.  Each pair
+// of codes becomes f16x2 in hardware; moving an f16's bits down by three
+// places reads it as a bf16 of the same sign and mantissa with the value
+// scaled by 2^-112 (zero stays zero), and the multiply by the block scale
+// times 2^112 restores it.  Every step is exact: e2m1 values have one
+// mantissa bit, and value x scale fits bf16.
 template <int WT>
 __device__ __forceinline__ void expand_fp4_half(const unsigned char* raw_row, int half, uint32_t sc,
-                                                const uint32_t* lut_e2m1, const uint16_t* lut_e4m3,
-                                                unsigned char* dst_row, int row) {
+                                                const uint16_t* lut_e4m3, unsigned char* dst_row, int row) {
   const uint4 p = reinterpret_cast<const uint4*>(raw_row)[half];
   const uint32_t packed[4] = {p.x, p.y, p.z, p.w};
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj) {  // 8 elements (one 16-byte chunk) per step
     const int j = half * 4 + jj;
-    uint32_t sbits;
-    if (WT == FT_W_NVFP4) sbits = lut_e4m3[(sc >> (8 * (jj >> 1))) & 0xff];
-    else sbits = e8m0_bf16_bits(sc & 0xff);
+    const uint32_t sbyte = WT == FT_W_NVFP4 ? (sc >> (8 * (jj >> 1))) & 0xff : sc & 0xff;
+    const uint32_t sbits = scale_bits_x2p112<WT>(sbyte, lut_e4m3);
     const uint32_t s2 = sbits | (sbits << 16);
     const __nv_bfloat162 sv = *reinterpret_cast<const __nv_bfloat162*>(&s2);
     uint32_t o[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      const uint32_t v = lut_e2m1[(packed[jj] >> (8 * b)) & 0xff];
+      const uint32_t h = e2m1x2_to_f16x2((packed[jj] >> (8 * b)) & 0xff);
+      const uint32_t v = ((h >> 3) & 0x0fff0fffu) | (h & 0x80008000u);
       __nv_bfloat162 w = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&v), sv);
       o[b] = *reinterpret_cast<uint32_t*>(&w);
     }
@@ -288,8 +306,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* scan_buf = const_cast<int*>(reinterpret_cast<volatile int*>(tmem_holder + 2));  // [C::THREADS / 32]
   uint32_t* epi_buf = reinterpret_cast<uint32_t*>(tail + 256);
-  uint32_t* lut_e2m1 = reinterpret_cast<uint32_t*>(tail + 256 + EPI_BYTES);
-  uint16_t* lut_e4m3 = reinterpret_cast<uint16_t*>(lut_e2m1 + 256);
+  uint16_t* lut_e4m3 = reinterpret_cast<uint16_t*>(tail + 256 + EPI_BYTES);
   int* act_e = reinterpret_cast<int*>(tail + 256 + EPI_BYTES + LUT_BYTES);
   int* act_pref = act_e + a.E;
 
@@ -324,7 +341,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
     tmem_relinquish();
   }
-  if (FP4) fill_fp4_tables(lut_e2m1, lut_e4m3, C::THREADS);
+  if (FP4) fill_fp4_tables(lut_e4m3, C::THREADS);
+  pdl_begin();  // set-up above touches no global memory; the expert list below reads the routing
   const int n_tiles_n = MODE == GATEUP ? a.I / (BN / 2) : ceil_div(a.H, BN);
   const int K = MODE == GATEUP ? a.H : a.I;
   const int nk = K / BK;
@@ -427,7 +445,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
       for (int ks = 0; ks < nk; ++ks) {
         const uint32_t sc = ring.next(srow_p, 0, nk, ks, half);
         if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
-        expand_fp4_half<WT>(smem + raw_off(stage) + row * 32, half, sc, lut_e2m1, lut_e4m3,
+        expand_fp4_half<WT>(smem + raw_off(stage) + row * 32, half, sc, lut_e4m3,
                             smem + stage * STAGE_BYTES + A_BYTES + row * 128, row);
         fence_proxy_async_smem();  // make the generic-proxy writes visible to the tensor core
         __syncwarp();
@@ -534,6 +552,7 @@ template <typename XT>
 __global__ void __launch_bounds__(256)
 gather_rows_kernel(const XT* __restrict__ x, const int32_t* __restrict__ perm, int T, int k, int H, int n_rows,
                    __nv_bfloat16* __restrict__ xp, int32_t* __restrict__ zero, int n_zero) {
+  pdl_begin();
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   for (long long i = tid; i < n_zero; i += (long long)gridDim.x * blockDim.x) zero[i] = 0;
   const int vpr = H / 8;  // 16-byte output vectors per row

@@ -22,10 +22,11 @@
 //   bf16 weights: TMA writes the 128-byte-swizzled weight tile directly.
 //   NVFP4 / MXFP4 weights: TMA stages the packed e2m1 bytes (32 per row per
 //   stage); warps 6..13 expand them to bf16 in the swizzled tile, half a row
-//   per thread, through a byte -> bf16x2 table, and multiply by the block scale
-//   (e4m3 or E8M0, read from the record SCALE_AHEAD stages ahead of use).  Every e2m1 value times its block
-//   scale is a bf16 number, so the expansion is exact; NVFP4's fp32 matrix
-//   scale multiplies the fp32 result in the epilogue.
+//   per thread (expand_fp4_half: hardware e2m1 -> f16 conversion and an exact
+//   multiply by the block scale, e4m3 or E8M0, read SCALE_AHEAD stages ahead
+//   of use).  Every e2m1 value times its block scale is a bf16 number, so the
+//   expansion is exact; NVFP4's fp32 matrix scale multiplies the fp32 result
+//   in the epilogue.
 #pragma once
 #include "expert_tc.cuh"
 
@@ -41,7 +42,7 @@ constexpr int SK_ACC_COLS = SK_NB;
 constexpr int SK_TMEM_COLS = 2 * SK_ACC_COLS;
 constexpr int SK_EX_STRIDE = SK_NB + 1;            // padded row of the hand-over buffer (no bank conflicts)
 constexpr int SK_EX_BYTES = 64 * SK_EX_STRIDE * 4; // gate/up: up values handed to the gate rows' threads
-constexpr int SK_LUT_BYTES = LUT_BYTES;             // e2m1 byte -> bf16x2, e4m3 byte -> bf16
+constexpr int SK_LUT_BYTES = LUT_BYTES;             // e4m3 byte -> bf16
 constexpr int SK_MAX_SPLITS = 8;
 
 template <int WT>
@@ -171,8 +172,7 @@ skinny_gemm_kernel(const __grid_constant__ CUtensorMap map_w0, const __grid_cons
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_holder + 2);
   int* scan_buf = const_cast<int*>(reinterpret_cast<volatile int*>(tmem_holder + 3));  // [C::WARPS]
   float* ex = reinterpret_cast<float*>(tail + 512);                                    // [64][SK_EX_STRIDE]
-  uint32_t* lut_e2m1 = reinterpret_cast<uint32_t*>(tail + 512 + SK_EX_BYTES);          // [256] bf16x2
-  uint16_t* lut_e4m3 = reinterpret_cast<uint16_t*>(lut_e2m1 + 256);                     // [256] bf16
+  uint16_t* lut_e4m3 = reinterpret_cast<uint16_t*>(tail + 512 + SK_EX_BYTES);          // [256] bf16
   int* act_e = reinterpret_cast<int*>(tail + 512 + SK_EX_BYTES + SK_LUT_BYTES);
   int* act_pref = act_e + a.E;
 
@@ -209,7 +209,8 @@ skinny_gemm_kernel(const __grid_constant__ CUtensorMap map_w0, const __grid_cons
     tmem_alloc(smem_u32(tmem_holder), SK_TMEM_COLS);
     tmem_relinquish();
   }
-  if (FP4) fill_fp4_tables(lut_e2m1, lut_e4m3, C::THREADS);
+  if (FP4) fill_fp4_tables(lut_e4m3, C::THREADS);
+  pdl_begin();  // set-up above touches no global memory; the expert list below reads the routing
   const int K = MODE == GATEUP ? a.H : a.I;
   const int nk = K / a.KS / BK;  // k-steps per split
   int n_act = 0;
@@ -318,8 +319,7 @@ skinny_gemm_kernel(const __grid_constant__ CUtensorMap map_w0, const __grid_cons
       for (int ks = 0; ks < nk; ++ks) {
         const uint32_t sc = ring.next(srow_p, kbase, nk, ks, half);
         if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
-        expand_fp4_half<WT>(smem + raw_off(stage) + c * 32, half, sc, lut_e2m1, lut_e4m3,
-                            smem + a_off(stage) + c * 128, c);
+        expand_fp4_half<WT>(smem + raw_off(stage) + c * 32, half, sc, lut_e4m3, smem + a_off(stage) + c * 128, c);
         fence_proxy_async_smem();  // make the generic-proxy writes visible to the tensor core
         __syncwarp();
         if (lane == 0) mbar_arrive(cvt_bar(stage));  // one arrival per converter warp

@@ -128,8 +128,7 @@ FT_API int ft_router_logits(const void* x, int x_type, const void* w_router, con
   cudaStream_t st = (cudaStream_t)s;
   auto go = [&](auto kernel, const auto* xx, const auto* ww) -> int {
     if (int r = set_smem(kernel, smem)) return r;
-    kernel<<<grid, RL_WARPS * 32, smem, st>>>(xx, ww, bias, T, H, E, logits);
-    FT_CHECK_LAUNCH();
+    FT_LAUNCH(kernel, grid, RL_WARPS * 32, smem, st, xx, ww, bias, T, H, E, logits);
     return FT_OK;
   };
   if (x_type == FT_X_BF16) {
@@ -161,13 +160,9 @@ FT_API int ft_route(const float* logits, int T, int E, int k, int32_t* topk_idx,
   dim3 grid(ceil_div(T, warps));
   cudaStream_t st = (cudaStream_t)s;
   const int per = ceil_div(E, 32);
-  if (per <= 1) route_kernel<1><<<grid, warps * 32, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
-  else if (per <= 2) route_kernel<2><<<grid, warps * 32, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
-  else if (per <= 4) route_kernel<4><<<grid, warps * 32, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
-  else if (per <= 8) route_kernel<8><<<grid, warps * 32, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
-  else if (per <= 16) route_kernel<16><<<grid, warps * 32, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
-  else route_kernel<32><<<grid, warps * 32, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
-  FT_CHECK_LAUNCH();
+  auto kr = per <= 1 ? route_kernel<1> : per <= 2 ? route_kernel<2> : per <= 4 ? route_kernel<4>
+          : per <= 8 ? route_kernel<8> : per <= 16 ? route_kernel<16> : route_kernel<32>;
+  FT_LAUNCH(kr, grid, warps * 32, 0, st, logits, T, E, k, topk_idx, topk_w);
   return FT_OK;
 }
 
@@ -181,8 +176,7 @@ FT_API int ft_permute(const int32_t* topk_idx, int T, int k, int E, int32_t* cou
   FT_REQUIRE(n == 0 || (topk_idx && perm && inv));
   const size_t smem = (size_t)(2 * E + PM_WARPS * E) * sizeof(int32_t);
   if (int st = set_smem(permute_kernel, smem)) return st;
-  permute_kernel<<<1, PM_THREADS, smem, (cudaStream_t)s>>>(topk_idx, (int)n, E, counts, offsets, perm, inv);
-  FT_CHECK_LAUNCH();
+  FT_LAUNCH(permute_kernel, 1, PM_THREADS, smem, s, topk_idx, (int)n, E, counts, offsets, perm, inv);
   return FT_OK;
 }
 
@@ -195,9 +189,7 @@ FT_API int ft_combine(const float* y, const int32_t* inv, const int32_t* topk_id
   FT_REQUIRE(y && inv && topk_idx && topk_w && out);
   FT_REQUIRE(T <= 65535 && k <= RT_MAXK);
   dim3 grid(ceil_div(H / 4, CB_THREADS), T);
-  combine_kernel<<<grid, CB_THREADS, 0, (cudaStream_t)s>>>(y, inv, topk_idx, topk_w, ext_flags, ext_partial, T, k, H, E,
-                                                            out);
-  FT_CHECK_LAUNCH();
+  FT_LAUNCH(combine_kernel, grid, CB_THREADS, 0, s, y, inv, topk_idx, topk_w, ext_flags, ext_partial, T, k, H, E, out);
   return FT_OK;
 }
 
@@ -275,17 +267,15 @@ int launch_expert(const ExpertArgs& a, cudaStream_t st) {
   if (a.x_type == FT_X_BF16) {
     auto kg = gateup_kernel<WT, __nv_bfloat16>;
     if (int s = set_smem(kg, smem_gu)) return s;
-    kg<<<occupancy_grid(kg, EX_THREADS, smem_gu), EX_THREADS, smem_gu, st>>>(a);
+    FT_LAUNCH(kg, occupancy_grid(kg, EX_THREADS, smem_gu), EX_THREADS, smem_gu, st, a);
   } else {
     auto kg = gateup_kernel<WT, float>;
     if (int s = set_smem(kg, smem_gu)) return s;
-    kg<<<occupancy_grid(kg, EX_THREADS, smem_gu), EX_THREADS, smem_gu, st>>>(a);
+    FT_LAUNCH(kg, occupancy_grid(kg, EX_THREADS, smem_gu), EX_THREADS, smem_gu, st, a);
   }
-  FT_CHECK_LAUNCH();
   auto kd = down_kernel<WT>;
   if (int s = set_smem(kd, smem_dn)) return s;
-  kd<<<occupancy_grid(kd, EX_THREADS, smem_dn), EX_THREADS, smem_dn, st>>>(a);
-  FT_CHECK_LAUNCH();
+  FT_LAUNCH(kd, occupancy_grid(kd, EX_THREADS, smem_dn), EX_THREADS, smem_dn, st, a);
   return FT_OK;
 }
 
@@ -355,10 +345,8 @@ int launch_tc_gemms(const CUtensorMap& mx, const CUtensorMap& mg, const CUtensor
   auto kd = tc::grouped_gemm_kernel<tc::DOWN, BN, WT>;
   if (int s = set_smem(kg, smem)) return s;
   if (int s = set_smem(kd, smem)) return s;
-  kg<<<sms(), NT, smem, st>>>(mx, mg, mu, a);
-  FT_CHECK_LAUNCH();
-  kd<<<sms(), NT, smem, st>>>(ma, md, md, a);
-  FT_CHECK_LAUNCH();
+  FT_LAUNCH(kg, sms(), NT, smem, st, mx, mg, mu, a);
+  FT_LAUNCH(kd, sms(), NT, smem, st, ma, md, md, a);
   return FT_OK;
 }
 
@@ -410,12 +398,10 @@ int launch_skinny_wt(const ExpertArgs& ea, const ft_expert_layout& L, const TcWo
   if (int s = set_smem(kd, smem)) return s;
   a.KS = w.ks_gu;
   a.counters = counters;
-  kg<<<sms(), NT, smem, st>>>(mg, mu, mx, a);
-  FT_CHECK_LAUNCH();
+  FT_LAUNCH(kg, sms(), NT, smem, st, mg, mu, mx, a);
   a.KS = w.ks_dn;
   a.counters = counters + w.g_gu;
-  kd<<<sms(), NT, smem, st>>>(md, md, ma, a);
-  FT_CHECK_LAUNCH();
+  FT_LAUNCH(kd, sms(), NT, smem, st, md, md, ma, a);
   return FT_OK;
 }
 
@@ -444,12 +430,11 @@ int launch_expert_tc(int wtype, const ExpertArgs& ea, const ft_expert_layout& L,
     int32_t* zero = skinny ? reinterpret_cast<int32_t*>(ws + w.off_counters) : nullptr;
     const int n_zero = skinny ? (int)(w.g_gu + w.g_dn) : 0;
     if (ea.x_type == FT_X_BF16)
-      tc::gather_rows_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)ea.x, ea.perm, ea.T, ea.k, H,
-                                                                  (int)Tk, xp, zero, n_zero);
+      FT_LAUNCH(tc::gather_rows_kernel<__nv_bfloat16>, grid, 256, 0, st, (const __nv_bfloat16*)ea.x, ea.perm, ea.T,
+                ea.k, H, (int)Tk, xp, zero, n_zero);
     else
-      tc::gather_rows_kernel<float><<<grid, 256, 0, st>>>((const float*)ea.x, ea.perm, ea.T, ea.k, H, (int)Tk, xp,
-                                                          zero, n_zero);
-    FT_CHECK_LAUNCH();
+      FT_LAUNCH(tc::gather_rows_kernel<float>, grid, 256, 0, st, (const float*)ea.x, ea.perm, ea.T, ea.k, H, (int)Tk,
+                xp, zero, n_zero);
   }
   if (skinny) return launch_expert_skinny(wtype, ea, L, w, ws, st);
   CUtensorMap mx, mg, mu, ma, md;
@@ -600,12 +585,11 @@ FT_API int ft_cache_step(ft_cache* c, int layer, const int32_t* counts, double f
   if (c->streaming) return FT_ESTATE;
   cudaStream_t st = (cudaStream_t)s;
   const size_t smem = cache_control_smem(c->N, c->E);
-  cache_control_kernel<<<1, CC_THREADS, smem, st>>>(cache_dev(c), layer, counts, fill_ratio, wave, slot_of, ext_flags,
-                                                     step_counts);
-  FT_CHECK_LAUNCH();
-  cache_fill_kernel<<<c->fill_grid, FILL_THREADS, 0, st>>>(c->host_dev, c->pool, c->S, c->Lp * c->E, c->max_slots,
-                                                           c->fill_src, c->fill_dst, c->n_fill);
-  FT_CHECK_LAUNCH();
+  FT_LAUNCH(cache_control_kernel, 1, CC_THREADS, smem, st, cache_dev(c), layer, counts, fill_ratio, wave, slot_of,
+            ext_flags, step_counts);
+  FT_LAUNCH(cache_fill_kernel, c->fill_grid, FILL_THREADS, 0, st, (const uint8_t*)c->host_dev, c->pool, c->S,
+            c->Lp * c->E, c->max_slots, (const int32_t*)c->fill_src, (const int32_t*)c->fill_dst,
+            (const int32_t*)c->n_fill);
   return FT_OK;
 }
 
@@ -683,8 +667,7 @@ FT_API int ft_stream_layer(ft_stream* st, int layer, int next_layer, int32_t* sl
     st->next_buf = b ^ 1;
   }
   FT_CHECK_CUDA(cudaStreamWaitEvent(cs, st->ready[b], 0));
-  set_buffer_slots_kernel<<<ceil_div(c->E, 256), 256, 0, cs>>>(slot_of, c->E, st->base + b * c->E);
-  FT_CHECK_LAUNCH();
+  FT_LAUNCH(set_buffer_slots_kernel, ceil_div(c->E, 256), 256, 0, cs, slot_of, c->E, st->base + b * c->E);
   st->pending_layer = -1;
   if (next_layer >= 0 && buffer_of(st, next_layer) < 0) {
     const int nb = b ^ 1;

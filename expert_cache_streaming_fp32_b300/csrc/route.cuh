@@ -37,11 +37,22 @@ __global__ void __launch_bounds__(RL_WARPS * 32)
 router_logits_kernel(const XT* __restrict__ x, const XT* __restrict__ wr, const float* __restrict__ bias,
                      int T, int H, int E, float* __restrict__ z) {
   extern __shared__ float xs[];  // [RT][H]
+  pdl_begin();
   const int t0 = blockIdx.y * RT;
   const int nrows = min(RT, T - t0);
-  for (int i = threadIdx.x; i < RT * H; i += blockDim.x) {
-    int r = i / H, h = i - r * H;
-    xs[i] = r < nrows ? (float)x[(size_t)(t0 + r) * H + h] : 0.0f;
+  // stage the rows 8 elements (one 16-byte bf16 load or two fp32 loads) per thread step
+  for (int r = 0; r < RT; ++r) {
+    for (int h = threadIdx.x * 8; h < H; h += blockDim.x * 8) {
+      float v[8];
+      if (r < nrows) {
+        load8<XT>(x + (size_t)(t0 + r) * H + h, v);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+      }
+      *reinterpret_cast<float4*>(xs + r * H + h) = make_float4(v[0], v[1], v[2], v[3]);
+      *reinterpret_cast<float4*>(xs + r * H + h + 4) = make_float4(v[4], v[5], v[6], v[7]);
+    }
   }
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -100,6 +111,7 @@ template <int PER_LANE>
 __global__ void __launch_bounds__(256)
 route_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ idx_out,
              float* __restrict__ w_out) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -176,6 +188,7 @@ __global__ void __launch_bounds__(PM_THREADS)
 permute_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __restrict__ counts,
                int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
   extern __shared__ int32_t pm_smem[];
+  pdl_begin();
   int32_t* cnt = pm_smem;                    // [E]
   int32_t* base = cnt + E;                // [E] running position per expert (absolute)
   int32_t* wc = base + E;                 // [PM_WARPS][E]
@@ -274,6 +287,7 @@ __global__ void __launch_bounds__(CB_THREADS)
 combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv, const int32_t* __restrict__ idx,
                const float* __restrict__ w, const int32_t* __restrict__ ext, const float* __restrict__ P,
                int T, int k, int H, int E, float* __restrict__ out) {
+  pdl_begin();
   const int t = blockIdx.y;
   const int h4 = blockIdx.x * blockDim.x + threadIdx.x;
   if (h4 * 4 >= H) return;

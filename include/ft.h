@@ -75,8 +75,10 @@ enum {
   FT_DERR_SLOT_INDEX = 2,    /* a slot outside the pool */
   FT_DERR_ROW_INDEX = 3,     /* a permutation row outside [0, T*k) */
   FT_DERR_TABLE = 4,         /* cache tables inconsistent */
-  FT_DERR_TIMEOUT = 5        /* a kernel's bounded wait on an on-chip barrier ran out; the kernel
+  FT_DERR_TIMEOUT = 5,       /* a kernel's bounded wait on an on-chip barrier ran out; the kernel
                                 stopped early and its outputs are incomplete */
+  FT_DERR_SCALE_RANGE = 6    /* an MXFP4 block scale above 2^15 (E8M0 byte > 142), beyond the range
+                                of the tensor-core expansion; the affected outputs are wrong */
 };
 
 const char* ft_status_str(int status);
