@@ -372,19 +372,39 @@ def prefill_leg(ft, cfg, pool, routers0, dev, prompts, link_gbs, peaks, chunk=81
     torch.cuda.synchronize()
     lay.forward_slots(xs[0], routers0[0][0], zero, slot_of, sp, pool.S, n_slots)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    reps = 3
+    reps = 5
     e0.record()
     for _ in range(reps):
         lay.forward_slots(xs[0], routers0[0][0], zero, slot_of, sp, pool.S, n_slots)
     e1.record()
     torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    # the expert call alone (ft_expert_grouped on the resident layer), timed the same way
+    xq = xs[0]
+    e0.record()
+    for _ in range(reps):
+        lay.experts(xq, slot_of, sp, pool.S, n_slots)
+    e1.record()
+    torch.cuda.synchronize()
+    ms_exp = e0.elapsed_time(e1) / reps
     st.layer_done(0)
     st.destroy()
-    ms = e0.elapsed_time(e1) / reps
-    flops = 2.0 * 8192 * cfg.top_k * 3 * cfg.hidden * cfg.inter
+    Tk, H, I, E_ = chunk * cfg.top_k, cfg.hidden, cfg.inter, cfg.n_experts
+    U = int((lay.counts > 0).sum())
+    wb = int(ft.ft_expert_layout_get(cfg.wtype, H, I).payload_bytes) / 3.0   # bytes of one weight matrix
+    flops_gu, flops_dn = 2.0 * Tk * 2 * H * I, 2.0 * Tk * H * I
+    bytes_gu = U * 2 * wb + chunk * H * 2 + Tk * I * 2                         # weights, rows of x, intermediate
+    bytes_dn = U * wb + Tk * I * 2 + Tk * H * 4                                # weights, intermediate, fp32 output
+    roof_s = (max(flops_gu / (peaks["bf16_tflops"] * 1e12), bytes_gu / (peaks["hbm_gbs"] * 1e9)) +
+              max(flops_dn / (peaks["bf16_tflops"] * 1e12), bytes_dn / (peaks["hbm_gbs"] * 1e9)))
+    flops = flops_gu + flops_dn
     res["compute_only_ms_per_layer"] = ms
-    res["expert_tflops"] = flops / (ms * 1e-3) / 1e12
+    res["expert_call_ms"] = ms_exp
+    res["expert_tflops"] = flops / (ms_exp * 1e-3) / 1e12
     res["expert_tensor_frac_of_bf16"] = res["expert_tflops"] / peaks["bf16_tflops"]
+    res["expert_roofline_frac"] = roof_s / (ms_exp * 1e-3)
+    res["expert_roofline_note"] = ("per product max(FLOPs / bf16 peak, bytes / HBM peak): gate/up and down are "
+                                   "both near the ridge (about 256 rows per expert); down writes fp32 output")
     res["loss_without_overlap"] = 1.0 - res["serialized"]["tokens_per_s"] / res["overlapped"]["tokens_per_s"]
     cache.destroy()
     del sp, lay

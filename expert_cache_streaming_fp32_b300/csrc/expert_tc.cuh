@@ -59,15 +59,24 @@ constexpr int CVT_THREADS = 256;
 // Stages of block scales a converter thread keeps in flight ahead of use.
 constexpr int SCALE_AHEAD = 8;
 
+// Threads that gather token rows straight from x (GA mode): one 16-byte chunk
+// of 8 rows per stage each.
+constexpr int GATHER_THREADS = 128;
+// Stages a gather thread keeps in flight before it marks the oldest ready.
+constexpr int GATHER_DEPTH = 2;
+
 // bf16 weights: TMA writes the swizzled B tile.  NVFP4 / MXFP4: TMA stages
 // the packed rows (32 bytes per row per stage) and eight more warps expand them
-// (expand_fp4_half).
-template <int BN, int WT = FT_W_BF16>
+// (expand_fp4_half).  GA: the A tile (token rows) is gathered from x by four
+// more warps with 16-byte cp.async copies instead of a TMA load of
+// pre-gathered rows.
+template <int BN, int WT = FT_W_BF16, bool GA = false>
 struct Cfg {
   static_assert(BN == 128 || BN == 256, "UMMA N");
   static constexpr bool FP4 = is_fp4(WT);
   static_assert(!FP4 || BN == 128, "FP4 expansion covers 128-row weight tiles");
-  static constexpr int THREADS = FP4 ? 192 + CVT_THREADS : 192;
+  static_assert(!(FP4 && GA), "one helper role per kernel");
+  static constexpr int THREADS = 192 + (FP4 ? CVT_THREADS : 0) + (GA ? GATHER_THREADS : 0);
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int RAW_BYTES = FP4 ? BN * BK / 2 : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + RAW_BYTES;
@@ -78,9 +87,9 @@ struct Cfg {
 
 // Bytes of dynamic shared memory: 1 KiB alignment slack, the stages, the
 // barriers, the epilogue transpose buffers, the FP4 tables, then the expert list.
-template <int BN, int WT = FT_W_BF16>
+template <int BN, int WT = FT_W_BF16, bool GA = false>
 __host__ __device__ constexpr size_t smem_bytes(int E) {
-  return 1024 + (size_t)Cfg<BN, WT>::STAGES * Cfg<BN, WT>::STAGE_BYTES + 256 + EPI_BYTES + LUT_BYTES +
+  return 1024 + (size_t)Cfg<BN, WT, GA>::STAGES * Cfg<BN, WT, GA>::STAGE_BYTES + 256 + EPI_BYTES + LUT_BYTES +
          (size_t)(2 * E + 2) * 4;
 }
 
@@ -181,6 +190,8 @@ struct Args {
   uint64_t off_scale[3];
   uint64_t off_gscale;
   uint64_t S;
+  const __nv_bfloat16* x;    // [T][H] (GA: token rows are gathered from here)
+  const int32_t* perm;       // [T*k] (GA)
   __nv_bfloat16* Aint;       // [T*k][I]
   float* y;                  // [T*k][H]
 };
@@ -280,12 +291,12 @@ __device__ __forceinline__ Tile decode_tile(const Args& a, const int* act_e, con
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int MODE, int BN, int WT>
-__global__ void __launch_bounds__(Cfg<BN, WT>::THREADS, 1)
+template <int MODE, int BN, int WT, bool GA>
+__global__ void __launch_bounds__(Cfg<BN, WT, GA>::THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
                     const __grid_constant__ CUtensorMap map_b1, Args a) {
   using namespace sm100;
-  using C = Cfg<BN, WT>;
+  using C = Cfg<BN, WT, GA>;
   constexpr bool FP4 = C::FP4;
   constexpr int STAGES = C::STAGES;
   constexpr int STAGE_BYTES = C::STAGE_BYTES;
@@ -322,7 +333,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
+      // GA: the producer's arrival (B bytes) plus one per gather warp (A rows)
+      mbar_init(full_bar(s), GA ? 1 + GATHER_THREADS / 32 : 1);
       mbar_init(empty_bar(s), 1);
       mbar_init(cvt_bar(s), CVT_THREADS / 32);
     }
@@ -369,8 +381,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
           const uint32_t sb = FP4 ? sbase + raw_off(stage) : sa + A_BYTES;
           const int kb = FP4 ? ks * BK / 2 : ks * BK;
           const uint32_t half = FP4 ? RAW_BYTES / 2 : B_BYTES / 2;
-          mbar_arrive_expect_tx(full_bar(stage), A_BYTES + (FP4 ? RAW_BYTES : B_BYTES));
-          tma_load_2d(sa, &map_a, full_bar(stage), ks * BK, t.row0);
+          mbar_arrive_expect_tx(full_bar(stage), (GA ? 0 : A_BYTES) + (FP4 ? RAW_BYTES : B_BYTES));
+          if (!GA) tma_load_2d(sa, &map_a, full_bar(stage), ks * BK, t.row0);
           if (MODE == GATEUP) {
             tma_load_3d(sb, &map_b0, full_bar(stage), kb, t.nt * (BN / 2), t.slot);
             tma_load_3d(sb + half, &map_b1, full_bar(stage), kb, t.nt * (BN / 2), t.slot);
@@ -425,7 +437,58 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
         mbar_drain(drain_bar, 0);
       }
     }
-  } else if (warp >= 6) {
+  } else if (GA && warp >= 6) {
+    // ---------------------------------------------------------------- token-row gather (warps 6..9)
+    // Thread g copies chunk c = g % 8 (16 bytes = 8 elements along K) of tile
+    // rows g / 8 + 16 j, j = 0..7, into the 128-byte-swizzled A tile.  The
+    // copies of a stage are marked ready GATHER_DEPTH stages later, once this
+    // thread's cp.async group for it has completed.
+    const int g = threadIdx.x - 192;
+    const int c = g & 7, r0 = g >> 3;
+    const long long Tk = (long long)a.T * a.k;
+    int stage = 0, pending = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+      const Tile t = decode_tile(a, act_e, act_pref, n_act, item);
+      const __nv_bfloat16* src[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const long long p = min((long long)t.row0 + r0 + 16 * j, Tk - 1);  // rows past the end: any valid row
+        int tok = a.perm[p] / a.k;
+        if ((unsigned)tok >= (unsigned)a.T) {
+          record_error(FT_DERR_ROW_INDEX);
+          tok = 0;
+        }
+        src[j] = a.x + (size_t)tok * a.H + c * 8;
+      }
+      for (int ks = 0; ks < nk; ++ks) {
+        if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag)) { ok = false; break; }
+        const uint32_t sa = sbase + stage * STAGE_BYTES;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = r0 + 16 * j;
+          cp_async16(sa + r * 128 + ((c ^ (r & 7)) << 4), src[j] + ks * BK);
+        }
+        cp_async_commit();
+        if (++pending > GATHER_DEPTH) {
+          cp_async_wait<GATHER_DEPTH>();   // the group of stage (stage - GATHER_DEPTH) has landed
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full_bar((stage - GATHER_DEPTH + STAGES) % STAGES));
+          --pending;
+        }
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+    }
+    cp_async_wait<0>();
+    if (ok) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      for (; pending > 0; --pending)
+        if (lane == 0) mbar_arrive(full_bar((stage - pending + STAGES) % STAGES));
+    }
+  } else if (FP4 && warp >= 6) {
     // ---------------------------------------------------------------- FP4 expansion (warps 6..13)
     const int c = threadIdx.x - 192;
     const int row = c >> 1, half = c & 1;  // B-tile row and which 32 of its 64 elements

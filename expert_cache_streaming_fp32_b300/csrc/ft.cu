@@ -336,19 +336,20 @@ bool tc_path_applies(int wtype, int T, int k, int H, int I, int E) {
 
 // Tile width: 256 columns from FT_TC_WIDE_ASSIGNMENTS assignments up (fewer,
 // larger tiles), 128 below (twice the tiles, so a few experts still cover the SMs).
-template <int BN, int WT>
+template <int BN, int WT, bool GA>
 int launch_tc_gemms(const CUtensorMap& mx, const CUtensorMap& mg, const CUtensorMap& mu, const CUtensorMap& ma,
                     const CUtensorMap& md, const tc::Args& a, cudaStream_t st) {
-  const size_t smem = tc::smem_bytes<BN, WT>(a.E);
-  constexpr int NT = tc::Cfg<BN, WT>::THREADS;
-  auto kg = tc::grouped_gemm_kernel<tc::GATEUP, BN, WT>;
-  auto kd = tc::grouped_gemm_kernel<tc::DOWN, BN, WT>;
+  // gate/up gathers its token rows itself in GA mode; down reads the intermediate in permuted order
+  const size_t smem = tc::smem_bytes<BN, WT, GA>(a.E), smem_d = tc::smem_bytes<BN, WT, false>(a.E);
+  auto kg = tc::grouped_gemm_kernel<tc::GATEUP, BN, WT, GA>;
+  auto kd = tc::grouped_gemm_kernel<tc::DOWN, BN, WT, false>;
   if (int s = set_smem(kg, smem)) return s;
-  if (int s = set_smem(kd, smem)) return s;
-  FT_LAUNCH(kg, sms(), NT, smem, st, mx, mg, mu, a);
-  FT_LAUNCH(kd, sms(), NT, smem, st, ma, md, md, a);
+  if (int s = set_smem(kd, smem_d)) return s;
+  FT_LAUNCH(kg, sms(), (tc::Cfg<BN, WT, GA>::THREADS), smem, st, mx, mg, mu, a);
+  FT_LAUNCH(kd, sms(), (tc::Cfg<BN, WT, false>::THREADS), smem_d, st, ma, md, md, a);
   return FT_OK;
 }
+
 
 // Small batches: weights on the MMA's M side, token rows on N, K split when few experts are routed.
 template <int WT>
@@ -423,8 +424,10 @@ int launch_expert_tc(int wtype, const ExpertArgs& ea, const ft_expert_layout& L,
   __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(ws);
   __nv_bfloat16* aint = reinterpret_cast<__nv_bfloat16*>(ws + w.off_aint);
   const bool skinny = Tk < FT_TC_WIDE_ASSIGNMENTS;
-  // gather the permuted rows (bf16); clear the split counters of the small-batch kernels
-  {
+  // large batches of bf16 rows with bf16 weights: the gate/up kernel gathers its rows itself
+  const bool direct = !skinny && wtype == FT_W_BF16 && ea.x_type == FT_X_BF16;
+  // otherwise gather the permuted rows (bf16); clear the split counters of the small-batch kernels
+  if (!direct) {
     const long long vecs = Tk * (H / 8);
     const int grid = (int)std::min<long long>(ceil_div((int)std::min<long long>(vecs, 1ll << 30), 256), 8 * sms());
     int32_t* zero = skinny ? reinterpret_cast<int32_t*>(ws + w.off_counters) : nullptr;
@@ -465,13 +468,17 @@ int launch_expert_tc(int wtype, const ExpertArgs& ea, const ft_expert_layout& L,
   a.pool = ea.pool;
   for (int m = 0; m < 3; ++m) a.off_scale[m] = L.off_scale[m];
   a.off_gscale = L.off_gscale;
+  a.x = reinterpret_cast<const __nv_bfloat16*>(ea.x);
+  a.perm = ea.perm;
   a.Aint = aint; a.y = ea.y;
   switch (wtype) {
     case FT_W_BF16:
-      return BN == 256 ? launch_tc_gemms<256, FT_W_BF16>(mx, mg, mu, ma, md, a, st)
-                       : launch_tc_gemms<128, FT_W_BF16>(mx, mg, mu, ma, md, a, st);
-    case FT_W_NVFP4: return launch_tc_gemms<128, FT_W_NVFP4>(mx, mg, mu, ma, md, a, st);
-    case FT_W_MXFP4: return launch_tc_gemms<128, FT_W_MXFP4>(mx, mg, mu, ma, md, a, st);
+      if (direct) return BN == 256 ? launch_tc_gemms<256, FT_W_BF16, true>(mx, mg, mu, ma, md, a, st)
+                                   : launch_tc_gemms<128, FT_W_BF16, true>(mx, mg, mu, ma, md, a, st);
+      return BN == 256 ? launch_tc_gemms<256, FT_W_BF16, false>(mx, mg, mu, ma, md, a, st)
+                       : launch_tc_gemms<128, FT_W_BF16, false>(mx, mg, mu, ma, md, a, st);
+    case FT_W_NVFP4: return launch_tc_gemms<128, FT_W_NVFP4, false>(mx, mg, mu, ma, md, a, st);
+    case FT_W_MXFP4: return launch_tc_gemms<128, FT_W_MXFP4, false>(mx, mg, mu, ma, md, a, st);
   }
   return FT_EINVAL;
 }

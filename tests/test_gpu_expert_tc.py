@@ -29,8 +29,8 @@ def ft(ftlib):
     return ftlib
 
 
-def _setup(ft, H, I, E, k, T, seed, skewed=False, wtype=synth.W_BF16):
-    cfg = synth.MoEConfig(f"tc_{H}_{I}_{E}", H, E, k, I, 1, wtype, "bf16", seed=seed)
+def _setup(ft, H, I, E, k, T, seed, skewed=False, wtype=synth.W_BF16, xdt="bf16"):
+    cfg = synth.MoEConfig(f"tc_{H}_{I}_{E}", H, E, k, I, 1, wtype, xdt, seed=seed)
     L = ft.ft_expert_layout_get(wtype, H, I)
     S = int(L.bytes)
     n_slots = E + 5
@@ -199,3 +199,19 @@ def test_tc_fp4_expert_parity(ft, wtype, H, I, E, k, T, seed):
     assert np.isfinite(got).all()
     assert_close_layer(got, ref, fro=1e-2)
     assert rel_fro(got, ref) < 2e-3
+
+
+@pytest.mark.parametrize("T,k", [(300, 8), (20, 4)])
+def test_tc_fp32_activations_are_rounded_to_bf16(ft, T, k):
+    """fp32 x with bf16 weights: the rows are rounded to bf16 (RNE) on their way to the tensor cores."""
+    H, I, E = 512, 256, 8
+    cfg, L, S, n_slots, pool, slot_perm, comps, x, idx = _setup(ft, H, I, E, k, T, 31, xdt="f32")
+    assert x.dtype == torch.float32
+    counts, offsets, perm, inv = moe.permute(idx, E)
+    Y = _run(ft, x, k, I, E, perm, offsets, slot_perm.astype(np.int32), pool, S, n_slots)
+    xs = formats.round_to_bf16(formats.to_f64(x))
+    ref = np.concatenate([moe.expert_ffn(xs[perm[offsets[e]:offsets[e + 1]] // k],
+                                         *(formats.dequant(comps[e][m], synth.W_BF16) for m in ("gate", "up", "down")),
+                                         act_round=formats.round_to_bf16) for e in range(E)])
+    assert_close_layer(Y, ref, fro=1e-2)
+    assert rel_fro(Y, ref) < 2e-3
