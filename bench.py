@@ -42,6 +42,8 @@ TRAFFIC_PER_BYTE = {"fill": (0.133e6 + 140.343e6) / 201.327e6,
                     "experts": (207.776e6 + 3.545e6 + 103.355e6 + 2.734e6) / (205.5e6 + 0.5e6 + 102.8e6)}
 CACHE_FRAC = 0.40
 METRIC = "MoE-layer tokens/s (decode T=1..64, prefill 8192) and % of layer roofline"
+WORKLOAD = ("decode_bf16_40L: H=2048 E=256 top-8 I=512, bf16 weights, 40 layers, "
+            "cache 40% (4096 slots) per batch size, AR(1)+Zipf(1.1) traces")
 
 
 def parse():
@@ -95,22 +97,25 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(world, v: float) -> float:
+def _reduce(world, v: float, op_name: str) -> float:
+    """All-reduce of one float over the ranks (device tensor for NCCL, host tensor for gloo)."""
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=getattr(dist.ReduceOp, op_name))
     return float(t.item())
+
+
+def max_over_ranks(world, v: float) -> float:
+    """The slowest rank's time: the job takes as long as its slowest replica."""
+    return _reduce(world, v, "MAX")
 
 
 def sum_over_ranks(world, v: float) -> float:
-    if world == 1:
-        return v
-    import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
+    """Work summed over the replicas (each rank runs its own traces)."""
+    return _reduce(world, v, "SUM")
 
 
 # ---------------------------------------------------------------- measurement helpers
@@ -644,7 +649,7 @@ def reference_main(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "decode_bf16_40L (oracle sample)", "batches": [1]},
+        "config": {"workload": WORKLOAD, "batches": list(BATCHES), "parallelism": "replicas1"},
         "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
@@ -950,8 +955,7 @@ def main():
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": "decode_bf16_40L: H=2048 E=256 top-8 I=512, bf16 weights, 40 layers, "
-                                   "cache 40% (4096 slots) per batch size, AR(1)+Zipf(1.1) traces",
+            "config": {"workload": WORKLOAD,
                        "batches": batches, "tokens_per_step": tokens_per_step, "host_pool_layers": n_phys,
                        "host_pool_gb": pool.n_phys * E * S / 1e9, "weights": "bf16", "accumulate": "f32",
                        "l2": "inputs larger than L2 (each step reads >= 2 GB of expert weights)",

@@ -35,7 +35,7 @@ EXPORTED = [
     "ft_cache_destroy", "ft_cache_n_waves", "ft_cache_step", "ft_cache_resize", "ft_cache_stats",
     "ft_cache_export", "ft_expert_grouped_workspace", "ft_expert_grouped", "ft_combine", "ft_stream_create",
     "ft_stream_layer", "ft_stream_layer_done", "ft_stream_bytes", "ft_stream_destroy", "ft_qsplit",
-    "ft_expert_grouped_noalloc",
+    "ft_expert_grouped_noalloc", "ft_debug_bounded_wait",
 ]
 FT_NOALLOC_MAX_ELEMS = 1 << 20
 
@@ -96,6 +96,7 @@ _sigs = {
     "ft_stream_destroy": (_I, [_P]),
     "ft_qsplit": (_I, [_I, ctypes.c_double, ctypes.c_double]),
     "ft_expert_grouped_noalloc": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, ctypes.c_uint64, _I, _P, _P]),
+    "ft_debug_bounded_wait": (_I, [ctypes.c_int64, _P, _P]),
 }
 for _name, (_res, _args) in _sigs.items():
     _f = getattr(_lib, _name)
@@ -152,6 +153,11 @@ def ft_expert_layout_get(wtype: int, hidden: int, inter: int) -> ExpertLayout:
     L = ExpertLayout()
     _check("ft_expert_layout_get", _lib.ft_expert_layout_get(wtype, hidden, inter, ctypes.byref(L)))
     return L
+
+
+def ft_debug_bounded_wait(limit_ns: int, completed, stream=None):
+    """Runs the bounded-wait failure path on purpose (a barrier that nothing completes)."""
+    _check("ft_debug_bounded_wait", _lib.ft_debug_bounded_wait(int(limit_ns), _ptr(completed), _stream(stream)))
 
 
 def ft_qsplit(m: int, bw_fill: float, bw_host: float) -> int:

@@ -80,6 +80,12 @@ FT_API int ft_get_device_error(int* code) {
   return v ? FT_EDEVICE : FT_OK;
 }
 
+FT_API int ft_debug_bounded_wait(int64_t limit_ns, int* completed, ft_cuda_stream s) {
+  FT_REQUIRE(completed && limit_ns > 0 && limit_ns <= 2000000000ll);
+  FT_LAUNCH(sm100::bounded_wait_probe_kernel, 1, 32, 0, s, (uint64_t)limit_ns, completed);
+  return FT_OK;
+}
+
 FT_API int ft_expert_layout_get(int wtype, int hidden, int inter, ft_expert_layout* out) {
   FT_REQUIRE(out);
   return expert_layout(wtype, hidden, inter, out);

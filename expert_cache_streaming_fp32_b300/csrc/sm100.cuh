@@ -61,14 +61,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Waits for the phase with the given parity to complete.  Returns false (and
 // raises *abort) if another role already aborted or the wait ran past the
 // limit; the caller then stops issuing work.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 0) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         *abort = 1;
         record_error(FT_DERR_TIMEOUT);
         return false;
@@ -82,6 +83,22 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity))
     if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+}
+
+// A wait on a barrier that nothing completes: it must give up after limit_ns,
+// record FT_DERR_TIMEOUT and return (the failure path of every wait above,
+// exercised on purpose with a short limit).
+__global__ void bounded_wait_probe_kernel(uint64_t limit_ns, int* result) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  pdl_begin();
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) *result = mbar_wait(smem_u32(&bar), 0, &abort_flag, limit_ns) ? 1 : 0;
 }
 
 // ------------------------------------------------------------------ TMA

@@ -90,6 +90,12 @@ int ft_last_cuda_error(void);
  * non-zero, FT_OK otherwise. */
 int ft_get_device_error(int* code);
 
+/* Test hook for the failure path of the kernels' bounded waits.  Launches one
+ * CTA that waits on an on-chip barrier which nothing completes; after limit_ns
+ * (1 .. 2e9) the wait gives up, the kernel records FT_DERR_TIMEOUT, writes 0
+ * to *completed (dev int) and returns, leaving the context usable. */
+int ft_debug_bounded_wait(int64_t limit_ns, int* completed, ft_cuda_stream s);
+
 /* ------------------------------------------------------------------------
  * Expert record layout.
  *

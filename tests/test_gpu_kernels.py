@@ -227,3 +227,22 @@ def test_out_of_range_expert_is_recorded_not_faulted(ft):
     assert ft.ft_get_device_error() == 0      # cleared by the read
     o = out.cpu().numpy()
     assert np.allclose(o[[0, 1, 3]], 1.0) and np.allclose(o[2], 0.5)
+
+
+def test_bounded_wait_gives_up_and_reports(ft):
+    """A barrier wait that nothing completes times out, records FT_DERR_TIMEOUT and returns.
+
+    This is the failure path of every on-chip wait in the tensor-core kernels,
+    run on purpose with a 20 ms limit; afterwards the context keeps working."""
+    assert ft.ft_get_device_error() == 0
+    done = torch.full((1,), 7, dtype=torch.int32, device=DEV)
+    ft.ft_debug_bounded_wait(20_000_000, done)
+    torch.cuda.synchronize()
+    assert int(done) == 0                       # the wait did not complete
+    assert ft.ft_get_device_error() == 5        # FT_DERR_TIMEOUT, cleared by the read
+    assert ft.ft_get_device_error() == 0
+    # the context is still usable: a routing call gives the oracle's answer
+    z = torch.tensor([[0.5, 2.0, -1.0, 2.0]], device=DEV)
+    idx, w = _i32((1, 2)), _f32((1, 2))
+    ft.ft_route(z, 2, idx, w)
+    assert idx.cpu().tolist() == [[1, 3]]
