@@ -62,7 +62,13 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graphs", action="store_true", help="issue the decode steps eagerly instead of as CUDA graphs")
-    p.add_argument("--kernel-case", default="", choices=["", "experts_decode", "experts_prefill", "fill"],
+    p.add_argument("--split-min-assignments", type=int, default=0,
+                   help="smallest decode batch T*k for the split form (0: the library's policy)")
+    p.add_argument("--no-split-fill", action="store_true",
+                   help="decode with ft_cache_step (fill, then all experts) instead of the split form "
+                        "(hits evaluated while the fill copies)")
+    p.add_argument("--kernel-case", default="", choices=["", "experts_decode", "experts_prefill", "fill",
+                                                         "fill_overlap"],
                    help="time one expert-kernel case on a small resident pool (profiling aid; prints its own line)")
     p.add_argument("--reps", type=int, default=5)
     p.add_argument("--case-config", default="", help="workload of --kernel-case (a synth config name)")
@@ -204,8 +210,11 @@ def host_ram_bytes() -> int:
 class DecodeTrace:
     """One batch size: its cache, per-step buffers, resident inputs and per-layer-step counters."""
 
-    def __init__(self, ft, cfg, T, pool, routers, n_steps, dev, e2e, n_slots=None):
+    def __init__(self, ft, cfg, T, pool, routers, n_steps, dev, e2e, n_slots=None, split_min=64):
         self.ft, self.cfg, self.T = ft, cfg, T
+        # the split form where it pays
+        self.fill_stream = (torch.cuda.Stream(device=dev) if split_min and ft.split_pays(T, cfg.top_k, split_min)
+                            else None)
         L, E = cfg.n_layers, cfg.n_experts
         self.n_slots = n_slots or int(round(CACHE_FRAC * L * E))
         self.S = pool.S
@@ -240,7 +249,10 @@ class DecodeTrace:
     def launches_per_step(self) -> int:
         # router_logits, route, permute, (control, fill, expert kernels) per wave, combine;
         # bf16 experts run gather + gate/up + down on the tensor cores, other formats gate/up + down
+        # (the split form evaluates hits and filled experts in two expert calls)
         n_exp = 3 if self.cfg.wtype == synth.W_BF16 else 2
+        if self.fill_stream is not None:
+            n_exp *= 2
         return self.cfg.n_layers * (3 + (2 + n_exp) * self.n_waves + 1)
 
     def capture(self, t, e2e=False, timed=True):
@@ -265,10 +277,28 @@ class DecodeTrace:
             for w in range(self.n_waves):
                 if ev is not None:
                     ev.rec("cache")
-                cache.step(l, lay.counts, 1.0, w, lay.slot_of, lay.ext, self.hist[t, l, w])
+                if self.fill_stream is None:
+                    cache.step(l, lay.counts, 1.0, w, lay.slot_of, lay.ext, self.hist[t, l, w])
+                    if ev is not None:
+                        ev.rec("fill_end")
+                    lay.experts(x, lay.slot_of, self.sp, self.S, self.n_slots)
+                    if ev is not None:
+                        ev.rec("expert_end")
+                    continue
+                fs = self.fill_stream
+                cache.step_split(l, lay.counts, 1.0, w, lay.slot_of, lay.slot_fill, lay.ext, self.hist[t, l, w],
+                                 fill_stream=fs)
                 if ev is not None:
-                    ev.rec("cache_end")
-                lay.experts(x, lay.slot_of, self.sp, self.S, self.n_slots)
+                    ev.rec("ctrl_end")
+                    ev.rec("fill_end", fs)
+                lay.experts(x, lay.slot_of, self.sp, self.S, self.n_slots)          # hits, during the fill
+                if ev is not None:
+                    ev.rec("hit_end")
+                cache.fill_join()
+                if ev is not None:
+                    torch.cuda.current_stream().wait_stream(fs)                    # joins the timing event too
+                    ev.rec("join")
+                lay.experts(x, lay.slot_fill, self.sp, self.S, self.n_slots)        # the filled experts
                 if ev is not None:
                     ev.rec("expert_end")
             out = lay.combine(self.T, lay.ext, None)
@@ -295,18 +325,44 @@ class EventLog:
         self.ev = []
         self.external = external
 
-    def rec(self, tag):
+    def rec(self, tag, stream=None):
         e = torch.cuda.Event(enable_timing=True, external=self.external)
-        e.record()
+        e.record(stream)
         self.ev.append((tag, e))
 
     def spans(self, start_tag, end_tag):
+        """Each start_tag event to the next end_tag event after it."""
         out = []
         for i, (tag, e) in enumerate(self.ev):
             if tag == start_tag:
-                out.append(e.elapsed_time(self.ev[i + 1][1]))
-                assert self.ev[i + 1][0] == end_tag
+                j = next(j for j in range(i + 1, len(self.ev)) if self.ev[j][0] == end_tag)
+                out.append(e.elapsed_time(self.ev[j][1]))
         return out
+
+    def cache_expert_spans(self):
+        """Per wave: (control + fill span, expert span).  In the split form the
+        expert span is the hits' call plus the filled experts' call after the join."""
+        cache = self.spans("cache", "fill_end")
+        if any(tag == "hit_end" for tag, _ in self.ev):
+            hit, miss = self.spans("ctrl_end", "hit_end"), self.spans("join", "expert_end")
+            return cache, [a + b for a, b in zip(hit, miss)]
+        return cache, self.spans("fill_end", "expert_end")
+
+
+def spans_us(logs):
+    """Mean CUDA-event spans per wave (us): control + fill, and the expert calls
+    (in the split form: the hits' call, which runs beside the fill, and the
+    filled experts' call after the join)."""
+    def mean(v):
+        return 1e3 * sum(v) / max(len(v), 1)
+    out = {"control_fill": mean([v for ev in logs for v in ev.spans("cache", "fill_end")])}
+    if any(tag == "hit_end" for tag, _ in logs[0].ev):
+        out["hits"] = mean([v for ev in logs for v in ev.spans("ctrl_end", "hit_end")])
+        out["wait_for_fill"] = mean([v for ev in logs for v in ev.spans("hit_end", "join")])
+        out["filled"] = mean([v for ev in logs for v in ev.spans("join", "expert_end")])
+    else:
+        out["experts"] = mean([v for ev in logs for v in ev.spans("fill_end", "expert_end")])
+    return out
 
 
 def layer_roofline_seconds(hist: np.ndarray, T: int, cfg, S_payload: int, peaks, link_gbs: float):
@@ -419,9 +475,9 @@ def prefill_leg(ft, cfg, pool, routers0, dev, prompts, link_gbs, peaks, chunk=81
 
 # ---------------------------------------------------------------- secondary workloads
 
-def decode_trace_leg(ft, cfg, T, pool, routers, n_slots, steps, warmup, dev, peaks, link, payload):
+def decode_trace_leg(ft, cfg, T, pool, routers, n_slots, steps, warmup, dev, peaks, link, payload, split_min=64):
     """One batch size on its own cache: eager warm-up, then ``steps`` graph-replayed decode steps."""
-    tr = DecodeTrace(ft, cfg, T, pool, routers, warmup + steps, dev, False, n_slots=n_slots)
+    tr = DecodeTrace(ft, cfg, T, pool, routers, warmup + steps, dev, False, n_slots=n_slots, split_min=split_min)
     for t in range(warmup):
         tr.step(t)
     graphs = [tr.capture(warmup + k) for k in range(steps)]
@@ -435,8 +491,8 @@ def decode_trace_leg(ft, cfg, T, pool, routers, n_slots, steps, warmup, dev, pea
     ms = e0.elapsed_time(e1)
     h = tr.counts(warmup, warmup + steps)
     roof, _ = layer_roofline_seconds(h, T, cfg, payload, peaks, link)
-    cache_ms = sum(v for _, ev in graphs for v in ev.spans("cache", "cache_end"))
-    expert_ms = sum(v for _, ev in graphs for v in ev.spans("cache_end", "expert_end"))
+    cache_ms = sum(v for _, ev in graphs for v in ev.cache_expert_spans()[0])
+    expert_ms = sum(v for _, ev in graphs for v in ev.cache_expert_spans()[1])
     out = {"tokens_per_s": T * steps / (ms * 1e-3), "ms_per_step": ms / steps,
            "layer_roofline_frac": roof / (ms * 1e-3), "hit_rate": float(h[..., 1].sum() / max(h[..., 0].sum(), 1)),
            "fill_gbs": float(h[..., 2].sum()) * payload / max(cache_ms * 1e-3, 1e-12) / 1e9,
@@ -448,7 +504,7 @@ def decode_trace_leg(ft, cfg, T, pool, routers, n_slots, steps, warmup, dev, pea
     return out
 
 
-def nvfp4_leg(ft, dev, peaks, link, batches, steps, warmup):
+def nvfp4_leg(ft, dev, peaks, link, batches, steps, warmup, split_min=64):
     """The 43-layer NVFP4 stack: decode at 40% cache per batch size, and 8192-token streamed prefill.
 
     The host pool stores a cyclic window of 4 physical layers (logical layer l
@@ -464,7 +520,7 @@ def nvfp4_leg(ft, dev, peaks, link, batches, steps, warmup):
     for T in batches:
         log(f"nvfp4 decode T={T}")
         res["decode"][str(T)] = decode_trace_leg(ft, cfg, T, pool, routers, n_slots, steps, warmup, dev, peaks, link,
-                                                 payload)
+                                                 payload, split_min)
     log("nvfp4 prefill")
     pf = prefill_leg(ft, cfg, pool, routers, dev, [8192], link, peaks)
     res["prefill_8192"] = pf
@@ -472,7 +528,7 @@ def nvfp4_leg(ft, dev, peaks, link, batches, steps, warmup):
     return res
 
 
-def mxfp4_mixed_leg(ft, dev, peaks, link, decode_steps=512, cycles=4):
+def mxfp4_mixed_leg(ft, dev, peaks, link, decode_steps=512, cycles=4, split_min=64):
     """The MXFP4 agent-like trace on 4 layers: cycles of (8192-token prefill, T=1 decode run).
 
     The cache is resized at the safe point before each cycle (57.8% -> 40% ->
@@ -502,13 +558,15 @@ def mxfp4_mixed_leg(ft, dev, peaks, link, decode_steps=512, cycles=4):
     trace = synth.AR1Trace(cfg, 1, dev, tag=5)
     slot_of = torch.empty(E, dtype=torch.int32, device=dev)
     ratio = 0.7
+    fs = torch.cuda.Stream(device=dev)                        # the fill stream of the split form
+    fs_d = fs if split_min and ft.split_pays(1, cfg.top_k, split_min) else None
+    fs_p = fs if split_min and ft.split_pays(8192, cfg.top_k, split_min) else None
 
     def decode_layers():
         for l in range(L):
             lay_d.route(x_d, *routers[l])
             for w in range(cache.n_waves()):
-                cache.step(l, lay_d.counts, ratio, w, lay_d.slot_of, lay_d.ext, counts_d[l, w])
-                lay_d.experts(x_d, lay_d.slot_of, sp, pool.S, max_slots)
+                lay_d.cached_wave(x_d, l, cache, pool.S, ratio, w, counts_d[l, w], fill_stream=fs_d)
             lay_d.combine(1, lay_d.ext, P_d)
 
     cyc = []
@@ -529,7 +587,8 @@ def mxfp4_mixed_leg(ft, dev, peaks, link, decode_steps=512, cycles=4):
                 st.layer_done(l)
         else:
             for l in range(L):
-                lay_p.forward_cached(xp, routers[l][0], zero_b, l, cache, pool.S, fill_ratio=ratio, ext_partial=P_p)
+                lay_p.forward_cached(xp, routers[l][0], zero_b, l, cache, pool.S, fill_ratio=ratio, ext_partial=P_p,
+                                     fill_stream=fs_p)
         e1.record()
         torch.cuda.synchronize()
         p_ms = e0.elapsed_time(e1)
@@ -693,6 +752,78 @@ def fill_case(args):
                       "device_error": ft.ft_get_device_error()}))
 
 
+def fill_overlap_case(args):
+    """Fill blocks vs the fill's rate alone and beside an expert call.
+
+    The 32-expert fill of ``fill`` on a second stream, with 20 back-to-back
+    64-token expert calls over a resident layer on the first (the overlap of
+    a split cache step), for several fill block counts."""
+    import expert_cache_streaming_fp32_b300 as ft
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    cfg = synth.DECODE_BF16
+    E = cfg.n_experts
+    pool = ft.ExpertPool(cfg, 1)
+    pool.fill(dev)
+    S = pool.S
+    payload = int(ft.ft_expert_layout_get(cfg.wtype, cfg.hidden, cfg.inter).payload_bytes)
+    resident = pool.host[: E * S].to(dev)
+    so = torch.arange(E, dtype=torch.int32, device=dev)
+    counts = torch.zeros(E, dtype=torch.int32, device=dev)
+    counts[torch.arange(0, E, E // 32)] = 1
+    slot_of = torch.empty(E, dtype=torch.int32, device=dev)
+    sc = torch.zeros(4, dtype=torch.int32, device=dev)
+    sp = torch.empty(64 * S, dtype=torch.uint8, device=dev)
+    fs = torch.cuda.Stream()
+    T, n_calls = 64, 20
+    lay = ft.MoELayer(cfg, T, dev)
+    x = synth.activations(cfg, T, tag=1, device=dev)
+    lay.route(x, *synth.router_weights(cfg, 0, dev))
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    def experts():
+        for _ in range(n_calls):
+            lay.experts(x, so, resident, S, E)
+
+    def once(blocks, beside):
+        cache = ft.Cache(1, E, 1, 64, 64, S, pool.ptr, sp)
+        cache.set_fill_blocks(blocks)
+        torch.cuda.synchronize()
+        f0, f1, m0, m1 = ev(), ev(), ev(), ev()
+        f0.record(fs)
+        cache.step(0, counts, 1.0, 0, slot_of, None, sc, stream=fs)
+        f1.record(fs)
+        if beside:
+            m0.record()
+            experts()
+            m1.record()
+        torch.cuda.synchronize()
+        cache.destroy()
+        return f0.elapsed_time(f1), (m0.elapsed_time(m1) if beside else None)
+
+    m0, m1 = ev(), ev()
+    alone = []
+    for _ in range(3):
+        m0.record()
+        experts()
+        m1.record()
+        torch.cuda.synchronize()
+        alone.append(m0.elapsed_time(m1))
+    rows = []
+    for blocks in (4, 8, 16, 32, 64, 148, 296):
+        a = [once(blocks, False)[0] for _ in range(3)][1:]
+        b = [once(blocks, True) for _ in range(3)][1:]
+        rows.append({"fill_blocks": blocks,
+                     "fill_alone_gbs": 32 * payload / (np.mean(a) * 1e-3) / 1e9,
+                     "fill_beside_gbs": 32 * payload / (np.mean([f for f, _ in b]) * 1e-3) / 1e9,
+                     "experts_beside_ms": float(np.mean([m for _, m in b]))})
+    print(json.dumps({"kernel_case": "fill_overlap", "fill_experts": 32, "expert_calls": n_calls, "T": T,
+                      "experts_alone_ms": float(np.median(alone)), "rows": rows,
+                      "device_error": ft.ft_get_device_error()}))
+
+
 def kernel_case(args):
     """One layer's experts resident in a 256-record slot pool (1.6 GB); ft_expert_grouped timed alone.
 
@@ -750,6 +881,9 @@ def main():
     if args.kernel_case == "fill":
         fill_case(args)
         return
+    if args.kernel_case == "fill_overlap":
+        fill_overlap_case(args)
+        return
     if args.kernel_case:
         kernel_case(args)
         return
@@ -757,6 +891,8 @@ def main():
     dev = f"cuda:{local}"
     cfg = synth.DECODE_BF16
     peaks = load_peaks()
+    # smallest decode batch (T*k) run in the split form; 0: never
+    split_min = 0 if args.no_split_fill else (args.split_min_assignments or ft.SPLIT_MIN_ASSIGNMENTS)
     batches = [int(b) for b in args.batches.split(",")]
     L, E = cfg.n_layers, cfg.n_experts
     lay_bytes = ft.ft_expert_layout_get(cfg.wtype, cfg.hidden, cfg.inter)
@@ -772,7 +908,8 @@ def main():
     routers = [synth.router_weights(cfg, l, dev) for l in range(L)]
     link = link_peak_gbs(pool.host, E * S, dev)
     n_steps = args.warmup + args.steps
-    traces = [DecodeTrace(ft, cfg, T, pool, routers, n_steps, dev, not args.no_e2e) for T in batches]
+    traces = [DecodeTrace(ft, cfg, T, pool, routers, n_steps, dev, not args.no_e2e, split_min=split_min)
+              for T in batches]
     tokens_per_step = sum(batches)
 
     log(f"pool of {n_phys} layers filled in {t_fill:.1f} s; link {link:.1f} GB/s")
@@ -795,6 +932,7 @@ def main():
     log(f"{len(graphs)} step graphs captured")
     # timed region
     logs = []
+    logs_T = {}
     tb = []
     barrier(world)
     torch.cuda.synchronize()
@@ -814,6 +952,7 @@ def main():
                 ev = EventLog()
                 tr.step(t, ev)
             logs.append(ev)
+            logs_T.setdefault(tr.T, []).append(ev)
     e_end.record()
     torch.cuda.synchronize()
     barrier(world)
@@ -830,8 +969,8 @@ def main():
     for i in range(len(tb)):
         per_T[marks[i][0]] += marks[i][1].elapsed_time(marks[i + 1][1])
     # kernel spans
-    cache_ms = [v for ev in logs for v in ev.spans("cache", "cache_end")]
-    expert_ms = [v for ev in logs for v in ev.spans("cache_end", "expert_end")]
+    cache_ms = [v for ev in logs for v in ev.cache_expert_spans()[0]]
+    expert_ms = [v for ev in logs for v in ev.cache_expert_spans()[1]]
 
     # roofline over the timed layer steps
     roof_s, roof_detail = 0.0, {"hbm_bytes": 0.0, "link_bytes": 0.0, "flops": 0.0}
@@ -933,9 +1072,10 @@ def main():
         pool.free()
         torch.cuda.empty_cache()
         log("nvfp4 stack")
-        nvfp4 = nvfp4_leg(ft, dev, peaks, link, batches, args.fp4_steps, args.warmup)
+        nvfp4 = nvfp4_leg(ft, dev, peaks, link, batches, args.fp4_steps, args.warmup, split_min)
         log("mxfp4 mixed trace")
-        mixed = mxfp4_mixed_leg(ft, dev, peaks, link, decode_steps=args.mixed_decode_steps)
+        mixed = mxfp4_mixed_leg(ft, dev, peaks, link, decode_steps=args.mixed_decode_steps,
+                                split_min=split_min)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -959,12 +1099,16 @@ def main():
                        "batches": batches, "tokens_per_step": tokens_per_step, "host_pool_layers": n_phys,
                        "host_pool_gb": pool.n_phys * E * S / 1e9, "weights": "bf16", "accumulate": "f32",
                        "l2": "inputs larger than L2 (each step reads >= 2 GB of expert weights)",
+                       "fill": ("ft_cache_step (fill, then all experts)" if args.no_split_fill else
+                                f"{split_min} <= T*k < {ft.FT_TC_WIDE_ASSIGNMENTS}: ft_cache_step_split (hits "
+                                "evaluated while the fill copies on a second stream); other batches: ft_cache_step"),
                        "parallelism": f"replicas{world}"},
             "layer_roofline_frac": layer_roofline_frac,
             "per_batch": {str(T): {"tokens_per_s": T * args.steps / (per_T[T] * 1e-3),
                                    "ms_per_step": per_T[T] / args.steps,
                                    "layer_roofline_frac": per_T_roof[T] / (per_T[T] * 1e-3),
-                                   "hit_rate": hit_rate[T]}
+                                   "hit_rate": hit_rate[T],
+                                   "us_per_wave": spans_us(logs_T[T])}
                           for T in batches},
             "roofline": dominant,
             "roofline_experts": roof_exp,

@@ -35,9 +35,11 @@ EXPORTED = [
     "ft_cache_destroy", "ft_cache_n_waves", "ft_cache_step", "ft_cache_resize", "ft_cache_stats",
     "ft_cache_export", "ft_expert_grouped_workspace", "ft_expert_grouped", "ft_combine", "ft_stream_create",
     "ft_stream_layer", "ft_stream_layer_done", "ft_stream_bytes", "ft_stream_destroy", "ft_qsplit",
-    "ft_expert_grouped_noalloc", "ft_debug_bounded_wait",
+    "ft_expert_grouped_noalloc", "ft_debug_bounded_wait", "ft_cache_step_split", "ft_cache_fill_join",
+    "ft_cache_set_fill_blocks",
 ]
 FT_NOALLOC_MAX_ELEMS = 1 << 20
+FT_TC_WIDE_ASSIGNMENTS = 2048
 
 
 class FTError(RuntimeError):
@@ -82,6 +84,9 @@ _sigs = {
     "ft_cache_destroy": (_I, [_P]),
     "ft_cache_n_waves": (_I, [_P]),
     "ft_cache_step": (_I, [_P, _I, _P, ctypes.c_double, _I, _P, _P, _P, _P]),
+    "ft_cache_step_split": (_I, [_P, _I, _P, ctypes.c_double, _I, _P, _P, _P, _P, _P, _P]),
+    "ft_cache_fill_join": (_I, [_P, _P]),
+    "ft_cache_set_fill_blocks": (_I, [_P, _I]),
     "ft_cache_resize": (_I, [_P, _I]),
     "ft_cache_stats": (_I, [_P, ctypes.POINTER(CacheStats)]),
     "ft_cache_export": (_I, [_P, _P, _P, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_uint32)]),
@@ -275,6 +280,19 @@ class Cache:
                                                    _ptr(slot_of), _ptr(ext_flags), _ptr(step_counts),
                                                    _stream(stream)))
 
+    def step_split(self, layer, counts, fill_ratio, wave, slot_hit, slot_fill, ext_flags=None, step_counts=None,
+                   stream=None, fill_stream=None):
+        _check("ft_cache_step_split",
+               _lib.ft_cache_step_split(self.h, layer, _ptr(counts), float(fill_ratio), wave, _ptr(slot_hit),
+                                        _ptr(slot_fill), _ptr(ext_flags), _ptr(step_counts), _stream(stream),
+                                        _stream(fill_stream)))
+
+    def set_fill_blocks(self, blocks: int):
+        _check("ft_cache_set_fill_blocks", _lib.ft_cache_set_fill_blocks(self.h, blocks))
+
+    def fill_join(self, stream=None):
+        _check("ft_cache_fill_join", _lib.ft_cache_fill_join(self.h, _stream(stream)))
+
     def resize(self, n_slots):
         _check("ft_cache_resize", _lib.ft_cache_resize(self.h, n_slots))
 
@@ -320,4 +338,4 @@ class Stream:
             _check("ft_stream_destroy", st)
 
 
-from .layer import ExpertPool, MoELayer, pack_expert  # noqa: E402,F401
+from .layer import SPLIT_MIN_ASSIGNMENTS, ExpertPool, MoELayer, pack_expert, split_pays  # noqa: E402,F401

@@ -23,6 +23,9 @@ struct ft_cache {
   int32_t* fill_dst;        // [E] slot
   int32_t* n_fill;          // [1]
   int fill_grid;
+  cudaEvent_t ev_ctrl;      // split steps: control done on the compute stream
+  cudaEvent_t ev_fill;      // split steps: fill done on the fill stream
+  int pending_join;         // a split step's fill has not been joined yet
   int streaming;            // a stream handle holds the last 2E slots
   int n_full;               // capacity to restore after streaming
   int dev;
@@ -79,10 +82,12 @@ __device__ __forceinline__ int cc_scan(int v, int* buf, int& total) {
 }
 
 // One wave of one layer step (one CTA).  Shared memory: order copy [N] ints,
-// touched flags [N] bytes, victims [E] ints.
+// touched flags [N] bytes, victims [E] ints.  With slot_fill (the split form)
+// the filled experts' slots go there and slot_of keeps only the hits.
 __global__ void __launch_bounds__(CC_THREADS)
 cache_control_kernel(CacheDev d, int layer, const int32_t* __restrict__ counts, double ratio, int wave,
-                     int32_t* __restrict__ slot_of, int32_t* __restrict__ ext_flags, int32_t* __restrict__ step_counts) {
+                     int32_t* __restrict__ slot_of, int32_t* __restrict__ slot_fill, int32_t* __restrict__ ext_flags,
+                     int32_t* __restrict__ step_counts) {
   extern __shared__ __align__(16) unsigned char cc_smem[];
   __shared__ int buf[33];
   pdl_begin();
@@ -107,6 +112,7 @@ cache_control_kernel(CacheDev d, int layer, const int32_t* __restrict__ counts, 
   const bool in_wave = routed && rank >= w0 && rank < w0 + N;
   if (valid_e) {
     slot_of[e] = -1;
+    if (slot_fill) slot_fill[e] = -1;
     if (wave == 0 && ext_flags) ext_flags[e] = 0;
   }
   const int nW = max(0, min(N, nU - w0));
@@ -167,7 +173,8 @@ cache_control_kernel(CacheDev d, int layer, const int32_t* __restrict__ counts, 
     d.slot_of_key[key] = v;
     d.stamp[v] = c;
     s_touched[v] = 1;
-    slot_of[e] = v;
+    if (slot_fill) slot_fill[e] = v;
+    else slot_of[e] = v;
     d.fill_src[mrank] = (layer % d.Lp) * E + e;
     d.fill_dst[mrank] = v;
   }

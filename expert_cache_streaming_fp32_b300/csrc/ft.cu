@@ -567,12 +567,27 @@ FT_API int ft_cache_create(const ft_cache_config* cfg, ft_cache** out) {
   t.clock = 0;
   if (!st) st = upload_tables(c, t);
   if (!st) st = set_smem(cache_control_kernel, cache_control_smem(c->max_slots, c->E));
+  // The fill may run beside the expert kernels (split steps), which need most of
+  // the shared memory: ask for the largest shared-memory carveout so that an SM
+  // running fill blocks need not drain to take an expert block.
+  if (!st && cudaFuncSetAttribute(cache_fill_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+    st = FT_ECUDA;
+  if (!st && (cudaEventCreateWithFlags(&c->ev_ctrl, cudaEventDisableTiming) != cudaSuccess ||
+              cudaEventCreateWithFlags(&c->ev_fill, cudaEventDisableTiming) != cudaSuccess))
+    st = FT_ECUDA;
   if (!st && cudaDeviceSynchronize() != cudaSuccess) st = FT_ECUDA;
   if (st) {
     ft_cache_destroy(c);
     return st;
   }
-  c->fill_grid = 2 * sms();
+  // 8 blocks of 256 threads, 4 x 16 B reads in flight per thread: 128 KiB in
+  // flight already keeps the host link busy (51.4 GB/s for 8 or for 296 blocks,
+  // measured on B300).  More reads in flight only queue in the memory system,
+  // where they held up the HBM reads of expert kernels running beside the fill
+  // (a 64-token expert call took 3.4x as long beside 148 fill blocks, 1.2x
+  // beside 8).
+  c->fill_grid = 8;
   *out = c;
   return FT_OK;
 }
@@ -581,6 +596,8 @@ FT_API int ft_cache_destroy(ft_cache* c) {
   if (!c) return FT_OK;
   cudaFree(c->slot_of_key); cudaFree(c->key_of_slot); cudaFree(c->stamp); cudaFree(c->order);
   cudaFree(c->clock); cudaFree(c->stats); cudaFree(c->fill_src); cudaFree(c->fill_dst); cudaFree(c->n_fill);
+  if (c->ev_ctrl) cudaEventDestroy(c->ev_ctrl);
+  if (c->ev_fill) cudaEventDestroy(c->ev_fill);
   delete c;
   return FT_OK;
 }
@@ -595,20 +612,64 @@ FT_API int ft_cache_step(ft_cache* c, int layer, const int32_t* counts, double f
   FT_REQUIRE(c && counts && slot_of);
   FT_REQUIRE(layer >= 0 && layer < c->L && wave >= 0 && wave < ceil_div(c->E, c->N));
   FT_REQUIRE(fill_ratio > 0.0);
-  if (c->streaming) return FT_ESTATE;
+  if (c->streaming || c->pending_join) return FT_ESTATE;
   cudaStream_t st = (cudaStream_t)s;
   const size_t smem = cache_control_smem(c->N, c->E);
   FT_LAUNCH(cache_control_kernel, 1, CC_THREADS, smem, st, cache_dev(c), layer, counts, fill_ratio, wave, slot_of,
-            ext_flags, step_counts);
+            (int32_t*)nullptr, ext_flags, step_counts);
   FT_LAUNCH(cache_fill_kernel, c->fill_grid, FILL_THREADS, 0, st, (const uint8_t*)c->host_dev, c->pool, c->S,
             c->Lp * c->E, c->max_slots, (const int32_t*)c->fill_src, (const int32_t*)c->fill_dst,
             (const int32_t*)c->n_fill);
   return FT_OK;
 }
 
+FT_API int ft_cache_step_split(ft_cache* c, int layer, const int32_t* counts, double fill_ratio, int wave,
+                               int32_t* slot_hit, int32_t* slot_fill, int32_t* ext_flags, int32_t* step_counts,
+                               ft_cuda_stream s, ft_cuda_stream fill_s) {
+  FT_REQUIRE(c && counts && slot_hit && slot_fill && slot_hit != slot_fill);
+  FT_REQUIRE(layer >= 0 && layer < c->L && wave >= 0 && wave < ceil_div(c->E, c->N));
+  FT_REQUIRE(fill_ratio > 0.0);
+  if (c->streaming || c->pending_join) return FT_ESTATE;
+  cudaStream_t st = (cudaStream_t)s, fs = (cudaStream_t)fill_s;
+  const size_t smem = cache_control_smem(c->N, c->E);
+  FT_LAUNCH(cache_control_kernel, 1, CC_THREADS, smem, st, cache_dev(c), layer, counts, fill_ratio, wave, slot_hit,
+            slot_fill, ext_flags, step_counts);
+  if (fs == st) {
+    FT_LAUNCH(cache_fill_kernel, c->fill_grid, FILL_THREADS, 0, st, (const uint8_t*)c->host_dev, c->pool, c->S,
+              c->Lp * c->E, c->max_slots, (const int32_t*)c->fill_src, (const int32_t*)c->fill_dst,
+              (const int32_t*)c->n_fill);
+    return FT_OK;
+  }
+  // fork: the fill stream starts after the control launch; a plain launch there
+  // (its only predecessor that matters is the control kernel on the other stream)
+  FT_CHECK_CUDA(cudaEventRecord(c->ev_ctrl, st));
+  FT_CHECK_CUDA(cudaStreamWaitEvent(fs, c->ev_ctrl, 0));
+  cache_fill_kernel<<<c->fill_grid, FILL_THREADS, 0, fs>>>((const uint8_t*)c->host_dev, c->pool, c->S,
+                                                            c->Lp * c->E, c->max_slots, (const int32_t*)c->fill_src,
+                                                            (const int32_t*)c->fill_dst, (const int32_t*)c->n_fill);
+  FT_CHECK_CUDA(cudaGetLastError());
+  FT_CHECK_CUDA(cudaEventRecord(c->ev_fill, fs));
+  c->pending_join = 1;
+  return FT_OK;
+}
+
+FT_API int ft_cache_set_fill_blocks(ft_cache* c, int blocks) {
+  FT_REQUIRE(c && blocks >= 1 && blocks <= 4 * sms());
+  c->fill_grid = blocks;
+  return FT_OK;
+}
+
+FT_API int ft_cache_fill_join(ft_cache* c, ft_cuda_stream s) {
+  FT_REQUIRE(c);
+  if (!c->pending_join) return FT_OK;
+  FT_CHECK_CUDA(cudaStreamWaitEvent((cudaStream_t)s, c->ev_fill, 0));
+  c->pending_join = 0;
+  return FT_OK;
+}
+
 FT_API int ft_cache_resize(ft_cache* c, int n_slots) {
   FT_REQUIRE(c && n_slots >= 1 && n_slots <= c->max_slots);
-  if (c->streaming) return FT_ESTATE;
+  if (c->streaming || c->pending_join) return FT_ESTATE;
   return cache_resize_impl(c, n_slots);
 }
 
@@ -635,7 +696,7 @@ FT_API int ft_cache_export(ft_cache* c, int32_t* key_of_slot, uint32_t* stamp, i
 FT_API int ft_stream_create(ft_cache* c, int serialized, ft_stream** out) {
   FT_REQUIRE(c && out);
   *out = nullptr;
-  if (c->streaming) return FT_ESTATE;
+  if (c->streaming || c->pending_join) return FT_ESTATE;
   if (c->N < 2 * c->E) return FT_EUNSUPPORTED;
   ft_stream* st = new (std::nothrow) ft_stream();
   if (!st) return FT_ENOMEM;

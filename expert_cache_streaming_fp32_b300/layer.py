@@ -8,6 +8,10 @@ one MoE layer step in order:
     ft_router_logits -> ft_route -> ft_permute -> [ft_cache_step per wave ->
     ft_expert_grouped] -> ft_combine
 
+or, with a fill stream, per wave: ft_cache_step_split -> ft_expert_grouped
+(hits, while the fill copies) -> ft_cache_fill_join -> ft_expert_grouped
+(the filled experts).
+
 Nothing here computes: it allocates buffers and sequences the C calls.
 """
 from __future__ import annotations
@@ -16,9 +20,27 @@ from typing import Optional
 
 import torch
 
-from . import (FT_W_BF16, FT_W_F32, FT_W_FP8E4M3, FT_W_MXFP4, FT_W_NVFP4, Cache, PinnedBuffer, ft_combine,
+from . import (FT_TC_WIDE_ASSIGNMENTS, FT_W_BF16, FT_W_F32, FT_W_FP8E4M3, FT_W_MXFP4, FT_W_NVFP4, Cache,
+               PinnedBuffer, ft_combine,
                ft_expert_grouped, ft_expert_grouped_workspace, ft_expert_layout_get, ft_permute, ft_route,
                ft_router_logits)
+
+
+# Decode batches of at least this many assignments (T*k) evaluate their hits
+# while the miss fill copies (ft_cache_step_split).  Smaller batches take
+# ft_cache_step: their hits take about as long as the second expert call the
+# split form adds.  Measured on B300, 40-layer BF16 decode (H=2048, E=256,
+# k=8), per layer step: 135 -> 144 us at T=1, 200 -> 202 us at T=4,
+# 293 -> 283 us at T=16, 375 -> 346 us at T=64.
+SPLIT_MIN_ASSIGNMENTS = 64
+# Batches on the large-batch tensor-core tiling (prefill waves) take
+# ft_cache_step too: beside those kernels, which fill every SM, the fill's
+# reads wait behind theirs and the copy slowed to a third of the link.
+SPLIT_MAX_ASSIGNMENTS = FT_TC_WIDE_ASSIGNMENTS
+
+
+def split_pays(T: int, k: int, min_assignments: int = SPLIT_MIN_ASSIGNMENTS) -> bool:
+    return min_assignments <= T * k < SPLIT_MAX_ASSIGNMENTS
 
 
 def pack_expert(comps: dict, wtype: int, layout, out: torch.Tensor) -> None:
@@ -93,6 +115,7 @@ class MoELayer:
         self.perm = torch.empty(T_max * k, **i32)
         self.inv = torch.empty(T_max * k, **i32)
         self.slot_of = torch.empty(E, **i32)
+        self.slot_fill = torch.empty(E, **i32)
         self.ext = torch.zeros(E, **i32)
         self.step_counts = torch.zeros(4, **i32)
         self.y = torch.empty(T_max * k, H, **f32)
@@ -116,14 +139,31 @@ class MoELayer:
                    self.cfg.n_experts, self.out[:T], stream)
         return self.out[:T]
 
+    def cached_wave(self, x, layer: int, cache: Cache, slot_bytes: int, fill_ratio: float, wave: int,
+                    step_counts=None, stream=None, fill_stream=None):
+        """Cache control, miss fill and expert evaluation of one wave.
+
+        With ``fill_stream`` the fill runs there while the hits are evaluated on
+        ``stream``; the filled experts follow after the join."""
+        sc = self.step_counts if step_counts is None else step_counts
+        if fill_stream is None:
+            cache.step(layer, self.counts, fill_ratio, wave, self.slot_of, self.ext, sc, stream)
+            self.experts(x, self.slot_of, cache.slot_pool, slot_bytes, cache.max_slots, stream)
+            return
+        cache.step_split(layer, self.counts, fill_ratio, wave, self.slot_of, self.slot_fill, self.ext, sc, stream,
+                         fill_stream)
+        self.experts(x, self.slot_of, cache.slot_pool, slot_bytes, cache.max_slots, stream)
+        cache.fill_join(stream)
+        self.experts(x, self.slot_fill, cache.slot_pool, slot_bytes, cache.max_slots, stream)
+
     def forward_cached(self, x, w_router, bias, layer: int, cache: Cache, slot_bytes: int,
-                       fill_ratio: float = 1.0, ext_partial: Optional[torch.Tensor] = None, stream=None):
+                       fill_ratio: float = 1.0, ext_partial: Optional[torch.Tensor] = None, stream=None,
+                       fill_stream=None):
         """One layer step over the LRU cache (all waves), returning out [T, H] fp32."""
         T = x.shape[0]
         self.route(x, w_router, bias, stream)
         for wv in range(cache.n_waves()):
-            cache.step(layer, self.counts, fill_ratio, wv, self.slot_of, self.ext, self.step_counts, stream)
-            self.experts(x, self.slot_of, cache.slot_pool, slot_bytes, cache.max_slots, stream)
+            self.cached_wave(x, layer, cache, slot_bytes, fill_ratio, wv, None, stream, fill_stream)
         return self.combine(T, self.ext, ext_partial, stream)
 
     def forward_slots(self, x, w_router, bias, slot_of, slot_pool, slot_bytes, pool_slots, stream=None):

@@ -242,6 +242,38 @@ int ft_cache_n_waves(const ft_cache* c);
 int ft_cache_step(ft_cache* c, int layer, const int32_t* counts, double fill_ratio, int wave,
                   int32_t* slot_of, int32_t* ext_flags, int32_t* step_counts, ft_cuda_stream s);
 
+/* Split form of ft_cache_step: the miss fill runs on a second stream so that
+ * the hits can be evaluated while the filled experts are copied ([Review]
+ * §2.6: the fill is one launch after the control pass; hits need no copy).
+ * Same decisions, tables, counters and step_counts as ft_cache_step.
+ *   slot_hit    dev [E] int32 (written): slot for this wave's hits, -2 for its
+ *               external experts, -1 for every other expert (filled ones too)
+ *   slot_fill   dev [E] int32 (written): slot for this wave's filled experts,
+ *               -1 for every other expert
+ *   fill_s      stream of the fill copies; it waits for the control launch on
+ *               s.  fill_s == s runs both on s (ft_cache_fill_join is then a no-op)
+ * Reading the hit slots on s right after this call is safe: their records are
+ * resident and the fill writes only victims, which are slots this wave does
+ * not touch.  The filled slots may be read on s only after
+ * ft_cache_fill_join(c, s), which makes s wait for the fill.  Until that join,
+ * ft_cache_step, ft_cache_step_split, ft_cache_resize and ft_stream_create on
+ * this handle return FT_ESTATE.  Under stream capture the join must come
+ * before the capture ends (it joins fill_s back into s).
+ * Passing slot_hit to ft_expert_grouped, then slot_fill after the join, gives
+ * the same y as one call with ft_cache_step's slot_of (ft_expert_grouped's
+ * results do not depend on which other experts a call evaluates). */
+int ft_cache_step_split(ft_cache* c, int layer, const int32_t* counts, double fill_ratio, int wave,
+                        int32_t* slot_hit, int32_t* slot_fill, int32_t* ext_flags, int32_t* step_counts,
+                        ft_cuda_stream s, ft_cuda_stream fill_s);
+int ft_cache_fill_join(ft_cache* c, ft_cuda_stream s);
+
+/* Thread blocks of the fill launch (256 threads, 16 KiB of host reads in
+ * flight each), 1 .. 4 x the SM count; applies to later steps.  More blocks
+ * keep more reads in flight over the host link; reads queued beyond what the
+ * link needs also delay the device-memory reads of kernels running beside the
+ * fill (the hits of a split step). */
+int ft_cache_set_fill_blocks(ft_cache* c, int blocks);
+
 /* Safe-point rebuild for a new slot budget without touching the host pool
  * ([Review] §2.7, runtime cache reconfiguration).  Keeps the min(used, N')
  * most recent entries (largest (stamp, -slot)); kept entries below N' stay,

@@ -42,20 +42,34 @@ class OracleLayer:
         return self.src[p]
 
 
-def run_waves(ft, layer_obj, cache, layer, x, ratio, sim=None, events=None):
-    """All waves of one cached layer step, checking slot_of against the simulator after each wave."""
+def run_waves(ft, layer_obj, cache, layer, x, ratio, sim=None, events=None, fill_stream=None):
+    """All waves of one cached layer step, checking slot_of against the simulator after each wave.
+
+    With ``fill_stream`` each wave runs in the split form (hits evaluated while
+    the fill copies on that stream); the simulator then checks the hit and fill
+    slots merged."""
     idx = layer_obj.idx[: x.shape[0]].cpu().numpy()
     if sim is not None:
         ev, sim_slot_of = sim.step(layer, idx.reshape(-1), ratio)
         if events is not None:
             events.extend(ev)
     for w in range(cache.n_waves()):
-        cache.step(layer, layer_obj.counts, ratio, w, layer_obj.slot_of, layer_obj.ext, layer_obj.step_counts)
+        if fill_stream is None:
+            cache.step(layer, layer_obj.counts, ratio, w, layer_obj.slot_of, layer_obj.ext, layer_obj.step_counts)
+            got = layer_obj.slot_of
+        else:
+            cache.step_split(layer, layer_obj.counts, ratio, w, layer_obj.slot_of, layer_obj.slot_fill,
+                             layer_obj.ext, layer_obj.step_counts, fill_stream=fill_stream)
+            hit, fil = layer_obj.slot_of, layer_obj.slot_fill
+            assert not bool(((hit >= 0) & (fil >= 0)).any()), "an expert is both a hit and a fill"
+            got = torch.where(fil >= 0, fil, hit)
         if sim is not None:
-            got = layer_obj.slot_of.cpu().numpy()
             exp = sim_slot_of[w] if w < len(sim_slot_of) else [-1] * cache.E
-            assert got.tolist() == list(exp), f"layer {layer} wave {w}"
+            assert got.cpu().numpy().tolist() == list(exp), f"layer {layer} wave {w}"
         layer_obj.experts(x, layer_obj.slot_of, cache.slot_pool, layer_obj_S(cache), cache.max_slots)
+        if fill_stream is not None:
+            cache.fill_join()
+            layer_obj.experts(x, layer_obj.slot_fill, cache.slot_pool, layer_obj_S(cache), cache.max_slots)
 
 
 def layer_obj_S(cache):
@@ -172,6 +186,136 @@ def test_cache_trace_resize_split_matches_simulator(ft):
     assert ft.ft_get_device_error() == 0
 
 
+def test_split_fill_step_equals_plain_step(ft):
+    """ft_cache_step_split + two expert calls == ft_cache_step + one call, bit for bit.
+
+    Two caches over one host pool follow the same trace (T = 1, 4, 16; two waves
+    per step; miss split 0.6 from step 12).  The split side runs eagerly, then
+    from step 20 as CUDA graphs captured per layer step (the fill stream forks
+    from and joins the capture stream).  Decisions, step counts, outputs,
+    counters and the final tables must be identical."""
+    cfg = synth.MoEConfig("trace", 256, 64, 4, 256, 4, synth.W_BF16, "bf16", seed=5, zipf_s=1.1)
+    pool, sp, cache = make_cache(ft, cfg, 4, 40, 40)
+    sp2 = torch.empty(40 * pool.S, dtype=torch.uint8, device=DEV)
+    split = ft.Cache(cfg.n_layers, cfg.n_experts, 4, 40, 40, pool.S, pool.ptr, sp2)
+    assert cache.n_waves() == 2
+    routers = [synth.router_weights(cfg, l, DEV) for l in range(4)]
+    L, Ls = ft.MoELayer(cfg, 16), ft.MoELayer(cfg, 16)
+    fs = torch.cuda.Stream()
+    traces = {T: synth.AR1Trace(cfg, T, DEV, tag=T) for T in (1, 4, 16)}
+    xs = torch.empty(16, cfg.hidden, dtype=torch.bfloat16, device=DEV)
+    sc_p = torch.zeros(2, 4, dtype=torch.int32, device=DEV)
+    sc_s = torch.zeros(2, 4, dtype=torch.int32, device=DEV)
+    merged = torch.empty(2, cfg.n_experts, dtype=torch.int32, device=DEV)
+    graphs = []
+
+    def split_layer(T, l, ratio):
+        x = xs[:T]
+        Ls.route(x, *routers[l])
+        for w in range(2):
+            split.step_split(l, Ls.counts, ratio, w, Ls.slot_of, Ls.slot_fill, Ls.ext, sc_s[w], fill_stream=fs)
+            Ls.experts(x, Ls.slot_of, sp2, pool.S, 40)
+            split.fill_join()
+            merged[w].copy_(torch.where(Ls.slot_fill >= 0, Ls.slot_fill, Ls.slot_of))
+            Ls.experts(x, Ls.slot_fill, sp2, pool.S, 40)
+        return Ls.combine(T, Ls.ext, None)
+
+    n_fill = 0
+    for step in range(30):
+        T = (1, 4, 16)[step % 3]
+        x = traces[T].next()
+        xs[:T].copy_(x)
+        ratio = 1.0 if step < 12 else 0.6
+        for l in range(4):
+            L.route(x, *routers[l])
+            exp_slots = []
+            for w in range(2):
+                cache.step(l, L.counts, ratio, w, L.slot_of, L.ext, sc_p[w])
+                exp_slots.append(L.slot_of.clone())
+                L.experts(x, L.slot_of, sp, pool.S, 40)
+            out = L.combine(T, L.ext, None).clone()
+            if step < 20:
+                out_s = split_layer(T, l, ratio).clone()
+            else:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    out_g = split_layer(T, l, ratio)
+                g.replay()
+                graphs.append(g)
+                out_s = out_g.clone()
+            torch.cuda.synchronize()
+            for w in range(2):
+                assert torch.equal(merged[w], exp_slots[w]), f"step {step} layer {l} wave {w}"
+            assert torch.equal(sc_p, sc_s)
+            assert torch.equal(L.ext, Ls.ext)
+            assert torch.equal(out, out_s), f"step {step} layer {l}"
+            n_fill += int(sc_p[:, 2].sum())
+    assert n_fill > 0
+    a, b = cache.stats(), split.stats()
+    assert (a.steps, a.hits, a.fills, a.externals, a.bytes_h2d) == (b.steps, b.hits, b.fills, b.externals, b.bytes_h2d)
+    assert a.externals > 0
+    ka, sa, ca = cache.export()
+    kb, sb, cb = split.export()
+    assert ka.tolist() == kb.tolist() and sa.tolist() == sb.tolist() and ca == cb
+    for slot, key in enumerate(ka.tolist()):              # resident slots hold the same bytes
+        if key >= 0:
+            assert torch.equal(sp[slot * pool.S:(slot + 1) * pool.S], sp2[slot * pool.S:(slot + 1) * pool.S])
+    del graphs
+    assert ft.ft_get_device_error() == 0
+
+
+def test_split_fill_needs_join(ft):
+    """Until ft_cache_fill_join, the handle refuses the next step, a resize and streaming (FT_ESTATE)."""
+    cfg = synth.MoEConfig("trace", 256, 64, 4, 256, 4, synth.W_BF16, "bf16", seed=5, zipf_s=1.1)
+    pool, sp, cache = make_cache(ft, cfg, 4, 64, 64)
+    L = ft.MoELayer(cfg, 4)
+    x = synth.activations(cfg, 4, device=DEV)
+    L.route(x, *synth.router_weights(cfg, 0, DEV))
+    fs = torch.cuda.Stream()
+    cache.step_split(0, L.counts, 1.0, 0, L.slot_of, L.slot_fill, L.ext, L.step_counts, fill_stream=fs)
+    for call in (lambda: cache.step(1, L.counts, 1.0, 0, L.slot_of, L.ext),
+                 lambda: cache.step_split(1, L.counts, 1.0, 0, L.slot_of, L.slot_fill, L.ext, fill_stream=fs),
+                 lambda: cache.resize(32),
+                 lambda: ft.Stream(cache)):
+        with pytest.raises(ft.FTError) as ei:
+            call()
+        assert ei.value.status == ft.FT_ESTATE
+    cache.fill_join()
+    cache.fill_join()                                 # a second join is a no-op
+    cache.step(1, L.counts, 1.0, 0, L.slot_of, L.ext)
+    # fill_stream == stream: both launches on one stream, nothing to join
+    cache.step_split(2, L.counts, 1.0, 0, L.slot_of, L.slot_fill, L.ext)
+    cache.step(3, L.counts, 1.0, 0, L.slot_of, L.ext)
+    torch.cuda.synchronize()
+    assert cache.stats().steps == 4
+    assert ft.ft_get_device_error() == 0
+
+
+def test_fill_blocks_setting(ft):
+    """The fill's block count changes its speed only: one block still copies every record exactly."""
+    cfg = synth.MoEConfig("trace", 256, 64, 4, 256, 4, synth.W_BF16, "bf16", seed=5, zipf_s=1.1)
+    pool, sp, cache = make_cache(ft, cfg, 4, 64, 64)
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    for bad in (0, -1, 4 * n_sm + 1):
+        with pytest.raises(ft.FTError) as ei:
+            cache.set_fill_blocks(bad)
+        assert ei.value.status == ft.FT_EINVAL
+    cache.set_fill_blocks(4 * n_sm)
+    cache.set_fill_blocks(1)
+    L = ft.MoELayer(cfg, 16)
+    x = synth.activations(cfg, 16, device=DEV)
+    L.route(x, *synth.router_weights(cfg, 2, DEV))
+    cache.step(2, L.counts, 1.0, 0, L.slot_of, L.ext, L.step_counts)
+    torch.cuda.synchronize()
+    assert int(L.step_counts[2]) > 1
+    key, _, _ = cache.export()
+    for slot, kk in enumerate(key.tolist()):
+        if kk >= 0:
+            l, e = divmod(kk, 64)
+            assert torch.equal(sp[slot * pool.S:(slot + 1) * pool.S], pool.row(l % 4, e).to(DEV)), f"slot {slot}"
+    assert ft.ft_get_device_error() == 0
+
+
 # ---------------------------------------------------------------- prefill streaming
 
 def test_stream_double_buffered_and_serialized(ft):
@@ -243,7 +387,8 @@ def test_stream_needs_two_layers_of_slots(ft):
 # ---------------------------------------------------------------- full-size decode and prefill shapes
 
 def test_decode_full_size_sampled(ft):
-    """H=2048, E=256, k=8, I=512, 40 logical layers over 2 physical layers, 4096 slots, T=64."""
+    """H=2048, E=256, k=8, I=512, 40 logical layers over 2 physical layers, 4096 slots, T=64;
+    the first step with ft_cache_step, the others with the split form."""
     cfg = synth.DECODE_BF16
     n_phys = 2
     pool, sp, cache = make_cache(ft, cfg, n_phys, 4096, 4096)
@@ -253,6 +398,7 @@ def test_decode_full_size_sampled(ft):
     routers = [synth.router_weights(cfg, l, DEV) for l in range(cfg.n_layers)]
     tr = synth.AR1Trace(cfg, 64, DEV)
     sample = [0, 9, 33, 63]
+    fill_stream = torch.cuda.Stream()
     for step in range(3):
         x = tr.next()
         for l in range(cfg.n_layers):
@@ -260,7 +406,8 @@ def test_decode_full_size_sampled(ft):
             z = L.logits[:64].cpu().numpy().astype(np.float64)
             ri, rw = moe.route(z, 8)
             assert np.array_equal(L.idx[:64].cpu().numpy(), ri)
-            run_waves(ft, L, cache, l, x, 1.0, sim)
+            # steps 1 and 2 overlap the fill with the hits (split form)
+            run_waves(ft, L, cache, l, x, 1.0, sim, fill_stream=fill_stream if step else None)
             out = L.combine(64, L.ext, None)
             if (step, l) in ((0, 0), (0, 21), (2, 39), (2, 7)):
                 xs = formats.to_f64(x[sample])
