@@ -63,7 +63,7 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graphs", action="store_true", help="issue the decode steps eagerly instead of as CUDA graphs")
     p.add_argument("--split-min-assignments", type=int, default=0,
-                   help="smallest decode batch T*k for the split form (0: the library's policy)")
+                   help="smallest decode batch T*k for the split form, every format (0: the policy per format)")
     p.add_argument("--no-split-fill", action="store_true",
                    help="decode with ft_cache_step (fill, then all experts) instead of the split form "
                         "(hits evaluated while the fill copies)")
@@ -210,11 +210,11 @@ def host_ram_bytes() -> int:
 class DecodeTrace:
     """One batch size: its cache, per-step buffers, resident inputs and per-layer-step counters."""
 
-    def __init__(self, ft, cfg, T, pool, routers, n_steps, dev, e2e, n_slots=None, split_min=64):
+    def __init__(self, ft, cfg, T, pool, routers, n_steps, dev, e2e, n_slots=None, split_min=0):
         self.ft, self.cfg, self.T = ft, cfg, T
         # the split form where it pays
-        self.fill_stream = (torch.cuda.Stream(device=dev) if split_min and ft.split_pays(T, cfg.top_k, split_min)
-                            else None)
+        self.fill_stream = (torch.cuda.Stream(device=dev)
+                            if split_min >= 0 and ft.split_pays(T, cfg.top_k, cfg.wtype, split_min) else None)
         L, E = cfg.n_layers, cfg.n_experts
         self.n_slots = n_slots or int(round(CACHE_FRAC * L * E))
         self.S = pool.S
@@ -475,7 +475,7 @@ def prefill_leg(ft, cfg, pool, routers0, dev, prompts, link_gbs, peaks, chunk=81
 
 # ---------------------------------------------------------------- secondary workloads
 
-def decode_trace_leg(ft, cfg, T, pool, routers, n_slots, steps, warmup, dev, peaks, link, payload, split_min=64):
+def decode_trace_leg(ft, cfg, T, pool, routers, n_slots, steps, warmup, dev, peaks, link, payload, split_min=0):
     """One batch size on its own cache: eager warm-up, then ``steps`` graph-replayed decode steps."""
     tr = DecodeTrace(ft, cfg, T, pool, routers, warmup + steps, dev, False, n_slots=n_slots, split_min=split_min)
     for t in range(warmup):
@@ -504,7 +504,7 @@ def decode_trace_leg(ft, cfg, T, pool, routers, n_slots, steps, warmup, dev, pea
     return out
 
 
-def nvfp4_leg(ft, dev, peaks, link, batches, steps, warmup, split_min=64):
+def nvfp4_leg(ft, dev, peaks, link, batches, steps, warmup, split_min=0):
     """The 43-layer NVFP4 stack: decode at 40% cache per batch size, and 8192-token streamed prefill.
 
     The host pool stores a cyclic window of 4 physical layers (logical layer l
@@ -528,7 +528,7 @@ def nvfp4_leg(ft, dev, peaks, link, batches, steps, warmup, split_min=64):
     return res
 
 
-def mxfp4_mixed_leg(ft, dev, peaks, link, decode_steps=512, cycles=4, split_min=64):
+def mxfp4_mixed_leg(ft, dev, peaks, link, decode_steps=512, cycles=4, split_min=0):
     """The MXFP4 agent-like trace on 4 layers: cycles of (8192-token prefill, T=1 decode run).
 
     The cache is resized at the safe point before each cycle (57.8% -> 40% ->
@@ -559,8 +559,8 @@ def mxfp4_mixed_leg(ft, dev, peaks, link, decode_steps=512, cycles=4, split_min=
     slot_of = torch.empty(E, dtype=torch.int32, device=dev)
     ratio = 0.7
     fs = torch.cuda.Stream(device=dev)                        # the fill stream of the split form
-    fs_d = fs if split_min and ft.split_pays(1, cfg.top_k, split_min) else None
-    fs_p = fs if split_min and ft.split_pays(8192, cfg.top_k, split_min) else None
+    fs_d = fs if split_min >= 0 and ft.split_pays(1, cfg.top_k, cfg.wtype, split_min) else None
+    fs_p = fs if split_min >= 0 and ft.split_pays(8192, cfg.top_k, cfg.wtype, split_min) else None
 
     def decode_layers():
         for l in range(L):
@@ -811,6 +811,22 @@ def fill_overlap_case(args):
         m1.record()
         torch.cuda.synchronize()
         alone.append(m0.elapsed_time(m1))
+    # the same bytes by the copy engine (one cudaMemcpyAsync of 32 contiguous records) beside the same calls
+    dst = torch.empty(32 * S, dtype=torch.uint8, device=dev)
+    ce = []
+    for _ in range(3):
+        torch.cuda.synchronize()
+        f0, f1, c0, c1 = ev(), ev(), ev(), ev()
+        f0.record(fs)
+        with torch.cuda.stream(fs):
+            dst.copy_(pool.host[: 32 * S], non_blocking=True)
+        f1.record(fs)
+        c0.record()
+        experts()
+        c1.record()
+        torch.cuda.synchronize()
+        ce.append((f0.elapsed_time(f1), c0.elapsed_time(c1)))
+    ce = ce[1:]
     rows = []
     for blocks in (4, 8, 16, 32, 64, 148, 296):
         a = [once(blocks, False)[0] for _ in range(3)][1:]
@@ -821,6 +837,8 @@ def fill_overlap_case(args):
                      "experts_beside_ms": float(np.mean([m for _, m in b]))})
     print(json.dumps({"kernel_case": "fill_overlap", "fill_experts": 32, "expert_calls": n_calls, "T": T,
                       "experts_alone_ms": float(np.median(alone)), "rows": rows,
+                      "copy_engine": {"copy_gbs": 32 * S / (np.mean([f for f, _ in ce]) * 1e-3) / 1e9,
+                                      "experts_beside_ms": float(np.mean([m for _, m in ce]))},
                       "device_error": ft.ft_get_device_error()}))
 
 
@@ -891,8 +909,8 @@ def main():
     dev = f"cuda:{local}"
     cfg = synth.DECODE_BF16
     peaks = load_peaks()
-    # smallest decode batch (T*k) run in the split form; 0: never
-    split_min = 0 if args.no_split_fill else (args.split_min_assignments or ft.SPLIT_MIN_ASSIGNMENTS)
+    # smallest decode batch (T*k) run in the split form: 0 the library's policy, -1 never
+    split_min = -1 if args.no_split_fill else args.split_min_assignments
     batches = [int(b) for b in args.batches.split(",")]
     L, E = cfg.n_layers, cfg.n_experts
     lay_bytes = ft.ft_expert_layout_get(cfg.wtype, cfg.hidden, cfg.inter)
@@ -1100,8 +1118,9 @@ def main():
                        "host_pool_gb": pool.n_phys * E * S / 1e9, "weights": "bf16", "accumulate": "f32",
                        "l2": "inputs larger than L2 (each step reads >= 2 GB of expert weights)",
                        "fill": ("ft_cache_step (fill, then all experts)" if args.no_split_fill else
-                                f"{split_min} <= T*k < {ft.FT_TC_WIDE_ASSIGNMENTS}: ft_cache_step_split (hits "
-                                "evaluated while the fill copies on a second stream); other batches: ft_cache_step"),
+                                f"{split_min or ft.SPLIT_MIN_ASSIGNMENTS[cfg.wtype]} <= T*k < "
+                                f"{ft.FT_TC_WIDE_ASSIGNMENTS}: ft_cache_step_split (hits evaluated while the fill "
+                                "copies on a second stream); other batches: ft_cache_step"),
                        "parallelism": f"replicas{world}"},
             "layer_roofline_frac": layer_roofline_frac,
             "per_batch": {str(T): {"tokens_per_s": T * args.steps / (per_T[T] * 1e-3),

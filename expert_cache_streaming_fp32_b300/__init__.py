@@ -338,4 +338,5 @@ class Stream:
             _check("ft_stream_destroy", st)
 
 
-from .layer import SPLIT_MIN_ASSIGNMENTS, ExpertPool, MoELayer, pack_expert, split_pays  # noqa: E402,F401
+from .layer import (SPLIT_MAX_ASSIGNMENTS, SPLIT_MIN_ASSIGNMENTS, ExpertPool, MoELayer, pack_expert,  # noqa: E402,F401
+                    split_pays)

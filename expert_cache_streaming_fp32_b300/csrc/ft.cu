@@ -585,7 +585,7 @@ FT_API int ft_cache_create(const ft_cache_config* cfg, ft_cache** out) {
   // flight already keeps the host link busy (51.4 GB/s for 8 or for 296 blocks,
   // measured on B300).  More reads in flight only queue in the memory system,
   // where they held up the HBM reads of expert kernels running beside the fill
-  // (a 64-token expert call took 3.4x as long beside 148 fill blocks, 1.2x
+  // (64-token expert calls took 3.4x as long beside 148 fill blocks, 1.2-1.4x
   // beside 8).
   c->fill_grid = 8;
   *out = c;

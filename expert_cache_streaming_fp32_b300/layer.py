@@ -27,20 +27,27 @@ from . import (FT_TC_WIDE_ASSIGNMENTS, FT_W_BF16, FT_W_F32, FT_W_FP8E4M3, FT_W_M
 
 
 # Decode batches of at least this many assignments (T*k) evaluate their hits
-# while the miss fill copies (ft_cache_step_split).  Smaller batches take
-# ft_cache_step: their hits take about as long as the second expert call the
-# split form adds.  Measured on B300, 40-layer BF16 decode (H=2048, E=256,
-# k=8), per layer step: 135 -> 144 us at T=1, 200 -> 202 us at T=4,
-# 293 -> 283 us at T=16, 375 -> 346 us at T=64.
-SPLIT_MIN_ASSIGNMENTS = 64
+# while the miss fill copies (ft_cache_step_split); smaller batches take
+# ft_cache_step.  The split form adds a second expert call after the fill, and
+# only layer steps with a fill gain from it.  Measured on B300 per batch size
+# (tokens/s, plain -> split):
+#   BF16, 40 layers, H=2048, I=512, k=8: T=1 186 -> 174, T=4 504 -> 498,
+#     T=16 1364 -> 1435, T=64 4270 -> 4655;
+#   NVFP4, 43 layers, H=4096, I=2048, k=6: T=1 61.5 -> 64.3, T=4 139 -> 160;
+#   MXFP4, 4 layers, H=6144, I=2048, k=8, T=1: 2-6% more with the split form.
+# FP4 experts cost more to evaluate (the in-kernel expansion), so their hits
+# cover the extra call already at T=1.
+SPLIT_MIN_ASSIGNMENTS = {FT_W_F32: 64, FT_W_BF16: 64, FT_W_FP8E4M3: 64, FT_W_NVFP4: 1, FT_W_MXFP4: 1}
 # Batches on the large-batch tensor-core tiling (prefill waves) take
 # ft_cache_step too: beside those kernels, which fill every SM, the fill's
 # reads wait behind theirs and the copy slowed to a third of the link.
 SPLIT_MAX_ASSIGNMENTS = FT_TC_WIDE_ASSIGNMENTS
 
 
-def split_pays(T: int, k: int, min_assignments: int = SPLIT_MIN_ASSIGNMENTS) -> bool:
-    return min_assignments <= T * k < SPLIT_MAX_ASSIGNMENTS
+def split_pays(T: int, k: int, wtype: int, min_assignments: int = 0) -> bool:
+    """Whether a cached layer step of T tokens should use the split form."""
+    lo = min_assignments or SPLIT_MIN_ASSIGNMENTS[wtype]
+    return lo <= T * k < SPLIT_MAX_ASSIGNMENTS
 
 
 def pack_expert(comps: dict, wtype: int, layout, out: torch.Tensor) -> None:

@@ -48,17 +48,26 @@ class Experts:
         return get
 
 
-def _waves(ft, L, cache, layer, x, ratio, sim, S, pool_slots):
+def _waves(ft, L, cache, layer, x, ratio, sim, S, pool_slots, fill_stream=None):
+    """All waves of a layer step; with ``fill_stream`` in the split form (hits beside the fill)."""
     idx = L.idx[: x.shape[0]].cpu().numpy()
     ev, sim_slot_of = sim.step(layer, idx.reshape(-1), ratio)
     counts = np.zeros(4, dtype=np.int64)
     for w in range(cache.n_waves()):
-        cache.step(layer, L.counts, ratio, w, L.slot_of, L.ext, L.step_counts)
-        got = L.slot_of.cpu().numpy()
         exp = sim_slot_of[w] if w < len(sim_slot_of) else [-1] * cache.E
-        assert got.tolist() == list(exp), f"layer {layer} wave {w}"
+        if fill_stream is None:
+            cache.step(layer, L.counts, ratio, w, L.slot_of, L.ext, L.step_counts)
+            assert L.slot_of.cpu().numpy().tolist() == list(exp), f"layer {layer} wave {w}"
+            L.experts(x, L.slot_of, cache.slot_pool, S, pool_slots)
+        else:
+            cache.step_split(layer, L.counts, ratio, w, L.slot_of, L.slot_fill, L.ext, L.step_counts,
+                             fill_stream=fill_stream)
+            L.experts(x, L.slot_of, cache.slot_pool, S, pool_slots)
+            cache.fill_join()
+            L.experts(x, L.slot_fill, cache.slot_pool, S, pool_slots)
+            got = torch.where(L.slot_fill >= 0, L.slot_fill, L.slot_of)
+            assert got.cpu().numpy().tolist() == list(exp), f"layer {layer} wave {w}"
         counts += L.step_counts.cpu().numpy()
-        L.experts(x, L.slot_of, cache.slot_pool, S, pool_slots)
     return counts
 
 
@@ -77,6 +86,7 @@ def test_nvfp4_stack_decode_and_prefill(ft):
     lay = ft.MoELayer(cfg, T)
     tr = synth.AR1Trace(cfg, T, DEV)
     sample = [0, 7, 15]
+    fs = torch.cuda.Stream()
     for step in range(4):
         x = tr.next()
         for l in layers:
@@ -84,7 +94,8 @@ def test_nvfp4_stack_decode_and_prefill(ft):
             z = lay.logits[:T].cpu().numpy().astype(np.float64)
             ri, rw = moe.route(z, cfg.top_k)
             assert np.array_equal(lay.idx[:T].cpu().numpy(), ri)
-            _waves(ft, lay, cache, l, x, 1.0, sim, pool.S, n_slots)
+            # odd steps in the split form (the decode form used for FP4 weights)
+            _waves(ft, lay, cache, l, x, 1.0, sim, pool.S, n_slots, fill_stream=fs if step % 2 else None)
             out = lay.combine(T, lay.ext, None).cpu().numpy()
             if (step, l) in ((0, 0), (3, 21), (3, 42)):
                 xs = formats.to_f64(x[sample])
@@ -116,7 +127,8 @@ def test_nvfp4_stack_decode_and_prefill(ft):
 
 
 def test_mxfp4_mixed_resizes_and_split(ft):
-    """Decode steps with the 0.7 miss split and safe-point resizes 592 -> 410 -> 205 -> 592 slots.
+    """Decode steps with the 0.7 miss split and safe-point resizes 592 -> 410 -> 205 -> 592 slots
+    (from step 3 in the split cache-step form).
 
     The external experts' partial output is supplied by the oracle (fp64 ->
     fp32): the layer output must match the oracle's full layer, whatever the
@@ -136,6 +148,7 @@ def test_mxfp4_mixed_resizes_and_split(ft):
     tr = synth.AR1Trace(cfg, 1, DEV, tag=3)
     schedule = {6: 410, 12: 205, 18: 592}
     n_ext = 0
+    fs = torch.cuda.Stream()
     for step in range(22):
         if step in schedule:
             cache.resize(schedule[step])
@@ -146,7 +159,7 @@ def test_mxfp4_mixed_resizes_and_split(ft):
             z = lay.logits[:1].cpu().numpy().astype(np.float64)
             ri, rw = moe.route(z, cfg.top_k)
             assert np.array_equal(lay.idx[:1].cpu().numpy(), ri)
-            _waves(ft, lay, cache, l, x, 0.7, sim, pool.S, max_slots)
+            _waves(ft, lay, cache, l, x, 0.7, sim, pool.S, max_slots, fill_stream=fs if step >= 3 else None)
             ext = lay.ext.cpu().numpy()
             C = [e for e in range(E) if ext[e]]
             n_ext += len(C)

@@ -28,6 +28,16 @@ def test_library_exports_every_declared_symbol(ftlib):
     assert sorted(ftlib.EXPORTED) == declared_functions()
 
 
+def test_binding_constants_match_the_header(ftlib):
+    src = open(os.path.join(ROOT, "include", "ft.h")).read()
+    defines = {m[0]: m[1] for m in re.findall(r"^#define (FT_\w+) (.+)$", src, flags=re.M)}
+    assert set(defines) >= {"FT_TC_WIDE_ASSIGNMENTS", "FT_NOALLOC_MAX_ELEMS"}
+    for name, expr in defines.items():
+        if name == "FT_H":
+            continue
+        assert getattr(ftlib, name) == eval(expr.replace("u", "")), name
+
+
 def test_qsplit_table1(ftlib):
     ms = [1, 2, 3, 4, 6, 8, 16]
     for name, bp, bh, *qs in read_golden("table1_bandwidths.txt"):
