@@ -38,7 +38,7 @@ BATCHES = (1, 4, 16, 64)
 # same launch; profiles/cache_fill_bf16_32experts.md, profiles/expert_tc_bf16_decode_T64.md).
 # The fill's reads come over the host link, so its DRAM traffic is the writes of
 # the filled experts that reached DRAM before the launch ended.
-TRAFFIC_PER_BYTE = {"fill": (0.133e6 + 140.343e6) / 201.327e6,
+TRAFFIC_PER_BYTE = {"fill": (0.025e6 + 140.025e6) / 201.327e6,
                     "experts": (207.776e6 + 3.545e6 + 103.355e6 + 2.734e6) / (205.5e6 + 0.5e6 + 102.8e6)}
 CACHE_FRAC = 0.40
 METRIC = "MoE-layer tokens/s (decode T=1..64, prefill 8192) and % of layer roofline"
