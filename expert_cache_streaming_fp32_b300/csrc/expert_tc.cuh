@@ -59,21 +59,14 @@ constexpr int CVT_THREADS = 256;
 // Stages of block scales a converter thread keeps in flight ahead of use.
 constexpr int SCALE_AHEAD = 8;
 
-// Threads that gather token rows straight from x (GA mode): one 16-byte chunk
-// of 8 rows per stage each.
+// Threads that gather token rows straight from x (GA mode): one tile row
+// each; every fourth issues the TMA row loads of its row and the next three.
 constexpr int GATHER_THREADS = 128;
-// Stages a gather thread keeps in flight before it marks the oldest ready.
-// It must stay below the stage count (the copies for stage s wait for the MMA
-// to free s, and that MMA waits for the copies marked ready here).  A stage is
-// marked ready only after the thread has issued the next GATHER_DEPTH stages,
-// so depth also delays the MMA: 8192-token BF16 expert call 0.538 ms at depth
-// 1, 0.514 ms at 2, 0.603 ms at 3 (B300).
-constexpr int GATHER_DEPTH = 2;
 
 // bf16 weights: TMA writes the swizzled B tile.  NVFP4 / MXFP4: TMA stages
 // the packed rows (32 bytes per row per stage) and eight more warps expand them
 // (expand_fp4_half).  GA: the A tile (token rows) is gathered from x by four
-// more warps with 16-byte cp.async copies instead of a TMA load of
+// more warps with TMA tile::gather4 row loads instead of a TMA load of
 // pre-gathered rows.
 template <int BN, int WT = FT_W_BF16, bool GA = false>
 struct Cfg {
@@ -81,7 +74,6 @@ struct Cfg {
   static constexpr bool FP4 = is_fp4(WT);
   static_assert(!FP4 || BN == 128, "FP4 expansion covers 128-row weight tiles");
   static_assert(!(FP4 && GA), "one helper role per kernel");
-  static_assert(!GA || GATHER_DEPTH < STAGE_BUDGET / (A_BYTES + BN * BK * 2), "gather depth below the stage count");
   static constexpr int THREADS = 192 + (FP4 ? CVT_THREADS : 0) + (GA ? GATHER_THREADS : 0);
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int RAW_BYTES = FP4 ? BN * BK / 2 : 0;
@@ -339,8 +331,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      // GA: the producer's arrival (B bytes) plus one per gather warp (A rows)
-      mbar_init(full_bar(s), GA ? 1 + GATHER_THREADS / 32 : 1);
+      // one arrival (the producer's, expecting the A and B bytes); in GA mode the
+      // gather warps' row loads count their bytes on the same barrier
+      mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
       mbar_init(cvt_bar(s), CVT_THREADS / 32);
     }
@@ -387,7 +380,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
           const uint32_t sb = FP4 ? sbase + raw_off(stage) : sa + A_BYTES;
           const int kb = FP4 ? ks * BK / 2 : ks * BK;
           const uint32_t half = FP4 ? RAW_BYTES / 2 : B_BYTES / 2;
-          mbar_arrive_expect_tx(full_bar(stage), (GA ? 0 : A_BYTES) + (FP4 ? RAW_BYTES : B_BYTES));
+          mbar_arrive_expect_tx(full_bar(stage), A_BYTES + (FP4 ? RAW_BYTES : B_BYTES));
           if (!GA) tma_load_2d(sa, &map_a, full_bar(stage), ks * BK, t.row0);
           if (MODE == GATEUP) {
             tma_load_3d(sb, &map_b0, full_bar(stage), kb, t.nt * (BN / 2), t.slot);
@@ -445,55 +438,42 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     }
   } else if (GA && warp >= 6) {
     // ---------------------------------------------------------------- token-row gather (warps 6..9)
-    // Thread g copies chunk c = g % 8 (16 bytes = 8 elements along K) of tile
-    // rows g / 8 + 16 j, j = 0..7, into the 128-byte-swizzled A tile.  The
-    // copies of a stage are marked ready GATHER_DEPTH stages later, once this
-    // thread's cp.async group for it has completed.
+    // Thread g holds the token of tile row g; per stage, every fourth lane
+    // loads its row and the next three with one TMA tile::gather4 (64 columns
+    // of 4 rows of x) into the 128-byte-swizzled A tile.  The bytes count on
+    // the stage's full barrier, whose expected total the producer sets.
     const int g = threadIdx.x - 192;
-    const int c = g & 7, r0 = g >> 3;
     const long long Tk = (long long)a.T * a.k;
-    int stage = 0, pending = 0;
+    int stage = 0;
     uint32_t phase = 0;
-    bool ok = true;
-    for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+    uint32_t issued = 0, last_par = 0;  // per stage: a row load was issued / parity of its phase
+    for (int item = blockIdx.x; item < total; item += gridDim.x) {
       const Tile t = decode_tile(a, act_e, act_pref, n_act, item);
-      const __nv_bfloat16* src[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const long long p = min((long long)t.row0 + r0 + 16 * j, Tk - 1);  // rows past the end: any valid row
-        int tok = a.perm[p] / a.k;
-        if ((unsigned)tok >= (unsigned)a.T) {
-          record_error(FT_DERR_ROW_INDEX);
-          tok = 0;
-        }
-        src[j] = a.x + (size_t)tok * a.H + c * 8;
+      const long long p = min((long long)t.row0 + g, Tk - 1);  // rows past the end: any valid row
+      int tok = a.perm[p] / a.k;
+      if ((unsigned)tok >= (unsigned)a.T) {
+        record_error(FT_DERR_ROW_INDEX);
+        tok = 0;
       }
+      const int t1 = __shfl_down_sync(FT_FULL_MASK, tok, 1);
+      const int t2 = __shfl_down_sync(FT_FULL_MASK, tok, 2);
+      const int t3 = __shfl_down_sync(FT_FULL_MASK, tok, 3);
+      bool ok = true;
       for (int ks = 0; ks < nk; ++ks) {
         if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag)) { ok = false; break; }
-        const uint32_t sa = sbase + stage * STAGE_BYTES;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int r = r0 + 16 * j;
-          cp_async16(sa + r * 128 + ((c ^ (r & 7)) << 4), src[j] + ks * BK);
-        }
-        cp_async_commit();
-        if (++pending > GATHER_DEPTH) {
-          cp_async_wait<GATHER_DEPTH>();   // the group of stage (stage - GATHER_DEPTH) has landed
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(full_bar((stage - GATHER_DEPTH + STAGES) % STAGES));
-          --pending;
+        if ((lane & 3) == 0) {
+          tma_gather4(sbase + stage * STAGE_BYTES + g * 128, &map_a, full_bar(stage), ks * BK, tok, t1, t2, t3);
+          issued |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
         }
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
       }
+      if (!ok) break;
     }
-    cp_async_wait<0>();
-    if (ok) {
-      fence_proxy_async_smem();
-      __syncwarp();
-      for (; pending > 0; --pending)
-        if (lane == 0) mbar_arrive(full_bar((stage - pending + STAGES) % STAGES));
-    }
+    // after an abort, wait (bounded) for the row loads still in flight before the block exits
+    if (*abort_flag)
+      for (int s = 0; s < STAGES; ++s)
+        if (issued & (1u << s)) mbar_drain(full_bar(s), (last_par >> s) & 1);
   } else if (FP4 && warp >= 6) {
     // ---------------------------------------------------------------- FP4 expansion (warps 6..13)
     const int c = threadIdx.x - 192;

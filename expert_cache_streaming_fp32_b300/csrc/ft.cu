@@ -453,7 +453,9 @@ int launch_expert_tc(int wtype, const ExpertArgs& ea, const ft_expert_layout& L,
   {
     const uint64_t dx[2] = {(uint64_t)H, (uint64_t)Tk}, sx[1] = {(uint64_t)H * 2};
     const uint64_t da[2] = {(uint64_t)I, (uint64_t)Tk}, sa[1] = {(uint64_t)I * 2};
-    int r = make_map_bf16(&mx, xp, 2, dx, sx, tc::BM);
+    // direct: a map over x itself with one-row boxes, for the kernel's tile::gather4 row loads
+    const uint64_t dxd[2] = {(uint64_t)H, (uint64_t)ea.T};
+    int r = direct ? make_map_bf16(&mx, ea.x, 2, dxd, sx, 1) : make_map_bf16(&mx, xp, 2, dx, sx, tc::BM);
     if (!r) r = make_map_bf16(&ma, aint, 2, da, sa, tc::BM);
     if (tc::is_fp4(wtype)) {
       if (!r) r = make_map_fp4(&mg, pool + L.off_val[0], H, I, ea.pool_slots, ea.S, BN / 2);
