@@ -1,0 +1,66 @@
+"""bench.py's per-kernel span bookkeeping on CPU, with stand-in events (no GPU).
+
+Each wave of a decode step records tagged events; the fill span is "cache" to
+"fill_end", and the expert span is "fill_end" to "expert_end" for the plain cache
+step, or the hits' call plus the filled experts' call for the split step (whose
+"fill_end" is recorded on the fill stream and may come after "hit_end").
+"""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+class FakeEvent:
+    def __init__(self, t):
+        self.t = t
+
+    def elapsed_time(self, other):
+        return other.t - self.t
+
+
+def log_of(seq):
+    ev = bench.EventLog()
+    ev.ev = [(tag, FakeEvent(t)) for tag, t in seq]
+    return ev
+
+
+def test_plain_step_spans():
+    # two waves: cache 0..10 fill, experts 10..14; cache 20..21, experts 21..30
+    ev = log_of([("cache", 0), ("fill_end", 10), ("expert_end", 14),
+                 ("cache", 20), ("fill_end", 21), ("expert_end", 30)])
+    cache, experts = ev.cache_expert_spans()
+    assert cache == [10, 1] and experts == [4, 9]
+    s = bench.spans_us([ev])
+    assert s == {"control_fill": 5.5e3, "experts": 6.5e3}
+
+
+def test_split_step_spans():
+    # control ends at 2; the fill (other stream) ends at 12; hits run 2..6; join at 12; filled 12..15
+    ev = log_of([("cache", 0), ("ctrl_end", 2), ("fill_end", 12), ("hit_end", 6), ("join", 12),
+                 ("expert_end", 15),
+                 ("cache", 20), ("ctrl_end", 21), ("fill_end", 22), ("hit_end", 25), ("join", 25),
+                 ("expert_end", 26)])
+    cache, experts = ev.cache_expert_spans()
+    assert cache == [12, 2]
+    assert experts == [(6 - 2) + (15 - 12), (25 - 21) + (26 - 25)]
+    s = bench.spans_us([ev])
+    assert s["hits"] == 1e3 * (4 + 4) / 2 and s["filled"] == 1e3 * (3 + 1) / 2
+    assert s["wait_for_fill"] == 1e3 * (6 + 0) / 2
+
+
+def test_launch_count_per_step():
+    class Cfg:
+        n_layers, wtype = 40, bench.synth.W_BF16
+
+    class Tr:
+        cfg, n_waves = Cfg, 1
+        launches_per_step = bench.DecodeTrace.launches_per_step
+
+    t = Tr()
+    t.fill_stream = None
+    assert t.launches_per_step() == 40 * 9        # route x3, control, fill, gather + gate/up + down, combine
+    t.fill_stream = object()
+    assert t.launches_per_step() == 40 * 12       # a second expert call in the split form
