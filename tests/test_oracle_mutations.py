@@ -137,3 +137,38 @@ def test_mutant_lru_hit_does_not_refresh(monkeypatch):
         return ev, so
     monkeypatch.setattr(lru.LRUSim, "_wave", wave)
     _fails(t_lru.test_single_access_steps_match_ordered_dict_lru, 3, 8, 2, 1)
+
+
+def test_mutant_dispatch_codes_3_and_4_swapped(monkeypatch):
+    orig = formats.dequant
+
+    def dequant(component, wtype):
+        return orig(component, {3: 4, 4: 3}.get(wtype, wtype))
+    monkeypatch.setattr(formats, "dequant", dequant)
+    import test_oracle_dispatch as t_disp
+    # read as NVFP4, the MXFP4 row lacks the tensor scale or decodes to other values
+    for name in ("mxfp4_two_blocks", "nvfp4_three_blocks"):
+        with pytest.raises((AssertionError, ValueError, KeyError)):
+            t_disp.test_dequant_dispatch_on_hand_worked_blocks(name)
+
+
+def test_mutant_bf16_read_as_fp16(monkeypatch):
+    import torch
+    orig = formats.to_f64
+
+    def to_f64(t):
+        if isinstance(t, torch.Tensor) and t.dtype == torch.bfloat16:
+            return t.view(torch.float16).numpy().astype(np.float64)
+        return orig(t)
+    monkeypatch.setattr(formats, "to_f64", to_f64)
+    import test_oracle_dispatch as t_disp
+    _fails(t_disp.test_to_f64_bf16_bit_patterns)
+
+
+def test_mutant_expert_source_returns_up_first(monkeypatch):
+    def call(self, e):
+        c = self.fetch(e)
+        return tuple(formats.dequant(c[m], self.wtype) for m in ("up", "gate", "down"))
+    monkeypatch.setattr(moe.ExpertSource, "__call__", call)
+    import test_oracle_dispatch as t_disp
+    _fails(t_disp.test_expert_source_order_values_and_caching)
