@@ -25,7 +25,8 @@ if not os.path.exists(LIB_PATH):
 _lib = ctypes.CDLL(LIB_PATH)
 
 # status / enums (values of include/ft.h)
-FT_OK, FT_EINVAL, FT_ENOMEM, FT_ECUDA, FT_ETIMEOUT, FT_ESTATE, FT_EUNSUPPORTED, FT_EDEVICE = range(8)
+FT_OK, FT_EINVAL, FT_ENOMEM, FT_ECUDA, FT_ETIMEOUT, FT_ESTATE, FT_EUNSUPPORTED, FT_EDEVICE, FT_EIO = range(9)
+FT_INJECT_DEVICE_ALLOC, FT_INJECT_HOST_PIN, FT_INJECT_STREAM_EVENT = 1, 2, 3
 FT_W_F32, FT_W_BF16, FT_W_FP8E4M3, FT_W_NVFP4, FT_W_MXFP4 = range(5)
 FT_X_F32, FT_X_BF16 = 0, 1
 
@@ -36,7 +37,8 @@ EXPORTED = [
     "ft_cache_export", "ft_expert_grouped_workspace", "ft_expert_grouped", "ft_combine", "ft_stream_create",
     "ft_stream_layer", "ft_stream_layer_done", "ft_stream_bytes", "ft_stream_destroy", "ft_qsplit",
     "ft_expert_grouped_noalloc", "ft_debug_bounded_wait", "ft_cache_step_split", "ft_cache_fill_join",
-    "ft_cache_set_fill_blocks",
+    "ft_cache_set_fill_blocks", "ft_debug_inject_failure", "ft_debug_live_resources", "ft_pool_read",
+    "ft_host_register", "ft_host_unregister",
 ]
 FT_NOALLOC_MAX_ELEMS = 1 << 20
 FT_TC_WIDE_ASSIGNMENTS = 2048
@@ -102,6 +104,11 @@ _sigs = {
     "ft_qsplit": (_I, [_I, ctypes.c_double, ctypes.c_double]),
     "ft_expert_grouped_noalloc": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, ctypes.c_uint64, _I, _P, _P]),
     "ft_debug_bounded_wait": (_I, [ctypes.c_int64, _P, _P]),
+    "ft_debug_inject_failure": (_I, [_I, _I]),
+    "ft_debug_live_resources": (_I, [ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),
+    "ft_pool_read": (_I, [ctypes.c_char_p, ctypes.c_uint64, _P, ctypes.c_uint64, _I]),
+    "ft_host_register": (_I, [_P, ctypes.c_uint64]),
+    "ft_host_unregister": (_I, [_P]),
 }
 for _name, (_res, _args) in _sigs.items():
     _f = getattr(_lib, _name)
@@ -163,6 +170,30 @@ def ft_expert_layout_get(wtype: int, hidden: int, inter: int) -> ExpertLayout:
 def ft_debug_bounded_wait(limit_ns: int, completed, stream=None):
     """Runs the bounded-wait failure path on purpose (a barrier that nothing completes)."""
     _check("ft_debug_bounded_wait", _lib.ft_debug_bounded_wait(int(limit_ns), _ptr(completed), _stream(stream)))
+
+
+def ft_debug_inject_failure(site: int, after: int):
+    """Arms (after >= 0) or disarms (after < 0) a host-side failure at one site of the library."""
+    _check("ft_debug_inject_failure", _lib.ft_debug_inject_failure(site, after))
+
+
+def ft_debug_live_resources():
+    """(device allocations, streams + events) held by the library's handles."""
+    a, b = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check("ft_debug_live_resources", _lib.ft_debug_live_resources(ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+def ft_pool_read(path: str, offset: int, dst_ptr: int, nbytes: int, threads: int = 0):
+    _check("ft_pool_read", _lib.ft_pool_read(os.fsencode(path), offset, ctypes.c_void_p(dst_ptr), nbytes, threads))
+
+
+def ft_host_register(ptr: int, nbytes: int):
+    _check("ft_host_register", _lib.ft_host_register(ctypes.c_void_p(ptr), nbytes))
+
+
+def ft_host_unregister(ptr: int):
+    _check("ft_host_unregister", _lib.ft_host_unregister(ctypes.c_void_p(ptr)))
 
 
 def ft_qsplit(m: int, bw_fill: float, bw_host: float) -> int:
@@ -239,6 +270,50 @@ class PinnedBuffer:
             self.tensor = None
             _check("ft_host_free", _lib.ft_host_free(ctypes.c_void_p(self.ptr)))
             self.ptr = 0
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+class RegisteredBuffer:
+    """Read-then-pin host memory: a page-aligned anonymous mapping that is filled
+    first (its pages are faulted in by that write) and pinned afterwards with
+    ft_host_register, viewed as a uint8 tensor.  ``pin()`` must come before the
+    GPU reads it."""
+
+    def __init__(self, nbytes: int):
+        import mmap
+        import numpy as np
+        self.map = mmap.mmap(-1, nbytes, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+        arr = np.frombuffer(self.map, dtype=np.uint8)
+        self.ptr = arr.ctypes.data
+        self.nbytes = nbytes
+        self.tensor = torch.from_numpy(arr)
+        self.pinned = False
+
+    def read(self, path: str, offset: int = 0, threads: int = 0):
+        """Fills the whole buffer from a pool file with libft's parallel reader."""
+        ft_pool_read(path, offset, self.ptr, self.nbytes, threads)
+
+    def pin(self):
+        if not self.pinned:
+            ft_host_register(self.ptr, self.nbytes)
+            self.pinned = True
+
+    def free(self):
+        if self.ptr:
+            if self.pinned:
+                ft_host_unregister(self.ptr)
+                self.pinned = False
+            self.tensor = None
+            self.ptr = 0
+            try:
+                self.map.close()
+            except BufferError:       # a view is still alive; the mapping goes with it
+                pass
 
     def __del__(self):
         try:

@@ -1,6 +1,7 @@
 // libft: the exported C ABI (include/ft.h).  Single translation unit: the
 // kernels live in the included .cuh files.
 #include "common.cuh"
+#include "host.cuh"
 #include "route.cuh"
 #include "expert.cuh"
 #include "expert_tc.cuh"
@@ -62,6 +63,7 @@ FT_API const char* ft_status_str(int status) {
     case FT_ESTATE: return "call not allowed in this state";
     case FT_EUNSUPPORTED: return "unsupported configuration";
     case FT_EDEVICE: return "device-side index error";
+    case FT_EIO: return "file could not be read";
     default: return "unknown status";
   }
 }
@@ -86,6 +88,19 @@ FT_API int ft_debug_bounded_wait(int64_t limit_ns, int* completed, ft_cuda_strea
   return FT_OK;
 }
 
+FT_API int ft_debug_inject_failure(int site, int after) {
+  FT_REQUIRE(site >= 1 && site < INJ_SITES);
+  g_inject_after[site] = after < 0 ? -1 : after;
+  return FT_OK;
+}
+
+FT_API int ft_debug_live_resources(int64_t* device_allocs, int64_t* streams_events) {
+  FT_REQUIRE(device_allocs && streams_events);
+  *device_allocs = g_live_dev_allocs.load();
+  *streams_events = g_live_streams_events.load();
+  return FT_OK;
+}
+
 FT_API int ft_expert_layout_get(int wtype, int hidden, int inter, ft_expert_layout* out) {
   FT_REQUIRE(out);
   return expert_layout(wtype, hidden, inter, out);
@@ -101,6 +116,7 @@ FT_API int ft_qsplit(int m, double bw_fill, double bw_host) {
 FT_API int ft_host_alloc(uint64_t bytes, void** out) {
   FT_REQUIRE(out && bytes > 0);
   *out = nullptr;
+  if (inject_fail(INJ_HOST_PIN)) return FT_ENOMEM;
   void* p = nullptr;
   cudaError_t e = cudaHostAlloc(&p, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
   if (e != cudaSuccess) {
@@ -115,6 +131,31 @@ FT_API int ft_host_alloc(uint64_t bytes, void** out) {
 FT_API int ft_host_free(void* p) {
   if (!p) return FT_OK;
   FT_CHECK_CUDA(cudaFreeHost(p));
+  return FT_OK;
+}
+
+FT_API int ft_pool_read(const char* path, uint64_t offset, void* dst, uint64_t bytes, int threads) {
+  FT_REQUIRE(path && (dst || bytes == 0) && threads >= 0 && threads <= 256);
+  if (bytes == 0) return FT_OK;
+  if (threads == 0) threads = (int)std::min<unsigned>(64u, std::max(1u, std::thread::hardware_concurrency()));
+  return pool_read(path, offset, dst, bytes, threads);
+}
+
+FT_API int ft_host_register(void* p, uint64_t bytes) {
+  FT_REQUIRE(p && bytes > 0 && ((uintptr_t)p & 4095) == 0);
+  if (inject_fail(INJ_HOST_PIN)) return FT_ENOMEM;
+  cudaError_t e = cudaHostRegister(p, bytes, cudaHostRegisterMapped | cudaHostRegisterPortable);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    g_last_cuda_error = (int)e;
+    return FT_ENOMEM;
+  }
+  return FT_OK;
+}
+
+FT_API int ft_host_unregister(void* p) {
+  FT_REQUIRE(p);
+  FT_CHECK_CUDA(cudaHostUnregister(p));
   return FT_OK;
 }
 
@@ -549,13 +590,11 @@ FT_API int ft_cache_create(const ft_cache_config* cfg, ft_cache** out) {
   c->host = (const uint8_t*)cfg->host_pool; c->host_dev = (const uint8_t*)hd; c->pool = (uint8_t*)cfg->slot_pool;
   cudaGetDevice(&c->dev);
   const size_t nk = (size_t)c->L * c->E;
-  bool ok = cudaMalloc(&c->slot_of_key, nk * 4) == cudaSuccess &&
-            cudaMalloc(&c->key_of_slot, (size_t)c->max_slots * 4) == cudaSuccess &&
-            cudaMalloc(&c->stamp, (size_t)c->max_slots * 4) == cudaSuccess &&
-            cudaMalloc(&c->order, (size_t)c->max_slots * 4) == cudaSuccess &&
-            cudaMalloc(&c->clock, 4) == cudaSuccess && cudaMalloc(&c->stats, 5 * 8) == cudaSuccess &&
-            cudaMalloc(&c->fill_src, (size_t)c->E * 4) == cudaSuccess &&
-            cudaMalloc(&c->fill_dst, (size_t)c->E * 4) == cudaSuccess && cudaMalloc(&c->n_fill, 4) == cudaSuccess;
+  auto dm = [](auto** p, size_t n) { return dev_malloc(reinterpret_cast<void**>(p), n) == cudaSuccess; };
+  bool ok = dm(&c->slot_of_key, nk * 4) && dm(&c->key_of_slot, (size_t)c->max_slots * 4) &&
+            dm(&c->stamp, (size_t)c->max_slots * 4) && dm(&c->order, (size_t)c->max_slots * 4) &&
+            dm(&c->clock, 4) && dm(&c->stats, 5 * 8) && dm(&c->fill_src, (size_t)c->E * 4) &&
+            dm(&c->fill_dst, (size_t)c->E * 4) && dm(&c->n_fill, 4);
   if (!ok) {
     cudaGetLastError();
     ft_cache_destroy(c);
@@ -575,9 +614,11 @@ FT_API int ft_cache_create(const ft_cache_config* cfg, ft_cache** out) {
   if (!st && cudaFuncSetAttribute(cache_fill_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                   (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
     st = FT_ECUDA;
-  if (!st && (cudaEventCreateWithFlags(&c->ev_ctrl, cudaEventDisableTiming) != cudaSuccess ||
-              cudaEventCreateWithFlags(&c->ev_fill, cudaEventDisableTiming) != cudaSuccess))
-    st = FT_ECUDA;
+  if (!st) {
+    cudaError_t e2 = make_event(&c->ev_ctrl);
+    if (e2 == cudaSuccess) e2 = make_event(&c->ev_fill);
+    if (e2 != cudaSuccess) st = cuda_status(e2);
+  }
   if (!st && cudaDeviceSynchronize() != cudaSuccess) st = FT_ECUDA;
   if (st) {
     ft_cache_destroy(c);
@@ -596,10 +637,10 @@ FT_API int ft_cache_create(const ft_cache_config* cfg, ft_cache** out) {
 
 FT_API int ft_cache_destroy(ft_cache* c) {
   if (!c) return FT_OK;
-  cudaFree(c->slot_of_key); cudaFree(c->key_of_slot); cudaFree(c->stamp); cudaFree(c->order);
-  cudaFree(c->clock); cudaFree(c->stats); cudaFree(c->fill_src); cudaFree(c->fill_dst); cudaFree(c->n_fill);
-  if (c->ev_ctrl) cudaEventDestroy(c->ev_ctrl);
-  if (c->ev_fill) cudaEventDestroy(c->ev_fill);
+  dev_free(c->slot_of_key); dev_free(c->key_of_slot); dev_free(c->stamp); dev_free(c->order);
+  dev_free(c->clock); dev_free(c->stats); dev_free(c->fill_src); dev_free(c->fill_dst); dev_free(c->n_fill);
+  drop_event(c->ev_ctrl);
+  drop_event(c->ev_fill);
   delete c;
   return FT_OK;
 }
@@ -695,6 +736,16 @@ FT_API int ft_cache_export(ft_cache* c, int32_t* key_of_slot, uint32_t* stamp, i
 }
 
 // ------------------------------------------------------------------ stream
+// Destroys a stream handle's CUDA stream and events (those that exist) and the handle.
+static void stream_release(ft_stream* st) {
+  drop_stream(st->copy);
+  for (int b = 0; b < 2; ++b) {
+    drop_event(st->ready[b]);
+    drop_event(st->freed[b]);
+  }
+  delete st;
+}
+
 FT_API int ft_stream_create(ft_cache* c, int serialized, ft_stream** out) {
   FT_REQUIRE(c && out);
   *out = nullptr;
@@ -702,9 +753,21 @@ FT_API int ft_stream_create(ft_cache* c, int serialized, ft_stream** out) {
   if (c->N < 2 * c->E) return FT_EUNSUPPORTED;
   ft_stream* st = new (std::nothrow) ft_stream();
   if (!st) return FT_ENOMEM;
+  // the stream and events first: a failure here leaves the cache untouched
+  cudaError_t e = make_stream(&st->copy);
+  for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+    e = make_event(&st->ready[b]);
+    if (e == cudaSuccess) e = make_event(&st->freed[b]);
+  }
+  if (e != cudaSuccess) {
+    stream_release(st);
+    return cuda_status(e);
+  }
   const int n_full = c->N;
-  int s = cache_resize_impl(c, n_full - 2 * c->E);
-  if (s) { delete st; return s; }
+  if (int s = cache_resize_impl(c, n_full - 2 * c->E)) {
+    stream_release(st);
+    return s;
+  }
   c->n_full = n_full;
   c->streaming = 1;
   st->c = c;
@@ -716,17 +779,6 @@ FT_API int ft_stream_create(ft_cache* c, int serialized, ft_stream** out) {
   st->pending_layer = -1;
   st->bytes = 0;
   st->n_hist = 0;
-  cudaError_t e = cudaStreamCreateWithFlags(&st->copy, cudaStreamNonBlocking);
-  for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
-    e = cudaEventCreateWithFlags(&st->ready[b], cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st->freed[b], cudaEventDisableTiming);
-  }
-  if (e != cudaSuccess) {
-    c->streaming = 0;
-    c->N = n_full;
-    delete st;
-    return cuda_status(e);
-  }
   *out = st;
   return FT_OK;
 }
@@ -786,12 +838,7 @@ FT_API int ft_stream_destroy(ft_stream* st) {
   cudaStreamSynchronize(st->copy);
   int s = stream_adopt(st);
   c->streaming = 0;
-  cudaStreamDestroy(st->copy);
-  for (int b = 0; b < 2; ++b) {
-    cudaEventDestroy(st->ready[b]);
-    cudaEventDestroy(st->freed[b]);
-  }
-  delete st;
+  stream_release(st);
   return s;
 }
 
@@ -806,25 +853,60 @@ static constexpr size_t kNoAllocMaxElems = (size_t)1 << 20;  // fp32 elements: 4
 static __device__ __align__(256) float ft_noalloc_scratch[kNoAllocMaxElems];
 
 static constexpr int kNoAllocMaxDevices = 64;
-static void* g_noalloc_addr[kNoAllocMaxDevices];  // device address of the array, per device
+struct NoAllocAddr {
+  unsigned long long ctx_id = 0;  // context the address belongs to (0: not looked up yet)
+  void* addr = nullptr;
+};
+static NoAllocAddr g_noalloc_addr[kNoAllocMaxDevices];
 static std::mutex g_noalloc_mu;
 
-// Device address of the scratch array on the current device (set up on first use).
+// Id of the current CUDA context (0 when it cannot be read).  The array's
+// address belongs to one context: after cudaDeviceReset the next context has a
+// new id and the address is looked up again.
+static unsigned long long current_context_id() {
+  using GetCurrentFn = CUresult (*)(CUcontext*);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+    cudaGetLastError();
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, &id) == CUDA_SUCCESS) return id;
+  return 0;
+}
+
+// Device address of the scratch array in the current device's context: looked
+// up with cudaGetSymbolAddress on the first call in each context, then reused
+// (looked up on every call if the context id cannot be read).
 static int noalloc_scratch_address(void** out) {
   int d = 0;
   FT_CHECK_CUDA(cudaGetDevice(&d));
   if (d < 0 || d >= kNoAllocMaxDevices) return FT_EUNSUPPORTED;
+  unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_addr[d]) {
+  NoAllocAddr& a = g_noalloc_addr[d];
+  if (ctx == 0 || a.ctx_id != ctx || !a.addr) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress((void**)&p, ft_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) {
       cudaGetLastError();
       return cuda_status(e == cudaSuccess ? cudaErrorInvalidSymbol : e);
     }
-    g_noalloc_addr[d] = p;
+    a.addr = p;
+    a.ctx_id = ctx ? ctx : current_context_id();  // the lookup created the context if there was none
   }
-  *out = g_noalloc_addr[d];
+  *out = a.addr;
   return FT_OK;
 }
 

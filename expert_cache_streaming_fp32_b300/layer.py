@@ -16,12 +16,13 @@ Nothing here computes: it allocates buffers and sequences the C calls.
 """
 from __future__ import annotations
 
+import time
 from typing import Optional
 
 import torch
 
 from . import (FT_TC_WIDE_ASSIGNMENTS, FT_W_BF16, FT_W_F32, FT_W_FP8E4M3, FT_W_MXFP4, FT_W_NVFP4, Cache,
-               PinnedBuffer, ft_combine,
+               PinnedBuffer, RegisteredBuffer, ft_combine, ft_pool_read,
                ft_expert_grouped, ft_expert_grouped_workspace, ft_expert_layout_get, ft_permute, ft_route,
                ft_router_logits)
 
@@ -70,16 +71,64 @@ def pack_expert(comps: dict, wtype: int, layout, out: torch.Tensor) -> None:
 
 
 class ExpertPool:
-    """Pinned host pool of expert records for ``n_phys_layers`` layers of a config."""
+    """Pinned host pool of expert records for ``n_phys_layers`` layers of a config.
 
-    def __init__(self, cfg, n_phys_layers: int):
+    Built empty and pinned (``ExpertPool(cfg, n)``, then ``fill``), or from a
+    pool file with ``ExpertPool.load`` (read first, pinned afterwards by
+    default).  ``setup_s`` records the setup phases in seconds."""
+
+    def __init__(self, cfg, n_phys_layers: int, _buf=None):
         self.cfg = cfg
         self.n_phys = n_phys_layers
         self.layout = ft_expert_layout_get(cfg.wtype, cfg.hidden, cfg.inter)
         self.S = int(self.layout.bytes)
         self.E = cfg.n_experts
-        self.buf = PinnedBuffer(self.n_phys * self.E * self.S)
+        self.setup_s = {}
+        if _buf is None:
+            t0 = time.perf_counter()
+            _buf = PinnedBuffer(self.n_phys * self.E * self.S)
+            self.setup_s["alloc_pinned"] = time.perf_counter() - t0
+        self.buf = _buf
         self.host = self.buf.tensor
+
+    @property
+    def nbytes(self) -> int:
+        return self.n_phys * self.E * self.S
+
+    @classmethod
+    def load(cls, cfg, n_phys_layers: int, path: str, read_then_pin: bool = True, threads: int = 0):
+        """A pool read from a pool file (records in row order l*E + e, as ``save`` writes them).
+
+        read_then_pin: the records are read into fresh pageable memory, which the
+        read itself faults in, and the filled buffer is pinned afterwards
+        (ft_pool_read, then ft_host_register).  Otherwise the pool is pinned
+        first (ft_host_alloc) and the file read into the pinned pages."""
+        layout = ft_expert_layout_get(cfg.wtype, cfg.hidden, cfg.inter)
+        n = n_phys_layers * cfg.n_experts * int(layout.bytes)
+        times = {}
+        t0 = time.perf_counter()
+        if read_then_pin:
+            buf = RegisteredBuffer(n)
+            t1 = time.perf_counter()
+            buf.read(path, 0, threads)
+            t2 = time.perf_counter()
+            buf.pin()
+            t3 = time.perf_counter()
+            times = {"alloc_pageable": t1 - t0, "read": t2 - t1, "pin": t3 - t2}
+        else:
+            buf = PinnedBuffer(n)
+            t1 = time.perf_counter()
+            ft_pool_read(path, 0, buf.ptr, n, threads)
+            t2 = time.perf_counter()
+            times = {"alloc_pinned": t1 - t0, "read": t2 - t1}
+        pool = cls(cfg, n_phys_layers, _buf=buf)
+        pool.setup_s = times
+        return pool
+
+    def save(self, path: str) -> None:
+        """Writes the pool's records, in row order, to a pool file."""
+        with open(path, "wb") as f:
+            f.write(memoryview(self.host.numpy()))
 
     @property
     def ptr(self) -> int:

@@ -53,7 +53,8 @@ typedef enum {
   FT_ETIMEOUT = 4,      /* a bounded wait ran out */
   FT_ESTATE = 5,        /* call not allowed in the handle's current state */
   FT_EUNSUPPORTED = 6,  /* configuration the library does not handle */
-  FT_EDEVICE = 7        /* a kernel recorded an index error (see ft_get_device_error) */
+  FT_EDEVICE = 7,       /* a kernel recorded an index error (see ft_get_device_error) */
+  FT_EIO = 8            /* a file could not be opened or read to the end */
 } ft_status;
 
 /* Stored expert-weight formats ([Overview] feature table: MXFP4, NVFP4, FP8, BF16). */
@@ -96,6 +97,20 @@ int ft_get_device_error(int* code);
  * to *completed (dev int) and returns, leaving the context usable. */
 int ft_debug_bounded_wait(int64_t limit_ns, int* completed, ft_cuda_stream s);
 
+/* Host-side failure injection, for tests of the failure paths; nothing is
+ * issued to the GPU for a failed call.  With after >= 0, the next `after`
+ * calls at `site` succeed and the one after them fails as if the CUDA runtime
+ * had refused it (the site then disarms itself); after < 0 disarms the site.
+ *   FT_INJECT_DEVICE_ALLOC   device allocations of the handles' tables (ft_cache_create)
+ *   FT_INJECT_HOST_PIN       pinning: ft_host_alloc, ft_host_register
+ *   FT_INJECT_STREAM_EVENT   streams and events of the handles (ft_cache_create, ft_stream_create) */
+enum { FT_INJECT_DEVICE_ALLOC = 1, FT_INJECT_HOST_PIN = 2, FT_INJECT_STREAM_EVENT = 3 };
+int ft_debug_inject_failure(int site, int after);
+
+/* Device allocations and streams/events currently held by the library's
+ * handles (every call that fails must leave both unchanged). */
+int ft_debug_live_resources(int64_t* device_allocs, int64_t* streams_events);
+
 /* ------------------------------------------------------------------------
  * Expert record layout.
  *
@@ -136,6 +151,28 @@ int ft_expert_layout_get(int wtype, int hidden, int inter, ft_expert_layout* out
  * ---------------------------------------------------------------------- */
 int ft_host_alloc(uint64_t bytes, void** out);  /* *out = pinned, mapped, 4 KiB aligned */
 int ft_host_free(void* p);
+
+/* Read-then-pin pool setup ([Review] §2.7, fast engine start: the experts are
+ * read into their final host layout first and pinned only afterwards, because
+ * pinning first makes the driver fault in and zero every page of a pool of
+ * tens of GB before the read writes it again).
+ *
+ * ft_pool_read: reads `bytes` of the file `path` from byte `offset` into host
+ * memory dst (any host memory; typically a fresh page-aligned anonymous mapping
+ * that the read itself faults in) with `threads` threads (1 .. 256; 0 picks
+ * the hardware thread count, at most 64).  The file holds expert records in
+ * the pool's row order l*E + e (one record of ft_expert_layout.bytes per row),
+ * so one contiguous read fills whole layers.  FT_EIO when the file cannot be
+ * opened or ends early.  Host only; no GPU is touched.
+ *
+ * ft_host_register: pins and maps an already-filled host buffer (p 4 KiB
+ * aligned, bytes > 0) so that copies and kernels can read it over the host
+ * link, as memory from ft_host_alloc.  FT_ENOMEM when pinning fails (there is
+ * no unpinned fallback).  ft_host_unregister undoes it (the memory stays the
+ * caller's). */
+int ft_pool_read(const char* path, uint64_t offset, void* dst, uint64_t bytes, int threads);
+int ft_host_register(void* p, uint64_t bytes);
+int ft_host_unregister(void* p);
 
 /* ------------------------------------------------------------------------
  * Router logits: z[t][e] = sum_h x[t][h] * W_r[h][e] + bias[e] (fp32 accumulate).
@@ -308,14 +345,21 @@ int ft_cache_export(ft_cache* c, int32_t* key_of_slot, uint32_t* stamp, int* n_s
  * or on the slot used.
  *
  * Two execution paths, chosen by the weight format:
- *   - bf16 weights: tcgen05 tensor cores at every batch size, 128-row tiles
- *     of each expert's rows against 128 or 256 weight rows (256 from
- *     FT_TC_WIDE_ASSIGNMENTS assignments T*k up, when H is a multiple of 256).
- *     x is rounded to bf16 (round to nearest even) for the products, and the
- *     intermediate silu(G)*U is rounded to bf16 before the down product;
- *     products accumulate in fp32.
- *   - other formats: CUDA cores, weights streamed once per 8-row chunk of an
- *     expert's rows and dequantised in registers; x and the intermediate
+ *   - bf16, NVFP4 and MXFP4 weights: tcgen05 tensor cores at every batch
+ *     size.  Below FT_TC_WIDE_ASSIGNMENTS assignments (T*k) the weights are the
+ *     MMA's M side (128 weight rows) and up to 64 of an expert's token rows its
+ *     N side, with the K range split when few experts are routed; from
+ *     FT_TC_WIDE_ASSIGNMENTS up, 128 token rows against 128 or 256 weight rows
+ *     (256 for bf16 when H is a multiple of 256).  x is rounded to bf16 (round
+ *     to nearest even) for the products, the intermediate silu(G)*U is rounded
+ *     to bf16 before the down product, and products accumulate in fp32.  FP4
+ *     weights are expanded to bf16 in shared memory first; the expansion is
+ *     exact (e2m1 value times block scale is a bf16 value), except that an
+ *     MXFP4 block scale above 2^15 (E8M0 byte > 142) is beyond its range: the
+ *     kernel records FT_DERR_SCALE_RANGE and those outputs are wrong.  NVFP4's
+ *     fp32 matrix scale multiplies the fp32 results.
+ *   - fp32 and FP8 weights: CUDA cores, weights streamed once per 8-row chunk
+ *     of an expert's rows and dequantised in registers; x and the intermediate
  *     silu(G)*U stay in fp32.
  * ---------------------------------------------------------------------- */
 #define FT_TC_WIDE_ASSIGNMENTS 2048
@@ -326,24 +370,31 @@ int ft_expert_grouped(const void* x, int x_type, int T, int k, int hidden, int i
                       void* workspace, size_t workspace_bytes, ft_cuda_stream s);
 
 /* ------------------------------------------------------------------------
- * ft_expert_grouped_noalloc: the same computation and arguments as
+ * ft_expert_grouped_noalloc: the grouped expert FFN with the arguments of
  * ft_expert_grouped, without the workspace.  The pages have no counterpart:
  * this entry point exists for callers that cannot call cudaMalloc -- a host
  * application that owns every device allocation through its own allocator or
  * fixed budget, or a latency-critical path where cudaMalloc's implicit device
  * synchronisation is not acceptable.  The library allocates nothing here.
  *
+ * It always runs the CUDA-core kernels, for every weight format: weights
+ * dequantised in registers, x and the intermediate silu(G)*U in fp32.  Its
+ * results therefore differ from ft_expert_grouped's for bf16, NVFP4 and MXFP4
+ * weights (which run on the tensor cores with a bf16 intermediate) within the
+ * tolerance of that rounding, not bit for bit, and it is slower for them.
+ *
  * The fp32 intermediate lives in one fixed device array inside the library,
  * FT_NOALLOC_MAX_ELEMS floats (4 MiB), which every GPU that loads the library
  * holds until the process exits.  Calls with T*k*inter > FT_NOALLOC_MAX_ELEMS
  * return FT_EINVAL and launch nothing.
  *
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  All calls share the one array and it keeps the
- * last call's contents (nothing needs clearing: each call writes every element
- * it reads before reading it).  Calls that overlap on the GPU -- on different
- * streams, or from different host threads -- race on the array: order them.
+ * The first call in each CUDA context (per device; again after a
+ * cudaDeviceReset) looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current); make that first call before any stream capture.
+ * All calls share the one array and it keeps the last call's contents
+ * (nothing needs clearing: each call writes every element it reads before
+ * reading it).  Calls that overlap on the GPU -- on different streams, or from
+ * different host threads -- race on the array: order them.
  * ---------------------------------------------------------------------- */
 #define FT_NOALLOC_MAX_ELEMS (1u << 20)
 int ft_expert_grouped_noalloc(const void* x, int x_type, int T, int k, int hidden, int inter, int E,

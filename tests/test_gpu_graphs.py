@@ -1,0 +1,117 @@
+"""A whole decode step captured in one CUDA graph, replayed, and re-captured
+after safe-point resizes ([Review] §2.6: the cache control runs on the device
+with fixed-shape buffers and device-side counts, so the step can be put into
+a CUDA graph; §2.7: a new cache configuration re-captures the execution
+path).
+
+The graph holds every layer of the step: router logits, routing,
+permutation, every wave of the split cache step (hits evaluated while the
+miss fill copies on a second stream, then the filled experts after the join)
+and the combine.  After each replay the test compares every layer's output
+with the fp64 oracle and the cache's residency tables and per-wave counts
+with the LRU simulator; after each resize (which changes the wave count) it
+captures a new graph and goes on.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from conftest import assert_close_layer
+from oracle import formats, moe
+from oracle.lru import LRUSim
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def ft(ftlib):
+    assert torch.cuda.is_available()
+    return ftlib
+
+
+def test_captured_decode_step_with_resize_and_recapture(ft):
+    cfg = synth.MoEConfig("graph", 256, 32, 4, 128, 3, synth.W_BF16, "bf16", seed=13, zipf_s=1.1)
+    L, E, k, T = cfg.n_layers, cfg.n_experts, cfg.top_k, 8
+    pool = ft.ExpertPool(cfg, L)
+    pool.fill(DEV)
+    S = pool.S
+    max_slots = 16
+    sp = torch.empty(max_slots * S, dtype=torch.uint8, device=DEV)
+    cache = ft.Cache(L, E, L, 12, max_slots, S, pool.ptr, sp)
+    sim = LRUSim(12, E)
+    lay = ft.MoELayer(cfg, T)
+    routers = [synth.router_weights(cfg, l, DEV) for l in range(L)]
+    src = [moe.ExpertSource(lambda e, l=l: synth.expert_weights(cfg, l, e, DEV), cfg.wtype) for l in range(L)]
+    x_buf = torch.empty(T, cfg.hidden, dtype=torch.bfloat16, device=DEV)
+    outs = torch.empty(L, T, cfg.hidden, dtype=torch.float32, device=DEV)
+    counts = torch.zeros(L, 8, 4, dtype=torch.int32, device=DEV)     # per layer, per wave
+    fs = torch.cuda.Stream(device=DEV)
+    trace = synth.AR1Trace(cfg, T, DEV, tag=2)
+
+    def decode_step(ratio):
+        for l in range(L):
+            lay.route(x_buf, *routers[l])
+            for w in range(cache.n_waves()):
+                lay.cached_wave(x_buf, l, cache, S, ratio, w, counts[l, w], fill_stream=fs)
+            outs[l].copy_(lay.combine(T, lay.ext, None))
+
+    def check(ratio):
+        """Oracle outputs and simulator decisions for the step just run on x_buf."""
+        x64 = formats.to_f64(x_buf)
+        got_out = outs.cpu().numpy()
+        got_counts = counts.cpu().numpy()
+        for l in range(L):
+            wr, b = routers[l]
+            z = moe.router_logits(x64, formats.to_f64(wr), formats.to_f64(b))
+            assert not moe.near_ties(z, k).any()
+            idx, w = moe.route(z, k)
+            events, _ = sim.step(l, idx.reshape(-1), ratio)
+            U = sorted(set(idx.reshape(-1).tolist()))
+            nw = cache.n_waves()
+            for wv in range(nw):
+                wave = set(U[wv * sim.N:(wv + 1) * sim.N])
+                ev = [e for e in events if e[1] in wave]
+                want = [len(ev), sum(e[0] == "hit" for e in ev), sum(e[0] == "fill" for e in ev),
+                        sum(e[0] == "ext" for e in ev)]
+                assert got_counts[l, wv].tolist() == want, (l, wv)
+            on_gpu = [e[1] for e in events if e[0] != "ext"]
+            ref = moe.moe_layer(x64, idx, w, src[l], act_round=formats.round_to_bf16, only=on_gpu)
+            assert_close_layer(got_out[l], ref, fro=1e-2)
+        key, stamp, clock = cache.export()
+        sk, ss = sim.state()
+        assert key.tolist() == sk.tolist() and stamp.tolist() == ss.tolist() and clock == sim.clock
+
+    schedule = [(12, 1.0, 4), (7, 0.7, 4), (12, 0.7, 3)]     # (slots, fill ratio, replays)
+    for phase, (N, ratio, reps) in enumerate(schedule):
+        if phase:
+            torch.cuda.synchronize()
+            cache.resize(N)                                     # safe point: nothing in flight
+            sim.resize(N)
+            key, stamp, clock = cache.export()
+            sk, ss = sim.state()
+            assert key.tolist() == sk.tolist() and stamp.tolist() == ss.tolist()
+        assert cache.n_waves() == -(-E // N)
+        # one eager step (kernel attributes set outside capture), then the graph
+        x_buf.copy_(trace.next())
+        counts.zero_()
+        decode_step(ratio)
+        torch.cuda.synchronize()
+        check(ratio)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            decode_step(ratio)
+        for _ in range(reps):
+            x_buf.copy_(trace.next())
+            counts.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            check(ratio)
+        del g
+    st = cache.stats()
+    assert (st.hits, st.fills, st.externals) == (sim.hits, sim.fills, sim.externals)
+    assert sim.externals > 0 and sim.fills > 0 and sim.hits > 0
+    assert ft.ft_get_device_error() == 0
+    cache.destroy()
+    pool.free()

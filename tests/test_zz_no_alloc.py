@@ -4,10 +4,12 @@ ft_expert_grouped_noalloc serves callers that cannot call cudaMalloc (a host
 application that owns all device memory through its own allocator, or a
 latency-critical path that cannot afford cudaMalloc's implicit device
 synchronisation).  Its intermediate lives in a fixed 4 MiB array inside the
-library instead of a caller workspace.  These tests call it through the C ABI
-twice in a row and compare each result with ft_expert_grouped's on the same
-inputs, within the tolerance the other parity tests use.  This file is named
-so that pytest collects it after every other test file.
+library instead of a caller workspace, and it always runs the CUDA-core
+kernels (fp32 intermediate).  These tests call it through the C ABI twice in a
+row and compare each result with the fp64 oracle and with ft_expert_grouped's
+on the same inputs, within the tolerances the other parity tests use, and
+check the size limit on both sides of it.  This file is named so that pytest
+collects it after every other test file.
 """
 import numpy as np
 import pytest
@@ -15,7 +17,7 @@ import torch
 
 import synth
 from conftest import assert_close_layer
-from oracle import moe
+from oracle import formats, moe
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -30,6 +32,20 @@ def _setup(ft, wtype, H, I, E, seed):
     for e in range(E):
         ft.pack_expert(synth.expert_weights(cfg, 0, e, DEV), wtype, L, pool[(e + 1) * S:(e + 2) * S])
     return cfg, pool, S, n_slots
+
+
+def _oracle_rows(cfg, x, perm, offsets, k, experts):
+    """The oracle's Y rows (permuted order) for the given experts; others stay NaN."""
+    xs = formats.to_f64(x)
+    Y = np.full((perm.size, cfg.hidden), np.nan)
+    for e in experts:
+        rows = np.arange(offsets[e], offsets[e + 1])
+        if rows.size == 0:
+            continue
+        c = synth.expert_weights(cfg, 0, e, DEV)
+        g, u, d = (formats.dequant(c[m], cfg.wtype) for m in ("gate", "up", "down"))
+        Y[rows] = moe.expert_ffn(xs[perm[rows] // k], g, u, d)
+    return Y
 
 
 def _one_call(ft, cfg, pool, S, n_slots, T, k, tag):
@@ -53,7 +69,12 @@ def _one_call(ft, cfg, pool, S, n_slots, T, k, tag):
     skipped = np.arange(offsets[0], offsets[1])
     assert np.isnan(a[skipped]).all()
     keep = np.setdiff1d(np.arange(T * k), skipped)
-    assert_close_layer(a[keep], b[keep])
+    # against the oracle (fp32 intermediate on this path: the plain bar, and far inside it)
+    ref = _oracle_rows(cfg, x, perm, offsets, k, range(1, E))
+    assert_close_layer(a[keep], ref[keep])
+    assert np.linalg.norm(a[keep] - ref[keep]) / np.linalg.norm(ref[keep]) < 2e-5
+    # against the workspace entry point (tensor cores for bf16 / FP4: bf16 intermediate)
+    assert_close_layer(a[keep], b[keep], fro=1e-2)
 
 
 def test_noalloc_matches_workspace_entry_point_twice(ftlib):
@@ -69,6 +90,15 @@ def test_noalloc_matches_for_a_block_scaled_format(ftlib):
     cfg, pool, S, n_slots = _setup(ft, ft.FT_W_MXFP4, 1024, 512, 16, seed=22)
     _one_call(ft, cfg, pool, S, n_slots, T=33, k=8, tag=3)
     _one_call(ft, cfg, pool, S, n_slots, T=33, k=8, tag=4)
+
+
+def test_noalloc_accepts_a_call_exactly_at_the_limit(ftlib):
+    ft = ftlib
+    k, I = 8, 2048
+    T = ft.FT_NOALLOC_MAX_ELEMS // (k * I)             # T*k*I == FT_NOALLOC_MAX_ELEMS (T = 64)
+    assert T * k * I == ft.FT_NOALLOC_MAX_ELEMS
+    cfg, pool, S, n_slots = _setup(ft, ft.FT_W_BF16, 512, I, 16, seed=23)
+    _one_call(ft, cfg, pool, S, n_slots, T=T, k=k, tag=5)
 
 
 def test_noalloc_refuses_sizes_beyond_its_array(ftlib):
