@@ -3,12 +3,14 @@
 
 Workload (one GPU): the 40-layer BF16 MoE stack (hidden 2048, 256 experts,
 top-8, SwiGLU intermediate 512, weights N(0, 0.02)), whose 10,240 experts
-(64.4 GB) sit in pinned host memory.  One step is one decode step of every
-layer at each batch size T = 1, 4, 16, 64: four independent decode traces
-(AR(1) hidden states h_t = 0.9 h_{t-1} + 0.436 N(0,1), Zipf(1.1) router
-prior), each over its own LRU expert cache holding 40% of the (layer,
-expert) slots (4096 slots).  A second leg streams 8192-token prefill chunks
-through two whole-layer buffers (double-buffered and serialized).
+(64.4 GB) sit in pinned host memory.  One step is one pass of the decode
+trace: at each batch size T = 1, 4, 16, 64, 256 decode steps of every layer
+(T independent AR(1) chains h_t = 0.9 h_{t-1} + 0.436 N(0,1), Zipf(1.1) router
+prior) over an LRU expert cache holding 40% of the (layer, expert) slots
+(4096 slots), starting from an empty cache, so the cold start is counted.
+Further legs: prefill chunks streamed through two whole-layer buffers
+(double-buffered and serialized), pool setup pin-first vs read-then-pin, the
+NVFP4 stack and the MXFP4 mixed trace.
 
 Output: one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
 oracle on a bounded sample of the same workload instead.
@@ -35,21 +37,24 @@ BATCHES = (1, 4, 16, 64)
 
 # DRAM traffic per algorithmic byte, from one ncu capture of each kernel
 # (dram__bytes_read.sum + dram__bytes_write.sum over the algorithmic bytes of the
-# same launch; profiles/cache_fill_bf16_32experts.md, profiles/expert_tc_bf16_decode_T64.md).
-# The fill's reads come over the host link, so its DRAM traffic is the writes of
-# the filled experts that reached DRAM before the launch ended.
+# same launch: the 32-expert fill case, and the 64-token bf16 expert call).  The
+# bench scales these to its own launches and labels the result as scaled.  The
+# fill's reads come over the host link, so its DRAM traffic is the writes of the
+# filled experts that reached DRAM before the launch ended.
 TRAFFIC_PER_BYTE = {"fill": (0.025e6 + 140.025e6) / 201.327e6,
                     "experts": (207.776e6 + 3.545e6 + 103.355e6 + 2.734e6) / (205.5e6 + 0.5e6 + 102.8e6)}
 CACHE_FRAC = 0.40
+FP4_OVER_BF16 = 13.5 / 2.25       # nominal dense FP4 / bf16 tensor rates of the B300
 METRIC = "MoE-layer tokens/s (decode T=1..64, prefill 8192) and % of layer roofline"
-WORKLOAD = ("decode_bf16_40L: H=2048 E=256 top-8 I=512, bf16 weights, 40 layers, "
-            "cache 40% (4096 slots) per batch size, AR(1)+Zipf(1.1) traces")
+WORKLOAD = ("decode_bf16_40L: H=2048 E=256 top-8 I=512, bf16 weights, 40 layers, 64.4 GB pinned host pool, "
+            "LRU cache of 40% (4096 slots), 256-step AR(1)+Zipf(1.1) decode trace at T=1,4,16,64, each from a "
+            "cold cache")
 
 
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=12)
+    p.add_argument("--steps", type=int, default=2, help="timed passes of the whole decode trace")
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--phys-layers", type=int, default=0, help="host pool layers (0: all 40 when RAM allows)")
@@ -57,11 +62,16 @@ def parse():
     p.add_argument("--prompts", default="4096,8192,16384", help="prefill prompt lengths (chunks of <= 8192)")
     p.add_argument("--no-prefill", action="store_true")
     p.add_argument("--no-fp4", action="store_true", help="skip the NVFP4 stack and the MXFP4 mixed-trace legs")
-    p.add_argument("--fp4-steps", type=int, default=6, help="timed decode steps per batch size, NVFP4 stack")
+    p.add_argument("--fp4-steps", type=int, default=24, help="decode steps per batch size from a cold cache, NVFP4 stack")
+    p.add_argument("--trace-steps", type=int, default=256, help="decode steps of the trace per batch size")
+    p.add_argument("--steady-from", type=int, default=32, help="first step of the steady-state figures")
+    p.add_argument("--cpu-tokens", type=int, default=2, help="T=1 tokens per round of the CPU oracle baseline")
+    p.add_argument("--cpu-budget-s", type=float, default=12.0, help="wall seconds of timed CPU baseline rounds")
+    p.add_argument("--no-pool-setup", action="store_true", help="skip the pin-first vs read-then-pin setup leg")
+    p.add_argument("--setup-layers", type=int, default=2, help="layers of the pool file in the setup leg")
     p.add_argument("--mixed-decode-steps", type=int, default=512)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--no-graphs", action="store_true", help="issue the decode steps eagerly instead of as CUDA graphs")
     p.add_argument("--split-min-assignments", type=int, default=0,
                    help="smallest decode batch T*k for the split form, every format (0: the policy per format)")
     p.add_argument("--no-split-fill", action="store_true",
@@ -207,112 +217,152 @@ def host_ram_bytes() -> int:
 
 # ---------------------------------------------------------------- the decode workload
 
-class DecodeTrace:
-    """One batch size: its cache, per-step buffers, resident inputs and per-layer-step counters."""
+class DecodeRun:
+    """The decode trace of one stacked workload, every batch size from a cold cache.
 
-    def __init__(self, ft, cfg, T, pool, routers, n_steps, dev, e2e, n_slots=None, split_min=0):
-        self.ft, self.cfg, self.T = ft, cfg, T
-        # the split form where it pays
-        self.fill_stream = (torch.cuda.Stream(device=dev)
-                            if split_min >= 0 and ft.split_pays(T, cfg.top_k, cfg.wtype, split_min) else None)
-        L, E = cfg.n_layers, cfg.n_experts
-        self.n_slots = n_slots or int(round(CACHE_FRAC * L * E))
-        self.S = pool.S
-        self.sp = torch.empty(self.n_slots * pool.S, dtype=torch.uint8, device=dev)
-        self.pool = pool
-        self.cache = ft.Cache(L, E, pool.n_phys, self.n_slots, self.n_slots, pool.S, pool.ptr, self.sp)
-        self.layer = ft.MoELayer(cfg, T, dev)
-        tr = synth.AR1Trace(cfg, T, dev, tag=T)
-        self.xs = torch.stack([tr.next() for _ in range(n_steps)])          # [steps, T, H] resident
+    For each batch size T: ``n_steps`` decode steps of all layers (T independent
+    AR(1) chains, inputs resident on the device), starting from an empty cache
+    ([Review] §2.7: no warm-up, the first request meets a cold cache).  One slot
+    pool and one cache handle serve the batch sizes in turn: ``ft_cache_reset``
+    empties the cache before each.  Every (T, step) is one CUDA graph, captured
+    once and replayed in every pass; its layer outputs go to a per-T device
+    buffer, and its per-wave cache counters to a per-step record."""
+
+    def __init__(self, ft, cfg, pool, routers, batches, n_steps, dev, n_slots, split_min=0, e2e=False):
+        self.ft, self.cfg, self.pool, self.routers = ft, cfg, pool, routers
+        self.batches, self.n_steps, self.dev = list(batches), n_steps, dev
+        L, E, H = cfg.n_layers, cfg.n_experts, cfg.hidden
+        self.S, self.n_slots = pool.S, n_slots
+        self.sp = torch.empty(n_slots * pool.S, dtype=torch.uint8, device=dev)
+        self.cache = ft.Cache(L, E, pool.n_phys, n_slots, n_slots, pool.S, pool.ptr, self.sp)
         self.n_waves = self.cache.n_waves()
-        self.hist = torch.zeros(n_steps, L, self.n_waves, 4, dtype=torch.int32, device=dev)  # per wave
-        self.routers = routers
-        if e2e:
-            self.x_host = torch.empty(n_steps, T, cfg.hidden, dtype=torch.bfloat16).pin_memory()
-            self.x_host.copy_(self.xs.cpu())
-            self.x_dev = torch.empty(T, cfg.hidden, dtype=torch.bfloat16, device=dev)
-            self.outs = torch.empty(L, T, cfg.hidden, dtype=torch.float32, device=dev)
-            self.out_host = torch.empty(L, T, cfg.hidden, dtype=torch.float32).pin_memory()
+        self.fs = torch.cuda.Stream(device=dev)
+        self.b = {}
+        for T in self.batches:
+            tr = synth.AR1Trace(cfg, T, dev, tag=T)
+            d = {"layer": ft.MoELayer(cfg, T, dev),
+                 "split": split_min >= 0 and ft.split_pays(T, cfg.top_k, cfg.wtype, split_min),
+                 "xs": torch.stack([tr.next() for _ in range(n_steps)]),                 # [steps, T, H] resident
+                 "hist": torch.zeros(n_steps, L, self.n_waves, 4, dtype=torch.int32, device=dev),
+                 "outs": torch.empty(L, T, H, dtype=torch.float32, device=dev)}
+            if e2e:
+                d["x_host"] = torch.empty(n_steps, T, H, dtype=d["xs"].dtype).pin_memory()
+                d["x_host"].copy_(d["xs"].cpu())
+                d["out_host"] = torch.empty(L, T, H, dtype=torch.float32).pin_memory()
+            self.b[T] = d
+        self.graphs = {}
 
-    def reset_cache(self):
-        """A new, empty cache on the same slot pool (the state the trace started from)."""
-        cfg, pool = self.cfg, self.pool
-        self.cache.destroy()
-        self.cache = self.ft.Cache(cfg.n_layers, cfg.n_experts, pool.n_phys, self.n_slots, self.n_slots, pool.S,
-                                   pool.ptr, self.sp)
-        self.hist.zero_()
-
-    def counts(self, t0, t1) -> np.ndarray:
-        """Per layer step {experts, hits, fills, externals} of steps t0..t1-1 (summed over waves)."""
-        return self.hist[t0:t1].sum(dim=2).cpu().numpy()
-
-    def launches_per_step(self) -> int:
+    def launches_per_step(self, T) -> int:
         # router_logits, route, permute, (control, fill, expert kernels) per wave, combine;
         # bf16 experts run gather + gate/up + down on the tensor cores, other formats gate/up + down
         # (the split form evaluates hits and filled experts in two expert calls)
         n_exp = 3 if self.cfg.wtype == synth.W_BF16 else 2
-        if self.fill_stream is not None:
+        if self.b[T]["split"]:
             n_exp *= 2
         return self.cfg.n_layers * (3 + (2 + n_exp) * self.n_waves + 1)
 
-    def capture(self, t, e2e=False, timed=True):
-        """One CUDA graph of decode step t (all layers).
+    def launches_per_pass(self) -> int:
+        return sum(self.n_steps * self.launches_per_step(T) for T in self.batches)
 
-        With ``timed`` the graph also records timing events (event-record nodes);
-        the returned EventLog owns them and must outlive every replay of the graph."""
-        g = torch.cuda.CUDAGraph()
-        ev = EventLog(external=True) if timed else None
-        with torch.cuda.graph(g):
-            self.step(t, ev, e2e)
-        return g, ev
-
-    def step(self, t, ev=None, e2e=False):
-        """One decode step of every layer.  With ``e2e`` the input is read from the device
-        staging buffer ``x_dev`` and every layer's output is kept in ``outs`` for the host."""
-        lay, cache, L = self.layer, self.cache, self.cfg.n_layers
-        x = self.x_dev if e2e else self.xs[t]
-        for l in range(L):
-            wr, b = self.routers[l]
-            lay.route(x, wr, b)
+    def step(self, T, t, ev=None):
+        """Decode step t of batch size T through every layer (eager, or recorded under capture)."""
+        ft, cfg, d = self.ft, self.cfg, self.b[T]
+        lay, cache, x = d["layer"], self.cache, d["xs"][t]
+        fs = self.fs if d["split"] else None
+        k, S, N = cfg.top_k, self.S, self.n_slots
+        for l in range(cfg.n_layers):
+            lay.route(x, *self.routers[l])
             for w in range(self.n_waves):
+                sc = d["hist"][t, l, w]
                 if ev is not None:
                     ev.rec("cache")
-                if self.fill_stream is None:
-                    cache.step(l, lay.counts, 1.0, w, lay.slot_of, lay.ext, self.hist[t, l, w])
+                if fs is None:
+                    cache.step(l, lay.counts, 1.0, w, lay.slot_of, lay.ext, sc)
                     if ev is not None:
                         ev.rec("fill_end")
-                    lay.experts(x, lay.slot_of, self.sp, self.S, self.n_slots)
+                    lay.experts(x, lay.slot_of, self.sp, S, N)
                     if ev is not None:
                         ev.rec("expert_end")
                     continue
-                fs = self.fill_stream
-                cache.step_split(l, lay.counts, 1.0, w, lay.slot_of, lay.slot_fill, lay.ext, self.hist[t, l, w],
-                                 fill_stream=fs)
+                cache.step_split(l, lay.counts, 1.0, w, lay.slot_of, lay.slot_fill, lay.ext, sc, fill_stream=fs)
                 if ev is not None:
                     ev.rec("ctrl_end")
                     ev.rec("fill_end", fs)
-                lay.experts(x, lay.slot_of, self.sp, self.S, self.n_slots)          # hits, during the fill
+                lay.experts(x, lay.slot_of, self.sp, S, N)          # hits, during the fill
                 if ev is not None:
                     ev.rec("hit_end")
                 cache.fill_join()
                 if ev is not None:
-                    torch.cuda.current_stream().wait_stream(fs)                    # joins the timing event too
+                    torch.cuda.current_stream().wait_stream(fs)     # joins the timing event too
                     ev.rec("join")
-                lay.experts(x, lay.slot_fill, self.sp, self.S, self.n_slots)        # the filled experts
+                lay.experts(x, lay.slot_fill, self.sp, S, N)        # the filled experts
                 if ev is not None:
                     ev.rec("expert_end")
-            out = lay.combine(self.T, lay.ext, None)
-            if e2e:
-                self.outs[l].copy_(out, non_blocking=True)
+            ft.ft_combine(lay.y[: T * k], lay.inv, lay.idx[:T], lay.w[:T], lay.ext, None, cfg.n_experts,
+                          d["outs"][l])
 
-    def e2e_step(self, t, graph=None):
-        """Host input -> device, the step (graph replay or eager), every layer's output -> host."""
-        self.x_dev.copy_(self.x_host[t], non_blocking=True)
-        if graph is not None:
-            graph.replay()
-        else:
-            self.step(t, None, e2e=True)
-        self.out_host.copy_(self.outs, non_blocking=True)
+    def capture(self, timed=True):
+        """One eager step per batch size (kernel attributes and modules set up outside capture),
+        a cold reset, then one graph per (T, step).  With ``timed`` every graph also records
+        its timing events (event-record nodes), kept in its EventLog."""
+        for T in self.batches:
+            self.step(T, 0)
+        torch.cuda.synchronize()
+        self.cache.reset()
+        for T in self.batches:
+            for t in range(self.n_steps):
+                g = torch.cuda.CUDAGraph()
+                ev = EventLog(external=True) if timed else None
+                with torch.cuda.graph(g):
+                    self.step(T, t, ev)
+                self.graphs[(T, t)] = (g, ev)
+        torch.cuda.synchronize()
+
+    def run_pass(self, marks=None, e2e=False):
+        """The whole trace once: per batch size, a cold reset and every step's graph.
+
+        ``marks`` (a list) receives (T, t, event) before each step and (T, -1,
+        event) after each batch size's last step.  With ``e2e`` each step's input is first copied from
+        pinned host memory and every layer's output copied back to it."""
+        for T in self.batches:
+            d = self.b[T]
+            self.cache.reset()                      # cold start (synchronises)
+            for t in range(self.n_steps):
+                if e2e:
+                    d["xs"][t].copy_(d["x_host"][t], non_blocking=True)
+                if marks is not None:
+                    e = torch.cuda.Event(enable_timing=True)
+                    e.record()
+                    marks.append((T, t, e))
+                self.graphs[(T, t)][0].replay()
+                if e2e:
+                    d["out_host"].copy_(d["outs"], non_blocking=True)
+            if marks is not None:
+                e = torch.cuda.Event(enable_timing=True)
+                e.record()
+                marks.append((T, -1, e))
+
+    def hist(self, T) -> np.ndarray:
+        """Per (step, layer, wave) {experts, hits, fills, externals} of the last pass."""
+        return self.b[T]["hist"].cpu().numpy()
+
+    def logs(self, T, t0=0):
+        return [self.graphs[(T, t)][1] for t in range(t0, self.n_steps)]
+
+    def release(self):
+        self.graphs.clear()
+        torch.cuda.synchronize()
+        self.cache.destroy()
+
+
+def step_times_ms(marks):
+    """{T: [ms of each step]} from the events recorded before each step and after each T's last."""
+    out = {}
+    for i in range(len(marks) - 1):
+        T, t, e = marks[i]
+        if t >= 0:
+            out.setdefault(T, []).append(e.elapsed_time(marks[i + 1][2]))
+    return out
 
 
 class EventLog:
@@ -463,6 +513,13 @@ def prefill_leg(ft, cfg, pool, routers0, dev, prompts, link_gbs, peaks, chunk=81
     res["expert_call_ms"] = ms_exp
     res["expert_tflops"] = flops / (ms_exp * 1e-3) / 1e12
     res["expert_tensor_frac_of_bf16"] = res["expert_tflops"] / peaks["bf16_tflops"]
+    if cfg.wtype in (synth.W_NVFP4, synth.W_MXFP4):
+        # the peak of the weights' own dtype: FP4 dense = bf16 measured x the nominal ratio 13.5 / 2.25
+        fp4 = peaks["bf16_tflops"] * FP4_OVER_BF16
+        res["expert_tensor_frac_of_fp4"] = res["expert_tflops"] / fp4
+        res["fp4_peak_tflops"] = fp4
+        res["fp4_peak_source"] = (f"bf16 measured burst x {FP4_OVER_BF16:g} (nominal dense FP4 / bf16); the "
+                                  "products run as kind::f16 MMAs on weights expanded exactly to bf16")
     res["expert_roofline_frac"] = roof_s / (ms_exp * 1e-3)
     res["expert_roofline_note"] = ("per product max(FLOPs / bf16 peak, bytes / HBM peak): gate/up and down are "
                                    "both near the ridge (about 256 rows per expert); down writes fp32 output")
@@ -475,37 +532,74 @@ def prefill_leg(ft, cfg, pool, routers0, dev, prompts, link_gbs, peaks, chunk=81
 
 # ---------------------------------------------------------------- secondary workloads
 
-def decode_trace_leg(ft, cfg, T, pool, routers, n_slots, steps, warmup, dev, peaks, link, payload, split_min=0):
-    """One batch size on its own cache: eager warm-up, then ``steps`` graph-replayed decode steps."""
-    tr = DecodeTrace(ft, cfg, T, pool, routers, warmup + steps, dev, False, n_slots=n_slots, split_min=split_min)
-    for t in range(warmup):
-        tr.step(t)
-    graphs = [tr.capture(warmup + k) for k in range(steps)]
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for g, _ in graphs:
-        g.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    h = tr.counts(warmup, warmup + steps)
-    roof, _ = layer_roofline_seconds(h, T, cfg, payload, peaks, link)
-    cache_ms = sum(v for _, ev in graphs for v in ev.cache_expert_spans()[0])
-    expert_ms = sum(v for _, ev in graphs for v in ev.cache_expert_spans()[1])
-    out = {"tokens_per_s": T * steps / (ms * 1e-3), "ms_per_step": ms / steps,
-           "layer_roofline_frac": roof / (ms * 1e-3), "hit_rate": float(h[..., 1].sum() / max(h[..., 0].sum(), 1)),
-           "fill_gbs": float(h[..., 2].sum()) * payload / max(cache_ms * 1e-3, 1e-12) / 1e9,
-           "expert_weight_gbs": float(h[..., 0].sum()) * payload / max(expert_ms * 1e-3, 1e-12) / 1e9}
-    del graphs
-    tr.cache.destroy()
-    del tr
-    torch.cuda.empty_cache()
-    return out
+def decode_report(run, marks, cfg, peaks, link, payload, steady_from):
+    """Per batch size and overall: tokens/s over the whole trace (cold start included) and
+    from step ``steady_from`` on, the layer-roofline fractions, hit rates, and the fill and
+    expert spans of the captured steps (CUDA events on the launching streams, last pass)."""
+    st = step_times_ms(marks)
+    per = {}
+    acc = {"ms": 0.0, "tok": 0, "roof": 0.0, "ms_s": 0.0, "tok_s": 0, "roof_s": 0.0}
+    cache_ms, expert_ms, fills, unique = [], [], 0, 0
+    for T in run.batches:
+        h = run.hist(T).sum(axis=2)                     # [steps, L, 4], summed over waves
+        ms = np.asarray(st[T], dtype=np.float64)
+        n = len(ms)
+        sf = min(steady_from, n - 1)
+        r_all, _ = layer_roofline_seconds(h, T, cfg, payload, peaks, link)
+        r_st, _ = layer_roofline_seconds(h[sf:], T, cfg, payload, peaks, link)
+        logs = run.logs(T)
+        for ev in logs:
+            c, e = ev.cache_expert_spans()
+            cache_ms += c
+            expert_ms += e
+        fills += int(h[..., 2].sum())
+        unique += int(h[..., 0].sum())
+        per[str(T)] = {
+            "tokens_per_s": T * n / (ms.sum() * 1e-3), "ms_per_step": float(ms.mean()),
+            "first_step_ms": float(ms[0]), "layer_roofline_frac": r_all / (ms.sum() * 1e-3),
+            "hit_rate": float(h[..., 1].sum() / max(h[..., 0].sum(), 1)),
+            "steady_tokens_per_s": T * (n - sf) / (ms[sf:].sum() * 1e-3),
+            "steady_layer_roofline_frac": r_st / (ms[sf:].sum() * 1e-3),
+            "steady_hit_rate": float(h[sf:, :, 1].sum() / max(h[sf:, :, 0].sum(), 1)),
+            "us_per_wave": spans_us(logs)}
+        acc["ms"] += ms.sum()
+        acc["tok"] += T * n
+        acc["roof"] += r_all
+        acc["ms_s"] += ms[sf:].sum()
+        acc["tok_s"] += T * (n - sf)
+        acc["roof_s"] += r_st
+    n_ls = len(cache_ms)
+    fill_bytes = fills * payload
+    cache_s, expert_s = sum(cache_ms) * 1e-3, sum(expert_ms) * 1e-3
+    expert_hbm = unique * payload
+    scaled = ("scaled, not measured in this run: DRAM bytes per algorithmic byte from one ncu capture of the "
+              "same kernel (profiles/)")
+    roof_fill = {"kernel": "ft_cache_step (control + fill launches)", "bound": "link",
+                 "achieved": fill_bytes / cache_s / 1e9, "peak": link, "unit": "GB/s",
+                 "frac": fill_bytes / cache_s / 1e9 / link,
+                 "traffic": TRAFFIC_PER_BYTE["fill"] * fill_bytes / max(n_ls, 1), "traffic_source": scaled,
+                 "algorithmic_bytes_per_launch": fill_bytes / max(n_ls, 1),
+                 "avg_launch_ms": sum(cache_ms) / max(n_ls, 1),
+                 "peak_source": "cudaMemcpyAsync pinned->device, measured in this run"}
+    roof_exp = {"kernel": "ft_expert_grouped (tcgen05 expert launches)", "bound": "hbm",
+                "achieved": expert_hbm / expert_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": expert_hbm / expert_s / 1e9 / peaks["hbm_gbs"],
+                "traffic": TRAFFIC_PER_BYTE["experts"] * expert_hbm / max(n_ls, 1), "traffic_source": scaled,
+                "algorithmic_bytes_per_launch": expert_hbm / max(n_ls, 1),
+                "avg_launch_ms": sum(expert_ms) / max(n_ls, 1),
+                "peak_source": f"MEASURED_PEAKS hbm_gbs ({peaks['source']}, of measured)"}
+    return {"per_batch": per,
+            "layer_roofline_frac": acc["roof"] / (acc["ms"] * 1e-3),
+            "steady_state": {"from_step": steady_from, "tokens_per_s": acc["tok_s"] / (acc["ms_s"] * 1e-3),
+                             "layer_roofline_frac": acc["roof_s"] / (acc["ms_s"] * 1e-3)},
+            "trace_tokens_per_s": acc["tok"] / (acc["ms"] * 1e-3),
+            "roofline": roof_fill if cache_s >= expert_s else roof_exp,
+            "roofline_fill": roof_fill, "roofline_experts": roof_exp}
 
 
-def nvfp4_leg(ft, dev, peaks, link, batches, steps, warmup, split_min=0):
-    """The 43-layer NVFP4 stack: decode at 40% cache per batch size, and 8192-token streamed prefill.
+def nvfp4_leg(ft, dev, peaks, link, batches, steps, split_min=0):
+    """The 43-layer NVFP4 stack: ``steps`` decode steps per batch size from a cold 40% cache,
+    and 8192-token streamed prefill.
 
     The host pool stores a cyclic window of 4 physical layers (logical layer l
     reads physical l mod 4); cache keys and bytes moved stay logical."""
@@ -515,15 +609,22 @@ def nvfp4_leg(ft, dev, peaks, link, batches, steps, warmup, split_min=0):
     payload = int(ft.ft_expert_layout_get(cfg.wtype, cfg.hidden, cfg.inter).payload_bytes)
     routers = [synth.router_weights(cfg, l, dev) for l in range(cfg.n_layers)]
     n_slots = int(round(CACHE_FRAC * cfg.n_layers * cfg.n_experts))
+    run = DecodeRun(ft, cfg, pool, routers, batches, steps, dev, n_slots, split_min)
+    run.capture()
+    marks = []
+    run.run_pass(marks)
+    torch.cuda.synchronize()
+    rep = decode_report(run, marks, cfg, peaks, link, payload, steady_from=min(8, steps - 1))
+    run.release()
+    del run
+    torch.cuda.empty_cache()
     res = {"workload": "nvfp4_43L: H=4096 E=256 top-6 I=2048, NVFP4 weights, 43 layers over a 4-layer host window",
-           "cache_slots": n_slots, "decode": {}}
-    for T in batches:
-        log(f"nvfp4 decode T={T}")
-        res["decode"][str(T)] = decode_trace_leg(ft, cfg, T, pool, routers, n_slots, steps, warmup, dev, peaks, link,
-                                                 payload, split_min)
+           "cache_slots": n_slots, "decode_steps": steps,
+           "decode": {"from_cold": rep["per_batch"], "layer_roofline_frac": rep["layer_roofline_frac"],
+                      "steady_state": rep["steady_state"], "roofline_experts": rep["roofline_experts"],
+                      "roofline_fill": rep["roofline_fill"]}}
     log("nvfp4 prefill")
-    pf = prefill_leg(ft, cfg, pool, routers, dev, [8192], link, peaks)
-    res["prefill_8192"] = pf
+    res["prefill_8192"] = prefill_leg(ft, cfg, pool, routers, dev, [8192], link, peaks)
     pool.free()
     return res
 
@@ -647,40 +748,109 @@ def mxfp4_mixed_leg(ft, dev, peaks, link, decode_steps=512, cycles=4, split_min=
 
 # ---------------------------------------------------------------- CPU oracle baseline
 
-def oracle_sample(cfg, pool_phys, routers_cpu, x_tokens, layers, dev):
-    """Prefetch (untimed) the stored components the oracle needs for x_tokens through ``layers``."""
+def _oracle_items(cfg, items):
+    """Untimed preparation of (token, layer) samples: the token's hidden state, the
+    layer's router, and the stored components of the experts it routes to."""
     from oracle import formats, moe
-    comps = {}
-    for l in layers:
-        wr, b = routers_cpu[l]
-        z = moe.router_logits(formats.to_f64(x_tokens), formats.to_f64(wr), formats.to_f64(b))
+    trace = synth.AR1Trace(cfg, 1, "cpu", tag=1)
+    n_tok = 1 + max(t for t, _ in items)
+    xs = [trace.next().clone() for _ in range(n_tok)]
+    routers, out = {}, []
+    for t, l in items:
+        if l not in routers:
+            routers[l] = synth.router_weights(cfg, l, "cpu")
+        wr, b = routers[l]
+        z = moe.router_logits(formats.to_f64(xs[t]), formats.to_f64(wr), formats.to_f64(b))
         idx, _ = moe.route(z, cfg.top_k)
-        for e in sorted(set(idx.reshape(-1).tolist())):
-            c = synth.expert_weights(cfg, l % pool_phys, e, dev)
-            comps[(l, e)] = {m: {kk: (v.cpu() if torch.is_tensor(v) else v) for kk, v in c[m].items()}
-                             for m in ("gate", "up", "down")}
-    return comps
+        comps = {int(e): synth.expert_weights(cfg, l, int(e), "cpu") for e in sorted(set(idx.reshape(-1).tolist()))}
+        out.append((xs[t], wr, b, comps))
+    return out
 
 
-def oracle_run(cfg, comps, routers_cpu, x_tokens, layers):
-    """The oracle on the sample: routing, decoding the stored weights, the expert FFNs and the sum."""
+def _oracle_eval(cfg, prepared):
+    """The oracle on prepared samples: routing, decoding the stored weights, the expert FFNs and the sum."""
     from oracle import formats, moe
-    x = formats.to_f64(x_tokens)
-    for l in layers:
-        wr, b = routers_cpu[l]
-        z = moe.router_logits(x, formats.to_f64(wr), formats.to_f64(b))
+    for x, wr, b, comps in prepared:
+        x64 = formats.to_f64(x)
+        z = moe.router_logits(x64, formats.to_f64(wr), formats.to_f64(b))
         idx, w = moe.route(z, cfg.top_k)
-        src = moe.ExpertSource(lambda e, l=l: comps[(l, e)], cfg.wtype)
-        moe.moe_layer(x, idx, w, src)
+        moe.moe_layer(x64, idx, w, moe.ExpertSource(lambda e: comps[e], cfg.wtype))
 
 
-def blas_threads() -> int:
+def _oracle_worker(rank, n_workers, cfg_name, items, barrier, more):
+    """One process of the CPU baseline: one BLAS thread, its share of the samples,
+    prepared before the first barrier, then evaluated once per round."""
+    from threadpoolctl import threadpool_limits
+    threadpool_limits(1)
+    torch.set_num_threads(1)
+    cfg = synth.CONFIGS[cfg_name]
+    mine = items[rank::n_workers]
+    prepared = _oracle_items(cfg, mine) if mine else []
+    barrier.wait()
+    while True:
+        barrier.wait()                  # go
+        if not more.value:
+            return
+        _oracle_eval(cfg, prepared)
+        barrier.wait()                  # done
+
+
+class OraclePool:
+    """The fp64 oracle on the host cores: one spawned process per core (at most
+    ``max_workers``), each with one BLAS thread, evaluating its share of
+    (token, layer) samples once per round.  Rounds are timed on the wall clock."""
+
+    def __init__(self, cfg, n_tokens, max_workers=32):
+        import multiprocessing as mp
+        self.cfg = cfg
+        self.cores = max(1, min(len(os.sched_getaffinity(0)), max_workers))
+        self.items = [(t, l) for t in range(n_tokens) for l in range(cfg.n_layers)]
+        self.n_tokens = n_tokens
+        ctx = mp.get_context("spawn")
+        n = min(self.cores, len(self.items))
+        self.n = n
+        self.barrier = ctx.Barrier(n + 1)
+        self.more = ctx.Value("i", 1)
+        self.procs = [ctx.Process(target=_oracle_worker, args=(r, n, cfg.name, self.items, self.barrier, self.more),
+                                  daemon=True) for r in range(n)]
+        for p in self.procs:
+            p.start()
+        self.barrier.wait(timeout=900)  # every worker prepared its samples
+
+    def round(self) -> float:
+        """Evaluates every sample once; wall seconds."""
+        t0 = time.perf_counter()
+        self.barrier.wait(timeout=900)
+        self.barrier.wait(timeout=900)
+        return time.perf_counter() - t0
+
+    def close(self):
+        self.more.value = 0
+        try:
+            self.barrier.wait(timeout=60)
+        except Exception:
+            pass
+        for p in self.procs:
+            p.join(timeout=30)
+
+    def sample(self) -> str:
+        return (f"{self.n_tokens} T=1 decode token(s) of the AR(1) trace through all {self.cfg.n_layers} layers "
+                f"({len(self.items)} (token, layer) samples, weights drawn on the CPU with the same generator and "
+                f"decoded from the stored format inside the timed region), over {self.n} processes")
+
+
+def oracle_baseline(cfg, n_tokens=2, reps=None, budget_s=12.0):
+    """cpu_baseline: rounds of the oracle pool until about ``budget_s`` seconds of wall time."""
+    op = OraclePool(cfg, n_tokens)
     try:
-        from threadpoolctl import threadpool_info
-        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
-        return max(n) if n else 1
-    except Exception:
-        return 1
+        t = [op.round()]
+        n = reps or max(1, int(budget_s / max(t[0], 1e-3)))
+        t = [op.round() for _ in range(n)]
+    finally:
+        op.close()
+    v = n_tokens * len(t) / sum(t)
+    return {"value": v, "unit": "tokens/s", "cores": op.n, "kind": "oracle", "sample": op.sample() +
+            f", {len(t)} timed rounds"}
 
 
 def reference_main(args, world, rank):
@@ -688,30 +858,58 @@ def reference_main(args, world, rank):
     if rank != 0:
         return
     cfg = synth.DECODE_BF16
-    dev = "cuda" if torch.cuda.is_available() else "cpu"
-    layers = list(range(0, cfg.n_layers, 5))            # 8 of the 40 layers per sampled token
-    routers = [tuple(t.cpu() for t in synth.router_weights(cfg, l, dev)) for l in range(cfg.n_layers)]
-    tr = synth.AR1Trace(cfg, 1, dev, tag=1)
-    x = tr.next().cpu()
-    comps = oracle_sample(cfg, cfg.n_layers, routers, x, layers, dev)
-    for _ in range(args.warmup):
-        oracle_run(cfg, comps, routers, x, layers)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle_run(cfg, comps, routers, x, layers)
-    dt = time.perf_counter() - t0
-    frac = len(layers) / cfg.n_layers
-    v = args.steps * frac / dt
-    cores = blas_threads()
-    sample = f"one T=1 decode token through {len(layers)} of the 40 layers per step, scaled to 40 layers"
+    op = OraclePool(cfg, args.cpu_tokens)
+    try:
+        for _ in range(args.warmup):
+            op.round()
+        t = [op.round() for _ in range(args.steps)]
+    finally:
+        op.close()
+    dt = sum(t)
+    v = args.cpu_tokens * args.steps / dt
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "batches": list(BATCHES), "parallelism": "replicas1"},
-        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "config": {"workload": WORKLOAD, "batches": [1], "parallelism": "replicas1",
+                   "step": f"{args.cpu_tokens} T=1 decode token(s) through all {cfg.n_layers} layers"},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": op.n, "kind": "oracle", "sample": op.sample()},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
+
+
+def pool_setup_leg(ft, cfg, pool, n_layers):
+    """Pool setup from a pool file, pin first (ft_host_alloc, then the read) against read
+    then pin (the read into fresh pageable memory, then ft_host_register), for the first
+    ``n_layers`` layers of the pool ([Review] §2.7, fast engine start).  The file is
+    written once beforehand and read back through the page cache."""
+    import shutil
+    E, S = cfg.n_experts, pool.S
+    n = n_layers * E * S
+    d = tempfile.gettempdir()
+    if shutil.disk_usage(d).free < 1.5 * n:
+        return {"skipped": f"not enough free space in {d} for a {n / 1e9:.1f} GB pool file"}
+    path = os.path.join(d, f"ft_pool_{os.getpid()}.bin")
+    try:
+        with open(path, "wb") as f:
+            f.write(memoryview(pool.host[:n].numpy()))
+        runs = {"pin_first": [], "read_then_pin": []}
+        for _ in range(2):
+            for mode in ("pin_first", "read_then_pin"):
+                t0 = time.perf_counter()
+                p = ft.ExpertPool.load(cfg, n_layers, path, read_then_pin=(mode == "read_then_pin"))
+                total = time.perf_counter() - t0
+                ok = bool(torch.equal(p.host[: 1 << 20], pool.host[: 1 << 20]))
+                runs[mode].append(dict(p.setup_s, total=total, same_bytes=ok))
+                p.free()
+        best = {m: min(r, key=lambda x: x["total"]) for m, r in runs.items()}
+        return {"layers": n_layers, "bytes": n, "runs": runs,
+                "gbs": {m: n / b["total"] / 1e9 for m, b in best.items()},
+                "speedup_read_then_pin": best["pin_first"]["total"] / best["read_then_pin"]["total"],
+                "source": "pool file in the page cache (no disk reads); threads: hardware count, at most 64"}
+    finally:
+        if os.path.exists(path):
+            os.unlink(path)
 
 
 # ---------------------------------------------------------------- single expert-kernel cases (profiling)
@@ -925,172 +1123,93 @@ def main():
     t_fill = time.perf_counter() - t_fill
     routers = [synth.router_weights(cfg, l, dev) for l in range(L)]
     link = link_peak_gbs(pool.host, E * S, dev)
-    n_steps = args.warmup + args.steps
-    traces = [DecodeTrace(ft, cfg, T, pool, routers, n_steps, dev, not args.no_e2e, split_min=split_min)
-              for T in batches]
-    tokens_per_step = sum(batches)
-
+    n_trace = args.trace_steps
+    run = DecodeRun(ft, cfg, pool, routers, batches, n_trace, dev, int(round(CACHE_FRAC * L * E)), split_min,
+                    e2e=not args.no_e2e)
+    tokens_per_pass = n_trace * sum(batches)
     log(f"pool of {n_phys} layers filled in {t_fill:.1f} s; link {link:.1f} GB/s")
-    # warm-up (cold caches fill here, as they would in service)
-    for t in range(args.warmup):
-        for tr in traces:
-            tr.step(t)
-    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    run.capture()
+    log(f"{len(run.graphs)} step graphs captured in {time.perf_counter() - t0:.1f} s")
 
-    # each timed step is one CUDA graph per batch size (captured now, replayed once in the timed
-    # region); the graphs hold the same library calls as the eager warm-up steps
-    graphs = {}
-    log("warm-up done")
-    if not args.no_graphs:
-        for k in range(args.steps):
-            for tr in traces:
-                graphs[(tr.T, args.warmup + k)] = tr.capture(args.warmup + k)
-        torch.cuda.synchronize()
+    # warm-up passes (each the whole trace from cold caches); the first two must make
+    # the same cache decisions, since every pass replays the same trace from the same state
+    first = []
+    for w in range(args.warmup):
+        run.run_pass()
+        if w < 2:
+            first.append({T: run.hist(T) for T in batches})
+    deterministic = (all(np.array_equal(first[0][T], first[1][T]) for T in batches) if len(first) == 2 else None)
+    log(f"warm-up done ({args.warmup} passes; identical decisions: {deterministic})")
 
-    log(f"{len(graphs)} step graphs captured")
-    # timed region
-    logs = []
-    logs_T = {}
-    tb = []
+    # timed region: K passes of the whole trace
     barrier(world)
     torch.cuda.synchronize()
     clk = Clocks(local)
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    marks = []
     e_start.record()
     for k in range(args.steps):
-        t = args.warmup + k
-        for tr in traces:
-            e = torch.cuda.Event(enable_timing=True)
-            e.record()
-            tb.append((tr.T, e))
-            if graphs:
-                g, ev = graphs[(tr.T, t)]
-                g.replay()
-            else:
-                ev = EventLog()
-                tr.step(t, ev)
-            logs.append(ev)
-            logs_T.setdefault(tr.T, []).append(ev)
+        marks = []
+        run.run_pass(marks)
     e_end.record()
     torch.cuda.synchronize()
     barrier(world)
     clocks = clk.stop()
     ms = e_start.elapsed_time(e_end)
     ms_max = max_over_ranks(world, ms)
-    tokens = sum_over_ranks(world, tokens_per_step * args.steps)
+    tokens = sum_over_ranks(world, tokens_per_pass * args.steps)
     value = tokens / (ms_max * 1e-3)
+    log(f"timed region: {ms:.1f} ms ({args.steps} passes)")
+    payload = int(lay_bytes.payload_bytes)
+    rep = decode_report(run, marks, cfg, peaks, link, payload, args.steady_from)
 
-    log(f"timed region: {ms:.1f} ms")
-    # per-batch breakdown
-    per_T = {T: 0.0 for T in batches}
-    marks = tb + [(None, e_end)]
-    for i in range(len(tb)):
-        per_T[marks[i][0]] += marks[i][1].elapsed_time(marks[i + 1][1])
-    # kernel spans
-    cache_ms = [v for ev in logs for v in ev.cache_expert_spans()[0]]
-    expert_ms = [v for ev in logs for v in ev.cache_expert_spans()[1]]
-
-    # roofline over the timed layer steps
-    roof_s, roof_detail = 0.0, {"hbm_bytes": 0.0, "link_bytes": 0.0, "flops": 0.0}
-    per_T_roof = {}
-    hit_rate = {}
-    fills_total, unique_total = 0, 0
-    for tr in traces:
-        h = tr.counts(args.warmup, args.warmup + args.steps)
-        s, d = layer_roofline_seconds(h, tr.T, cfg, int(lay_bytes.payload_bytes), peaks, link)
-        per_T_roof[tr.T] = s
-        roof_s += s
-        for kk in ("hbm_bytes", "link_bytes", "flops"):
-            roof_detail[kk] += d[kk]
-        fills_total += int(h[..., 2].sum())
-        unique_total += int(h[..., 0].sum())
-        hit_rate[tr.T] = float(h[..., 1].sum() / max(h[..., 0].sum(), 1))
-    layer_roofline_frac = roof_s / (ms * 1e-3)
-
-    n_ls = len(cache_ms)
-    fill_bytes = fills_total * int(lay_bytes.payload_bytes)
-    cache_total_s = sum(cache_ms) * 1e-3
-    expert_total_s = sum(expert_ms) * 1e-3
-    expert_hbm = unique_total * int(lay_bytes.payload_bytes)
-    roof_fill = {"kernel": "ft_cache_step (control + fill launches)", "bound": "link",
-                 "achieved": fill_bytes / cache_total_s / 1e9, "peak": link, "unit": "GB/s",
-                 "frac": fill_bytes / cache_total_s / 1e9 / link,
-                 "traffic": TRAFFIC_PER_BYTE["fill"] * fill_bytes / max(n_ls, 1),
-                 "algorithmic_bytes_per_launch": fill_bytes / max(n_ls, 1),
-                 "avg_launch_ms": sum(cache_ms) / max(n_ls, 1),
-                 "peak_source": "cudaMemcpyAsync pinned->device, measured in this run"}
-    roof_exp = {"kernel": "ft_expert_grouped (row gather + tcgen05 gate/up + down launches)", "bound": "hbm",
-                "achieved": expert_hbm / expert_total_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": expert_hbm / expert_total_s / 1e9 / peaks["hbm_gbs"],
-                "traffic": TRAFFIC_PER_BYTE["experts"] * expert_hbm / max(n_ls, 1),
-                "algorithmic_bytes_per_launch": expert_hbm / max(n_ls, 1),
-                "avg_launch_ms": sum(expert_ms) / max(n_ls, 1),
-                "peak_source": f"MEASURED_PEAKS hbm_gbs ({peaks['source']})"}
-    dominant = roof_fill if cache_total_s >= expert_total_s else roof_exp
-
-    # end to end through the public API with host buffers: every step copies its
-    # inputs from pinned host memory, runs (as a graph of device work only), and
-    # copies every layer's output back to pinned host memory
-    # (fresh caches, the same warm-up and the same trace steps as the device-resident run)
+    # end to end through the public API with host buffers: every step copies its input
+    # from pinned host memory and every layer's output back to pinned host memory
     e2e = None
     if not args.no_e2e:
-        del graphs, logs
-        for tr in traces:
-            tr.reset_cache()
-        for t in range(args.warmup):
-            for tr in traces:
-                tr.step(t)
-        # (the same timing events as the device-resident graphs, so both carry the same instrumentation)
-        egraphs, elogs = {}, []
-        if not args.no_graphs:
-            for k in range(args.steps):
-                for tr in traces:
-                    g, lg = tr.capture(args.warmup + k, e2e=True, timed=True)
-                    egraphs[(tr.T, k)] = g
-                    elogs.append(lg)
-        torch.cuda.synchronize()
-        log(f"{len(egraphs)} end-to-end step graphs captured")
+        n_e2e = max(1, min(args.steps, 2))
         barrier(world)
+        torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for k in range(args.steps):
-            t = args.warmup + k
-            for tr in traces:
-                tr.e2e_step(t, egraphs.get((tr.T, k)))
+        for _ in range(n_e2e):
+            run.run_pass(e2e=True)
         e1.record()
         torch.cuda.synchronize()
         barrier(world)
         ms_e = max_over_ranks(world, e0.elapsed_time(e1))
-        h2d = sum(T * cfg.hidden * 2 for T in batches)
-        d2h = sum(L * T * cfg.hidden * 4 for T in batches)
-        e2e = {"value": tokens / (ms_e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        h2d = n_trace * sum(T * cfg.hidden * 2 for T in batches)
+        d2h = n_trace * sum(L * T * cfg.hidden * 4 for T in batches)
+        e2e = {"value": sum_over_ranks(world, tokens_per_pass * n_e2e) / (ms_e * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "note": "same graphs; each decode step's input copied from pinned host memory first and "
+                       "every layer's output copied back after it"}
+        log(f"end-to-end: {e2e['value']:.1f} tokens/s over {n_e2e} passes")
 
-    # the graphs reference the traces' buffers: release them before the traces go
-    if args.no_e2e:
-        del graphs, logs
-    else:
-        del egraphs, elogs
-    torch.cuda.synchronize()
+    launches = run.launches_per_pass() * args.steps
+    run.release()
+    del run
+    torch.cuda.empty_cache()
     log("decode legs done")
     derr = ft.ft_get_device_error()
-    stats = {T: tr.cache.stats() for T, tr in zip(batches, traces)}
-    launches = sum(tr.launches_per_step() for tr in traces) * args.steps
 
     prefill = None
     if not args.no_prefill:
-        for tr in traces:
-            tr.cache.destroy()
-        del tr, traces
-        torch.cuda.empty_cache()
         log("prefill leg")
         prefill = prefill_leg(ft, cfg, pool, routers, dev, [int(p) for p in args.prompts.split(",")], link, peaks)
+
+    setup = None
+    if not args.no_pool_setup and rank == 0:
+        log("pool setup: pin first vs read then pin")
+        setup = pool_setup_leg(ft, cfg, pool, args.setup_layers)
 
     nvfp4 = mixed = None
     if not args.no_fp4 and world == 1:
         pool.free()
         torch.cuda.empty_cache()
         log("nvfp4 stack")
-        nvfp4 = nvfp4_leg(ft, dev, peaks, link, batches, args.fp4_steps, args.warmup, split_min)
+        nvfp4 = nvfp4_leg(ft, dev, peaks, link, batches, args.fp4_steps, split_min)
         log("mxfp4 mixed trace")
         mixed = mxfp4_mixed_leg(ft, dev, peaks, link, decode_steps=args.mixed_decode_steps,
                                 split_min=split_min)
@@ -1098,15 +1217,7 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         log("cpu baseline")
-        layers = list(range(cfg.n_layers))
-        rcpu = [tuple(t.cpu() for t in r) for r in routers]
-        x1 = synth.AR1Trace(cfg, 1, dev, tag=1).next().cpu()
-        comps = oracle_sample(cfg, n_phys, rcpu, x1, layers, dev)
-        t0 = time.perf_counter()
-        oracle_run(cfg, comps, rcpu, x1, layers)
-        dt = time.perf_counter() - t0
-        cpu = {"value": 1.0 / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-               "sample": "one T=1 decode token through all 40 layers (weights decoded from the stored bf16)"}
+        cpu = oracle_baseline(cfg, n_tokens=args.cpu_tokens, reps=None, budget_s=args.cpu_budget_s)
 
     if rank == 0:
         line = {
@@ -1114,32 +1225,35 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": WORKLOAD,
-                       "batches": batches, "tokens_per_step": tokens_per_step, "host_pool_layers": n_phys,
-                       "host_pool_gb": pool.n_phys * E * S / 1e9, "weights": "bf16", "accumulate": "f32",
-                       "l2": "inputs larger than L2 (each step reads >= 2 GB of expert weights)",
+                       "step": (f"one pass of the decode trace: {n_trace} decode steps of all {L} layers at each "
+                                f"T in {tuple(batches)}, each T from a cold (empty) cache"),
+                       "batches": batches, "trace_steps": n_trace, "tokens_per_step": tokens_per_pass,
+                       "steady_from_step": args.steady_from,
+                       "host_pool_layers": n_phys, "host_pool_gb": n_phys * E * S / 1e9, "weights": "bf16",
+                       "accumulate": "f32",
+                       "l2": "inputs larger than L2 (each decode step reads >= 50 MB of expert weights, "
+                             "each pass >= 2 GB per T)",
                        "fill": ("ft_cache_step (fill, then all experts)" if args.no_split_fill else
                                 f"{split_min or ft.SPLIT_MIN_ASSIGNMENTS[cfg.wtype]} <= T*k < "
                                 f"{ft.FT_TC_WIDE_ASSIGNMENTS}: ft_cache_step_split (hits evaluated while the fill "
                                 "copies on a second stream); other batches: ft_cache_step"),
                        "parallelism": f"replicas{world}"},
-            "layer_roofline_frac": layer_roofline_frac,
-            "per_batch": {str(T): {"tokens_per_s": T * args.steps / (per_T[T] * 1e-3),
-                                   "ms_per_step": per_T[T] / args.steps,
-                                   "layer_roofline_frac": per_T_roof[T] / (per_T[T] * 1e-3),
-                                   "hit_rate": hit_rate[T],
-                                   "us_per_wave": spans_us(logs_T[T])}
-                          for T in batches},
-            "roofline": dominant,
-            "roofline_experts": roof_exp,
-            "roofline_fill": roof_fill,
+            "layer_roofline_frac": rep["layer_roofline_frac"],
+            "steady_state": rep["steady_state"],
+            "per_batch": rep["per_batch"],
+            "deterministic_passes": deterministic,
+            "roofline": rep["roofline"],
+            "roofline_experts": rep["roofline_experts"],
+            "roofline_fill": rep["roofline_fill"],
             "link_peak_gbs": link,
             "peaks": peaks,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,
-            "cuda_graphs": not args.no_graphs,
+            "cuda_graphs": True,
             "clocks": clocks,
             "prefill_bf16": prefill,
+            "pool_setup": setup,
             "nvfp4_43L": nvfp4,
             "mxfp4_mixed": mixed,
             "device_error": derr,

@@ -38,7 +38,7 @@ EXPORTED = [
     "ft_stream_layer", "ft_stream_layer_done", "ft_stream_bytes", "ft_stream_destroy", "ft_qsplit",
     "ft_expert_grouped_noalloc", "ft_debug_bounded_wait", "ft_cache_step_split", "ft_cache_fill_join",
     "ft_cache_set_fill_blocks", "ft_debug_inject_failure", "ft_debug_live_resources", "ft_pool_read",
-    "ft_host_register", "ft_host_unregister",
+    "ft_host_register", "ft_host_unregister", "ft_cache_reset",
 ]
 FT_NOALLOC_MAX_ELEMS = 1 << 20
 FT_TC_WIDE_ASSIGNMENTS = 2048
@@ -90,6 +90,7 @@ _sigs = {
     "ft_cache_fill_join": (_I, [_P, _P]),
     "ft_cache_set_fill_blocks": (_I, [_P, _I]),
     "ft_cache_resize": (_I, [_P, _I]),
+    "ft_cache_reset": (_I, [_P]),
     "ft_cache_stats": (_I, [_P, ctypes.POINTER(CacheStats)]),
     "ft_cache_export": (_I, [_P, _P, _P, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_uint32)]),
     "ft_expert_grouped_workspace": (ctypes.c_size_t, [_I, _I, _I, _I]),
@@ -370,6 +371,10 @@ class Cache:
 
     def resize(self, n_slots):
         _check("ft_cache_resize", _lib.ft_cache_resize(self.h, n_slots))
+
+    def reset(self):
+        """Cold restart: every slot empty, clock and counters zero (graphs over the handle stay valid)."""
+        _check("ft_cache_reset", _lib.ft_cache_reset(self.h))
 
     def stats(self) -> CacheStats:
         s = CacheStats()

@@ -716,6 +716,21 @@ FT_API int ft_cache_resize(ft_cache* c, int n_slots) {
   return cache_resize_impl(c, n_slots);
 }
 
+FT_API int ft_cache_reset(ft_cache* c) {
+  FT_REQUIRE(c);
+  if (c->streaming || c->pending_join) return FT_ESTATE;
+  FT_CHECK_CUDA(cudaDeviceSynchronize());
+  HostTables t;
+  t.key.assign(c->N, -1);
+  t.stamp.assign(c->N, 0);
+  t.clock = 0;
+  if (int s = upload_tables(c, t)) return s;
+  FT_CHECK_CUDA(cudaMemset(c->stats, 0, 5 * 8));
+  FT_CHECK_CUDA(cudaMemset(c->n_fill, 0, 4));
+  FT_CHECK_CUDA(cudaDeviceSynchronize());
+  return FT_OK;
+}
+
 FT_API int ft_cache_stats(ft_cache* c, ft_cache_stats_t* out) {
   FT_REQUIRE(c && out);
   unsigned long long v[5];

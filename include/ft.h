@@ -319,7 +319,15 @@ int ft_cache_set_fill_blocks(ft_cache* c, int blocks);
  * holds the pool's buffers. */
 int ft_cache_resize(ft_cache* c, int n_slots);
 
-/* Counters since creation.  Synchronises. */
+/* Cold restart at a safe point ([Review] §2.7: the engine serves its first
+ * request from a cold cache, with no warm-up): every slot empty, the recency
+ * clock and the counters back to zero, the capacity kept.  The handle's device
+ * tables stay where they are, so CUDA graphs captured over the handle remain
+ * valid.  Synchronises the device.  FT_ESTATE while a stream handle holds the
+ * pool's buffers or a split step waits for its join. */
+int ft_cache_reset(ft_cache* c);
+
+/* Counters since creation or the last ft_cache_reset.  Synchronises. */
 int ft_cache_stats(ft_cache* c, ft_cache_stats_t* out);
 
 /* Copies the residency state to host arrays of at least max_slots entries:

@@ -55,12 +55,32 @@ def test_launch_count_per_step():
     class Cfg:
         n_layers, wtype = 40, bench.synth.W_BF16
 
-    class Tr:
-        cfg, n_waves = Cfg, 1
-        launches_per_step = bench.DecodeTrace.launches_per_step
+    class Run:
+        cfg, n_waves, n_steps, batches = Cfg, 1, 256, [1, 64]
+        launches_per_step = bench.DecodeRun.launches_per_step
+        launches_per_pass = bench.DecodeRun.launches_per_pass
 
-    t = Tr()
-    t.fill_stream = None
-    assert t.launches_per_step() == 40 * 9        # route x3, control, fill, gather + gate/up + down, combine
-    t.fill_stream = object()
-    assert t.launches_per_step() == 40 * 12       # a second expert call in the split form
+    r = Run()
+    r.b = {1: {"split": False}, 64: {"split": True}}
+    assert r.launches_per_step(1) == 40 * 9       # route x3, control, fill, gather + gate/up + down, combine
+    assert r.launches_per_step(64) == 40 * 12     # a second expert call in the split form
+    assert r.launches_per_pass() == 256 * 40 * (9 + 12)
+
+
+def test_step_times_per_batch_exclude_the_reset_between_batches():
+    # T=1: steps at 0, 2, 5, end 6; (reset); T=4: steps at 10, 11, end 15
+    marks = [(1, 0, FakeEvent(0)), (1, 1, FakeEvent(2)), (1, 2, FakeEvent(5)), (1, -1, FakeEvent(6)),
+             (4, 0, FakeEvent(10)), (4, 1, FakeEvent(11)), (4, -1, FakeEvent(15))]
+    assert bench.step_times_ms(marks) == {1: [2, 3, 1], 4: [1, 4]}
+
+
+def test_oracle_pool_times_rounds_on_spawned_processes():
+    """The CPU baseline's process pool (spawned workers, one BLAS thread each) on the tiny layer."""
+    op = bench.OraclePool(bench.synth.TINY_F32, n_tokens=3, max_workers=2)
+    try:
+        t = [op.round() for _ in range(2)]
+    finally:
+        op.close()
+    assert op.n == min(2, len(os.sched_getaffinity(0))) and all(x > 0 for x in t)
+    assert "3 T=1 decode token(s)" in op.sample()
+    assert all(not p.is_alive() for p in op.procs)

@@ -40,7 +40,7 @@ def test_captured_decode_step_with_resize_and_recapture(ft):
     max_slots = 16
     sp = torch.empty(max_slots * S, dtype=torch.uint8, device=DEV)
     cache = ft.Cache(L, E, L, 12, max_slots, S, pool.ptr, sp)
-    sim = LRUSim(12, E)
+    box = {"sim": LRUSim(12, E)}
     lay = ft.MoELayer(cfg, T)
     routers = [synth.router_weights(cfg, l, DEV) for l in range(L)]
     src = [moe.ExpertSource(lambda e, l=l: synth.expert_weights(cfg, l, e, DEV), cfg.wtype) for l in range(L)]
@@ -59,6 +59,7 @@ def test_captured_decode_step_with_resize_and_recapture(ft):
 
     def check(ratio):
         """Oracle outputs and simulator decisions for the step just run on x_buf."""
+        sim = box["sim"]
         x64 = formats.to_f64(x_buf)
         got_out = outs.cpu().numpy()
         got_counts = counts.cpu().numpy()
@@ -84,6 +85,7 @@ def test_captured_decode_step_with_resize_and_recapture(ft):
         assert key.tolist() == sk.tolist() and stamp.tolist() == ss.tolist() and clock == sim.clock
 
     schedule = [(12, 1.0, 4), (7, 0.7, 4), (12, 0.7, 3)]     # (slots, fill ratio, replays)
+    sim = box["sim"]
     for phase, (N, ratio, reps) in enumerate(schedule):
         if phase:
             torch.cuda.synchronize()
@@ -108,10 +110,35 @@ def test_captured_decode_step_with_resize_and_recapture(ft):
             g.replay()
             torch.cuda.synchronize()
             check(ratio)
-        del g
+        if phase < len(schedule) - 1:
+            del g
     st = cache.stats()
     assert (st.hits, st.fills, st.externals) == (sim.hits, sim.fills, sim.externals)
     assert sim.externals > 0 and sim.fills > 0 and sim.hits > 0
+
+    # a cold restart keeps the handle's tables in place: the last graph replays from an
+    # empty cache, twice over the same inputs, with the same decisions as a fresh simulator
+    xs = [trace.next() for _ in range(3)]
+    for rnd in range(2):
+        torch.cuda.synchronize()
+        cache.reset()
+        key, stamp, clock = cache.export()
+        assert (key == -1).all() and (stamp == 0).all() and clock == 0
+        s0 = cache.stats()
+        assert (s0.steps, s0.hits, s0.fills, s0.externals, s0.bytes_h2d) == (0, 0, 0, 0, 0)
+        box["sim"] = LRUSim(12, E)
+        for xt in xs:
+            x_buf.copy_(xt)
+            counts.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            check(0.7)
+        if rnd == 0:
+            first = cache.export()
+        else:
+            again = cache.export()
+            assert all(np.array_equal(a, b) for a, b in zip(first[:2], again[:2])) and first[2] == again[2]
+    del g
     assert ft.ft_get_device_error() == 0
     cache.destroy()
     pool.free()
