@@ -68,6 +68,7 @@ def parse():
     p.add_argument("--cpu-tokens", type=int, default=2, help="T=1 tokens per round of the CPU oracle baseline")
     p.add_argument("--cpu-budget-s", type=float, default=12.0, help="wall seconds of timed CPU baseline rounds")
     p.add_argument("--no-pool-setup", action="store_true", help="skip the pin-first vs read-then-pin setup leg")
+    p.add_argument("--no-placement", action="store_true", help="skip the placement-policy replay")
     p.add_argument("--setup-layers", type=int, default=2, help="layers of the pool file in the setup leg")
     p.add_argument("--mixed-decode-steps", type=int, default=512)
     p.add_argument("--no-e2e", action="store_true")
@@ -878,6 +879,42 @@ def reference_main(args, world, rank):
     }))
 
 
+def placement_leg(ft, cfg, routers, dev, steps=1024, prompt=2048, fracs=(0.37, 0.11)):
+    """Placement-policy replay ([Review] §2.4): the routing of a T=1 decode trace and
+    of a prompt, both computed by the library's routing kernels, replayed on the host
+    (ft_placement_replay) under the shared LRU, a hot set fixed at prefill time and a
+    static split by layer, at 37% and 11% of the (layer, expert) pool."""
+    L, E, k = cfg.n_layers, cfg.n_experts, cfg.top_k
+    lay = ft.MoELayer(cfg, max(prompt, steps), dev)
+    x = synth.activations(cfg, prompt, tag=77, device=dev)
+    pc = torch.zeros(L, E, dtype=torch.int32, device=dev)
+    for l in range(L):
+        lay.route(x, *routers[l])
+        pc[l].copy_(lay.counts)
+    tr = synth.AR1Trace(cfg, 1, dev, tag=1)
+    xs = torch.cat([tr.next() for _ in range(steps)])               # [steps, H]: one token per step
+    ids = torch.empty(steps, L, k, dtype=torch.int32, device=dev)
+    for l in range(L):
+        lay.route(xs, *routers[l])
+        ids[:, l].copy_(lay.idx[:steps])
+    ids_h, pc_h = ids.cpu().numpy(), pc.cpu().numpy().reshape(-1)
+    out = {"decode_steps": steps, "batch": 1, "prompt_tokens": prompt,
+           "note": "synthetic AR(1)+Zipf(1.1) routing; the pages' 16%/39% (LRU), 41%/59% (prefill-time) and "
+                   "62%/89% (static) come from real routing traces that are not available here"}
+    names = {ft.FT_PLACE_GLOBAL_LRU: "global_lru", ft.FT_PLACE_PREFILL_HOT: "prefill_hot_set",
+             ft.FT_PLACE_STATIC_SPLIT: "static_split"}
+    for f in fracs:
+        cap = int(round(f * L * E))
+        row = {"capacity": cap}
+        for pol, name in names.items():
+            acc, miss = ft.ft_placement_replay(pol, L, E, cap, ids_h, pc_h if pol == ft.FT_PLACE_PREFILL_HOT else None)
+            row[name] = miss / max(acc, 1)
+        out[f"{round(f * 100)}%"] = row
+    del lay
+    torch.cuda.empty_cache()
+    return out
+
+
 def pool_setup_leg(ft, cfg, pool, n_layers):
     """Pool setup from a pool file, pin first (ft_host_alloc, then the read) against read
     then pin (the read into fresh pageable memory, then ft_host_register), for the first
@@ -1194,6 +1231,11 @@ def main():
     log("decode legs done")
     derr = ft.ft_get_device_error()
 
+    placement = None
+    if rank == 0 and not args.no_placement:
+        log("placement replay")
+        placement = placement_leg(ft, cfg, routers, dev)
+
     prefill = None
     if not args.no_prefill:
         log("prefill leg")
@@ -1254,6 +1296,7 @@ def main():
             "clocks": clocks,
             "prefill_bf16": prefill,
             "pool_setup": setup,
+            "placement_replay": placement,
             "nvfp4_43L": nvfp4,
             "mxfp4_mixed": mixed,
             "device_error": derr,

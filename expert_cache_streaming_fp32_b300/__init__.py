@@ -27,6 +27,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 # status / enums (values of include/ft.h)
 FT_OK, FT_EINVAL, FT_ENOMEM, FT_ECUDA, FT_ETIMEOUT, FT_ESTATE, FT_EUNSUPPORTED, FT_EDEVICE, FT_EIO = range(9)
 FT_INJECT_DEVICE_ALLOC, FT_INJECT_HOST_PIN, FT_INJECT_STREAM_EVENT = 1, 2, 3
+FT_PLACE_GLOBAL_LRU, FT_PLACE_PREFILL_HOT, FT_PLACE_STATIC_SPLIT = 0, 1, 2
 FT_W_F32, FT_W_BF16, FT_W_FP8E4M3, FT_W_NVFP4, FT_W_MXFP4 = range(5)
 FT_X_F32, FT_X_BF16 = 0, 1
 
@@ -38,7 +39,7 @@ EXPORTED = [
     "ft_stream_layer", "ft_stream_layer_done", "ft_stream_bytes", "ft_stream_destroy", "ft_qsplit",
     "ft_expert_grouped_noalloc", "ft_debug_bounded_wait", "ft_cache_step_split", "ft_cache_fill_join",
     "ft_cache_set_fill_blocks", "ft_debug_inject_failure", "ft_debug_live_resources", "ft_pool_read",
-    "ft_host_register", "ft_host_unregister", "ft_cache_reset",
+    "ft_host_register", "ft_host_unregister", "ft_cache_reset", "ft_placement_replay",
 ]
 FT_NOALLOC_MAX_ELEMS = 1 << 20
 FT_TC_WIDE_ASSIGNMENTS = 2048
@@ -91,6 +92,8 @@ _sigs = {
     "ft_cache_set_fill_blocks": (_I, [_P, _I]),
     "ft_cache_resize": (_I, [_P, _I]),
     "ft_cache_reset": (_I, [_P]),
+    "ft_placement_replay": (_I, [_I, _I, _I, _I, _P, _P, _I, _I, ctypes.POINTER(ctypes.c_uint64),
+                                 ctypes.POINTER(ctypes.c_uint64)]),
     "ft_cache_stats": (_I, [_P, ctypes.POINTER(CacheStats)]),
     "ft_cache_export": (_I, [_P, _P, _P, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_uint32)]),
     "ft_expert_grouped_workspace": (ctypes.c_size_t, [_I, _I, _I, _I]),
@@ -195,6 +198,19 @@ def ft_host_register(ptr: int, nbytes: int):
 
 def ft_host_unregister(ptr: int):
     _check("ft_host_unregister", _lib.ft_host_unregister(ctypes.c_void_p(ptr)))
+
+
+def ft_placement_replay(policy: int, n_layers: int, n_experts: int, capacity: int, trace, prefill_counts=None):
+    """(accesses, misses) of a routing trace (int32 array [steps, layers, width]) under a placement policy."""
+    import numpy as np
+    tr = np.ascontiguousarray(trace, dtype=np.int32)
+    assert tr.ndim == 3 and tr.shape[1] == n_layers
+    pc = None if prefill_counts is None else np.ascontiguousarray(prefill_counts, dtype=np.int32).reshape(-1)
+    acc, miss = ctypes.c_uint64(0), ctypes.c_uint64(0)
+    _check("ft_placement_replay", _lib.ft_placement_replay(
+        policy, n_layers, n_experts, capacity, None if pc is None else pc.ctypes.data_as(_P), tr.ctypes.data_as(_P),
+        tr.shape[0], tr.shape[2], ctypes.byref(acc), ctypes.byref(miss)))
+    return acc.value, miss.value
 
 
 def ft_qsplit(m: int, bw_fill: float, bw_host: float) -> int:

@@ -8,6 +8,7 @@
 #include "expert_tc_decode.cuh"
 #include "cache.cuh"
 #include "stream.cuh"
+#include "placement.cuh"
 
 #include <cudaTypedefs.h>
 
@@ -747,6 +748,39 @@ FT_API int ft_cache_export(ft_cache* c, int32_t* key_of_slot, uint32_t* stamp, i
   for (int i = 0; i < c->N; ++i) { key_of_slot[i] = t.key[i]; stamp[i] = t.stamp[i]; }
   *n_slots = c->N;
   *clock = t.clock;
+  return FT_OK;
+}
+
+// ------------------------------------------------------------------ placement replay
+FT_API int ft_placement_replay(int policy, int n_layers, int n_experts, int capacity, const int32_t* prefill_counts,
+                               const int32_t* trace, int n_steps, int width, uint64_t* accesses, uint64_t* misses) {
+  FT_REQUIRE(accesses && misses && n_layers >= 1 && n_experts >= 1 && n_steps >= 0 && width >= 1);
+  const long long keys = (long long)n_layers * n_experts;
+  FT_REQUIRE(keys < (1ll << 30) && capacity >= 1 && capacity <= keys);
+  FT_REQUIRE(trace || n_steps == 0);
+  uint64_t acc = 0, miss = 0;
+  if (policy == FT_PLACE_GLOBAL_LRU) {
+    FT_REQUIRE(capacity >= n_experts);
+    replay_lru(n_layers, n_experts, capacity, trace, n_steps, width, acc, miss);
+  } else if (policy == FT_PLACE_PREFILL_HOT || policy == FT_PLACE_STATIC_SPLIT) {
+    std::vector<char> resident((size_t)keys, 0);
+    if (policy == FT_PLACE_STATIC_SPLIT) {
+      for (int k = 0; k < capacity; ++k) resident[k] = 1;
+    } else {
+      FT_REQUIRE(prefill_counts);
+      std::vector<int> order;
+      for (int k = 0; k < keys; ++k)
+        if (prefill_counts[k] > 0) order.push_back(k);
+      std::stable_sort(order.begin(), order.end(),
+                       [&](int a, int b) { return prefill_counts[a] > prefill_counts[b]; });
+      for (size_t i = 0; i < order.size() && (int)i < capacity; ++i) resident[order[i]] = 1;
+    }
+    replay_fixed(n_layers, n_experts, resident, trace, n_steps, width, acc, miss);
+  } else {
+    return FT_EINVAL;
+  }
+  *accesses = acc;
+  *misses = miss;
   return FT_OK;
 }
 

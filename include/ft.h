@@ -464,6 +464,29 @@ int ft_stream_bytes(const ft_stream* st, uint64_t* bytes);
 int ft_stream_destroy(ft_stream* st);
 
 /* ------------------------------------------------------------------------
+ * Placement-policy replay (host only) ([Review] §2.4, the ablation that
+ * replays routing traces under three placements of equal capacity and counts
+ * the routed experts that are not in GPU memory).
+ *   FT_PLACE_GLOBAL_LRU      the shared LRU of ft_cache, starting empty, every
+ *                            miss filled (the cache step's victim rules);
+ *                            capacity >= n_experts
+ *   FT_PLACE_PREFILL_HOT     a hot set fixed at prefill time: the `capacity`
+ *                            keys with the most prefill assignments
+ *                            (prefill_counts, host [n_layers*n_experts]), ties
+ *                            to the lower key, resident for the whole trace
+ *   FT_PLACE_STATIC_SPLIT    a routing-agnostic split made at load time: keys
+ *                            0 .. capacity-1 (whole layers in order) resident
+ *   trace       host [n_steps][n_layers][width] int32 expert ids of each layer
+ *               step's assignments (duplicates allowed, -1 = padding)
+ *   accesses    (written) unique routed experts over all layer steps
+ *   misses      (written) those not resident when routed
+ * Keys are layer * n_experts + expert; 1 <= capacity <= n_layers*n_experts.
+ * ---------------------------------------------------------------------- */
+enum { FT_PLACE_GLOBAL_LRU = 0, FT_PLACE_PREFILL_HOT = 1, FT_PLACE_STATIC_SPLIT = 2 };
+int ft_placement_replay(int policy, int n_layers, int n_experts, int capacity, const int32_t* prefill_counts,
+                        const int32_t* trace, int n_steps, int width, uint64_t* accesses, uint64_t* misses);
+
+/* ------------------------------------------------------------------------
  * ft_qsplit (host only, pure): q* = m B_P / B_H, rounded half up, at least 1,
  * at most m; m when B_H <= B_P; 0 when m <= 0 ([Review] §2.5, balance equation
  * and the rounding rule after it).

@@ -172,3 +172,21 @@ def test_mutant_expert_source_returns_up_first(monkeypatch):
     monkeypatch.setattr(moe.ExpertSource, "__call__", call)
     import test_oracle_dispatch as t_disp
     _fails(t_disp.test_expert_source_order_values_and_caching)
+
+
+def test_mutant_prefill_hot_set_ties_to_the_higher_key(monkeypatch):
+    import oracle.placement as placement
+    import test_oracle_placement as t_pl
+
+    def hot(counts, capacity):
+        ranked = sorted((k for k, c in counts.items() if c > 0), key=lambda k: (-counts[k], -k))
+        return set(ranked[:capacity])
+    monkeypatch.setattr(placement, "prefill_hot_set", hot)
+    _fails(t_pl.test_hand_worked_trace)
+
+
+def test_mutant_static_split_by_expert_instead_of_layer(monkeypatch):
+    import oracle.placement as placement
+    import test_oracle_placement as t_pl
+    monkeypatch.setattr(placement, "static_set", lambda L, E, cap: {(i % L) * E + i // L for i in range(cap)})
+    _fails(t_pl.test_hand_worked_trace)
