@@ -44,6 +44,7 @@ BATCHES = (1, 4, 16, 64)
 TRAFFIC_PER_BYTE = {"fill": (0.025e6 + 140.025e6) / 201.327e6,
                     "experts": (207.776e6 + 3.545e6 + 103.355e6 + 2.734e6) / (205.5e6 + 0.5e6 + 102.8e6)}
 CACHE_FRAC = 0.40
+ROUTE_FUSED_MAX_T = 16            # batches routed by one ft_route_fused launch
 FP4_OVER_BF16 = 13.5 / 2.25       # nominal dense FP4 / bf16 tensor rates of the B300
 METRIC = "MoE-layer tokens/s (decode T=1..64, prefill 8192) and % of layer roofline"
 WORKLOAD = ("decode_bf16_40L: H=2048 E=256 top-8 I=512, bf16 weights, 40 layers, 64.4 GB pinned host pool, "
@@ -254,13 +255,15 @@ class DecodeRun:
         self.graphs = {}
 
     def launches_per_step(self, T) -> int:
-        # router_logits, route, permute, (control, fill, expert kernels) per wave, combine;
+        # routing (one fused launch, or router_logits + route + permute), (control, fill, expert
+        # kernels) per wave, combine;
         # bf16 experts run gather + gate/up + down on the tensor cores, other formats gate/up + down
         # (the split form evaluates hits and filled experts in two expert calls)
         n_exp = 3 if self.cfg.wtype == synth.W_BF16 else 2
         if self.b[T]["split"]:
             n_exp *= 2
-        return self.cfg.n_layers * (3 + (2 + n_exp) * self.n_waves + 1)
+        n_route = 1 if T <= ROUTE_FUSED_MAX_T else 3       # ft_route_fused: one cluster launch up to 16 tokens
+        return self.cfg.n_layers * (n_route + (2 + n_exp) * self.n_waves + 1)
 
     def launches_per_pass(self) -> int:
         return sum(self.n_steps * self.launches_per_step(T) for T in self.batches)

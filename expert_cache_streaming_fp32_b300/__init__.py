@@ -39,7 +39,8 @@ EXPORTED = [
     "ft_stream_layer", "ft_stream_layer_done", "ft_stream_bytes", "ft_stream_destroy", "ft_qsplit",
     "ft_expert_grouped_noalloc", "ft_debug_bounded_wait", "ft_cache_step_split", "ft_cache_fill_join",
     "ft_cache_set_fill_blocks", "ft_debug_inject_failure", "ft_debug_live_resources", "ft_pool_read",
-    "ft_host_register", "ft_host_unregister", "ft_cache_reset", "ft_placement_replay",
+    "ft_host_register", "ft_host_unregister", "ft_cache_reset", "ft_placement_replay", "ft_cpu_create",
+    "ft_cpu_destroy", "ft_cpu_experts", "ft_cpu_experts_enqueue", "ft_cpu_status", "ft_route_fused",
 ]
 FT_NOALLOC_MAX_ELEMS = 1 << 20
 FT_TC_WIDE_ASSIGNMENTS = 2048
@@ -70,6 +71,14 @@ class CacheStats(ctypes.Structure):
                 ("externals", ctypes.c_uint64), ("bytes_h2d", ctypes.c_uint64)]
 
 
+class CpuJob(ctypes.Structure):
+    _fields_ = [("host_pool", ctypes.c_void_p), ("slot_bytes", ctypes.c_uint64), ("wtype", ctypes.c_int),
+                ("hidden", ctypes.c_int), ("inter", ctypes.c_int), ("n_experts", ctypes.c_int),
+                ("phys_layer", ctypes.c_int), ("x", ctypes.c_void_p), ("x_type", ctypes.c_int), ("T", ctypes.c_int),
+                ("k", ctypes.c_int), ("topk_idx", ctypes.c_void_p), ("topk_w", ctypes.c_void_p),
+                ("ext_flags", ctypes.c_void_p), ("partial", ctypes.c_void_p)]
+
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _sigs = {
@@ -83,6 +92,7 @@ _sigs = {
     "ft_router_logits": (_I, [_P, _I, _P, _P, _I, _I, _I, _P, _P]),
     "ft_route": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "ft_permute": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "ft_route_fused": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "ft_cache_create": (_I, [ctypes.POINTER(CacheConfig), ctypes.POINTER(_P)]),
     "ft_cache_destroy": (_I, [_P]),
     "ft_cache_n_waves": (_I, [_P]),
@@ -92,6 +102,11 @@ _sigs = {
     "ft_cache_set_fill_blocks": (_I, [_P, _I]),
     "ft_cache_resize": (_I, [_P, _I]),
     "ft_cache_reset": (_I, [_P]),
+    "ft_cpu_create": (_I, [_I, ctypes.POINTER(_P)]),
+    "ft_cpu_destroy": (_I, [_P]),
+    "ft_cpu_experts": (_I, [_P, ctypes.POINTER(CpuJob)]),
+    "ft_cpu_experts_enqueue": (_I, [_P, ctypes.POINTER(CpuJob), _P]),
+    "ft_cpu_status": (_I, [_P]),
     "ft_placement_replay": (_I, [_I, _I, _I, _I, _P, _P, _I, _I, ctypes.POINTER(ctypes.c_uint64),
                                  ctypes.POINTER(ctypes.c_uint64)]),
     "ft_cache_stats": (_I, [_P, ctypes.POINTER(CacheStats)]),
@@ -233,6 +248,14 @@ def ft_permute(topk_idx, E, counts, offsets, perm, inv, stream=None):
     T, k = topk_idx.shape
     _check("ft_permute", _lib.ft_permute(_ptr(topk_idx), T, k, E, _ptr(counts), _ptr(offsets), _ptr(perm),
                                          _ptr(inv), _stream(stream)))
+
+
+def ft_route_fused(x, w_router, bias, k, logits, topk_idx, topk_w, counts, offsets, perm, inv, stream=None):
+    T, H = x.shape
+    E = w_router.shape[0]
+    _check("ft_route_fused", _lib.ft_route_fused(
+        _ptr(x), _xtype(x), _ptr(w_router), _ptr(bias), T, H, E, k, _ptr(logits), _ptr(topk_idx), _ptr(topk_w),
+        _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv), _stream(stream)))
 
 
 def ft_expert_grouped_workspace(T, k, hidden, inter) -> int:
@@ -408,6 +431,44 @@ class Cache:
         return key[: n.value].copy(), stamp[: n.value].copy(), clk.value
 
 
+class CpuExperts:
+    """Owner of an ft_cpu handle: the host-side expert executor (a pool of CPU threads)."""
+
+    def __init__(self, threads: int = 0):
+        h = _P()
+        _check("ft_cpu_create", _lib.ft_cpu_create(threads, ctypes.byref(h)))
+        self.h = h
+
+    @staticmethod
+    def job(host_pool_ptr, slot_bytes, wtype, hidden, inter, n_experts, phys_layer, x, T, k, topk_idx, topk_w,
+            ext_flags, partial) -> CpuJob:
+        """A job over host tensors (x [T, H] bf16/fp32, topk_idx/topk_w [T, k], ext_flags [E], partial [T, H] fp32)."""
+        for t in (x, topk_idx, topk_w, ext_flags, partial):
+            assert not t.is_cuda and t.is_contiguous()
+        return CpuJob(host_pool_ptr, slot_bytes, wtype, hidden, inter, n_experts, phys_layer, x.data_ptr(), _xtype(x),
+                      T, k, topk_idx.data_ptr(), topk_w.data_ptr(), ext_flags.data_ptr(), partial.data_ptr())
+
+    def run(self, job: CpuJob):
+        _check("ft_cpu_experts", _lib.ft_cpu_experts(self.h, ctypes.byref(job)))
+
+    def enqueue(self, job: CpuJob, stream=None):
+        _check("ft_cpu_experts_enqueue", _lib.ft_cpu_experts_enqueue(self.h, ctypes.byref(job), _stream(stream)))
+
+    def status(self) -> int:
+        return _lib.ft_cpu_status(self.h)
+
+    def destroy(self):
+        if self.h:
+            _lib.ft_cpu_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
 class Stream:
     """Owner of an ft_stream handle (whole-layer double-buffered prefill)."""
 
@@ -434,5 +495,5 @@ class Stream:
             _check("ft_stream_destroy", st)
 
 
-from .layer import (SPLIT_MAX_ASSIGNMENTS, SPLIT_MIN_ASSIGNMENTS, ExpertPool, MoELayer, pack_expert,  # noqa: E402,F401
-                    split_pays)
+from .layer import (SPLIT_MAX_ASSIGNMENTS, SPLIT_MIN_ASSIGNMENTS, ExpertPool, HostBranch, MoELayer,  # noqa: E402,F401
+                    pack_expert, split_pays)

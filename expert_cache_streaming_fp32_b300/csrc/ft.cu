@@ -9,6 +9,7 @@
 #include "cache.cuh"
 #include "stream.cuh"
 #include "placement.cuh"
+#include "cpu_experts.cuh"
 
 #include <cudaTypedefs.h>
 
@@ -226,6 +227,55 @@ FT_API int ft_permute(const int32_t* topk_idx, int T, int k, int E, int32_t* cou
   if (int st = set_smem(permute_kernel, smem)) return st;
   FT_LAUNCH(permute_kernel, 1, PM_THREADS, smem, s, topk_idx, (int)n, E, counts, offsets, perm, inv);
   return FT_OK;
+}
+
+// ------------------------------------------------------------------ fused routing
+namespace {
+template <typename XT, int RT>
+int launch_route_fused(const XT* x, const XT* wr, const float* bias, int T, int H, int E, int k, float* z,
+                       int32_t* idx, float* w, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                       cudaStream_t st) {
+  const size_t smem = (size_t)RT * H * sizeof(float);
+  auto kr = E <= 256 ? route_fused_kernel<XT, RT, 8> : route_fused_kernel<XT, RT, 16>;
+  if (int r = set_smem(kr, smem)) return r;
+  FT_CHECK_CUDA(launch_pdl_cluster(kr, dim3(RF_CL), dim3(RF_THREADS), smem, st, RF_CL, x, wr, bias, T, H, E, k, z,
+                                   idx, w, counts, offsets, perm, inv));
+  return FT_OK;
+}
+
+template <typename XT>
+int route_fused_rt(const void* x, const void* wr, const float* bias, int T, int H, int E, int k, float* z,
+                   int32_t* idx, float* w, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                   cudaStream_t st) {
+  const XT* xx = static_cast<const XT*>(x);
+  const XT* ww = static_cast<const XT*>(wr);
+  if (T >= 8) return launch_route_fused<XT, 8>(xx, ww, bias, T, H, E, k, z, idx, w, counts, offsets, perm, inv, st);
+  if (T >= 4) return launch_route_fused<XT, 4>(xx, ww, bias, T, H, E, k, z, idx, w, counts, offsets, perm, inv, st);
+  if (T >= 2) return launch_route_fused<XT, 2>(xx, ww, bias, T, H, E, k, z, idx, w, counts, offsets, perm, inv, st);
+  return launch_route_fused<XT, 1>(xx, ww, bias, T, H, E, k, z, idx, w, counts, offsets, perm, inv, st);
+}
+}  // namespace
+
+FT_API int ft_route_fused(const void* x, int x_type, const void* w_router, const float* bias, int T, int H, int E,
+                          int k, float* logits, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                          int32_t* perm, int32_t* inv, ft_cuda_stream s) {
+  FT_REQUIRE(T >= 0 && H > 0 && H % 8 == 0 && E >= 1 && E <= PM_MAXE && k >= 1 && k <= RT_MAXK && k <= E);
+  FT_REQUIRE(x_type == FT_X_F32 || x_type == FT_X_BF16);
+  FT_REQUIRE(counts && offsets);
+  if (T > 0) FT_REQUIRE(x && w_router && logits && topk_idx && topk_w && perm && inv);
+  const int RT = T >= 8 ? 8 : T >= 4 ? 4 : T >= 2 ? 2 : 1;
+  if (T == 0 || T > RF_MAXT || (size_t)RT * H * sizeof(float) > 200 * 1024) {
+    // larger batches (and the empty one): the three kernels
+    if (int r = ft_router_logits(x, x_type, w_router, bias, T, H, E, logits, s)) return r;
+    if (int r = ft_route(logits, T, E, k, topk_idx, topk_w, s)) return r;
+    return ft_permute(topk_idx, T, k, E, counts, offsets, perm, inv, s);
+  }
+  cudaStream_t st = (cudaStream_t)s;
+  if (x_type == FT_X_BF16)
+    return route_fused_rt<__nv_bfloat16>(x, w_router, bias, T, H, E, k, logits, topk_idx, topk_w, counts, offsets,
+                                         perm, inv, st);
+  return route_fused_rt<float>(x, w_router, bias, T, H, E, k, logits, topk_idx, topk_w, counts, offsets, perm, inv,
+                               st);
 }
 
 // ------------------------------------------------------------------ combine
@@ -749,6 +799,69 @@ FT_API int ft_cache_export(ft_cache* c, int32_t* key_of_slot, uint32_t* stamp, i
   *n_slots = c->N;
   *clock = t.clock;
   return FT_OK;
+}
+
+// ------------------------------------------------------------------ host-side expert executor
+FT_API int ft_cpu_create(int threads, ft_cpu** out) {
+  FT_REQUIRE(out && threads >= 0 && threads <= 255);
+  *out = nullptr;
+  if (threads == 0) threads = (int)std::min<unsigned>(255u, std::max(1u, std::thread::hardware_concurrency()) - 1);
+  ft_cpu* c = new (std::nothrow) ft_cpu();
+  if (!c) return FT_ENOMEM;
+  c->n_threads = threads + 1;
+  try {
+    for (int i = 0; i < threads; ++i) c->workers.emplace_back(cpu_worker, c);
+  } catch (...) {
+    ft_cpu_destroy(c);
+    return FT_ENOMEM;
+  }
+  *out = c;
+  return FT_OK;
+}
+
+FT_API int ft_cpu_destroy(ft_cpu* c) {
+  if (!c) return FT_OK;
+  {
+    std::lock_guard<std::mutex> lk(c->mu);
+    c->stop = true;
+  }
+  c->cv.notify_all();
+  for (auto& t : c->workers) t.join();
+  delete c;
+  return FT_OK;
+}
+
+FT_API int ft_cpu_experts(ft_cpu* c, const ft_cpu_job* job) {
+  FT_REQUIRE(c && job);
+  return cpu_experts_run(c, *job);
+}
+
+static void CUDART_CB cpu_host_fn(void* p) {
+  ft_cpu_job_rec* r = static_cast<ft_cpu_job_rec*>(p);
+  const int st = cpu_experts_run(r->cpu, r->job);
+  if (st) {
+    int zero = 0;
+    r->cpu->status.compare_exchange_strong(zero, st);  // the first failure is kept
+  }
+}
+
+FT_API int ft_cpu_experts_enqueue(ft_cpu* c, const ft_cpu_job* job, ft_cuda_stream s) {
+  FT_REQUIRE(c && job);
+  ft_expert_layout L;
+  if (expert_layout(job->wtype, job->hidden, job->inter, &L) != FT_OK) return FT_EINVAL;
+  FT_REQUIRE(job->host_pool && job->x && job->topk_idx && job->topk_w && job->ext_flags && job->partial);
+  FT_REQUIRE(job->T >= 0 && job->k >= 1 && job->n_experts >= 1 && job->slot_bytes >= L.bytes);
+  std::unique_ptr<ft_cpu_job_rec> r(new (std::nothrow) ft_cpu_job_rec{c, *job});
+  if (!r) return FT_ENOMEM;
+  FT_CHECK_CUDA(cudaLaunchHostFunc((cudaStream_t)s, cpu_host_fn, r.get()));
+  std::lock_guard<std::mutex> lk(c->run_mu);
+  c->jobs.push_back(std::move(r));
+  return FT_OK;
+}
+
+FT_API int ft_cpu_status(ft_cpu* c) {
+  FT_REQUIRE(c);
+  return c->status.exchange(0);
 }
 
 // ------------------------------------------------------------------ placement replay

@@ -32,15 +32,10 @@ __device__ __forceinline__ void load8<float>(const float* p, float (&o)[8]) {
   o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
 }
 
+// Stages token rows t0 .. t0+RT-1 of x (zeros past nrows) in shared memory as fp32.
 template <typename XT, int RT>
-__global__ void __launch_bounds__(RL_WARPS * 32)
-router_logits_kernel(const XT* __restrict__ x, const XT* __restrict__ wr, const float* __restrict__ bias,
-                     int T, int H, int E, float* __restrict__ z) {
-  extern __shared__ float xs[];  // [RT][H]
-  pdl_begin();
-  const int t0 = blockIdx.y * RT;
-  const int nrows = min(RT, T - t0);
-  // stage the rows 8 elements (one 16-byte bf16 load or two fp32 loads) per thread step
+__device__ __forceinline__ void stage_rows(const XT* __restrict__ x, int t0, int nrows, int H, float* xs) {
+  // 8 elements (one 16-byte bf16 load or two fp32 loads) per thread step
   for (int r = 0; r < RT; ++r) {
     for (int h = threadIdx.x * 8; h < H; h += blockDim.x * 8) {
       float v[8];
@@ -54,10 +49,16 @@ router_logits_kernel(const XT* __restrict__ x, const XT* __restrict__ wr, const 
       *reinterpret_cast<float4*>(xs + r * H + h + 4) = make_float4(v[4], v[5], v[6], v[7]);
     }
   }
-  __syncthreads();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+}
+
+// Logits of the staged rows for experts e0, e0 + e_step, ... (one warp per expert).
+template <typename XT, int RT>
+__device__ __forceinline__ void logits_of_rows(const float* xs, const XT* __restrict__ wr,
+                                               const float* __restrict__ bias, int t0, int nrows, int H, int E,
+                                               int e0, int e_step, float* __restrict__ z) {
+  const int lane = threadIdx.x & 31;
   constexpr int U = 8;  // 256-element chunks whose weight loads are in flight together
-  for (int e = blockIdx.x * RL_WARPS + warp; e < E; e += gridDim.x * RL_WARPS) {
+  for (int e = e0; e < E; e += e_step) {
     float acc[RT];
 #pragma unroll
     for (int r = 0; r < RT; ++r) acc[r] = 0.0f;
@@ -96,6 +97,20 @@ router_logits_kernel(const XT* __restrict__ x, const XT* __restrict__ wr, const 
   }
 }
 
+template <typename XT, int RT>
+__global__ void __launch_bounds__(RL_WARPS * 32)
+router_logits_kernel(const XT* __restrict__ x, const XT* __restrict__ wr, const float* __restrict__ bias,
+                     int T, int H, int E, float* __restrict__ z) {
+  extern __shared__ float xs[];  // [RT][H]
+  pdl_begin();
+  const int t0 = blockIdx.y * RT;
+  const int nrows = min(RT, T - t0);
+  stage_rows<XT, RT>(x, t0, nrows, H, xs);
+  __syncthreads();
+  logits_of_rows<XT, RT>(xs, wr, bias, t0, nrows, H, E, blockIdx.x * RL_WARPS + (threadIdx.x >> 5),
+                         gridDim.x * RL_WARPS, z);
+}
+
 // ====================================================================== top-k gating
 // One warp per token.  Lane l holds logits e = l, l+32, ...  Each of the k
 // rounds takes the warp-wide maximum of (value, -index) among the experts not
@@ -107,15 +122,11 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
+// Top-k of one token's logits z[0..E-1] by one warp; lane 0 writes idx_row and w_row.
 template <int PER_LANE>
-__global__ void __launch_bounds__(256)
-route_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ idx_out,
-             float* __restrict__ w_out) {
-  pdl_begin();
+__device__ __forceinline__ void route_token(const float* __restrict__ z, int E, int k, int32_t* __restrict__ idx_row,
+                                            float* __restrict__ w_row) {
   const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const float* z = logits + (size_t)t * E;
   float v[PER_LANE];
   unsigned taken = 0;
 #pragma unroll
@@ -167,10 +178,20 @@ route_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __r
     const float inv = 1.0f / s;
 #pragma unroll 1
     for (int j = 0; j < k; ++j) {
-      idx_out[(size_t)t * k + j] = sel_i[j];
-      w_out[(size_t)t * k + j] = ex[j] * inv;
+      idx_row[j] = sel_i[j];
+      w_row[j] = ex[j] * inv;
     }
   }
+}
+
+template <int PER_LANE>
+__global__ void __launch_bounds__(256)
+route_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ idx_out,
+             float* __restrict__ w_out) {
+  pdl_begin();
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  route_token<PER_LANE>(logits + (size_t)t * E, E, k, idx_out + (size_t)t * k, w_out + (size_t)t * k);
 }
 
 // ====================================================================== permutation
@@ -272,6 +293,115 @@ permute_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __restric
     // the scan above wrote every (w, ex) entry: reset the whole table for the next tile
     for (int i = tid; i < PM_WARPS * E; i += PM_THREADS) wc[i] = 0;
     __syncthreads();
+  }
+}
+
+// ====================================================================== fused routing (decode batches)
+// Router logits, top-k and the permutation of a small batch (T <= RF_MAXT) in
+// one launch: a cluster of RF_CL CTAs.  Each CTA computes the logits of its
+// share of the experts for every token (the same per-expert arithmetic as
+// router_logits_kernel, so the logits are bit-identical) and writes them out;
+// after a cluster barrier (release/acquire at cluster scope, so the other
+// CTAs' logits are visible) CTA 0 routes every token (one warp per token, as
+// route_kernel) and builds counts, offsets, perm and inv for the T*k
+// assignments: the rank of an assignment within its expert is the number of
+// earlier assignments to the same expert, so perm is stable.
+constexpr int RF_CL = 8;
+constexpr int RF_MAXT = 16;
+constexpr int RF_WARPS = 16;
+constexpr int RF_THREADS = RF_WARPS * 32;
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <typename XT, int RT, int PER_LANE>
+__global__ void __launch_bounds__(RF_THREADS)
+route_fused_kernel(const XT* __restrict__ x, const XT* __restrict__ wr, const float* __restrict__ bias, int T,
+                   int H, int E, int k, float* __restrict__ z, int32_t* __restrict__ idx_out,
+                   float* __restrict__ w_out, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                   int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+  extern __shared__ float xs[];                      // [RT][H]
+  __shared__ int32_t s_cnt[RT_MAXE + 1];
+  __shared__ int32_t s_idx[RF_MAXT * RT_MAXK];
+  __shared__ int32_t s_wsum[RF_WARPS];
+  pdl_begin();
+  const int rank = (int)cluster_ctarank();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int t0 = 0; t0 < T; t0 += RT) {
+    const int nrows = min(RT, T - t0);
+    stage_rows<XT, RT>(x, t0, nrows, H, xs);
+    __syncthreads();
+    logits_of_rows<XT, RT>(xs, wr, bias, t0, nrows, H, E, rank * RF_WARPS + warp, RF_CL * RF_WARPS, z);
+    __syncthreads();
+  }
+  __threadfence();
+  cluster_sync_all();
+  if (rank != 0) return;
+  // top-k per token
+  for (int t = warp; t < T; t += RF_WARPS)
+    route_token<PER_LANE>(z + (size_t)t * E, E, k, idx_out + (size_t)t * k, w_out + (size_t)t * k);
+  for (int e = threadIdx.x; e <= E; e += RF_THREADS) s_cnt[e] = 0;
+  __syncthreads();
+  // permutation of the n = T*k assignments
+  const int n = T * k;
+  for (int a = threadIdx.x; a < n; a += RF_THREADS) {
+    int e = idx_out[a];
+    if ((unsigned)e >= (unsigned)E) {
+      record_error(FT_DERR_EXPERT_INDEX);
+      e = -1;
+    } else {
+      atomicAdd(&s_cnt[e], 1);
+    }
+    s_idx[a] = e;
+  }
+  __syncthreads();
+  // exclusive scan of the counts: each thread a run of consecutive experts
+  const int per = ceil_div(E, RF_THREADS);
+  int local = 0;
+  for (int i = 0; i < per; ++i) {
+    const int e = threadIdx.x * per + i;
+    if (e < E) local += s_cnt[e];
+  }
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(FT_FULL_MASK, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  int before = 0;
+  for (int w = 0; w < warp; ++w) before += s_wsum[w];
+  int run = before + incl - local;
+  __syncthreads();                                   // every count is read before it is replaced by its offset
+  for (int i = 0; i < per; ++i) {
+    const int e = threadIdx.x * per + i;
+    if (e < E) {
+      const int c = s_cnt[e];
+      counts[e] = c;
+      offsets[e] = run;
+      s_cnt[e] = run;
+      run += c;
+    }
+  }
+  if (threadIdx.x == 0) offsets[E] = n;
+  __syncthreads();
+  for (int a = threadIdx.x; a < n; a += RF_THREADS) {
+    const int e = s_idx[a];
+    if (e < 0) continue;
+    int r = 0;
+    for (int b = 0; b < a; ++b) r += s_idx[b] == e;
+    const int pos = s_cnt[e] + r;
+    perm[pos] = a;
+    inv[a] = pos;
   }
 }
 

@@ -22,9 +22,9 @@ from typing import Optional
 import torch
 
 from . import (FT_TC_WIDE_ASSIGNMENTS, FT_W_BF16, FT_W_F32, FT_W_FP8E4M3, FT_W_MXFP4, FT_W_NVFP4, Cache,
-               PinnedBuffer, RegisteredBuffer, ft_combine, ft_pool_read,
+               CpuExperts, PinnedBuffer, RegisteredBuffer, ft_combine, ft_pool_read,
                ft_expert_grouped, ft_expert_grouped_workspace, ft_expert_layout_get, ft_permute, ft_route,
-               ft_router_logits)
+               ft_route_fused, ft_router_logits)
 
 
 # Decode batches of at least this many assignments (T*k) evaluate their hits
@@ -180,6 +180,13 @@ class MoELayer:
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=device)
 
     def route(self, x, w_router, bias, stream=None):
+        """Router logits, top-k and permutation (one launch for decode batches: ft_route_fused)."""
+        T = x.shape[0]
+        ft_route_fused(x, w_router, bias, self.cfg.top_k, self.logits[:T], self.idx[:T], self.w[:T], self.counts,
+                       self.offsets, self.perm, self.inv, stream)
+
+    def route_unfused(self, x, w_router, bias, stream=None):
+        """The same as ``route`` with the three separate kernels."""
         T = x.shape[0]
         ft_router_logits(x, w_router, bias, self.logits[:T], stream)
         ft_route(self.logits[:T], self.cfg.top_k, self.idx[:T], self.w[:T], stream)
@@ -196,18 +203,23 @@ class MoELayer:
         return self.out[:T]
 
     def cached_wave(self, x, layer: int, cache: Cache, slot_bytes: int, fill_ratio: float, wave: int,
-                    step_counts=None, stream=None, fill_stream=None):
+                    step_counts=None, stream=None, fill_stream=None, after_control=None):
         """Cache control, miss fill and expert evaluation of one wave.
 
         With ``fill_stream`` the fill runs there while the hits are evaluated on
-        ``stream``; the filled experts follow after the join."""
+        ``stream``; the filled experts follow after the join.  ``after_control``
+        (split form only) is called right after the control launch, before the
+        hits' evaluation: the point from which the wave's external set is known."""
         sc = self.step_counts if step_counts is None else step_counts
         if fill_stream is None:
+            assert after_control is None, "the host branch needs the split form"
             cache.step(layer, self.counts, fill_ratio, wave, self.slot_of, self.ext, sc, stream)
             self.experts(x, self.slot_of, cache.slot_pool, slot_bytes, cache.max_slots, stream)
             return
         cache.step_split(layer, self.counts, fill_ratio, wave, self.slot_of, self.slot_fill, self.ext, sc, stream,
                          fill_stream)
+        if after_control is not None:
+            after_control()
         self.experts(x, self.slot_of, cache.slot_pool, slot_bytes, cache.max_slots, stream)
         cache.fill_join(stream)
         self.experts(x, self.slot_fill, cache.slot_pool, slot_bytes, cache.max_slots, stream)
@@ -228,3 +240,48 @@ class MoELayer:
         self.route(x, w_router, bias, stream)
         self.experts(x, slot_of, slot_pool, slot_bytes, pool_slots, stream)
         return self.combine(T, None, None, stream)
+
+
+class HostBranch:
+    """The external experts of a layer step evaluated on the host (the CPU branch).
+
+    After the last wave's control launch, a side stream copies the step's
+    external marks, routing and tokens to pinned host buffers, runs the host
+    expert executor on them as a host function (a host node when captured),
+    and copies the partial output back to the device; ``P`` is then the
+    ``ext_partial`` of the combine, which waits for ``done``.  The fill and the
+    GPU experts run meanwhile.  Each layer's job is kept by the executor, so a
+    captured step enqueues it once and every replay runs it again."""
+
+    def __init__(self, cfg, T_max: int, pool: "ExpertPool", cpu: CpuExperts, device="cuda"):
+        self.cfg, self.pool, self.cpu, self.T_max = cfg, pool, cpu, T_max
+        H, k, E = cfg.hidden, cfg.top_k, cfg.n_experts
+        xdt = torch.bfloat16 if cfg.x_dtype == "bf16" else torch.float32
+        self.x_h = torch.empty(T_max, H, dtype=xdt).pin_memory()
+        self.idx_h = torch.empty(T_max, k, dtype=torch.int32).pin_memory()
+        self.w_h = torch.empty(T_max, k, dtype=torch.float32).pin_memory()
+        self.ext_h = torch.empty(E, dtype=torch.int32).pin_memory()
+        self.part_h = torch.empty(T_max, H, dtype=torch.float32).pin_memory()
+        self.P = torch.zeros(T_max, H, dtype=torch.float32, device=device)
+        self.stream = torch.cuda.Stream(device=device)
+        self.done = torch.cuda.Event()
+
+    def launch(self, lay: MoELayer, x, layer: int):
+        """Issues the branch for layer ``layer`` of the current step (tokens x on the device)."""
+        T = x.shape[0]
+        cur = torch.cuda.current_stream()
+        self.stream.wait_stream(cur)
+        with torch.cuda.stream(self.stream):
+            self.x_h[:T].copy_(x, non_blocking=True)
+            self.idx_h[:T].copy_(lay.idx[:T], non_blocking=True)
+            self.w_h[:T].copy_(lay.w[:T], non_blocking=True)
+            self.ext_h.copy_(lay.ext, non_blocking=True)
+            job = self.cpu.job(self.pool.ptr, self.pool.S, self.cfg.wtype, self.cfg.hidden, self.cfg.inter,
+                               self.cfg.n_experts, layer % self.pool.n_phys, self.x_h[:T], T, self.cfg.top_k,
+                               self.idx_h[:T], self.w_h[:T], self.ext_h, self.part_h[:T])
+            self.cpu.enqueue(job, self.stream)
+            self.P[:T].copy_(self.part_h[:T], non_blocking=True)
+            self.done.record(self.stream)
+
+    def join(self):
+        torch.cuda.current_stream().wait_event(self.done)

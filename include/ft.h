@@ -217,6 +217,20 @@ int ft_permute(const int32_t* topk_idx, int T, int k, int E, int32_t* counts, in
                int32_t* perm, int32_t* inv, ft_cuda_stream s);
 
 /* ------------------------------------------------------------------------
+ * ft_route_fused: ft_router_logits, ft_route and ft_permute of one batch, with
+ * the same arguments and results (the logits are bit-identical), for the
+ * per-token routing and grouping of a decode step.  Batches of at most 16
+ * tokens (with 8 * H * 4 bytes of staged rows <= 200 KiB) run as one launch of
+ * one 8-CTA thread-block cluster: each CTA computes a share of the experts'
+ * logits, and after a cluster barrier one CTA routes the tokens and groups
+ * the assignments.  Larger batches run the three kernels.
+ * T >= 0, H a multiple of 8, 1 <= E <= 512, 1 <= k <= min(E, 16).
+ * ---------------------------------------------------------------------- */
+int ft_route_fused(const void* x, int x_type, const void* w_router, const float* bias, int T, int H, int E, int k,
+                   float* logits, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                   int32_t* perm, int32_t* inv, ft_cuda_stream s);
+
+/* ------------------------------------------------------------------------
  * ft_cache: one LRU cache of expert records shared by all MoE layers, keyed by
  * the logical (layer, expert) ([Review] §2 opening, §2.4).  The full expert
  * pool stays in pinned host memory; GPU memory changes only speed, never the
@@ -462,6 +476,50 @@ int ft_stream_bytes(const ft_stream* st, uint64_t* bytes);
  * is refreshed and its buffer slot left empty): entries that survive prefill
  * warm decode ([Review] §2.2).  Synchronises. */
 int ft_stream_destroy(ft_stream* st);
+
+/* ------------------------------------------------------------------------
+ * Host-side expert executor ([Review] §2.5: the experts of C, the misses not
+ * filled into the cache, are evaluated where their weights live, from the
+ * host pool, and their gate-weighted outputs form a partial sum that the GPU
+ * adds to its own, so the layer output stays exact; §2.6: the CPU branch is a
+ * node of the captured step).  A handle owns a pool of CPU threads.
+ *
+ * One job evaluates, for every token t and every j with ext_flags[topk_idx[t][j]]
+ * != 0, w[t][j] * FFN_e(x[t]) from the host pool's record of (phys_layer, e),
+ * and writes partial[t] = their sum over j ascending (0 where there is none).
+ * Weights are decoded to fp32 row by row (every ft_wtype); x, the intermediate
+ * silu(G)*U and the accumulation are fp32.  Every pointer is host memory:
+ *   host_pool  [n_phys_layers*E][slot_bytes] records (the cache's pinned pool)
+ *   x          [T][hidden] of x_type;  topk_idx, topk_w  [T][k];
+ *   ext_flags  [n_experts] (ft_cache_step's external marks);  partial [T][hidden] fp32
+ * ---------------------------------------------------------------------- */
+typedef struct ft_cpu ft_cpu;
+typedef struct {
+  const void* host_pool;
+  uint64_t slot_bytes;
+  int wtype, hidden, inter, n_experts, phys_layer;
+  const void* x;
+  int x_type, T, k;
+  const int32_t* topk_idx;
+  const float* topk_w;
+  const int32_t* ext_flags;
+  float* partial;
+} ft_cpu_job;
+
+/* threads: worker threads besides the caller (0 = hardware threads - 1, at most 255). */
+int ft_cpu_create(int threads, ft_cpu** out);
+/* Waits for nothing: destroy only when no enqueued job can still run. */
+int ft_cpu_destroy(ft_cpu* c);
+/* Runs one job now, on the calling thread and the pool. */
+int ft_cpu_experts(ft_cpu* c, const ft_cpu_job* job);
+/* Enqueues one job as a host function on stream s (cudaLaunchHostFunc; under
+ * stream capture it becomes a host node of the graph, run at every replay).
+ * The job is copied into the handle and kept until ft_cpu_destroy; its
+ * pointers must stay valid for every run -- typically pinned buffers that
+ * copies on s fill before the node and drain after it.  A failed run records
+ * its status, which ft_cpu_status reads and clears. */
+int ft_cpu_experts_enqueue(ft_cpu* c, const ft_cpu_job* job, ft_cuda_stream s);
+int ft_cpu_status(ft_cpu* c);
 
 /* ------------------------------------------------------------------------
  * Placement-policy replay (host only) ([Review] §2.4, the ablation that

@@ -62,9 +62,9 @@ def test_launch_count_per_step():
 
     r = Run()
     r.b = {1: {"split": False}, 64: {"split": True}}
-    assert r.launches_per_step(1) == 40 * 9       # route x3, control, fill, gather + gate/up + down, combine
-    assert r.launches_per_step(64) == 40 * 12     # a second expert call in the split form
-    assert r.launches_per_pass() == 256 * 40 * (9 + 12)
+    assert r.launches_per_step(1) == 40 * 7       # fused route, control, fill, gather + gate/up + down, combine
+    assert r.launches_per_step(64) == 40 * 12     # route x3, a second expert call in the split form
+    assert r.launches_per_pass() == 256 * 40 * (7 + 12)
 
 
 def test_step_times_per_batch_exclude_the_reset_between_batches():

@@ -1,0 +1,69 @@
+"""The host-side expert executor against the fp64 oracle, on the CPU ([Review] §2.5).
+
+ft_cpu_experts evaluates the experts marked external from the host pool's
+records with a pool of CPU threads and writes the gate-weighted partial output
+per token.  The records here live in ordinary host memory (the executor reads
+any host memory), so these tests need no GPU.  Every weight format is checked
+on a second physical layer of the pool, with duplicate and absent experts.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from conftest import assert_close_layer, rel_fro
+from oracle import formats, moe
+
+
+@pytest.mark.parametrize("wtype,x_dtype", [(synth.W_F32, "f32"), (synth.W_BF16, "bf16"), (synth.W_FP8, "bf16"),
+                                           (synth.W_NVFP4, "bf16"), (synth.W_MXFP4, "f32")])
+def test_cpu_executor_matches_oracle(ftlib, wtype, x_dtype):
+    ft = ftlib
+    H, I, E, k, T = 256, 128, 8, 3, 6
+    cfg = synth.MoEConfig(f"cpu{wtype}", H, E, k, I, 2, wtype, x_dtype, seed=60 + wtype)
+    L = ft.ft_expert_layout_get(wtype, H, I)
+    S = int(L.bytes)
+    pool = torch.zeros(2 * E * S, dtype=torch.uint8)
+    for l in range(2):
+        for e in range(E):
+            ft.pack_expert(synth.expert_weights(cfg, l, e, "cpu"), wtype, L, pool[(l * E + e) * S:(l * E + e + 1) * S])
+    rng = np.random.default_rng(wtype)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    w = rng.random((T, k)).astype(np.float32)
+    ext = np.zeros(E, dtype=np.int32)
+    ext[[1, 4, 6]] = 1
+    idx[0] = [1, 4, 6]                        # a token with all its experts external
+    idx[1] = [0, 2, 3]                        # and one with none
+    x = synth.activations(cfg, T, tag=2)
+    part = torch.full((T, H), float("nan"))
+    cpu = ft.CpuExperts(threads=3)
+    tid, tw, te = torch.from_numpy(idx), torch.from_numpy(w), torch.from_numpy(ext)
+    job = cpu.job(pool.data_ptr(), S, wtype, H, I, E, 1, x, T, k, tid, tw, te, part)
+    cpu.run(job)
+    got = part.numpy()
+    src = moe.ExpertSource(lambda e: synth.expert_weights(cfg, 1, e, "cpu"), wtype)
+    ref = moe.moe_layer(formats.to_f64(x), idx, w.astype(np.float64), src, only=[1, 4, 6])
+    assert np.all(got[1] == 0.0)
+    assert_close_layer(got, ref)
+    assert rel_fro(got, ref) < 2e-5
+    # a second run on the same handle (scratch reused) gives the same bytes
+    part2 = torch.full((T, H), float("nan"))
+    cpu.run(cpu.job(pool.data_ptr(), S, wtype, H, I, E, 1, x, T, k, tid, tw, te, part2))
+    assert torch.equal(part, part2)
+    cpu.destroy()
+
+
+def test_cpu_executor_rejects_bad_jobs(ftlib):
+    ft = ftlib
+    cpu = ft.CpuExperts(threads=1)
+    x = torch.zeros(2, 256, dtype=torch.bfloat16)
+    i32 = torch.zeros(2, 2, dtype=torch.int32)
+    job = cpu.job(0, 1 << 20, ft.FT_W_BF16, 256, 128, 4, 0, x, 2, 2, i32, torch.zeros(2, 2),
+                  torch.zeros(4, dtype=torch.int32), torch.zeros(2, 256))
+    with pytest.raises(ft.FTError):           # no host pool
+        cpu.run(job)
+    job.host_pool = x.data_ptr()
+    job.inter = 100                           # not a multiple of 128
+    with pytest.raises(ft.FTError):
+        cpu.run(job)
+    cpu.destroy()

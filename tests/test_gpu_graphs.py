@@ -142,3 +142,77 @@ def test_captured_decode_step_with_resize_and_recapture(ft):
     assert ft.ft_get_device_error() == 0
     cache.destroy()
     pool.free()
+
+
+def test_captured_step_with_the_host_branch_keeps_the_layer_output(ft):
+    """The split with a real external share ([Review] §2.5, the exact merge; §2.6, the CPU
+    branch in the captured step): 30% of each wave's misses are evaluated by the host
+    expert executor from the pinned pool, as a host node of the graph, and their partial
+    output is added by the combine.  Every layer's output must equal the oracle's full
+    layer, whatever the split, and the cache must follow the simulator."""
+    cfg = synth.MoEConfig("hostbranch", 256, 32, 4, 128, 2, synth.W_BF16, "bf16", seed=17, zipf_s=1.1)
+    L, E, k, T = cfg.n_layers, cfg.n_experts, cfg.top_k, 8
+    pool = ft.ExpertPool(cfg, L)
+    pool.fill(DEV)
+    S = pool.S
+    cache = ft.Cache(L, E, L, 20, 20, S, pool.ptr, torch.empty(20 * S, dtype=torch.uint8, device=DEV))
+    sim = LRUSim(20, E)
+    lay = ft.MoELayer(cfg, T)
+    cpu = ft.CpuExperts(threads=4)
+    hb = ft.HostBranch(cfg, T, pool, cpu, DEV)
+    routers = [synth.router_weights(cfg, l, DEV) for l in range(L)]
+    src = [moe.ExpertSource(lambda e, l=l: synth.expert_weights(cfg, l, e, DEV), cfg.wtype) for l in range(L)]
+    x_buf = torch.empty(T, cfg.hidden, dtype=torch.bfloat16, device=DEV)
+    outs = torch.empty(L, T, cfg.hidden, dtype=torch.float32, device=DEV)
+    counts = torch.zeros(L, 4, 4, dtype=torch.int32, device=DEV)
+    fs = torch.cuda.Stream(device=DEV)
+    trace = synth.AR1Trace(cfg, T, DEV, tag=6)
+    ratio = 0.7
+
+    def decode_step():
+        for l in range(L):
+            lay.route(x_buf, *routers[l])
+            nw = cache.n_waves()
+            for w in range(nw):
+                after = (lambda l=l: hb.launch(lay, x_buf, l)) if w == nw - 1 else None
+                lay.cached_wave(x_buf, l, cache, S, ratio, w, counts[l, w], fill_stream=fs, after_control=after)
+            hb.join()
+            ft.ft_combine(lay.y[: T * k], lay.inv, lay.idx[:T], lay.w[:T], lay.ext, hb.P[:T], E, outs[l])
+
+    externals = 0
+
+    def check():
+        nonlocal externals
+        x64 = formats.to_f64(x_buf)
+        got = outs.cpu().numpy()
+        for l in range(L):
+            wr, b = routers[l]
+            idx, w = moe.route(moe.router_logits(x64, formats.to_f64(wr), formats.to_f64(b)), k)
+            events, _ = sim.step(l, idx.reshape(-1), ratio)
+            externals += sum(e[0] == "ext" for e in events)
+            ref = moe.moe_layer(x64, idx, w, src[l], act_round=formats.round_to_bf16)   # every expert
+            assert_close_layer(got[l], ref, fro=1e-2)
+        key, stamp, clock = cache.export()
+        sk, ss = sim.state()
+        assert key.tolist() == sk.tolist() and stamp.tolist() == ss.tolist()
+
+    x_buf.copy_(trace.next())
+    decode_step()                         # eager
+    torch.cuda.synchronize()
+    assert cpu.status() == 0
+    check()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        decode_step()
+    for _ in range(5):
+        x_buf.copy_(trace.next())
+        g.replay()
+        torch.cuda.synchronize()
+        assert cpu.status() == 0
+        check()
+    assert externals > 0
+    del g
+    assert ft.ft_get_device_error() == 0
+    cache.destroy()
+    cpu.destroy()
+    pool.free()

@@ -246,3 +246,57 @@ def test_bounded_wait_gives_up_and_reports(ft):
     idx, w = _i32((1, 2)), _f32((1, 2))
     ft.ft_route(z, 2, idx, w)
     assert idx.cpu().tolist() == [[1, 3]]
+
+
+# ---------------------------------------------------------------- fused routing (one cluster launch)
+
+@pytest.mark.parametrize("T,H,E,k,dt,zipf", [(1, 2048, 256, 8, "bf16", True), (4, 2048, 256, 8, "bf16", True),
+                                             (16, 2048, 256, 8, "bf16", False), (3, 4096, 256, 6, "bf16", True),
+                                             (9, 6144, 256, 8, "bf16", False), (5, 256, 16, 2, "f32", False),
+                                             (16, 512, 512, 16, "bf16", False), (7, 256, 40, 3, "f32", True),
+                                             (17, 2048, 256, 8, "bf16", True), (64, 2048, 256, 8, "bf16", True)])
+def test_route_fused_equals_the_three_kernels_and_the_oracle(ft, T, H, E, k, dt, zipf):
+    """ft_route_fused gives bit for bit the logits, routing and permutation of
+    ft_router_logits + ft_route + ft_permute (one cluster launch up to 16 tokens,
+    the three kernels above), and the oracle's routing and grouping of those logits."""
+    x = synth.normal((T, H), 1.0, 21 + T, DEV)
+    wr = synth.normal((E, H), 0.02, 22 + E, DEV)
+    if dt == "bf16":
+        x, wr = x.to(torch.bfloat16), wr.to(torch.bfloat16)
+    cfg = synth.MoEConfig("rf", H, E, k, 128, 1, synth.W_BF16, dt, seed=3, zipf_s=1.1 if zipf else 0.0)
+    b = synth.zipf_bias(cfg, 0).to(DEV)
+    outs = []
+    for fused in (True, False):
+        z, idx, w = _f32((T, E)), _i32((T, k)), _f32((T, k))
+        counts, offsets, perm, inv = _i32(E), _i32(E + 1), _i32(max(T * k, 1)), _i32(max(T * k, 1))
+        if fused:
+            ft.ft_route_fused(x, wr, b, k, z, idx, w, counts, offsets, perm, inv)
+        else:
+            ft.ft_router_logits(x, wr, b, z)
+            ft.ft_route(z, k, idx, w)
+            ft.ft_permute(idx, E, counts, offsets, perm, inv)
+        torch.cuda.synchronize()
+        outs.append([t.cpu().numpy() for t in (z, idx, w, counts, offsets, perm[: T * k], inv[: T * k])])
+    for a, c in zip(outs[0], outs[1]):
+        assert np.array_equal(a, c)
+    z, idx, w, counts, offsets, perm, inv = outs[0]
+    ref = moe.router_logits(formats.to_f64(x), formats.to_f64(wr), formats.to_f64(b))
+    assert np.abs(z - ref).max() <= 2e-5 * (1 + np.abs(ref).max())
+    ri, rw = moe.route(z.astype(np.float64), k)
+    assert np.array_equal(idx, ri)
+    assert np.abs(w - rw).max() <= 1e-6
+    rc, ro, rp, rinv = moe.permute(idx, E)
+    for got, want in ((counts, rc), (offsets, ro), (perm, rp), (inv, rinv)):
+        assert np.array_equal(got, want)
+    assert ft.ft_get_device_error() == 0
+
+
+def test_route_fused_empty_batch(ft):
+    E, k = 256, 8
+    counts, offsets = _i32(E), _i32(E + 1)
+    x = torch.zeros(0, 2048, dtype=torch.bfloat16, device=DEV)
+    wr = torch.zeros(E, 2048, dtype=torch.bfloat16, device=DEV)
+    one = _i32(1)
+    ft.ft_route_fused(x, wr, None, k, _f32((1, E)), _i32((1, k)), _f32((1, k)), counts, offsets, one, one)
+    torch.cuda.synchronize()
+    assert (counts.cpu().numpy() == 0).all() and (offsets.cpu().numpy() == 0).all()
