@@ -781,16 +781,19 @@ def _oracle_eval(cfg, prepared):
         moe.moe_layer(x64, idx, w, moe.ExpertSource(lambda e: comps[e], cfg.wtype))
 
 
-def _oracle_worker(rank, n_workers, cfg_name, items, barrier, more):
-    """One process of the CPU baseline: one BLAS thread, its share of the samples,
-    prepared before the first barrier, then evaluated once per round."""
-    from threadpoolctl import threadpool_limits
-    threadpool_limits(1)
-    torch.set_num_threads(1)
-    cfg = synth.CONFIGS[cfg_name]
-    mine = items[rank::n_workers]
-    prepared = _oracle_items(cfg, mine) if mine else []
-    barrier.wait()
+def _oracle_worker(rank, n_workers, cfg_name, items, barrier, more, ready):
+    """One process of the CPU baseline: one BLAS thread (set in the environment before
+    numpy loaded), its share of the samples, prepared before it reports ready, then
+    evaluated once per round."""
+    try:
+        torch.set_num_threads(1)
+        cfg = synth.CONFIGS[cfg_name]
+        mine = items[rank::n_workers]
+        prepared = _oracle_items(cfg, mine) if mine else []
+    except BaseException as e:          # report, so that the parent stops waiting
+        ready.put(("error", rank, repr(e)))
+        raise
+    ready.put(("ready", rank, ""))
     while True:
         barrier.wait()                  # go
         if not more.value:
@@ -804,8 +807,11 @@ class OraclePool:
     ``max_workers``), each with one BLAS thread, evaluating its share of
     (token, layer) samples once per round.  Rounds are timed on the wall clock."""
 
-    def __init__(self, cfg, n_tokens, max_workers=32):
+    THREAD_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS")
+
+    def __init__(self, cfg, n_tokens, max_workers=32, prepare_timeout_s=600.0):
         import multiprocessing as mp
+        import queue
         self.cfg = cfg
         self.cores = max(1, min(len(os.sched_getaffinity(0)), max_workers))
         self.items = [(t, l) for t in range(n_tokens) for l in range(cfg.n_layers)]
@@ -815,17 +821,47 @@ class OraclePool:
         self.n = n
         self.barrier = ctx.Barrier(n + 1)
         self.more = ctx.Value("i", 1)
-        self.procs = [ctx.Process(target=_oracle_worker, args=(r, n, cfg.name, self.items, self.barrier, self.more),
-                                  daemon=True) for r in range(n)]
+        ready = ctx.Queue()
+        self.procs = [ctx.Process(target=_oracle_worker, args=(r, n, cfg.name, self.items, self.barrier, self.more,
+                                                               ready), daemon=True) for r in range(n)]
+        saved = {v: os.environ.get(v) for v in self.THREAD_VARS}
+        try:
+            for v in self.THREAD_VARS:          # the children load numpy with one BLAS thread each
+                os.environ[v] = "1"
+            for p in self.procs:
+                p.start()
+        finally:
+            for v, old in saved.items():
+                if old is None:
+                    os.environ.pop(v, None)
+                else:
+                    os.environ[v] = old
+        got, t0 = 0, time.perf_counter()
+        while got < n:
+            try:
+                kind, rank, msg = ready.get(timeout=2.0)
+            except queue.Empty:
+                dead = [p.exitcode for p in self.procs if p.exitcode is not None]
+                if dead or time.perf_counter() - t0 > prepare_timeout_s:
+                    self._kill()
+                    raise RuntimeError(f"oracle workers failed to start (exit codes {dead})")
+                continue
+            if kind == "error":
+                self._kill()
+                raise RuntimeError(f"oracle worker {rank} failed: {msg}")
+            got += 1
+
+    def _kill(self):
         for p in self.procs:
-            p.start()
-        self.barrier.wait(timeout=900)  # every worker prepared its samples
+            if p.is_alive():
+                p.kill()
+            p.join(timeout=10)
 
     def round(self) -> float:
         """Evaluates every sample once; wall seconds."""
         t0 = time.perf_counter()
-        self.barrier.wait(timeout=900)
-        self.barrier.wait(timeout=900)
+        self.barrier.wait(timeout=600)
+        self.barrier.wait(timeout=600)
         return time.perf_counter() - t0
 
     def close(self):
@@ -836,6 +872,7 @@ class OraclePool:
             pass
         for p in self.procs:
             p.join(timeout=30)
+        self._kill()
 
     def sample(self) -> str:
         return (f"{self.n_tokens} T=1 decode token(s) of the AR(1) trace through all {self.cfg.n_layers} layers "
@@ -844,8 +881,13 @@ class OraclePool:
 
 
 def oracle_baseline(cfg, n_tokens=2, reps=None, budget_s=12.0):
-    """cpu_baseline: rounds of the oracle pool until about ``budget_s`` seconds of wall time."""
-    op = OraclePool(cfg, n_tokens)
+    """cpu_baseline: rounds of the oracle pool until about ``budget_s`` seconds of wall time
+    (None, with the reason logged, if the pool cannot run)."""
+    try:
+        op = OraclePool(cfg, n_tokens)
+    except RuntimeError as e:
+        log(f"cpu baseline skipped: {e}")
+        return None
     try:
         t = [op.round()]
         n = reps or max(1, int(budget_s / max(t[0], 1e-3)))

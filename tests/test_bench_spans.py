@@ -84,3 +84,13 @@ def test_oracle_pool_times_rounds_on_spawned_processes():
     assert op.n == min(2, len(os.sched_getaffinity(0))) and all(x > 0 for x in t)
     assert "3 T=1 decode token(s)" in op.sample()
     assert all(not p.is_alive() for p in op.procs)
+
+
+def test_oracle_pool_reports_a_failing_worker_quickly():
+    import time
+    import pytest
+    cfg = bench.synth.MoEConfig("not_a_registered_config", 256, 16, 2, 128, 1, bench.synth.W_F32, "f32")
+    t0 = time.perf_counter()
+    with pytest.raises(RuntimeError):
+        bench.OraclePool(cfg, n_tokens=1, max_workers=2)
+    assert time.perf_counter() - t0 < 120
