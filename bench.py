@@ -70,6 +70,8 @@ def parse():
     p.add_argument("--cpu-budget-s", type=float, default=12.0, help="wall seconds of timed CPU baseline rounds")
     p.add_argument("--no-pool-setup", action="store_true", help="skip the pin-first vs read-then-pin setup leg")
     p.add_argument("--no-placement", action="store_true", help="skip the placement-policy replay")
+    p.add_argument("--timed-spans", action="store_true",
+                   help="record the per-kernel timing events inside the timed passes (instead of one extra pass)")
     p.add_argument("--setup-layers", type=int, default=2, help="layers of the pool file in the setup leg")
     p.add_argument("--mixed-decode-steps", type=int, default=512)
     p.add_argument("--no-e2e", action="store_true")
@@ -252,7 +254,7 @@ class DecodeRun:
                 d["x_host"].copy_(d["xs"].cpu())
                 d["out_host"] = torch.empty(L, T, H, dtype=torch.float32).pin_memory()
             self.b[T] = d
-        self.graphs = {}
+        self.graphs, self.igraphs = {}, {}
 
     def launches_per_step(self, T) -> int:
         # routing (one fused launch, or router_logits + route + permute), (control, fill, expert
@@ -305,29 +307,33 @@ class DecodeRun:
             ft.ft_combine(lay.y[: T * k], lay.inv, lay.idx[:T], lay.w[:T], lay.ext, None, cfg.n_experts,
                           d["outs"][l])
 
-    def capture(self, timed=True):
+    def capture(self, instrumented=False):
         """One eager step per batch size (kernel attributes and modules set up outside capture),
-        a cold reset, then one graph per (T, step).  With ``timed`` every graph also records
-        its timing events (event-record nodes), kept in its EventLog."""
+        a cold reset, then one graph per (T, step).  ``instrumented`` graphs also record timing
+        events around the cache step and the expert calls (event-record nodes, kept in the
+        graph's EventLog); they go to a second set, since an event node between two launches
+        stops the second from launching early, which the plain graphs keep."""
         for T in self.batches:
             self.step(T, 0)
         torch.cuda.synchronize()
         self.cache.reset()
+        dst = self.igraphs if instrumented else self.graphs
         for T in self.batches:
             for t in range(self.n_steps):
                 g = torch.cuda.CUDAGraph()
-                ev = EventLog(external=True) if timed else None
+                ev = EventLog(external=True) if instrumented else None
                 with torch.cuda.graph(g):
                     self.step(T, t, ev)
-                self.graphs[(T, t)] = (g, ev)
+                dst[(T, t)] = (g, ev)
         torch.cuda.synchronize()
 
-    def run_pass(self, marks=None, e2e=False):
+    def run_pass(self, marks=None, e2e=False, instrumented=False):
         """The whole trace once: per batch size, a cold reset and every step's graph.
 
         ``marks`` (a list) receives (T, t, event) before each step and (T, -1,
         event) after each batch size's last step.  With ``e2e`` each step's input is first copied from
         pinned host memory and every layer's output copied back to it."""
+        graphs = self.igraphs if instrumented else self.graphs
         for T in self.batches:
             d = self.b[T]
             self.cache.reset()                      # cold start (synchronises)
@@ -338,7 +344,7 @@ class DecodeRun:
                     e = torch.cuda.Event(enable_timing=True)
                     e.record()
                     marks.append((T, t, e))
-                self.graphs[(T, t)][0].replay()
+                graphs[(T, t)][0].replay()
                 if e2e:
                     d["out_host"].copy_(d["outs"], non_blocking=True)
             if marks is not None:
@@ -351,10 +357,12 @@ class DecodeRun:
         return self.b[T]["hist"].cpu().numpy()
 
     def logs(self, T, t0=0):
-        return [self.graphs[(T, t)][1] for t in range(t0, self.n_steps)]
+        """EventLogs of the instrumented graphs (their last replay)."""
+        return [self.igraphs[(T, t)][1] for t in range(t0, self.n_steps)]
 
     def release(self):
         self.graphs.clear()
+        self.igraphs.clear()
         torch.cuda.synchronize()
         self.cache.destroy()
 
@@ -617,6 +625,9 @@ def nvfp4_leg(ft, dev, peaks, link, batches, steps, split_min=0):
     run.capture()
     marks = []
     run.run_pass(marks)
+    torch.cuda.synchronize()
+    run.capture(instrumented=True)
+    run.run_pass(instrumented=True)
     torch.cuda.synchronize()
     rep = decode_report(run, marks, cfg, peaks, link, payload, steady_from=min(8, steps - 1))
     run.release()
@@ -1211,7 +1222,9 @@ def main():
     tokens_per_pass = n_trace * sum(batches)
     log(f"pool of {n_phys} layers filled in {t_fill:.1f} s; link {link:.1f} GB/s")
     t0 = time.perf_counter()
-    run.capture()
+    run.capture(instrumented=args.timed_spans)
+    if args.timed_spans:
+        run.graphs = run.igraphs
     log(f"{len(run.graphs)} step graphs captured in {time.perf_counter() - t0:.1f} s")
 
     # warm-up passes (each the whole trace from cold caches); the first two must make
@@ -1243,6 +1256,17 @@ def main():
     tokens = sum_over_ranks(world, tokens_per_pass * args.steps)
     value = tokens / (ms_max * 1e-3)
     log(f"timed region: {ms:.1f} ms ({args.steps} passes)")
+    # per-kernel spans: the same trace once more through graphs that also hold timing events
+    spans_pass_ms = None
+    if not args.timed_spans:
+        run.capture(instrumented=True)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        run.run_pass(instrumented=True)
+        s1.record()
+        torch.cuda.synchronize()
+        spans_pass_ms = s0.elapsed_time(s1)
+        log(f"instrumented pass: {spans_pass_ms:.1f} ms")
     payload = int(lay_bytes.payload_bytes)
     rep = decode_report(run, marks, cfg, peaks, link, payload, args.steady_from)
 
@@ -1329,6 +1353,11 @@ def main():
             "steady_state": rep["steady_state"],
             "per_batch": rep["per_batch"],
             "deterministic_passes": deterministic,
+            "kernel_spans": ("CUDA events recorded inside the timed passes' graphs" if args.timed_spans else
+                             "CUDA events of one more pass of the same trace, from a cold cache, through graphs "
+                             "that also hold event-record nodes (which keep the next launch from starting early, "
+                             f"so the timed graphs carry none); that pass took {spans_pass_ms:.1f} ms against "
+                             f"{ms_max / args.steps:.1f} ms per timed pass"),
             "roofline": rep["roofline"],
             "roofline_experts": rep["roofline_experts"],
             "roofline_fill": rep["roofline_fill"],

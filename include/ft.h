@@ -403,7 +403,10 @@ int ft_expert_grouped(const void* x, int x_type, int T, int k, int hidden, int i
  * dequantised in registers, x and the intermediate silu(G)*U in fp32.  Its
  * results therefore differ from ft_expert_grouped's for bf16, NVFP4 and MXFP4
  * weights (which run on the tensor cores with a bf16 intermediate) within the
- * tolerance of that rounding, not bit for bit, and it is slower for them.
+ * tolerance of that rounding, not bit for bit, and it is slower for them
+ * except at one token (measured on B300, bf16 weights, H=2048, I=512, top-8:
+ * 0.019 against 0.026 ms at one token, 0.065 against 0.041 ms at 4 tokens,
+ * 0.605 against 0.075 ms at 64 tokens).
  *
  * The fp32 intermediate lives in one fixed device array inside the library,
  * FT_NOALLOC_MAX_ELEMS floats (4 MiB), which every GPU that loads the library
