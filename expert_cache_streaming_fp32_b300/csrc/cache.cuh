@@ -216,6 +216,7 @@ cache_control_kernel(CacheDev d, int layer, const int32_t* __restrict__ counts, 
     d.stats[4] += (unsigned long long)q * d.S;
     if (step_counts) { step_counts[0] = nW; step_counts[1] = nW - m; step_counts[2] = q; step_counts[3] = m - q; }
   }
+  pdl_end();
 }
 
 // Copies the filled experts host pool -> slots: one fixed-shape launch over a
@@ -259,12 +260,14 @@ cache_fill_kernel(const uint8_t* __restrict__ host, uint8_t* __restrict__ pool, 
       }
     }
   }
+  pdl_end();
 }
 
 __global__ void set_buffer_slots_kernel(int32_t* slot_of, int E, int base) {
   pdl_begin();
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e < E) slot_of[e] = base + e;
+  pdl_end();
 }
 
 static CacheDev cache_dev(const ft_cache* c) {

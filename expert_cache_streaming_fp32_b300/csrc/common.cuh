@@ -47,14 +47,16 @@ __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_derr, 0, c
 
 // ------------------------------------------------------------------ dependent launches
 // Every kernel of the library is launched with programmatic stream
-// serialization: it may start while the kernel before it on the stream is
-// still finishing, runs only set-up work that touches no global memory, and
-// then waits (griddepcontrol.wait) until that kernel has completed and its
-// memory is visible.  Right after the wait it lets the next kernel launch.
-__device__ __forceinline__ void pdl_begin() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
+// serialization.  It runs its set-up that touches no global memory (barrier
+// init, TMEM allocation, tensor-map prefetch), then waits (griddepcontrol.wait)
+// until the kernel before it on the stream has completed and its memory is
+// visible.  It lets the next kernel launch (griddepcontrol.launch_dependents)
+// only when its own work is done: a dependent launched earlier would hold SM
+// slots and shared memory while it waits, which the rest of a multi-wave grid
+// (or the other kernels of a split step) needs.
+__device__ __forceinline__ void pdl_begin() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_end() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 template <typename... KArgs, typename... Args>
 static inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,

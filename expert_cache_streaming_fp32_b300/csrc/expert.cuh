@@ -375,6 +375,7 @@ gateup_kernel(ExpertArgs a) {
     }
     __syncthreads();
   }
+  pdl_end();
 }
 
 // ------------------------------------------------------------------ down
@@ -483,6 +484,7 @@ down_kernel(ExpertArgs a) {
     }
     __syncthreads();
   }
+  pdl_end();
 }
 
 // ------------------------------------------------------------------ layout

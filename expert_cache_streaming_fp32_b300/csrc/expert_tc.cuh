@@ -592,6 +592,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
+  pdl_end();
 }
 
 // ------------------------------------------------------------------ gather
@@ -626,6 +627,7 @@ gather_rows_kernel(const XT* __restrict__ x, const int32_t* __restrict__ perm, i
     }
     reinterpret_cast<uint4*>(xp + (size_t)p * H)[v] = o;
   }
+  pdl_end();
 }
 
 }  // namespace tc

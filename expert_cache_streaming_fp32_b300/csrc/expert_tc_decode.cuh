@@ -423,6 +423,7 @@ skinny_gemm_kernel(const __grid_constant__ CUtensorMap map_w0, const __grid_cons
     tc_fence_after();
     tmem_dealloc(tmem_base, SK_TMEM_COLS);
   }
+  pdl_end();
 }
 
 }  // namespace tc

@@ -109,6 +109,7 @@ router_logits_kernel(const XT* __restrict__ x, const XT* __restrict__ wr, const 
   __syncthreads();
   logits_of_rows<XT, RT>(xs, wr, bias, t0, nrows, H, E, blockIdx.x * RL_WARPS + (threadIdx.x >> 5),
                          gridDim.x * RL_WARPS, z);
+  pdl_end();
 }
 
 // ====================================================================== top-k gating
@@ -192,6 +193,7 @@ route_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __r
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
   route_token<PER_LANE>(logits + (size_t)t * E, E, k, idx_out + (size_t)t * k, w_out + (size_t)t * k);
+  pdl_end();
 }
 
 // ====================================================================== permutation
@@ -294,6 +296,7 @@ permute_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __restric
     for (int i = tid; i < PM_WARPS * E; i += PM_THREADS) wc[i] = 0;
     __syncthreads();
   }
+  pdl_end();
 }
 
 // ====================================================================== fused routing (decode batches)
@@ -403,6 +406,7 @@ route_fused_kernel(const XT* __restrict__ x, const XT* __restrict__ wr, const fl
     perm[pos] = a;
     inv[a] = pos;
   }
+  pdl_end();
 }
 
 // ====================================================================== combine
@@ -456,6 +460,7 @@ combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv, con
     acc.x += p.x; acc.y += p.y; acc.z += p.z; acc.w += p.w;
   }
   reinterpret_cast<float4*>(out + (size_t)t * H)[h4] = acc;
+  pdl_end();
 }
 
 }  // namespace ft

@@ -99,6 +99,7 @@ __global__ void bounded_wait_probe_kernel(uint64_t limit_ns, int* result) {
   }
   __syncthreads();
   if (threadIdx.x == 0) *result = mbar_wait(smem_u32(&bar), 0, &abort_flag, limit_ns) ? 1 : 0;
+  pdl_end();
 }
 
 // ------------------------------------------------------------------ TMA
