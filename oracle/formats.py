@@ -145,3 +145,80 @@ def dequant(component: dict, wtype: int) -> np.ndarray:
     if wtype == 4:
         return dequant_mxfp4(np_(component["codes"]), np_(component["scales"]))
     raise ValueError(wtype)
+
+
+# ---------------------------------------------------------------- activation quantisation for FP4 tensor cores
+# When the expert weights are NVFP4 or MXFP4, the block-scaled FP4 MMA of the
+# tensor cores needs the other operand -- the token rows, and the intermediate
+# silu(G) * U before the down product -- in the same format.  The rule (a
+# reading of this build: the pages name the weight formats, not how activations
+# meet them) quantises each block of consecutive K elements on its own, in fp32
+# arithmetic, and the oracle evaluates the layer on the quantised values:
+#
+#   NVFP4 (blocks of 16):  s = e4m3(amax / 6), rounded to nearest even and
+#                          saturated at 448 (tensor scale 1);
+#                          q = e2m1(v / s), nearest even, saturated at +-6;
+#                          an all-zero block (s = 0) stays zero.
+#   MXFP4 (blocks of 32):  s = 2^(floor(log2 amax) - 2) as an E8M0 byte
+#                          (OCP MX v1.0 §6.3), clamped to 2^-127 .. 2^127;
+#                          q = e2m1(v / s), nearest even, saturated at +-6.
+# The value used is q * s.
+
+E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def e2m1_round(v: np.ndarray) -> np.ndarray:
+    """Nearest e2m1 value of each element (ties to the code with an even mantissa bit), saturated at +-6."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.minimum(np.abs(v), 6.0)
+    # distances to every grid point; ties go to the even code index (mantissa bit 0)
+    d = np.abs(a[..., None] - E2M1_GRID)
+    best = d.min(axis=-1, keepdims=True)
+    cand = d == best
+    even = cand & (np.arange(8) % 2 == 0)
+    idx = np.where(even.any(axis=-1), even.argmax(axis=-1), cand.argmax(axis=-1))
+    return np.sign(v) * E2M1_GRID[idx]
+
+
+def e4m3_round(v: np.ndarray) -> np.ndarray:
+    """Nearest e4m3 ("fn") value of non-negative fp32 numbers, ties to even, saturated at 448."""
+    v = np.asarray(v, dtype=np.float64)
+    vals = E4M3_TABLE[:127]                          # the non-negative finite codes 0x00 .. 0x7E, ascending
+    a = np.minimum(v, 448.0)
+    hi = np.searchsorted(vals, a, side="left")       # first value >= a
+    hi = np.minimum(hi, len(vals) - 1)
+    lo = np.maximum(hi - 1, 0)
+    dlo, dhi = a - vals[lo], vals[hi] - a
+    take_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0))
+    out = np.where(a == vals[hi], vals[hi], np.where(take_hi, vals[hi], vals[lo]))
+    return out
+
+
+def quant_act_nvfp4(v: np.ndarray) -> np.ndarray:
+    """Rows [..., K] (K a multiple of 16) quantised by the NVFP4 activation rule, as fp64 values."""
+    v32 = np.asarray(v, dtype=np.float32)
+    shp = v32.shape
+    b = v32.reshape(-1, 16)
+    amax = np.abs(b).max(axis=1)
+    s = e4m3_round((amax / np.float32(6.0)).astype(np.float32))
+    s32 = s.astype(np.float32)
+    safe = np.where(s32 > 0, s32, np.float32(1.0))
+    q = e2m1_round((b / safe[:, None]).astype(np.float32))
+    q = np.where(s32[:, None] > 0, q, 0.0)
+    return (q * s[:, None]).reshape(shp)
+
+
+def quant_act_mxfp4(v: np.ndarray) -> np.ndarray:
+    """Rows [..., K] (K a multiple of 32) quantised by the MXFP4 activation rule, as fp64 values."""
+    v32 = np.asarray(v, dtype=np.float32)
+    shp = v32.shape
+    b = v32.reshape(-1, 32).astype(np.float64)
+    amax = np.abs(b).max(axis=1)
+    e = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 2.0, -127.0)
+    # log2 of an exact power of two is exact; guard the floor against representation error
+    e = np.where(2.0 ** (e + 2) > amax, e - 1, e)
+    e = np.where(2.0 ** (e + 3) <= amax, e + 1, e)
+    e = np.clip(e, -127.0, 127.0)
+    s = 2.0 ** e
+    q = e2m1_round(b / s[:, None])
+    return (q * s[:, None]).reshape(shp)

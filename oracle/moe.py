@@ -78,13 +78,17 @@ def silu(g: np.ndarray) -> np.ndarray:
 
 
 def expert_ffn(X: np.ndarray, gate: np.ndarray, up: np.ndarray, down: np.ndarray,
-               act_round: Optional[Callable[[np.ndarray], np.ndarray]] = None) -> np.ndarray:
+               act_round: Optional[Callable[[np.ndarray], np.ndarray]] = None,
+               x_round: Optional[Callable[[np.ndarray], np.ndarray]] = None) -> np.ndarray:
     """SwiGLU expert on rows X [m, H]: Y = (silu(X gate^T) * (X up^T)) down^T, fp64.
 
-    ``act_round`` applies the activation rounding the evaluated kernel declares
-    for the intermediate A = silu(G) * U (None: A is not rounded).
+    ``x_round`` and ``act_round`` apply the rounding the evaluated kernel
+    declares for its token rows X and for the intermediate A = silu(G) * U
+    (None: not rounded), e.g. the FP4 activation rules of ``formats``.
     """
     X = np.asarray(X, np.float64)
+    if x_round is not None:
+        X = x_round(X)
     G = X @ gate.T
     U = X @ up.T
     A = silu(G) * U
@@ -122,7 +126,7 @@ def combine(Y: np.ndarray, inv: np.ndarray, w: np.ndarray, k: int,
 
 
 def moe_layer(x: np.ndarray, idx: np.ndarray, w: np.ndarray, experts: Callable[[int], tuple],
-              act_round=None, only: Optional[Iterable[int]] = None) -> np.ndarray:
+              act_round=None, only: Optional[Iterable[int]] = None, x_round=None) -> np.ndarray:
     """The layer output for given routing, token by token.
 
     out[t] = sum_j w[t,j] FFN_{idx[t,j]}(x[t]).  With ``only`` given, the sum is
@@ -139,7 +143,7 @@ def moe_layer(x: np.ndarray, idx: np.ndarray, w: np.ndarray, experts: Callable[[
             if keep is not None and e not in keep:
                 continue
             g, u, d = experts(e)
-            out[t] += w[t, j] * expert_ffn(x[t:t + 1], g, u, d, act_round)[0]
+            out[t] += w[t, j] * expert_ffn(x[t:t + 1], g, u, d, act_round, x_round)[0]
     return out
 
 
