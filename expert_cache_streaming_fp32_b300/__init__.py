@@ -28,6 +28,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 FT_OK, FT_EINVAL, FT_ENOMEM, FT_ECUDA, FT_ETIMEOUT, FT_ESTATE, FT_EUNSUPPORTED, FT_EDEVICE, FT_EIO = range(9)
 FT_INJECT_DEVICE_ALLOC, FT_INJECT_HOST_PIN, FT_INJECT_STREAM_EVENT = 1, 2, 3
 FT_PLACE_GLOBAL_LRU, FT_PLACE_PREFILL_HOT, FT_PLACE_STATIC_SPLIT = 0, 1, 2
+FT_FP4_BLOCK_SCALED, FT_FP4_EXPAND_BF16 = 0, 1
 FT_W_F32, FT_W_BF16, FT_W_FP8E4M3, FT_W_NVFP4, FT_W_MXFP4 = range(5)
 FT_X_F32, FT_X_BF16 = 0, 1
 
@@ -41,6 +42,7 @@ EXPORTED = [
     "ft_cache_set_fill_blocks", "ft_debug_inject_failure", "ft_debug_live_resources", "ft_pool_read",
     "ft_host_register", "ft_host_unregister", "ft_cache_reset", "ft_placement_replay", "ft_cpu_create",
     "ft_cpu_destroy", "ft_cpu_experts", "ft_cpu_experts_enqueue", "ft_cpu_status", "ft_route_fused",
+    "ft_expert_set_fp4_path",
 ]
 FT_NOALLOC_MAX_ELEMS = 1 << 20
 FT_TC_WIDE_ASSIGNMENTS = 2048
@@ -92,6 +94,7 @@ _sigs = {
     "ft_router_logits": (_I, [_P, _I, _P, _P, _I, _I, _I, _P, _P]),
     "ft_route": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "ft_permute": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "ft_expert_set_fp4_path": (_I, [_I]),
     "ft_route_fused": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "ft_cache_create": (_I, [ctypes.POINTER(CacheConfig), ctypes.POINTER(_P)]),
     "ft_cache_destroy": (_I, [_P]),
@@ -256,6 +259,11 @@ def ft_route_fused(x, w_router, bias, k, logits, topk_idx, topk_w, counts, offse
     _check("ft_route_fused", _lib.ft_route_fused(
         _ptr(x), _xtype(x), _ptr(w_router), _ptr(bias), T, H, E, k, _ptr(logits), _ptr(topk_idx), _ptr(topk_w),
         _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv), _stream(stream)))
+
+
+def ft_expert_set_fp4_path(path: int):
+    """FT_FP4_BLOCK_SCALED (block-scaled FP4 MMA, FP4 activations) or FT_FP4_EXPAND_BF16 (exact expansion)."""
+    _check("ft_expert_set_fp4_path", _lib.ft_expert_set_fp4_path(path))
 
 
 def ft_expert_grouped_workspace(T, k, hidden, inter) -> int:

@@ -6,6 +6,7 @@
 #include "expert.cuh"
 #include "expert_tc.cuh"
 #include "expert_tc_decode.cuh"
+#include "expert_bs_decode.cuh"
 #include "cache.cuh"
 #include "stream.cuh"
 #include "placement.cuh"
@@ -504,6 +505,89 @@ int launch_skinny_wt(const ExpertArgs& ea, const ft_expert_layout& L, const TcWo
   return FT_OK;
 }
 
+// Packed e2m1 bytes with the 128-byte swizzle, box {128 bytes = 256 elements, rows}: the
+// operand tile of the block-scaled MMA.  3-D over the slot pool: [K/2 bytes][rows][slot].
+int make_map_fp4_sw(CUtensorMap* m, const void* base, int K, int rows, int slots, uint64_t S, uint32_t box_rows) {
+  const uint64_t d[3] = {(uint64_t)K / 2, (uint64_t)rows, (uint64_t)slots}, st[2] = {(uint64_t)K / 2, S};
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 3, d, st, 128, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Splits of the block-scaled kernels: as sk_splits, with whole 256-element stages.
+static int bs_splits(long long Tk, int n_mt, int K) {
+  const long long est = std::min<long long>(Tk, 256) * n_mt;
+  int ks = 1;
+  while (ks < tc::SK_MAX_SPLITS && est * ks * 2 <= kSplitTargetTiles && (K / (ks * 2)) % tc::BS_BK == 0 &&
+         K / (ks * 2) >= 2 * tc::BS_BK)
+    ks *= 2;
+  return ks;
+}
+
+std::atomic<int> g_fp4_path{FT_FP4_BLOCK_SCALED};
+
+// Small batches of NVFP4 / MXFP4 weights on the block-scaled FP4 MMA: the token rows and the
+// intermediate are quantised to the weights' format.  H and I multiples of 256.
+template <int WT>
+int launch_bs_skinny(const ExpertArgs& ea, const ft_expert_layout& L, const TcWorkspace& w, uint8_t* ws,
+                     cudaStream_t st) {
+  constexpr int BLK = WT == FT_W_NVFP4 ? 16 : 32;
+  const long long Tk = (long long)ea.T * ea.k;
+  const int H = ea.H, I = ea.I;
+  uint8_t* xq = ws;
+  uint8_t* xs = ws + align256((size_t)Tk * H / 2);
+  uint8_t* aq = ws + w.off_aint;
+  uint8_t* as = aq + align256((size_t)Tk * I / 2);
+  int32_t* counters = reinterpret_cast<int32_t*>(ws + w.off_counters);
+  const int mt_gu = tc::sk_m_tiles(tc::GATEUP, H, I), mt_dn = tc::sk_m_tiles(tc::DOWN, H, I);
+  const int ks_gu = bs_splits(Tk, mt_gu, H), ks_dn = bs_splits(Tk, mt_dn, I);
+  {
+    const long long blocks = Tk * (H / BLK);
+    const int grid = (int)std::max<long long>(1, std::min<long long>((blocks + 255) / 256, 8ll * sms()));
+    const int n_zero = (int)(w.g_gu + w.g_dn);
+    if (ea.x_type == FT_X_BF16)
+      FT_LAUNCH((tc::quant_rows_kernel<__nv_bfloat16, WT>), grid, 256, 0, st, (const __nv_bfloat16*)ea.x, ea.perm,
+                ea.T, ea.k, H, (int)Tk, xq, xs, counters, n_zero);
+    else
+      FT_LAUNCH((tc::quant_rows_kernel<float, WT>), grid, 256, 0, st, (const float*)ea.x, ea.perm, ea.T, ea.k, H,
+                (int)Tk, xq, xs, counters, n_zero);
+  }
+  const int nb_box = (int)std::min<long long>(tc::SK_NB, (Tk + 15) / 16 * 16);
+  CUtensorMap mg, mu, md, mx, ma;
+  {
+    const uint8_t* pool = ea.pool;
+    int r = make_map_fp4_sw(&mg, pool + L.off_val[0], H, I, ea.pool_slots, ea.S, 64);
+    if (!r) r = make_map_fp4_sw(&mu, pool + L.off_val[1], H, I, ea.pool_slots, ea.S, 64);
+    if (!r) r = make_map_fp4_sw(&md, pool + L.off_val[2], I, H, ea.pool_slots, ea.S, tc::SK_MR);
+    const uint64_t dx[2] = {(uint64_t)H / 2, (uint64_t)Tk}, sx[1] = {(uint64_t)H / 2};
+    const uint64_t da[2] = {(uint64_t)I / 2, (uint64_t)Tk}, sa[1] = {(uint64_t)I / 2};
+    if (!r) r = make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, 2, dx, sx, 128, nb_box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!r) r = make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq, 2, da, sa, 128, nb_box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (r) return r;
+  }
+  tc::BsArgs a;
+  a.T = ea.T; a.k = ea.k; a.H = H; a.I = I; a.E = ea.E; a.pool_slots = ea.pool_slots;
+  a.nb_box = nb_box;
+  a.offsets = ea.offsets; a.slot_of = ea.slot_of;
+  a.pool = ea.pool; a.S = ea.S;
+  for (int m = 0; m < 3; ++m) a.off_scale[m] = L.off_scale[m];
+  a.off_gscale = L.off_gscale;
+  a.Aq = aq; a.As = as; a.y = ea.y;
+  a.part = reinterpret_cast<float*>(ws + w.off_part);
+  const size_t smem = tc::bs_smem_bytes(ea.E);
+  auto kg = tc::bs_skinny_kernel<tc::GATEUP, WT>;
+  auto kd = tc::bs_skinny_kernel<tc::DOWN, WT>;
+  if (int s = set_smem(kg, smem)) return s;
+  if (int s = set_smem(kd, smem)) return s;
+  a.KS = ks_gu;
+  a.bscale = xs;
+  a.counters = counters;
+  FT_LAUNCH(kg, sms(), tc::BS_THREADS, smem, st, mg, mu, mx, a);
+  a.KS = ks_dn;
+  a.bscale = as;
+  a.counters = counters + w.g_gu;
+  FT_LAUNCH(kd, sms(), tc::BS_THREADS, smem, st, md, md, ma, a);
+  return FT_OK;
+}
+
 int launch_expert_skinny(int wtype, const ExpertArgs& ea, const ft_expert_layout& L, const TcWorkspace& w,
                          uint8_t* ws, cudaStream_t st) {
   switch (wtype) {
@@ -522,6 +606,11 @@ int launch_expert_tc(int wtype, const ExpertArgs& ea, const ft_expert_layout& L,
   __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(ws);
   __nv_bfloat16* aint = reinterpret_cast<__nv_bfloat16*>(ws + w.off_aint);
   const bool skinny = Tk < FT_TC_WIDE_ASSIGNMENTS;
+  // small batches of FP4 weights: the block-scaled FP4 MMA (unless the exact expansion is asked for)
+  if (skinny && tc::is_fp4(wtype) && H % tc::BS_BK == 0 && I % tc::BS_BK == 0 &&
+      g_fp4_path.load() == FT_FP4_BLOCK_SCALED)
+    return wtype == FT_W_NVFP4 ? launch_bs_skinny<FT_W_NVFP4>(ea, L, w, ws, st)
+                               : launch_bs_skinny<FT_W_MXFP4>(ea, L, w, ws, st);
   // large batches of bf16 rows with bf16 weights: the gate/up kernel gathers its rows itself
   const bool direct = !skinny && wtype == FT_W_BF16 && ea.x_type == FT_X_BF16;
   // otherwise gather the permuted rows (bf16); clear the split counters of the small-batch kernels
@@ -584,6 +673,12 @@ int launch_expert_tc(int wtype, const ExpertArgs& ea, const ft_expert_layout& L,
 }
 
 }  // namespace
+
+FT_API int ft_expert_set_fp4_path(int path) {
+  FT_REQUIRE(path == FT_FP4_BLOCK_SCALED || path == FT_FP4_EXPAND_BF16);
+  g_fp4_path = path;
+  return FT_OK;
+}
 
 FT_API int ft_expert_grouped(const void* x, int x_type, int T, int k, int hidden, int inter, int E, int wtype,
                              const int32_t* perm, const int32_t* offsets, const int32_t* slot_of,

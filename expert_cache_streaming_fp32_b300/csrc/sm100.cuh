@@ -198,6 +198,62 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// Instruction descriptor of the block-scaled FP4 MMA (kind::mxf4nvf4): A and B
+// e2m1, both K-major, M x N, D fp32; ue4m3 block scales (NVFP4, a scale per 16
+// K elements) or ue8m0 (MXFP4, a scale per 32), and the byte pair of the
+// 32-bit scale words the MMA reads (sf_id, ue8m0 only: 0 or 2).
+__host__ __device__ constexpr uint32_t idesc_fp4_bs(int M, int N, bool ue8m0, uint32_t sf_id) {
+  return (sf_id << 4)                       // B scale-factor byte
+         | (1u << 7)                        // A format: e2m1
+         | (1u << 10)                       // B format: e2m1
+         | ((uint32_t)(N >> 3) << 17)       // N / 8
+         | ((ue8m0 ? 1u : 0u) << 23)        // scale type: 0 ue4m3, 1 ue8m0
+         | ((uint32_t)(M >> 4) << 24)       // M / 16
+         | (sf_id << 29);                   // A scale-factor byte
+}
+
+// D[tmem] (+)= (A * scale_A)[smem] * (B * scale_B)[smem]^T with e2m1 operands
+// and per-block scales read from tensor memory, issued by one thread.  UE4M3:
+// scale_vec::4X (four scales per row per K = 64); UE8M0: scale_vec::2X (two).
+template <bool UE8M0>
+__device__ __forceinline__ void mma_fp4_bs(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  if (UE8M0)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Shared-memory descriptor of 32 rows x 16 bytes stored contiguously (no
+// swizzle: 8-row core matrices 128 bytes apart), the source of a scale copy.
+__device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address / 16
+  d |= (uint64_t)(128 >> 4) << 16;           // leading byte offset
+  d |= (uint64_t)(128 >> 4) << 32;           // stride byte offset: 8 rows x 16 B
+  d |= (uint64_t)1 << 46;                    // descriptor version
+  return d;
+}
+
+// Copies a 512-byte block-scale atom (32 rows of 16 bytes in shared memory) to
+// four tensor-memory columns of lanes 0..31, repeated in each of the four lane
+// quarters: row r0's bytes 4j..4j+3 land in column j of lanes r0, 32+r0, ...
+// The atom holds the scales of tile rows r = r0 + 32j, four per row, so the
+// MMA finds row r's scales in lane r, column j = r / 32.
+__device__ __forceinline__ void tmem_cp_scale_atom(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Arrives once on the mbarrier when every tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
