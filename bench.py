@@ -85,6 +85,8 @@ def parse():
                                                          "fill_overlap"],
                    help="time one expert-kernel case on a small resident pool (profiling aid; prints its own line)")
     p.add_argument("--reps", type=int, default=5)
+    p.add_argument("--fp4-path", default="block_scaled", choices=["block_scaled", "expand"],
+                   help="small-batch NVFP4/MXFP4 experts: block-scaled FP4 MMA, or exact expansion to bf16")
     p.add_argument("--case-config", default="", help="workload of --kernel-case (a synth config name)")
     return p.parse_args()
 
@@ -1143,6 +1145,7 @@ def kernel_case(args):
     import expert_cache_streaming_fp32_b300 as ft
     dev = "cuda:0"
     torch.cuda.set_device(0)
+    ft.ft_expert_set_fp4_path(ft.FT_FP4_BLOCK_SCALED if args.fp4_path == "block_scaled" else ft.FT_FP4_EXPAND_BF16)
     cfg = synth.DECODE_BF16 if args.kernel_case == "experts_decode" else synth.PREFILL_BF16
     if args.case_config:
         cfg = synth.CONFIGS[args.case_config]
@@ -1173,7 +1176,8 @@ def kernel_case(args):
     wbytes = U * int(lay.payload_bytes)
     flops = 2.0 * T * k * 3 * H * I
     peaks = load_peaks()
-    print(json.dumps({"kernel_case": args.kernel_case, "config": cfg.name, "T": T, "unique_experts": U, "ms": ms,
+    print(json.dumps({"kernel_case": args.kernel_case, "config": cfg.name, "fp4_path": args.fp4_path, "T": T,
+                      "unique_experts": U, "ms": ms,
                       "weight_gbs": wbytes / (ms * 1e-3) / 1e9, "hbm_frac": wbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                       "tflops": flops / (ms * 1e-3) / 1e12, "bf16_frac": flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
                       "device_error": ft.ft_get_device_error()}))
@@ -1200,6 +1204,7 @@ def main():
     dev = f"cuda:{local}"
     cfg = synth.DECODE_BF16
     peaks = load_peaks()
+    ft.ft_expert_set_fp4_path(ft.FT_FP4_BLOCK_SCALED if args.fp4_path == "block_scaled" else ft.FT_FP4_EXPAND_BF16)
     # smallest decode batch (T*k) run in the split form: 0 the library's policy, -1 never
     split_min = -1 if args.no_split_fill else args.split_min_assignments
     batches = [int(b) for b in args.batches.split(",")]

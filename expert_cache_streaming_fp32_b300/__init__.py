@@ -42,7 +42,7 @@ EXPORTED = [
     "ft_cache_set_fill_blocks", "ft_debug_inject_failure", "ft_debug_live_resources", "ft_pool_read",
     "ft_host_register", "ft_host_unregister", "ft_cache_reset", "ft_placement_replay", "ft_cpu_create",
     "ft_cpu_destroy", "ft_cpu_experts", "ft_cpu_experts_enqueue", "ft_cpu_status", "ft_route_fused",
-    "ft_expert_set_fp4_path",
+    "ft_expert_set_fp4_path", "ft_debug_quant_fp4",
 ]
 FT_NOALLOC_MAX_ELEMS = 1 << 20
 FT_TC_WIDE_ASSIGNMENTS = 2048
@@ -95,6 +95,7 @@ _sigs = {
     "ft_route": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "ft_permute": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "ft_expert_set_fp4_path": (_I, [_I]),
+    "ft_debug_quant_fp4": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
     "ft_route_fused": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "ft_cache_create": (_I, [ctypes.POINTER(CacheConfig), ctypes.POINTER(_P)]),
     "ft_cache_destroy": (_I, [_P]),
@@ -264,6 +265,12 @@ def ft_route_fused(x, w_router, bias, k, logits, topk_idx, topk_w, counts, offse
 def ft_expert_set_fp4_path(path: int):
     """FT_FP4_BLOCK_SCALED (block-scaled FP4 MMA, FP4 activations) or FT_FP4_EXPAND_BF16 (exact expansion)."""
     _check("ft_expert_set_fp4_path", _lib.ft_expert_set_fp4_path(path))
+
+
+def ft_debug_quant_fp4(x, wtype, q, scales, stream=None):
+    rows, K = x.shape
+    _check("ft_debug_quant_fp4", _lib.ft_debug_quant_fp4(_ptr(x), _xtype(x), rows, K, wtype, _ptr(q), _ptr(scales),
+                                                         _stream(stream)))
 
 
 def ft_expert_grouped_workspace(T, k, hidden, inter) -> int:

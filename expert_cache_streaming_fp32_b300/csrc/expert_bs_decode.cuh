@@ -85,8 +85,9 @@ __device__ __forceinline__ float to_e2m1_range(float v, float inv) {
 }
 
 // Token rows in permuted order, quantised: xq[p][K/2] e2m1 bytes and xs[p][K/blk]
-// scale bytes for row p = assignment perm[p] (token perm[p] / k).  One thread per
-// block of 16 (NVFP4) or 32 (MXFP4) elements.  Also clears the split counters.
+// scale bytes for row p = assignment perm[p] (token perm[p] / k; perm NULL: row
+// p of x).  One thread per block of 16 (NVFP4) or 32 (MXFP4) elements.  Also
+// clears the split counters.
 template <typename XT, int WT>
 __global__ void __launch_bounds__(256)
 quant_rows_kernel(const XT* __restrict__ x, const int32_t* __restrict__ perm, int T, int k, int K, int Tk,
@@ -97,7 +98,7 @@ quant_rows_kernel(const XT* __restrict__ x, const int32_t* __restrict__ perm, in
   const long long total = (long long)Tk * nb;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
     const int p = (int)(i / nb), b = (int)(i % nb);
-    const int a = perm[p];
+    const int a = perm ? perm[p] : p;  // no permutation: row p of x
     if ((unsigned)a >= (unsigned)(T * k)) {
       record_error(FT_DERR_ROW_INDEX);
       continue;

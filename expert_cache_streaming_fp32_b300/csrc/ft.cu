@@ -674,6 +674,36 @@ int launch_expert_tc(int wtype, const ExpertArgs& ea, const ft_expert_layout& L,
 
 }  // namespace
 
+FT_API int ft_debug_quant_fp4(const void* x, int x_type, int rows, int K, int wtype, uint8_t* q, uint8_t* scales,
+                              ft_cuda_stream s) {
+  FT_REQUIRE(rows >= 0 && K > 0 && (wtype == FT_W_NVFP4 || wtype == FT_W_MXFP4) && K % 32 == 0);
+  FT_REQUIRE(x_type == FT_X_F32 || x_type == FT_X_BF16);
+  if (rows == 0) return FT_OK;
+  FT_REQUIRE(x && q && scales);
+  const int blk = wtype == FT_W_NVFP4 ? 16 : 32;
+  const long long blocks = (long long)rows * (K / blk);
+  const int grid = (int)std::max<long long>(1, std::min<long long>((blocks + 255) / 256, 8ll * sms()));
+  cudaStream_t st = (cudaStream_t)s;
+  const int32_t* no_perm = nullptr;
+  int32_t* no_zero = nullptr;
+  if (x_type == FT_X_BF16) {
+    if (wtype == FT_W_NVFP4)
+      FT_LAUNCH((tc::quant_rows_kernel<__nv_bfloat16, FT_W_NVFP4>), grid, 256, 0, st, (const __nv_bfloat16*)x,
+                no_perm, rows, 1, K, rows, q, scales, no_zero, 0);
+    else
+      FT_LAUNCH((tc::quant_rows_kernel<__nv_bfloat16, FT_W_MXFP4>), grid, 256, 0, st, (const __nv_bfloat16*)x,
+                no_perm, rows, 1, K, rows, q, scales, no_zero, 0);
+  } else {
+    if (wtype == FT_W_NVFP4)
+      FT_LAUNCH((tc::quant_rows_kernel<float, FT_W_NVFP4>), grid, 256, 0, st, (const float*)x, no_perm, rows, 1, K,
+                rows, q, scales, no_zero, 0);
+    else
+      FT_LAUNCH((tc::quant_rows_kernel<float, FT_W_MXFP4>), grid, 256, 0, st, (const float*)x, no_perm, rows, 1, K,
+                rows, q, scales, no_zero, 0);
+  }
+  return FT_OK;
+}
+
 FT_API int ft_expert_set_fp4_path(int path) {
   FT_REQUIRE(path == FT_FP4_BLOCK_SCALED || path == FT_FP4_EXPAND_BF16);
   g_fp4_path = path;

@@ -400,6 +400,13 @@ int ft_cache_export(ft_cache* c, int32_t* key_of_slot, uint32_t* stamp, int* n_s
  * Large batches always take the expansion. */
 enum { FT_FP4_BLOCK_SCALED = 0, FT_FP4_EXPAND_BF16 = 1 };
 int ft_expert_set_fp4_path(int path);
+
+/* Test hook: the activation quantiser of the block-scaled path on its own.
+ * Rows of x (dev [rows][K], x_type) -> q (dev [rows][K/2] e2m1 bytes, element
+ * 2i in the low nibble) and scales (dev [rows][K/16] e4m3 bytes for
+ * FT_W_NVFP4, [rows][K/32] E8M0 bytes for FT_W_MXFP4).  K a multiple of 32. */
+int ft_debug_quant_fp4(const void* x, int x_type, int rows, int K, int wtype, uint8_t* q, uint8_t* scales,
+                       ft_cuda_stream s);
 size_t ft_expert_grouped_workspace(int T, int k, int hidden, int inter);
 int ft_expert_grouped(const void* x, int x_type, int T, int k, int hidden, int inter, int E,
                       int wtype, const int32_t* perm, const int32_t* offsets, const int32_t* slot_of,

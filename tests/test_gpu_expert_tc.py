@@ -178,12 +178,17 @@ def test_tc_split_k_is_deterministic(ft):
     (synth.W_NVFP4, 4096, 2048, 4, 2, 1100, 28),  # the NVFP4 stack's expert shape, ~550 rows per expert
 ])
 def test_tc_fp4_expert_parity(ft, wtype, H, I, E, k, T, seed):
-    """NVFP4 / MXFP4 weights expanded to bf16 in shared memory (exact), then the same tensor-core path."""
+    """NVFP4 / MXFP4 weights expanded to bf16 in shared memory (exact), then the same tensor-core path
+    (the expansion is asked for explicitly: small batches otherwise take the block-scaled FP4 MMA)."""
     cfg, L, S, n_slots, pool, slot_perm, comps, x, idx = _setup(ft, H, I, E, k, T, seed, wtype=wtype)
     counts, offsets, perm, inv = moe.permute(idx, E)
     slot_of = slot_perm.astype(np.int32).copy()
     slot_of[E - 1] = -1
-    Y = _run(ft, x, k, I, E, perm, offsets, slot_of, pool, S, n_slots, wtype)
+    ft.ft_expert_set_fp4_path(ft.FT_FP4_EXPAND_BF16)
+    try:
+        Y = _run(ft, x, k, I, E, perm, offsets, slot_of, pool, S, n_slots, wtype)
+    finally:
+        ft.ft_expert_set_fp4_path(ft.FT_FP4_BLOCK_SCALED)
     xs = formats.to_f64(x)
     got, ref = [], []
     for e in range(E - 1):

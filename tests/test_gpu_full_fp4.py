@@ -4,8 +4,11 @@ Shapes are the workloads' own (NVFP4: H=4096, E=256, top-6, I=2048; MXFP4:
 H=6144, E=256, top-8, I=2048).  Routing, the cache's decisions (against the
 LRU simulator) and the miss split are compared exactly on every step; layer
 outputs are compared with the fp64 oracle on sampled steps and tokens (the
-oracle dequantises the same stored bytes; the tensor-core path rounds the
-intermediate to bf16 and so does the oracle; bar: relative Frobenius 1e-2).
+oracle dequantises the same stored bytes).  Decode batches run both FP4
+paths: the block-scaled FP4 MMA, which quantises the token rows and the
+intermediate to the weights' format (the oracle applies the same rule), and
+the exact expansion to bf16, which rounds the intermediate to bf16 (so does
+the oracle); bar: relative Frobenius 1e-2.  Prefill chunks take the expansion.
 The host pool holds a window of physical layers (logical l reads l mod the
 window), which changes neither keys nor outputs.
 """
@@ -27,6 +30,21 @@ TC_ROUND = formats.round_to_bf16
 def ft(ftlib):
     assert torch.cuda.is_available()
     return ftlib
+
+
+@pytest.fixture(params=["block_scaled", "expand"])
+def fp4_path(request, ft):
+    ft.ft_expert_set_fp4_path(ft.FT_FP4_BLOCK_SCALED if request.param == "block_scaled" else ft.FT_FP4_EXPAND_BF16)
+    yield request.param
+    ft.ft_expert_set_fp4_path(ft.FT_FP4_BLOCK_SCALED)
+
+
+def decode_rounding(wtype, path):
+    """(x_round, act_round) of a decode batch on the given FP4 path."""
+    if path == "expand":
+        return None, TC_ROUND
+    q = formats.quant_act_nvfp4 if wtype == synth.W_NVFP4 else formats.quant_act_mxfp4
+    return q, q
 
 
 class Experts:
@@ -71,8 +89,9 @@ def _waves(ft, L, cache, layer, x, ratio, sim, S, pool_slots, fill_stream=None):
     return counts
 
 
-def test_nvfp4_stack_decode_and_prefill(ft):
+def test_nvfp4_stack_decode_and_prefill(ft, fp4_path):
     cfg = synth.NVFP4_43L
+    xr, ar = decode_rounding(cfg.wtype, fp4_path)
     n_phys, n_slots = 2, 600
     pool = ft.ExpertPool(cfg, n_phys)
     pool.fill(DEV)
@@ -99,7 +118,7 @@ def test_nvfp4_stack_decode_and_prefill(ft):
             out = lay.combine(T, lay.ext, None).cpu().numpy()
             if (step, l) in ((0, 0), (3, 21), (3, 42)):
                 xs = formats.to_f64(x[sample])
-                ref = moe.moe_layer(xs, ri[sample], rw[sample], experts(l), act_round=TC_ROUND)
+                ref = moe.moe_layer(xs, ri[sample], rw[sample], experts(l), act_round=ar, x_round=xr)
                 assert_close_layer(out[sample], ref, fro=1e-2)
     st = cache.stats()
     assert (st.hits, st.fills) == (sim.hits, sim.fills)
@@ -126,7 +145,7 @@ def test_nvfp4_stack_decode_and_prefill(ft):
     pool.free()
 
 
-def test_mxfp4_mixed_resizes_and_split(ft):
+def test_mxfp4_mixed_resizes_and_split(ft, fp4_path):
     """Decode steps with the 0.7 miss split and safe-point resizes 592 -> 410 -> 205 -> 592 slots
     (from step 3 in the split cache-step form).
 
@@ -135,6 +154,7 @@ def test_mxfp4_mixed_resizes_and_split(ft):
     cache size or split; between resizes every cache decision matches the
     simulator."""
     cfg = synth.MXFP4_MIXED
+    xr, ar = decode_rounding(cfg.wtype, fp4_path)
     L_, E = cfg.n_layers, cfg.n_experts
     pool = ft.ExpertPool(cfg, L_)
     pool.fill(DEV)
@@ -172,7 +192,11 @@ def test_mxfp4_mixed_resizes_and_split(ft):
                 P = torch.zeros(1, cfg.hidden, dtype=torch.float32, device=DEV)
             out = lay.combine(1, lay.ext, P).cpu().numpy()
             if check:
-                ref = moe.moe_layer(formats.to_f64(x), ri, rw, experts(l), act_round=TC_ROUND)
+                # the GPU's experts with the path's rounding, plus the external part as supplied
+                on_gpu = [e for e in set(ri.reshape(-1).tolist()) if e not in C]
+                ref = moe.moe_layer(formats.to_f64(x), ri, rw, experts(l), act_round=ar, x_round=xr, only=on_gpu)
+                if C:
+                    ref = ref + P.cpu().numpy().astype(np.float64)
                 assert_close_layer(out, ref, fro=1e-2)
     st = cache.stats()
     assert (st.hits, st.fills, st.externals) == (sim.hits, sim.fills, sim.externals)

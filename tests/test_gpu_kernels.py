@@ -171,8 +171,13 @@ def test_expert_grouped_parity(ft, wtype, H, I, E, k, T, xdt):
         g, u, d = (formats.dequant(comps[e][m], wtype) for m in ("gate", "up", "down"))
         # bf16 weights, and NVFP4 / MXFP4 weights at these batch sizes, run on the
         # tensor cores, which round the intermediate to bf16
-        act_round = formats.round_to_bf16 if wtype in TC_FORMATS else None
-        ref.append(moe.expert_ffn(xs[perm[rows] // k], g, u, d, act_round=act_round))
+        # bf16 weights on the tensor cores round the intermediate to bf16; NVFP4 / MXFP4 weights
+        # at small batches (H and I multiples of 256) take the block-scaled FP4 MMA, which
+        # quantises the token rows and the intermediate to the weights' format
+        x_round, act_round = None, (formats.round_to_bf16 if wtype in TC_FORMATS else None)
+        if wtype in (synth.W_NVFP4, synth.W_MXFP4) and H % 256 == 0 and I % 256 == 0:
+            act_round = x_round = (formats.quant_act_nvfp4 if wtype == synth.W_NVFP4 else formats.quant_act_mxfp4)
+        ref.append(moe.expert_ffn(xs[perm[rows] // k], g, u, d, act_round=act_round, x_round=x_round))
         got.append(Y[rows])
     got, ref = np.concatenate(got), np.concatenate(ref)
     if wtype in TC_FORMATS:

@@ -60,7 +60,13 @@ def _one_call(ft, cfg, pool, S, n_slots, T, k, tag):
     d_slot = torch.from_numpy(slot_of).to(DEV)
     y_ref = torch.full((T * k, H), float("nan"), device=DEV)
     ws = torch.empty(ft.ft_expert_grouped_workspace(T, k, H, I), dtype=torch.uint8, device=DEV)
-    ft.ft_expert_grouped(x, k, I, E, cfg.wtype, d_perm, d_off, d_slot, pool, S, n_slots, y_ref, ws)
+    # the workspace entry point with the FP4 weights expanded exactly (bf16 products), not the
+    # block-scaled FP4 MMA, whose quantised activations sit outside this comparison's tolerance
+    ft.ft_expert_set_fp4_path(ft.FT_FP4_EXPAND_BF16)
+    try:
+        ft.ft_expert_grouped(x, k, I, E, cfg.wtype, d_perm, d_off, d_slot, pool, S, n_slots, y_ref, ws)
+    finally:
+        ft.ft_expert_set_fp4_path(ft.FT_FP4_BLOCK_SCALED)
     y_na = torch.full((T * k, H), float("nan"), device=DEV)
     ft.ft_expert_grouped_noalloc(x, k, I, E, cfg.wtype, d_perm, d_off, d_slot, pool, S, n_slots, y_na)
     torch.cuda.synchronize()
