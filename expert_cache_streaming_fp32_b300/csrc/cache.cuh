@@ -16,7 +16,6 @@ struct ft_cache {
   int32_t* slot_of_key;     // [L*E], -1 absent
   int32_t* key_of_slot;     // [max_slots], -1 empty
   uint32_t* stamp;          // [max_slots], 0 for empty
-  int32_t* order;           // [max_slots], slots 0..N-1 sorted by (stamp, slot)
   uint32_t* clock;          // [1]
   unsigned long long* stats;  // [5] steps, hits, fills, externals, bytes
   int32_t* fill_src;        // [E] host row
@@ -44,7 +43,6 @@ struct CacheDev {
   int32_t* slot_of_key;
   int32_t* key_of_slot;
   uint32_t* stamp;
-  int32_t* order;
   uint32_t* clock;
   unsigned long long* stats;
   int32_t* fill_src;
@@ -81,27 +79,30 @@ __device__ __forceinline__ int cc_scan(int v, int* buf, int& total) {
   return r;
 }
 
-// One wave of one layer step (one CTA).  Shared memory: order copy [N] ints,
-// touched flags [N] bytes, victims [E] ints.  With slot_fill (the split form)
-// the filled experts' slots go there and slot_of keeps only the hits.
+// One wave of one layer step (one CTA).  Shared memory: touched flags [N]
+// bytes and the victims [E].  With slot_fill (the split form) the filled
+// experts' slots go there and slot_of keeps only the hits.
+//
+// Victims are the q slots this wave has not touched with the smallest
+// (stamp, slot): empty slots hold stamp 0 and so come first, by slot; the
+// others follow from least to most recently used.  They are found by q rounds
+// of a block-wide minimum over the slots' keys, so no recency list is kept:
+// a wave without misses touches only its hits' entries.  Each miss costs a
+// whole expert over the host link, so the rounds are never the step's cost.
 __global__ void __launch_bounds__(CC_THREADS)
 cache_control_kernel(CacheDev d, int layer, const int32_t* __restrict__ counts, double ratio, int wave,
                      int32_t* __restrict__ slot_of, int32_t* __restrict__ slot_fill, int32_t* __restrict__ ext_flags,
                      int32_t* __restrict__ step_counts) {
   extern __shared__ __align__(16) unsigned char cc_smem[];
   __shared__ int buf[33];
+  __shared__ unsigned long long s_min[CC_WARPS];
   pdl_begin();
   const int N = d.N, E = d.E;
-  int32_t* s_order = reinterpret_cast<int32_t*>(cc_smem);          // [N]
-  int32_t* s_victim = s_order + N;                            // [E]
+  int32_t* s_victim = reinterpret_cast<int32_t*>(cc_smem);                   // [E]
   unsigned char* s_touched = reinterpret_cast<unsigned char*>(s_victim + E);  // [N]
-  const int tid = threadIdx.x;
-  const int IPT = ceil_div(N, CC_THREADS);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  for (int s = tid; s < N; s += CC_THREADS) {
-    s_order[s] = d.order[s];
-    s_touched[s] = 0;
-  }
+  for (int s = tid; s < N; s += CC_THREADS) s_touched[s] = 0;
   // experts: thread e (E <= 1024)
   const int e = tid;
   const bool valid_e = e < E;
@@ -121,6 +122,7 @@ cache_control_kernel(CacheDev d, int layer, const int32_t* __restrict__ counts, 
       *d.n_fill = 0;
       if (step_counts) { step_counts[0] = 0; step_counts[1] = 0; step_counts[2] = 0; step_counts[3] = 0; }
     }
+    pdl_end();
     return;
   }
   const uint32_t c = *d.clock + 1;
@@ -142,68 +144,56 @@ cache_control_kernel(CacheDev d, int layer, const int32_t* __restrict__ counts, 
     }
   }
   int m;
-  const int mrank = cc_scan(miss ? 1 : 0, buf, m);
+  const int mrank = cc_scan(miss ? 1 : 0, buf, m);  // its barriers also publish the touched flags
   const int q = qsplit_ratio(m, ratio);
   const bool fill = miss && mrank < q;
   if (miss && !fill) {
     slot_of[e] = -2;
     if (ext_flags) ext_flags[e] = 1;
   }
-  // victims: the first q entries of the recency order not touched by this wave
-  {
-    const int b0 = tid * IPT;
-    int cnt = 0;
-    for (int i = 0; i < IPT; ++i) {
-      const int p = b0 + i;
-      if (p < N && !s_touched[s_order[p]]) ++cnt;
+  if (q > 0) {
+    // keys (stamp, slot) of the slots not touched by this wave; slot s = tid + i * CC_THREADS
+    constexpr int MAXI = CACHE_MAX_SLOTS / CC_THREADS;
+    constexpr unsigned long long kNone = ~0ull;
+    unsigned long long kk[MAXI];
+#pragma unroll
+    for (int i = 0; i < MAXI; ++i) {
+      const int s = tid + i * CC_THREADS;
+      kk[i] = (s < N && !s_touched[s]) ? (((unsigned long long)d.stamp[s] << 32) | (unsigned)s) : kNone;
     }
-    int tot;
-    int pos = cc_scan(cnt, buf, tot);
-    for (int i = 0; i < IPT && pos < q; ++i) {
-      const int p = b0 + i;
-      if (p < N && !s_touched[s_order[p]]) s_victim[pos++] = s_order[p];
+    for (int r = 0; r < q; ++r) {
+      unsigned long long best = kk[0];
+#pragma unroll
+      for (int i = 1; i < MAXI; ++i) best = min(best, kk[i]);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) best = min(best, __shfl_xor_sync(FT_FULL_MASK, best, o));
+      if (lane == 0) s_min[warp] = best;
+      __syncthreads();
+      if (warp == 0) {
+        unsigned long long v = s_min[lane];
+#pragma unroll
+        for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(FT_FULL_MASK, v, o));
+        if (lane == 0) s_victim[r] = v == kNone ? -1 : (int)(v & 0xffffffffu);
+      }
+      __syncthreads();
+      const int vs = s_victim[r];
+      if (vs >= 0 && vs % CC_THREADS == tid) kk[vs / CC_THREADS] = kNone;
     }
   }
-  __syncthreads();
   if (fill) {
     const int v = s_victim[mrank];
-    const int old = d.key_of_slot[v];
-    if (old >= 0) d.slot_of_key[old] = -1;
-    d.key_of_slot[v] = key;
-    d.slot_of_key[key] = v;
-    d.stamp[v] = c;
-    s_touched[v] = 1;
-    if (slot_fill) slot_fill[e] = v;
-    else slot_of[e] = v;
-    d.fill_src[mrank] = (layer % d.Lp) * E + e;
-    d.fill_dst[mrank] = v;
-  }
-  __syncthreads();
-  // new order: untouched entries in their order, then touched slots by ascending slot
-  {
-    const int b0 = tid * IPT;
-    int cnt_u = 0, cnt_t = 0;
-    int keep[32];  // IPT <= 16 for N <= 16384
-    for (int i = 0; i < IPT; ++i) {
-      const int p = b0 + i;
-      keep[i] = p < N ? s_order[p] : -1;
-      if (p < N && !s_touched[keep[i]]) ++cnt_u;
-      if (p < N && s_touched[p]) ++cnt_t;
-    }
-    int nu;
-    const int pu = cc_scan(cnt_u, buf, nu);
-    int ntt;
-    const int pt = cc_scan(cnt_t, buf, ntt);
-    // all reads of s_order done (inside cc_scan's barriers); write the new order to global
-    int o = pu;
-    for (int i = 0; i < IPT; ++i) {
-      const int p = b0 + i;
-      if (p < N && !s_touched[keep[i]]) d.order[o++] = keep[i];
-    }
-    o = nu + pt;
-    for (int i = 0; i < IPT; ++i) {
-      const int p = b0 + i;
-      if (p < N && s_touched[p]) d.order[o++] = p;
+    if (v < 0) {
+      record_error(FT_DERR_TABLE);  // fewer free or untouched slots than fills: not reachable with nW <= N
+    } else {
+      const int old = d.key_of_slot[v];
+      if (old >= 0) d.slot_of_key[old] = -1;
+      d.key_of_slot[v] = key;
+      d.slot_of_key[key] = v;
+      d.stamp[v] = c;
+      if (slot_fill) slot_fill[e] = v;
+      else slot_of[e] = v;
+      d.fill_src[mrank] = (layer % d.Lp) * E + e;
+      d.fill_dst[mrank] = v;
     }
   }
   if (tid == 0) {
@@ -273,12 +263,12 @@ __global__ void set_buffer_slots_kernel(int32_t* slot_of, int E, int base) {
 static CacheDev cache_dev(const ft_cache* c) {
   CacheDev d;
   d.L = c->L; d.E = c->E; d.Lp = c->Lp; d.N = c->N; d.S = c->S;
-  d.slot_of_key = c->slot_of_key; d.key_of_slot = c->key_of_slot; d.stamp = c->stamp; d.order = c->order;
+  d.slot_of_key = c->slot_of_key; d.key_of_slot = c->key_of_slot; d.stamp = c->stamp;
   d.clock = c->clock; d.stats = c->stats; d.fill_src = c->fill_src; d.fill_dst = c->fill_dst; d.n_fill = c->n_fill;
   return d;
 }
 
-static size_t cache_control_smem(int N, int E) { return (size_t)N * 4 + (size_t)E * 4 + (size_t)N; }
+static size_t cache_control_smem(int N, int E) { return (size_t)E * 4 + (size_t)N; }
 
 // ------------------------------------------------------------------ host-side table state
 struct HostTables {
@@ -299,22 +289,19 @@ static int download_tables(ft_cache* c, HostTables& t) {
   return FT_OK;
 }
 
-// Writes key/stamp for slots [0, N) (N = t.key.size()), rebuilds slot_of_key and the order.
+// Writes key/stamp for slots [0, N) (N = t.key.size()) and rebuilds slot_of_key.
+// Empty slots get stamp 0, which the victim search relies on.
 static int upload_tables(ft_cache* c, const HostTables& t) {
   const int N = (int)t.key.size();
   std::vector<int32_t> sok((size_t)c->L * c->E, -1);
-  for (int s = 0; s < N; ++s)
+  std::vector<uint32_t> stamp(t.stamp);
+  for (int s = 0; s < N; ++s) {
     if (t.key[s] >= 0) sok[t.key[s]] = s;
-  std::vector<int32_t> order(N);
-  for (int s = 0; s < N; ++s) order[s] = s;
-  std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
-    uint32_t sa = t.key[a] < 0 ? 0u : t.stamp[a], sb = t.key[b] < 0 ? 0u : t.stamp[b];
-    return sa != sb ? sa < sb : a < b;
-  });
+    else stamp[s] = 0;
+  }
   if (N) {
     FT_CHECK_CUDA(cudaMemcpy(c->key_of_slot, t.key.data(), sizeof(int32_t) * N, cudaMemcpyHostToDevice));
-    FT_CHECK_CUDA(cudaMemcpy(c->stamp, t.stamp.data(), sizeof(uint32_t) * N, cudaMemcpyHostToDevice));
-    FT_CHECK_CUDA(cudaMemcpy(c->order, order.data(), sizeof(int32_t) * N, cudaMemcpyHostToDevice));
+    FT_CHECK_CUDA(cudaMemcpy(c->stamp, stamp.data(), sizeof(uint32_t) * N, cudaMemcpyHostToDevice));
   }
   FT_CHECK_CUDA(cudaMemcpy(c->slot_of_key, sok.data(), sizeof(int32_t) * sok.size(), cudaMemcpyHostToDevice));
   FT_CHECK_CUDA(cudaMemcpy(c->clock, &t.clock, sizeof(uint32_t), cudaMemcpyHostToDevice));

@@ -768,7 +768,7 @@ FT_API int ft_cache_create(const ft_cache_config* cfg, ft_cache** out) {
   const size_t nk = (size_t)c->L * c->E;
   auto dm = [](auto** p, size_t n) { return dev_malloc(reinterpret_cast<void**>(p), n) == cudaSuccess; };
   bool ok = dm(&c->slot_of_key, nk * 4) && dm(&c->key_of_slot, (size_t)c->max_slots * 4) &&
-            dm(&c->stamp, (size_t)c->max_slots * 4) && dm(&c->order, (size_t)c->max_slots * 4) &&
+            dm(&c->stamp, (size_t)c->max_slots * 4) &&
             dm(&c->clock, 4) && dm(&c->stats, 5 * 8) && dm(&c->fill_src, (size_t)c->E * 4) &&
             dm(&c->fill_dst, (size_t)c->E * 4) && dm(&c->n_fill, 4);
   if (!ok) {
@@ -813,7 +813,7 @@ FT_API int ft_cache_create(const ft_cache_config* cfg, ft_cache** out) {
 
 FT_API int ft_cache_destroy(ft_cache* c) {
   if (!c) return FT_OK;
-  dev_free(c->slot_of_key); dev_free(c->key_of_slot); dev_free(c->stamp); dev_free(c->order);
+  dev_free(c->slot_of_key); dev_free(c->key_of_slot); dev_free(c->stamp);
   dev_free(c->clock); dev_free(c->stats); dev_free(c->fill_src); dev_free(c->fill_dst); dev_free(c->n_fill);
   drop_event(c->ev_ctrl);
   drop_event(c->ev_fill);
