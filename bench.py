@@ -88,6 +88,8 @@ def parse():
     p.add_argument("--fp4-path", default="block_scaled", choices=["block_scaled", "expand"],
                    help="small-batch NVFP4/MXFP4 experts: block-scaled FP4 MMA, or exact expansion to bf16")
     p.add_argument("--case-config", default="", help="workload of --kernel-case (a synth config name)")
+    p.add_argument("--case-experts", type=int, default=0,
+                   help="experts per layer of --kernel-case (0: the config's; fewer keep a profiled pool small)")
     return p.parse_args()
 
 
@@ -1149,6 +1151,9 @@ def kernel_case(args):
     cfg = synth.DECODE_BF16 if args.kernel_case == "experts_decode" else synth.PREFILL_BF16
     if args.case_config:
         cfg = synth.CONFIGS[args.case_config]
+    if args.case_experts:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, name=f"{cfg.name}_e{args.case_experts}", n_experts=args.case_experts)
     T = int(args.batches.split(",")[0]) if args.kernel_case == "experts_decode" else 8192
     E, k, H, I = cfg.n_experts, cfg.top_k, cfg.hidden, cfg.inter
     lay = ft.ft_expert_layout_get(cfg.wtype, H, I)
