@@ -484,5 +484,319 @@ bs_skinny_kernel(const __grid_constant__ CUtensorMap map_w0, const __grid_consta
   pdl_end();
 }
 
+// ====================================================================== large batches (prefill)
+// The grouped GEMM of expert_tc.cuh with FP4 weights on the block-scaled FP4
+// MMA: 128 permuted token rows (M, quantised by quant_rows_kernel) x 128 weight
+// rows (N: 64 gate + the same 64 up rows for gate/up, 128 rows of W_d for down)
+// per tile, 256 K elements per stage, five stages.  The gate/up epilogue
+// quantises the intermediate per token row (one thread per row, blocks of 16 or
+// 32 along I) for the down product; down writes fp32 y.
+constexpr int BG_BN = 128;
+constexpr int BG_A_BYTES = BM * BS_BK / 2;        // 16 KiB of token rows
+constexpr int BG_B_BYTES = BG_BN * BS_BK / 2;     // 16 KiB of weight rows
+constexpr int BG_STAGE_BYTES = BG_A_BYTES + BG_B_BYTES + BS_SF_BYTES;
+constexpr int BG_STAGES = 5;
+constexpr int BG_THREADS = 320;                   // producer, MMA, 4 epilogue, 4 scale warps
+constexpr int BG_ACC_COLS = BG_BN;
+constexpr int BG_SC_COL0 = 2 * BG_ACC_COLS;
+constexpr int BG_TMEM_COLS = 512;                 // 256 + 5 x 32 = 416
+
+__host__ __device__ constexpr size_t bg_smem_bytes(int E) {
+  return 1024 + (size_t)BG_STAGES * BG_STAGE_BYTES + 256 + EPI_BYTES + (size_t)(2 * E + 2) * 4;
+}
+
+template <int MODE, int WT>
+__global__ void __launch_bounds__(BG_THREADS, 1)
+bs_grouped_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
+                  const __grid_constant__ CUtensorMap map_b1, Args a, const uint8_t* __restrict__ ascale,
+                  uint8_t* __restrict__ Aq, uint8_t* __restrict__ As) {
+  using namespace sm100;
+  constexpr bool MX = WT == FT_W_MXFP4;
+  constexpr int BLK = MX ? 32 : 16;
+  constexpr int ATOMS = MX ? 2 : 4;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t pad = (1024 - (raw_addr & 1023)) & 1023;
+  unsigned char* smem = smem_raw + pad;
+  const uint32_t sbase = raw_addr + pad;
+  unsigned char* tail = smem + (size_t)BG_STAGES * BG_STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tail);
+  // bars: full[S], sready[S], empty[S], tfull[2], tempty[2], drain
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * BG_STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* scan_buf = const_cast<int*>(reinterpret_cast<volatile int*>(tmem_holder + 2));  // [BG_THREADS / 32]
+  uint32_t* epi_buf = reinterpret_cast<uint32_t*>(tail + 256);
+  int* act_e = reinterpret_cast<int*>(tail + 256 + EPI_BYTES);
+  int* act_pref = act_e + a.E;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto full_bar = [&](int s) { return smem_u32(bars + s); };
+  auto sready_bar = [&](int s) { return smem_u32(bars + BG_STAGES + s); };
+  auto empty_bar = [&](int s) { return smem_u32(bars + 2 * BG_STAGES + s); };
+  auto tfull_bar = [&](int b) { return smem_u32(bars + 3 * BG_STAGES + b); };
+  auto tempty_bar = [&](int b) { return smem_u32(bars + 3 * BG_STAGES + 2 + b); };
+  const uint32_t drain_bar = smem_u32(bars + 3 * BG_STAGES + 4);
+  auto a_off = [&](int s) { return (uint32_t)(s * BG_STAGE_BYTES); };
+  auto b_off = [&](int s) { return (uint32_t)(s * BG_STAGE_BYTES + BG_A_BYTES); };
+  auto sf_off = [&](int s) { return (uint32_t)(s * BG_STAGE_BYTES + BG_A_BYTES + BG_B_BYTES); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < BG_STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(sready_bar(s), 4);  // the four scale warps
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 4 * 32);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&map_a);
+    tma_prefetch_desc(&map_b0);
+    if (MODE == GATEUP) tma_prefetch_desc(&map_b1);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), BG_TMEM_COLS);
+    tmem_relinquish();
+  }
+  pdl_begin();  // set-up above touches no global memory; the expert list below reads the routing
+  const int n_tiles_n = MODE == GATEUP ? a.I / (BG_BN / 2) : ceil_div(a.H, BG_BN);
+  const int K = MODE == GATEUP ? a.H : a.I;
+  const int nk = K / BS_BK;
+  int n_act = 0;
+  const int total = build_tiles<BG_THREADS>(a, n_tiles_n, act_e, act_pref, scan_buf, n_act);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const long long Tk = (long long)a.T * a.k;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (elect_one()) {
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, last_par = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+        const Tile t = decode_tile(a, act_e, act_pref, n_act, item);
+        for (int ks = 0; ks < nk; ++ks) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag)) { ok = false; break; }
+          const int kb = ks * BS_BK / 2;
+          mbar_arrive_expect_tx(full_bar(stage), BG_A_BYTES + BG_B_BYTES);
+          tma_load_2d(sbase + a_off(stage), &map_a, full_bar(stage), kb, t.row0);
+          const uint32_t sb = sbase + b_off(stage);
+          if (MODE == GATEUP) {
+            tma_load_3d(sb, &map_b0, full_bar(stage), kb, t.nt * (BG_BN / 2), t.slot);
+            tma_load_3d(sb + BG_B_BYTES / 2, &map_b1, full_bar(stage), kb, t.nt * (BG_BN / 2), t.slot);
+          } else {
+            tma_load_3d(sb, &map_b0, full_bar(stage), kb, t.nt * BG_BN, t.slot);
+          }
+          issued |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == BG_STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok)
+        for (int s = 0; s < BG_STAGES; ++s)
+          if (issued & (1u << s)) mbar_drain(full_bar(s), (last_par >> s) & 1);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- scale copies and MMA issuer
+    if (elect_one()) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true, any = false;
+      for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * BG_ACC_COLS;
+        for (int ks = 0; ks < nk; ++ks) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(sready_bar(stage), phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sc = tmem_base + BG_SC_COL0 + stage * BS_SF_COLS;  // 16 columns tokens (A), 16 weights (B)
+          const uint32_t sf = sbase + sf_off(stage);
+#pragma unroll
+          for (int j = 0; j < ATOMS; ++j) {
+            tmem_cp_scale_atom(sc + 4 * j, sdesc_rows16(sf + j * BS_ATOM));
+            tmem_cp_scale_atom(sc + 16 + 4 * j, sdesc_rows16(sf + (4 + j) * BS_ATOM));
+          }
+          const uint64_t da = sdesc_k_sw128(sbase + a_off(stage));
+          const uint64_t db = sdesc_k_sw128(sbase + b_off(stage));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t acc_in = (ks | kk) != 0 ? 1u : 0u;
+            if (MX)
+              mma_fp4_bs<true>(d, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2),
+                               idesc_fp4_bs(BM, BG_BN, true, 2u * (kk & 1)), sc + 4 * (kk >> 1),
+                               sc + 16 + 4 * (kk >> 1), acc_in);
+            else
+              mma_fp4_bs<false>(d, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2),
+                                idesc_fp4_bs(BM, BG_BN, false, 0), sc + 4 * kk, sc + 16 + 4 * kk, acc_in);
+          }
+          any = true;
+          mma_commit(empty_bar(stage));
+          if (++stage == BG_STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        mma_commit(tfull_bar(acc));
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      }
+      if (!ok && any) {
+        mma_commit(drain_bar);
+        mbar_drain(drain_bar, 0);
+      }
+    }
+  } else if (warp >= 6) {
+    // ---------------------------------------------------------------- scale atoms (warps 6..9)
+    // Thread i (0..127) handles token row i (A) and weight row i (B) of the tile.
+    const int i = threadIdx.x - 192;
+    const uint64_t wrow = (uint64_t)(K / BLK);       // scale bytes per matrix row
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+      const Tile t = decode_tile(a, act_e, act_pref, n_act, item);
+      const uint8_t* rec = a.pool + (uint64_t)t.slot * a.S;
+      const uint8_t* bsrc;
+      if (MODE == GATEUP)
+        bsrc = rec + (i < 64 ? a.off_scale[0] : a.off_scale[1]) + (uint64_t)(t.nt * 64 + (i & 63)) * wrow;
+      else
+        bsrc = rec + a.off_scale[2] + (uint64_t)(t.nt * BG_BN + i) * wrow;
+      const long long arow = (long long)t.row0 + i;
+      const uint8_t* asrc = arow < Tk ? ascale + (size_t)arow * wrow : nullptr;
+      const int w = 4 * (i & 31) + (i >> 5);
+      for (int ks = 0; ks < nk; ++ks) {
+        if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag)) { ok = false; break; }
+        const int kc = ks * BS_BK / BLK;
+        uint32_t* atoms = reinterpret_cast<uint32_t*>(smem + sf_off(stage));
+        uint32_t va[4] = {0u, 0u, 0u, 0u}, vb[4];
+        if (MX) {
+          if (asrc) { const uint2 u = *reinterpret_cast<const uint2*>(asrc + kc); va[0] = u.x; va[1] = u.y; }
+          const uint2 u = __ldg(reinterpret_cast<const uint2*>(bsrc + kc));
+          vb[0] = u.x; vb[1] = u.y;
+        } else {
+          if (asrc) {
+            const uint4 u = *reinterpret_cast<const uint4*>(asrc + kc);
+            va[0] = u.x; va[1] = u.y; va[2] = u.z; va[3] = u.w;
+          }
+          const uint4 u = __ldg(reinterpret_cast<const uint4*>(bsrc + kc));
+          vb[0] = u.x; vb[1] = u.y; vb[2] = u.z; vb[3] = u.w;
+        }
+#pragma unroll
+        for (int j = 0; j < ATOMS; ++j) {
+          atoms[j * BS_ATOM / 4 + w] = va[j];
+          atoms[(4 + j) * BS_ATOM / 4 + w] = vb[j];
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sready_bar(stage));
+        if (++stage == BG_STAGES) { stage = 0; phase ^= 1; }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (warps 2..5)
+    const int q = warp & 3;
+    uint32_t* buf = epi_buf + (warp - 2) * 32 * EPI_STRIDE;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int item = blockIdx.x; item < total; item += gridDim.x) {
+      const Tile t = decode_tile(a, act_e, act_pref, n_act, item);
+      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) break;
+      tc_fence_after();
+      const int rbase = t.mt * BM + q * 32;
+      const size_t pbase = (size_t)t.row0 + q * 32;
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BG_ACC_COLS;
+      float gs_g = 1.0f, gs_u = 1.0f, gs_d = 1.0f;
+      if (WT == FT_W_NVFP4) {
+        const float* gs = reinterpret_cast<const float*>(a.pool + (uint64_t)t.slot * a.S + a.off_gscale);
+        gs_g = gs[0]; gs_u = gs[1]; gs_d = gs[2];
+      }
+      const bool valid = rbase + lane < t.cnt;   // this lane's token row belongs to the tile's expert
+      if (MODE == GATEUP) {
+        // lane = token row: 32 outputs per step, quantised in blocks of BLK along I
+#pragma unroll 1
+        for (int c = 0; c < (BG_BN / 2) / 32; ++c) {
+          uint32_t g[32], u[32];
+          tmem_ld32(taddr + c * 32, g);
+          tmem_ld32(taddr + BG_BN / 2 + c * 32, u);
+          tmem_ld_wait();
+          float av[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) av[j] = silu(__uint_as_float(g[j]) * gs_g) * (__uint_as_float(u[j]) * gs_u);
+          const int n0 = t.nt * (BG_BN / 2) + c * 32;   // first output of this step
+          uint32_t code[4];
+          uint32_t sbytes = 0;
+#pragma unroll
+          for (int b = 0; b < 32 / BLK; ++b) {
+            float amax = 0.0f;
+#pragma unroll
+            for (int j = 0; j < BLK; ++j) amax = fmaxf(amax, fabsf(av[b * BLK + j]));
+            float inv;
+            sbytes |= block_scale<WT>(amax, inv) << (8 * b);
+#pragma unroll
+            for (int j = 0; j < BLK; j += 8) {
+              uint32_t word = 0;
+#pragma unroll
+              for (int h = 0; h < 4; ++h)
+                word |= cvt_e2m1x2(to_e2m1_range<WT>(av[b * BLK + j + 2 * h], inv),
+                                   to_e2m1_range<WT>(av[b * BLK + j + 2 * h + 1], inv)) << (8 * h);
+              code[(b * BLK + j) / 8] = word;
+            }
+          }
+          if (valid) {
+            const size_t row = pbase + lane;
+            *reinterpret_cast<uint4*>(Aq + row * (a.I / 2) + n0 / 2) = make_uint4(code[0], code[1], code[2], code[3]);
+            if (MX) As[row * (a.I / 32) + n0 / 32] = (uint8_t)sbytes;
+            else *reinterpret_cast<uint16_t*>(As + row * (a.I / 16) + n0 / 16) = (uint16_t)sbytes;
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BG_BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(taddr + c * 32, v);
+          tmem_ld_wait();
+          uint4* row = reinterpret_cast<uint4*>(buf + lane * EPI_STRIDE);
+          if (WT == FT_W_NVFP4) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * gs_d);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) row[j] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          __syncwarp();
+          const int col = t.nt * BG_BN + c * 32;
+          if (col < a.H) {
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+              const int r = it * 4 + (lane >> 3), piece = lane & 7;
+              if (rbase + r < t.cnt) {
+                const uint4 w = *reinterpret_cast<const uint4*>(buf + r * EPI_STRIDE + piece * 4);
+                *reinterpret_cast<uint4*>(a.y + (pbase + r) * a.H + col + piece * 4) = w;
+              }
+            }
+          }
+          __syncwarp();
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty_bar(acc));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, BG_TMEM_COLS);
+  }
+  pdl_end();
+}
+
 }  // namespace tc
 }  // namespace ft

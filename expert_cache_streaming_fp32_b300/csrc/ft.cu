@@ -588,6 +588,58 @@ int launch_bs_skinny(const ExpertArgs& ea, const ft_expert_layout& L, const TcWo
   return FT_OK;
 }
 
+// Large batches of NVFP4 / MXFP4 weights on the block-scaled FP4 MMA (tokens on M, weights on N).
+template <int WT>
+int launch_bs_grouped(const ExpertArgs& ea, const ft_expert_layout& L, const TcWorkspace& w, uint8_t* ws,
+                      cudaStream_t st) {
+  constexpr int BLK = WT == FT_W_NVFP4 ? 16 : 32;
+  const long long Tk = (long long)ea.T * ea.k;
+  const int H = ea.H, I = ea.I;
+  uint8_t* xq = ws;
+  uint8_t* xs = ws + align256((size_t)Tk * H / 2);
+  uint8_t* aq = ws + w.off_aint;
+  uint8_t* as = aq + align256((size_t)Tk * I / 2);
+  {
+    const long long blocks = Tk * (H / BLK);
+    const int grid = (int)std::max<long long>(1, std::min<long long>((blocks + 255) / 256, 8ll * sms()));
+    int32_t* no_zero = nullptr;
+    if (ea.x_type == FT_X_BF16)
+      FT_LAUNCH((tc::quant_rows_kernel<__nv_bfloat16, WT>), grid, 256, 0, st, (const __nv_bfloat16*)ea.x, ea.perm,
+                ea.T, ea.k, H, (int)Tk, xq, xs, no_zero, 0);
+    else
+      FT_LAUNCH((tc::quant_rows_kernel<float, WT>), grid, 256, 0, st, (const float*)ea.x, ea.perm, ea.T, ea.k, H,
+                (int)Tk, xq, xs, no_zero, 0);
+  }
+  CUtensorMap mx, mg, mu, ma, md;
+  {
+    const uint8_t* pool = ea.pool;
+    int r = make_map_fp4_sw(&mg, pool + L.off_val[0], H, I, ea.pool_slots, ea.S, tc::BG_BN / 2);
+    if (!r) r = make_map_fp4_sw(&mu, pool + L.off_val[1], H, I, ea.pool_slots, ea.S, tc::BG_BN / 2);
+    if (!r) r = make_map_fp4_sw(&md, pool + L.off_val[2], I, H, ea.pool_slots, ea.S, tc::BG_BN);
+    const uint64_t dx[2] = {(uint64_t)H / 2, (uint64_t)Tk}, sx[1] = {(uint64_t)H / 2};
+    const uint64_t da[2] = {(uint64_t)I / 2, (uint64_t)Tk}, sa[1] = {(uint64_t)I / 2};
+    if (!r) r = make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, 2, dx, sx, 128, tc::BM, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!r) r = make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq, 2, da, sa, 128, tc::BM, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (r) return r;
+  }
+  tc::Args a;
+  a.T = ea.T; a.k = ea.k; a.H = H; a.I = I; a.E = ea.E; a.pool_slots = ea.pool_slots;
+  a.offsets = ea.offsets; a.slot_of = ea.slot_of; a.S = ea.S;
+  a.pool = ea.pool;
+  for (int m = 0; m < 3; ++m) a.off_scale[m] = L.off_scale[m];
+  a.off_gscale = L.off_gscale;
+  a.x = nullptr; a.perm = ea.perm; a.Aint = nullptr; a.y = ea.y;
+  const size_t smem = tc::bg_smem_bytes(ea.E);
+  auto kg = tc::bs_grouped_kernel<tc::GATEUP, WT>;
+  auto kd = tc::bs_grouped_kernel<tc::DOWN, WT>;
+  if (int s = set_smem(kg, smem)) return s;
+  if (int s = set_smem(kd, smem)) return s;
+  uint8_t* none = nullptr;
+  FT_LAUNCH(kg, sms(), tc::BG_THREADS, smem, st, mx, mg, mu, a, (const uint8_t*)xs, aq, as);
+  FT_LAUNCH(kd, sms(), tc::BG_THREADS, smem, st, ma, md, md, a, (const uint8_t*)as, none, none);
+  return FT_OK;
+}
+
 int launch_expert_skinny(int wtype, const ExpertArgs& ea, const ft_expert_layout& L, const TcWorkspace& w,
                          uint8_t* ws, cudaStream_t st) {
   switch (wtype) {
@@ -606,11 +658,14 @@ int launch_expert_tc(int wtype, const ExpertArgs& ea, const ft_expert_layout& L,
   __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(ws);
   __nv_bfloat16* aint = reinterpret_cast<__nv_bfloat16*>(ws + w.off_aint);
   const bool skinny = Tk < FT_TC_WIDE_ASSIGNMENTS;
-  // small batches of FP4 weights: the block-scaled FP4 MMA (unless the exact expansion is asked for)
-  if (skinny && tc::is_fp4(wtype) && H % tc::BS_BK == 0 && I % tc::BS_BK == 0 &&
-      g_fp4_path.load() == FT_FP4_BLOCK_SCALED)
-    return wtype == FT_W_NVFP4 ? launch_bs_skinny<FT_W_NVFP4>(ea, L, w, ws, st)
-                               : launch_bs_skinny<FT_W_MXFP4>(ea, L, w, ws, st);
+  // FP4 weights: the block-scaled FP4 MMA (unless the exact expansion is asked for)
+  if (tc::is_fp4(wtype) && H % tc::BS_BK == 0 && I % tc::BS_BK == 0 && g_fp4_path.load() == FT_FP4_BLOCK_SCALED) {
+    if (skinny)
+      return wtype == FT_W_NVFP4 ? launch_bs_skinny<FT_W_NVFP4>(ea, L, w, ws, st)
+                                 : launch_bs_skinny<FT_W_MXFP4>(ea, L, w, ws, st);
+    return wtype == FT_W_NVFP4 ? launch_bs_grouped<FT_W_NVFP4>(ea, L, w, ws, st)
+                               : launch_bs_grouped<FT_W_MXFP4>(ea, L, w, ws, st);
+  }
   // large batches of bf16 rows with bf16 weights: the gate/up kernel gathers its rows itself
   const bool direct = !skinny && wtype == FT_W_BF16 && ea.x_type == FT_X_BF16;
   // otherwise gather the permuted rows (bf16); clear the split counters of the small-batch kernels

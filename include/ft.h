@@ -386,18 +386,19 @@ int ft_cache_export(ft_cache* c, int32_t* key_of_slot, uint32_t* stamp, int* n_s
  * ---------------------------------------------------------------------- */
 #define FT_TC_WIDE_ASSIGNMENTS 2048
 
-/* How the tensor cores evaluate NVFP4 / MXFP4 experts at small batches (below
- * FT_TC_WIDE_ASSIGNMENTS assignments), process-wide, for later calls:
+/* How the tensor cores evaluate NVFP4 / MXFP4 experts, process-wide, for later
+ * calls:
  *   FT_FP4_BLOCK_SCALED (default): the block-scaled FP4 MMA (kind::mxf4nvf4)
  *     reads the packed weights and their block scales directly; the token rows
  *     and the intermediate silu(G)*U are quantised to the weights' format,
  *     block by block along K in fp32 (NVFP4: blocks of 16, scale e4m3(amax/6),
  *     values e2m1(v/scale), both round to nearest even and saturating; MXFP4:
  *     blocks of 32, scale 2^(floor(log2 amax) - 2) as E8M0).  Needs H and I
- *     multiples of 256 (other shapes take the expansion).
+ *     multiples of 256 (other shapes take the expansion).  Small batches: 128
+ *     weight rows x up to 64 token rows per tile; large batches: 128 token
+ *     rows x 128 weight rows.
  *   FT_FP4_EXPAND_BF16: the weights are expanded exactly to bf16 in shared
- *     memory and multiplied as bf16 (x and the intermediate rounded to bf16).
- * Large batches always take the expansion. */
+ *     memory and multiplied as bf16 (x and the intermediate rounded to bf16). */
 enum { FT_FP4_BLOCK_SCALED = 0, FT_FP4_EXPAND_BF16 = 1 };
 int ft_expert_set_fp4_path(int path);
 

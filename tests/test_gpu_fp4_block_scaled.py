@@ -1,4 +1,4 @@
-"""The block-scaled FP4 tensor-core path of NVFP4 / MXFP4 experts (small batches).
+"""The block-scaled FP4 tensor-core path of NVFP4 / MXFP4 experts (small and large batches).
 
 The weights go to tcgen05.mma kind::mxf4nvf4 packed, with their block scales;
 the token rows and the intermediate silu(G)*U are quantised to the weights'
@@ -103,6 +103,11 @@ def _run(ft, x, k, I, E, wtype, perm, offsets, slot_of, pool, S, n_slots):
     (synth.W_MXFP4, 6144, 2048, 32, 8, 16, 5, True),
     (synth.W_MXFP4, 1024, 768, 8, 3, 50, 6, False),
     (synth.W_MXFP4, 256, 256, 2, 2, 1, 7, False),        # one stage per product
+    # large batches (T*k >= 2048): 128 token rows x 128 weight rows per tile
+    (synth.W_NVFP4, 1024, 512, 16, 8, 300, 8, False),    # 150 rows per expert: a ragged second row tile
+    (synth.W_NVFP4, 4096, 2048, 8, 6, 700, 9, True),     # the NVFP4 stack's shape, heavy and light experts
+    (synth.W_MXFP4, 2048, 1024, 8, 4, 600, 10, False),
+    (synth.W_MXFP4, 6144, 2048, 4, 8, 260, 13, False),   # the MXFP4 trace's shape, ~520 rows per expert
 ])
 def test_block_scaled_expert_parity(ft, wtype, H, I, E, k, T, seed, skewed):
     cfg, S, n_slots, pool, slot_perm, comps, x, idx = _setup(ft, wtype, H, I, E, k, T, seed, skewed)

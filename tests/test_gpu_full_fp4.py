@@ -8,7 +8,7 @@ oracle dequantises the same stored bytes).  Decode batches run both FP4
 paths: the block-scaled FP4 MMA, which quantises the token rows and the
 intermediate to the weights' format (the oracle applies the same rule), and
 the exact expansion to bf16, which rounds the intermediate to bf16 (so does
-the oracle); bar: relative Frobenius 1e-2.  Prefill chunks take the expansion.
+the oracle); bar: relative Frobenius 1e-2.  Prefill chunks take the same path.
 The host pool holds a window of physical layers (logical l reads l mod the
 window), which changes neither keys nor outputs.
 """
@@ -126,7 +126,7 @@ def test_nvfp4_stack_decode_and_prefill(ft, fp4_path):
     sk, ss = sim.state()
     assert key.tolist() == sk.tolist() and stamp.tolist() == ss.tolist() and clock == sim.clock
 
-    # one 8192-token prefill chunk of physical layer 1 with every expert resident (large-batch FP4 tiling)
+    # one 8192-token prefill chunk of physical layer 1 with every expert resident (large-batch tiling)
     fused = pool.host[1 * cfg.n_experts * pool.S:2 * cfg.n_experts * pool.S].to(DEV)
     lp = ft.MoELayer(cfg, 8192)
     wr, _ = synth.router_weights(cfg, 1, DEV)
@@ -138,7 +138,7 @@ def test_nvfp4_stack_decode_and_prefill(ft, fp4_path):
     ri, rw = moe.route(z, cfg.top_k)
     assert np.array_equal(lp.idx.cpu().numpy(), ri)
     rows = [5, 4000, 8191]
-    ref = moe.moe_layer(formats.to_f64(xp[rows]), ri[rows], rw[rows], experts(1), act_round=TC_ROUND)
+    ref = moe.moe_layer(formats.to_f64(xp[rows]), ri[rows], rw[rows], experts(1), act_round=ar, x_round=xr)
     assert_close_layer(out[rows], ref, fro=1e-2)
     assert ft.ft_get_device_error() == 0
     cache.destroy()
