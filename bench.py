@@ -648,16 +648,60 @@ def nvfp4_leg(ft, dev, peaks, link, batches, steps, split_min=0):
     return res
 
 
+def host_bandwidth(ft, cfg, pool, cpu, payload, tokens=8, reps=3):
+    """B_H ([Review] §2.5, Table 1): expert bytes per second of the host executor, one
+    token per expert, measured on ``tokens`` x top-k distinct experts of physical layer
+    0; with B_P (the pinned-copy rate of the same records) the ratio that sets q*."""
+    k, E = cfg.top_k, cfg.n_experts
+    n = min(tokens * k, E)
+    T = n // k
+    idx = torch.arange(T * k, dtype=torch.int32).reshape(T, k)
+    w = torch.full((T, k), 1.0 / k)
+    ext = torch.ones(E, dtype=torch.int32)
+    x = synth.activations(cfg, T, tag=9).to(torch.bfloat16 if cfg.x_dtype == "bf16" else torch.float32)
+    part = torch.empty(T, cfg.hidden)
+    job = cpu.job(pool.ptr, pool.S, cfg.wtype, cfg.hidden, cfg.inter, E, 0, x, T, k, idx, w, ext, part)
+    cpu.run(job)
+    best = float("inf")
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        cpu.run(job)
+        best = min(best, time.perf_counter() - t0)
+    d = torch.empty(n * pool.S, dtype=torch.uint8, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    bp = 0.0
+    for _ in range(reps):
+        e0.record()
+        d.copy_(pool.host[: n * pool.S], non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        bp = max(bp, n * payload / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    del d
+    bh = n * payload / best / 1e9
+    return {"experts": n, "bw_host_gbs": bh, "bw_fill_gbs": bp, "ratio_fill_over_host": bp / bh,
+            "q_for_m": {m: ft.ft_qsplit(m, bp, bh) for m in (1, 2, 3, 4, 6, 8, 16)},
+            "threads": cpu_threads()}
+
+
+def cpu_threads() -> int:
+    """Threads of an executor created with threads=0: the hardware threads, at most 256."""
+    return min(256, os.cpu_count() or 1)
+
+
 def mxfp4_mixed_leg(ft, dev, peaks, link, decode_steps=512, cycles=4, split_min=0):
     """The MXFP4 agent-like trace on 4 layers: cycles of (8192-token prefill, T=1 decode run).
 
     The cache is resized at the safe point before each cycle (57.8% -> 40% ->
     20% -> 57.8% of the 1024 (layer, expert) slots); misses are split with
-    ratio 0.7, so 30% of them go to the external path, whose partial output is
-    supplied to the combine (a zero placeholder here: the host share is not
-    part of this build).  With fewer slots than two whole layers the prefill
-    runs on demand through the cache in waves; otherwise it streams.  Every
-    resize re-captures the decode graph, since the wave count can change."""
+    ratio 0.7, so 30% of them go to the external path.  In decode the host
+    expert executor evaluates them from the pinned pool, as a host node of the
+    captured step, and the combine adds its partial output; in the 8192-token
+    on-demand prefill waves their partial is a zero placeholder (thousands of
+    token-expert products per wave, beyond a bounded bench run on host cores).
+    With fewer slots than two whole layers the prefill runs on demand through
+    the cache in waves; otherwise it streams.  Every resize re-captures the
+    decode graph, since the wave count can change.  Before the trace, the host
+    executor's expert bandwidth B_H is measured against the pinned-copy B_P."""
     cfg = synth.MXFP4_MIXED
     L, E, H = cfg.n_layers, cfg.n_experts, cfg.hidden
     budgets = [592, 410, 205, 592][:cycles]
@@ -681,13 +725,23 @@ def mxfp4_mixed_leg(ft, dev, peaks, link, decode_steps=512, cycles=4, split_min=
     fs = torch.cuda.Stream(device=dev)                        # the fill stream of the split form
     fs_d = fs if split_min >= 0 and ft.split_pays(1, cfg.top_k, cfg.wtype, split_min) else None
     fs_p = fs if split_min >= 0 and ft.split_pays(8192, cfg.top_k, cfg.wtype, split_min) else None
+    cpu = ft.CpuExperts(threads=0)
+    hb = ft.HostBranch(cfg, 1, pool, cpu, dev) if fs_d is not None else None
+    bh = host_bandwidth(ft, cfg, pool, cpu, payload)
 
     def decode_layers():
         for l in range(L):
             lay_d.route(x_d, *routers[l])
-            for w in range(cache.n_waves()):
-                lay_d.cached_wave(x_d, l, cache, pool.S, ratio, w, counts_d[l, w], fill_stream=fs_d)
-            lay_d.combine(1, lay_d.ext, P_d)
+            nw = cache.n_waves()
+            for w in range(nw):
+                after = (lambda l=l: hb.launch(lay_d, x_d, l)) if hb is not None and w == nw - 1 else None
+                lay_d.cached_wave(x_d, l, cache, pool.S, ratio, w, counts_d[l, w], fill_stream=fs_d,
+                                  after_control=after)
+            if hb is not None:
+                hb.join()
+                lay_d.combine(1, lay_d.ext, hb.P[:1])
+            else:
+                lay_d.combine(1, lay_d.ext, P_d)
 
     cyc = []
     total_ms, total_tokens, roof_s = 0.0, 0, 0.0
@@ -755,14 +809,19 @@ def mxfp4_mixed_leg(ft, dev, peaks, link, decode_steps=512, cycles=4, split_min=
         del g
     for c in cyc:
         c.pop("_bytes_after")
+    torch.cuda.synchronize()
+    cpu_status = cpu.status()
     cache.destroy()
+    cpu.destroy()
     pool.free()
     del sp
     torch.cuda.empty_cache()
     return {"workload": "mxfp4_mixed_4L: H=6144 E=256 top-8 I=2048, MXFP4 weights, 4 layers; "
                         "4 x (8192-token prefill, 512 T=1 decode steps); cache 592/410/205/592 slots; 30% external",
             "tokens_per_s": total_tokens / (total_ms * 1e-3), "layer_roofline_frac": roof_s / (total_ms * 1e-3),
-            "cycles": cyc}
+            "external_path": ("decode: host expert executor (graph host node); prefill waves: zero placeholder"
+                              if hb is not None else "zero placeholder"),
+            "host_executor_status": cpu_status, "host_bandwidth": bh, "cycles": cyc}
 
 
 # ---------------------------------------------------------------- CPU oracle baseline
