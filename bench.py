@@ -70,6 +70,9 @@ def parse():
     p.add_argument("--cpu-budget-s", type=float, default=12.0, help="wall seconds of timed CPU baseline rounds")
     p.add_argument("--no-pool-setup", action="store_true", help="skip the pin-first vs read-then-pin setup leg")
     p.add_argument("--no-placement", action="store_true", help="skip the placement-policy replay")
+    p.add_argument("--profile-eager-steps", type=int, default=0,
+                   help="after the timed region: per batch size, the trace's last N steps again, eagerly (no graphs), "
+                        "inside the NVTX range profile_steps (for an ncu launch list; 0: none)")
     p.add_argument("--timed-spans", action="store_true",
                    help="record the per-kernel timing events inside the timed passes (instead of one extra pass)")
     p.add_argument("--setup-layers", type=int, default=2, help="layers of the pool file in the setup leg")
@@ -369,6 +372,22 @@ class DecodeRun:
         self.igraphs.clear()
         torch.cuda.synchronize()
         self.cache.destroy()
+
+
+def profile_eager(run, n):
+    """Per batch size: the trace from a cold cache through its graphs up to its last n steps,
+    then those n steps eagerly inside the NVTX range "profile_steps" (a warm cache, launches
+    that a profiler can list one by one)."""
+    for T in run.batches:
+        run.cache.reset()
+        for t in range(run.n_steps - n):
+            run.graphs[(T, t)][0].replay()
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("profile_steps")
+        for t in range(run.n_steps - n, run.n_steps):
+            run.step(T, t)
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
 
 
 def step_times_ms(marks):
@@ -1336,6 +1355,8 @@ def main():
         torch.cuda.synchronize()
         spans_pass_ms = s0.elapsed_time(s1)
         log(f"instrumented pass: {spans_pass_ms:.1f} ms")
+    if args.profile_eager_steps > 0:
+        profile_eager(run, args.profile_eager_steps)
     payload = int(lay_bytes.payload_bytes)
     rep = decode_report(run, marks, cfg, peaks, link, payload, args.steady_from)
 

@@ -36,11 +36,11 @@ constexpr int BS_B_BYTES = SK_NB * BS_BK / 2;        // 8 KiB of token rows (max
 constexpr int BS_ATOM = 512;
 constexpr int BS_SF_BYTES = 8 * BS_ATOM;             // 4 atoms for the weights, 4 for the tokens
 constexpr int BS_STAGE_BYTES = BS_A_BYTES + BS_B_BYTES + BS_SF_BYTES;
-constexpr int BS_STAGES = 6;
+constexpr int BS_STAGES = 7;
 constexpr int BS_THREADS = 256;
 constexpr int BS_SF_COLS = 32;                       // tensor-memory columns of one stage's scales
 constexpr int BS_SC_COL0 = 2 * SK_ACC_COLS;          // scales after the two accumulators
-constexpr int BS_TMEM_COLS = 512;                    // 128 + 6 x 32 = 320, rounded up to a power of two
+constexpr int BS_TMEM_COLS = 512;                    // 128 + 7 x 32 = 352, rounded up to a power of two
 
 __host__ __device__ constexpr size_t bs_smem_bytes(int E) {
   return 1024 + (size_t)BS_STAGES * BS_STAGE_BYTES + 512 + SK_EX_BYTES + (size_t)(2 * E + 2) * 4;
