@@ -62,6 +62,7 @@ def test_quantiser_agrees_with_the_oracle_rule(ft, wtype, dt):
 
 
 def _setup(ft, wtype, H, I, E, k, T, seed, skewed=False):
+    assert k <= E, "each token routes to k distinct experts"
     cfg = synth.MoEConfig(f"bs{wtype}_{H}_{I}", H, E, k, I, 1, wtype, "bf16", seed=seed)
     L = ft.ft_expert_layout_get(wtype, H, I)
     S = int(L.bytes)
@@ -107,7 +108,7 @@ def _run(ft, x, k, I, E, wtype, perm, offsets, slot_of, pool, S, n_slots):
     (synth.W_NVFP4, 1024, 512, 16, 8, 300, 8, False),    # 150 rows per expert: a ragged second row tile
     (synth.W_NVFP4, 4096, 2048, 8, 6, 700, 9, True),     # the NVFP4 stack's shape, heavy and light experts
     (synth.W_MXFP4, 2048, 1024, 8, 4, 600, 10, False),
-    (synth.W_MXFP4, 6144, 2048, 4, 8, 260, 13, False),   # the MXFP4 trace's shape, ~520 rows per expert
+    (synth.W_MXFP4, 6144, 2048, 8, 8, 260, 13, False),   # the MXFP4 trace's shape, 260 rows per expert
 ])
 def test_block_scaled_expert_parity(ft, wtype, H, I, E, k, T, seed, skewed):
     cfg, S, n_slots, pool, slot_perm, comps, x, idx = _setup(ft, wtype, H, I, E, k, T, seed, skewed)
