@@ -46,6 +46,7 @@ EXPORTED = [
 ]
 FT_NOALLOC_MAX_ELEMS = 1 << 20
 FT_TC_WIDE_ASSIGNMENTS = 2048
+FT_ROUTE_ARRIVAL_WORDS = 16
 
 
 class FTError(RuntimeError):
@@ -96,7 +97,7 @@ _sigs = {
     "ft_permute": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "ft_expert_set_fp4_path": (_I, [_I]),
     "ft_debug_quant_fp4": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
-    "ft_route_fused": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "ft_route_fused": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "ft_cache_create": (_I, [ctypes.POINTER(CacheConfig), ctypes.POINTER(_P)]),
     "ft_cache_destroy": (_I, [_P]),
     "ft_cache_n_waves": (_I, [_P]),
@@ -254,12 +255,17 @@ def ft_permute(topk_idx, E, counts, offsets, perm, inv, stream=None):
                                          _ptr(inv), _stream(stream)))
 
 
-def ft_route_fused(x, w_router, bias, k, logits, topk_idx, topk_w, counts, offsets, perm, inv, stream=None):
+def ft_route_fused(x, w_router, bias, k, logits, topk_idx, topk_w, counts, offsets, perm, inv, arrivals,
+                   stream=None):
+    """``arrivals``: a zeroed device int32/uint32 tensor of FT_ROUTE_ARRIVAL_WORDS words, one per
+    routing that may be in flight at a time; every call leaves it zero."""
     T, H = x.shape
     E = w_router.shape[0]
+    if arrivals is not None and arrivals.numel() < FT_ROUTE_ARRIVAL_WORDS:
+        raise ValueError("arrivals needs FT_ROUTE_ARRIVAL_WORDS words")
     _check("ft_route_fused", _lib.ft_route_fused(
         _ptr(x), _xtype(x), _ptr(w_router), _ptr(bias), T, H, E, k, _ptr(logits), _ptr(topk_idx), _ptr(topk_w),
-        _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv), _stream(stream)))
+        _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv), _ptr(arrivals), _stream(stream)))
 
 
 def ft_expert_set_fp4_path(path: int):

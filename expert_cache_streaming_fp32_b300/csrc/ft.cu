@@ -231,52 +231,62 @@ FT_API int ft_permute(const int32_t* topk_idx, int T, int k, int E, int32_t* cou
 }
 
 // ------------------------------------------------------------------ fused routing
+// one counter for the batch and one per row chunk (at most RW_MAXT / 8 chunks)
+static_assert(1 + RW_MAXT / 8 <= FT_ROUTE_ARRIVAL_WORDS, "arrival counters");
+
 namespace {
 template <typename XT, int RT>
-int launch_route_fused(const XT* x, const XT* wr, const float* bias, int T, int H, int E, int k, float* z,
-                       int32_t* idx, float* w, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
-                       cudaStream_t st) {
-  const size_t smem = (size_t)RT * H * sizeof(float);
-  auto kr = E <= 256 ? route_fused_kernel<XT, RT, 8> : route_fused_kernel<XT, RT, 16>;
+int launch_route_grid(const XT* x, const XT* wr, const float* bias, int T, int H, int E, int k, float* z,
+                      int32_t* idx, float* w, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                      uint32_t* arrivals, cudaStream_t st) {
+  // staged rows, and after them the last CTA's grouping tables
+  const size_t smem = std::max((size_t)RT * H * sizeof(float), (size_t)(2 + RW_WARPS) * E * sizeof(int32_t));
+  const int chunks = ceil_div(T, RT);
+  const int groups = std::max(1, std::min(ceil_div(E, RW_WARPS), ceil_div(2 * sms(), chunks)));
+  auto kr = E <= 256 ? route_grid_kernel<XT, RT, 8> : route_grid_kernel<XT, RT, 16>;
   if (int r = set_smem(kr, smem)) return r;
-  FT_CHECK_CUDA(launch_pdl_cluster(kr, dim3(RF_CL), dim3(RF_THREADS), smem, st, RF_CL, x, wr, bias, T, H, E, k, z,
-                                   idx, w, counts, offsets, perm, inv));
+  FT_LAUNCH(kr, dim3(groups, chunks), RW_THREADS, smem, st, x, wr, bias, T, H, E, k, z, idx, w, counts, offsets,
+            perm, inv, arrivals);
   return FT_OK;
 }
 
 template <typename XT>
-int route_fused_rt(const void* x, const void* wr, const float* bias, int T, int H, int E, int k, float* z,
-                   int32_t* idx, float* w, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
-                   cudaStream_t st) {
+int route_grid_rt(const void* x, const void* wr, const float* bias, int T, int H, int E, int k, float* z,
+                  int32_t* idx, float* w, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                  uint32_t* arrivals, cudaStream_t st) {
   const XT* xx = static_cast<const XT*>(x);
   const XT* ww = static_cast<const XT*>(wr);
-  if (T >= 8) return launch_route_fused<XT, 8>(xx, ww, bias, T, H, E, k, z, idx, w, counts, offsets, perm, inv, st);
-  if (T >= 4) return launch_route_fused<XT, 4>(xx, ww, bias, T, H, E, k, z, idx, w, counts, offsets, perm, inv, st);
-  if (T >= 2) return launch_route_fused<XT, 2>(xx, ww, bias, T, H, E, k, z, idx, w, counts, offsets, perm, inv, st);
-  return launch_route_fused<XT, 1>(xx, ww, bias, T, H, E, k, z, idx, w, counts, offsets, perm, inv, st);
+  if (T >= 8)
+    return launch_route_grid<XT, 8>(xx, ww, bias, T, H, E, k, z, idx, w, counts, offsets, perm, inv, arrivals, st);
+  if (T >= 4)
+    return launch_route_grid<XT, 4>(xx, ww, bias, T, H, E, k, z, idx, w, counts, offsets, perm, inv, arrivals, st);
+  if (T >= 2)
+    return launch_route_grid<XT, 2>(xx, ww, bias, T, H, E, k, z, idx, w, counts, offsets, perm, inv, arrivals, st);
+  return launch_route_grid<XT, 1>(xx, ww, bias, T, H, E, k, z, idx, w, counts, offsets, perm, inv, arrivals, st);
 }
 }  // namespace
 
 FT_API int ft_route_fused(const void* x, int x_type, const void* w_router, const float* bias, int T, int H, int E,
                           int k, float* logits, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
-                          int32_t* perm, int32_t* inv, ft_cuda_stream s) {
+                          int32_t* perm, int32_t* inv, uint32_t* arrivals, ft_cuda_stream s) {
   FT_REQUIRE(T >= 0 && H > 0 && H % 8 == 0 && E >= 1 && E <= PM_MAXE && k >= 1 && k <= RT_MAXK && k <= E);
   FT_REQUIRE(x_type == FT_X_F32 || x_type == FT_X_BF16);
   FT_REQUIRE(counts && offsets);
   if (T > 0) FT_REQUIRE(x && w_router && logits && topk_idx && topk_w && perm && inv);
   const int RT = T >= 8 ? 8 : T >= 4 ? 4 : T >= 2 ? 2 : 1;
-  if (T == 0 || T > RF_MAXT || (size_t)RT * H * sizeof(float) > 200 * 1024) {
+  if (T == 0 || T > RW_MAXT || (size_t)RT * H * sizeof(float) > 200 * 1024) {
     // larger batches (and the empty one): the three kernels
     if (int r = ft_router_logits(x, x_type, w_router, bias, T, H, E, logits, s)) return r;
     if (int r = ft_route(logits, T, E, k, topk_idx, topk_w, s)) return r;
     return ft_permute(topk_idx, T, k, E, counts, offsets, perm, inv, s);
   }
+  FT_REQUIRE(arrivals);
   cudaStream_t st = (cudaStream_t)s;
   if (x_type == FT_X_BF16)
-    return route_fused_rt<__nv_bfloat16>(x, w_router, bias, T, H, E, k, logits, topk_idx, topk_w, counts, offsets,
-                                         perm, inv, st);
-  return route_fused_rt<float>(x, w_router, bias, T, H, E, k, logits, topk_idx, topk_w, counts, offsets, perm, inv,
-                               st);
+    return route_grid_rt<__nv_bfloat16>(x, w_router, bias, T, H, E, k, logits, topk_idx, topk_w, counts, offsets,
+                                        perm, inv, arrivals, st);
+  return route_grid_rt<float>(x, w_router, bias, T, H, E, k, logits, topk_idx, topk_w, counts, offsets, perm, inv,
+                              arrivals, st);
 }
 
 // ------------------------------------------------------------------ combine

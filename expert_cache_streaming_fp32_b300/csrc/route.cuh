@@ -124,8 +124,9 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
 }
 
 // Top-k of one token's logits z[0..E-1] by one warp; lane 0 writes idx_row and w_row.
+// The logits are read through L2: other CTAs of the same launch may have written them.
 template <int PER_LANE>
-__device__ __forceinline__ void route_token(const float* __restrict__ z, int E, int k, int32_t* __restrict__ idx_row,
+__device__ __forceinline__ void route_token(const float* z, int E, int k, int32_t* __restrict__ idx_row,
                                             float* __restrict__ w_row) {
   const int lane = threadIdx.x & 31;
   float v[PER_LANE];
@@ -133,11 +134,11 @@ __device__ __forceinline__ void route_token(const float* __restrict__ z, int E, 
 #pragma unroll
   for (int i = 0; i < PER_LANE; ++i) {
     int e = lane + 32 * i;
-    v[i] = e < E ? z[e] : -INFINITY;
+    v[i] = e < E ? __ldcg(z + e) : -INFINITY;
     if (e >= E) taken |= 1u << i;
   }
-  float sel_v[RT_MAXK];
-  int sel_i[RT_MAXK];
+  float my_v = 0.0f;  // lane j keeps the j-th choice
+  int my_i = 0;
 #pragma unroll 1
   for (int j = 0; j < k; ++j) {
     float bv = -INFINITY;
@@ -164,24 +165,24 @@ __device__ __forceinline__ void route_token(const float* __restrict__ z, int E, 
 #pragma unroll
       for (int o = 16; o; o >>= 1) cand = min(cand, __shfl_xor_sync(FT_FULL_MASK, cand, o));
       bi = cand;
-      bv = z[bi];
+      bv = __ldcg(z + bi);
     }
     if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    sel_v[j] = bv;
-    sel_i[j] = bi;
-  }
-  if (lane == 0) {
-    const float m = sel_v[0];
-    float s = 0.0f;
-    float ex[RT_MAXK];
-#pragma unroll 1
-    for (int j = 0; j < k; ++j) { ex[j] = expf(sel_v[j] - m); s += ex[j]; }
-    const float inv = 1.0f / s;
-#pragma unroll 1
-    for (int j = 0; j < k; ++j) {
-      idx_row[j] = sel_i[j];
-      w_row[j] = ex[j] * inv;
+    if (lane == j) {
+      my_v = bv;
+      my_i = bi;
     }
+  }
+  // softmax over the chosen logits; the sum runs in choice order
+  const float m = __shfl_sync(FT_FULL_MASK, my_v, 0);
+  const float ex = lane < k ? expf(my_v - m) : 0.0f;
+  float s = 0.0f;
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) s += __shfl_sync(FT_FULL_MASK, ex, j);
+  const float inv = 1.0f / s;
+  if (lane < k) {
+    idx_row[lane] = my_i;
+    w_row[lane] = ex * inv;
   }
 }
 
@@ -197,65 +198,68 @@ route_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __r
 }
 
 // ====================================================================== permutation
-// One CTA.  Pass 1: per-expert counts with shared-memory atomics, exclusive
-// scan into offsets.  Pass 2: assignments in tiles of blockDim; inside a warp,
+// Stable grouping of the n = T*k assignments by expert, by one CTA of W warps.
+// Pass 1: per-expert counts with shared-memory atomics, exclusive scan into
+// offsets.  Pass 2: assignments in tiles of 32*W; inside a warp,
 // __match_any_sync groups equal experts and the rank is the number of equal
 // lanes below; across warps a per-(warp, expert) count table is scanned in warp
 // order, continuing from the previous tiles.  Positions therefore follow the
-// assignment order a = t*k + j within each expert (stable).
+// assignment order a = t*k + j within each expert (stable), which makes the
+// result unique.  idx is read through L2 (it may have been written by other
+// CTAs of the same launch).  tab holds (2 + W) * E ints of shared memory.
 constexpr int PM_THREADS = 1024;
 constexpr int PM_WARPS = PM_THREADS / 32;
 constexpr int PM_MAXE = 512;
 
-__global__ void __launch_bounds__(PM_THREADS)
-permute_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __restrict__ counts,
-               int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
-  extern __shared__ int32_t pm_smem[];
-  pdl_begin();
-  int32_t* cnt = pm_smem;                    // [E]
+template <int W>
+__device__ __forceinline__ void permute_block(const int32_t* idx, int n, int E, int32_t* __restrict__ counts,
+                                              int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+                                              int32_t* __restrict__ inv, int32_t* tab, int32_t* warp_tot) {
+  static_assert(W >= 1 && W <= 32, "one warp scans the warp totals");
+  constexpr int NT = W * 32;
+  int32_t* cnt = tab;                     // [E]
   int32_t* base = cnt + E;                // [E] running position per expert (absolute)
-  int32_t* wc = base + E;                 // [PM_WARPS][E]
-  __shared__ int32_t warp_tot[PM_WARPS];
+  int32_t* wc = base + E;                 // [W][E]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int e = tid; e < E; e += PM_THREADS) cnt[e] = 0;
-  for (int i = tid; i < PM_WARPS * E; i += PM_THREADS) wc[i] = 0;
+  for (int e = tid; e < E; e += NT) cnt[e] = 0;
+  for (int i = tid; i < W * E; i += NT) wc[i] = 0;
   __syncthreads();
-  for (int a = tid; a < n; a += PM_THREADS) {
-    int e = idx[a];
+  for (int a = tid; a < n; a += NT) {
+    const int e = __ldcg(idx + a);
     if ((unsigned)e < (unsigned)E) atomicAdd(&cnt[e], 1);
     else record_error(FT_DERR_EXPERT_INDEX);
   }
   __syncthreads();
-  // exclusive scan of cnt (E <= 512): each thread sums a strided chunk, then warp scans
+  // exclusive scan of cnt: each thread sums a run of consecutive experts, then warp scans
   {
-    const int per = ceil_div(E, PM_THREADS);
+    const int per = ceil_div(E, NT);
     int local = 0;
     for (int i = 0; i < per; ++i) {
-      int e = tid * per + i;
+      const int e = tid * per + i;
       if (e < E) local += cnt[e];
     }
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(FT_FULL_MASK, incl, o);
+      const int y = __shfl_up_sync(FT_FULL_MASK, incl, o);
       if (lane >= o) incl += y;
     }
     if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-      int w = warp_tot[lane];
+      const int w = lane < W ? warp_tot[lane] : 0;
       int wi = w;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(FT_FULL_MASK, wi, o);
+        const int y = __shfl_up_sync(FT_FULL_MASK, wi, o);
         if (lane >= o) wi += y;
       }
-      warp_tot[lane] = wi - w;
+      if (lane < W) warp_tot[lane] = wi - w;
     }
     __syncthreads();
     int run = warp_tot[warp] + incl - local;
     for (int i = 0; i < per; ++i) {
-      int e = tid * per + i;
+      const int e = tid * per + i;
       if (e < E) {
         base[e] = run;
         offsets[e] = run;
@@ -266,20 +270,20 @@ permute_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __restric
     if (tid == 0) offsets[E] = n;
   }
   __syncthreads();
-  for (int t0 = 0; t0 < n; t0 += PM_THREADS) {
+  for (int t0 = 0; t0 < n; t0 += NT) {
     const int a = t0 + tid;
-    int e = a < n ? idx[a] : -1;
+    int e = a < n ? __ldcg(idx + a) : -1;
     if ((unsigned)e >= (unsigned)E) e = -1;
     const unsigned peers = __match_any_sync(FT_FULL_MASK, e);
     const int rank = __popc(peers & ((1u << lane) - 1));
     const int leader = __ffs(peers) - 1;
     if (e >= 0 && lane == leader) wc[warp * E + e] = __popc(peers);
     __syncthreads();
-    for (int ex = tid; ex < E; ex += PM_THREADS) {
+    for (int ex = tid; ex < E; ex += NT) {
       int run = base[ex];
 #pragma unroll 4
-      for (int w = 0; w < PM_WARPS; ++w) {
-        int c = wc[w * E + ex];
+      for (int w = 0; w < W; ++w) {
+        const int c = wc[w * E + ex];
         wc[w * E + ex] = run;
         run += c;
       }
@@ -293,119 +297,90 @@ permute_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __restric
     }
     __syncthreads();
     // the scan above wrote every (w, ex) entry: reset the whole table for the next tile
-    for (int i = tid; i < PM_WARPS * E; i += PM_THREADS) wc[i] = 0;
+    for (int i = tid; i < W * E; i += NT) wc[i] = 0;
     __syncthreads();
   }
+}
+
+__global__ void __launch_bounds__(PM_THREADS)
+permute_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __restrict__ counts,
+               int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+  extern __shared__ int32_t pm_smem[];       // [(2 + PM_WARPS) * E]
+  __shared__ int32_t warp_tot[PM_WARPS];
+  pdl_begin();
+  permute_block<PM_WARPS>(idx, n, E, counts, offsets, perm, inv, pm_smem, warp_tot);
   pdl_end();
 }
 
 // ====================================================================== fused routing (decode batches)
-// Router logits, top-k and the permutation of a small batch (T <= RF_MAXT) in
-// one launch: a cluster of RF_CL CTAs.  Each CTA computes the logits of its
-// share of the experts for every token (the same per-expert arithmetic as
-// router_logits_kernel, so the logits are bit-identical) and writes them out;
-// after a cluster barrier (release/acquire at cluster scope, so the other
-// CTAs' logits are visible) CTA 0 routes every token (one warp per token, as
-// route_kernel) and builds counts, offsets, perm and inv for the T*k
-// assignments: the rank of an assignment within its expert is the number of
-// earlier assignments to the same expert, so perm is stable.
-constexpr int RF_CL = 8;
-constexpr int RF_MAXT = 16;
-constexpr int RF_WARPS = 16;
-constexpr int RF_THREADS = RF_WARPS * 32;
+// Router logits, top-k and the permutation of a small batch (T <= RW_MAXT) in
+// one launch over the grid of router_logits_kernel (expert groups x row
+// chunks), so the router matrix is read by many SMs at once:
+//   1. each CTA computes the logits of its RT rows for its experts (the same
+//      per-expert arithmetic as router_logits_kernel: bit-identical logits);
+//   2. the CTA that completes a row chunk (the last of its expert groups to
+//      arrive on the chunk's counter) routes the chunk's rows, one warp each;
+//   3. the CTA that routes the last chunk (the last arrival on the batch
+//      counter) groups all T*k assignments (permute_block).
+// Arrival counters live in a caller-owned, zero-initialised device array; the
+// last arrival on a counter puts it back to zero, so every call finds them
+// zeroed.  Nothing waits: a CTA that is not last simply exits.
+constexpr int RW_MAXT = 64;
+constexpr int RW_WARPS = RL_WARPS;
+constexpr int RW_THREADS = RW_WARPS * 32;
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+// Counts this CTA's arrival on *ctr once all its threads' earlier global writes
+// are done, and tells whether it arrived last of n.  The last arrival puts the
+// counter back to zero and afterwards sees every other arrival's writes (read
+// them through L2).  An arrival number past n means the counter was not zero
+// at launch: recorded, never last.
+__device__ __forceinline__ bool last_arrival(uint32_t* ctr, uint32_t n, int* s_flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const uint32_t before = atomicAdd(ctr, 1u);
+    const bool last = before == n - 1;
+    if (before >= n) record_error(FT_DERR_TABLE);
+    if (last) {
+      atomicExch(ctr, 0u);
+      __threadfence();
+    }
+    *s_flag = last;
+  }
+  __syncthreads();
+  return *s_flag != 0;
 }
 
 template <typename XT, int RT, int PER_LANE>
-__global__ void __launch_bounds__(RF_THREADS)
-route_fused_kernel(const XT* __restrict__ x, const XT* __restrict__ wr, const float* __restrict__ bias, int T,
-                   int H, int E, int k, float* __restrict__ z, int32_t* __restrict__ idx_out,
-                   float* __restrict__ w_out, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                   int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
-  extern __shared__ float xs[];                      // [RT][H]
-  __shared__ int32_t s_cnt[RT_MAXE + 1];
-  __shared__ int32_t s_idx[RF_MAXT * RT_MAXK];
-  __shared__ int32_t s_wsum[RF_WARPS];
+__global__ void __launch_bounds__(RW_THREADS)
+route_grid_kernel(const XT* __restrict__ x, const XT* __restrict__ wr, const float* __restrict__ bias, int T,
+                  int H, int E, int k, float* z, int32_t* idx_out, float* w_out, int32_t* __restrict__ counts,
+                  int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                  uint32_t* __restrict__ arrivals) {
+  extern __shared__ float xs[];  // [RT][H] staged rows; the grouping tables of the last CTA afterwards
+  __shared__ int s_flag;
+  __shared__ int32_t s_wtot[RW_WARPS];
   pdl_begin();
-  const int rank = (int)cluster_ctarank();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int t0 = 0; t0 < T; t0 += RT) {
-    const int nrows = min(RT, T - t0);
-    stage_rows<XT, RT>(x, t0, nrows, H, xs);
-    __syncthreads();
-    logits_of_rows<XT, RT>(xs, wr, bias, t0, nrows, H, E, rank * RF_WARPS + warp, RF_CL * RF_WARPS, z);
-    __syncthreads();
+  const int warp = threadIdx.x >> 5;
+  const int chunk = blockIdx.y;
+  const int t0 = chunk * RT;
+  const int nrows = min(RT, T - t0);
+  stage_rows<XT, RT>(x, t0, nrows, H, xs);
+  __syncthreads();
+  logits_of_rows<XT, RT>(xs, wr, bias, t0, nrows, H, E, blockIdx.x * RW_WARPS + warp, gridDim.x * RW_WARPS, z);
+  if (!last_arrival(arrivals + 1 + chunk, gridDim.x, &s_flag)) {
+    pdl_end();
+    return;
   }
-  __threadfence();
-  cluster_sync_all();
-  if (rank != 0) return;
-  // top-k per token
-  for (int t = warp; t < T; t += RF_WARPS)
+  for (int r = warp; r < nrows; r += RW_WARPS) {
+    const int t = t0 + r;
     route_token<PER_LANE>(z + (size_t)t * E, E, k, idx_out + (size_t)t * k, w_out + (size_t)t * k);
-  for (int e = threadIdx.x; e <= E; e += RF_THREADS) s_cnt[e] = 0;
-  __syncthreads();
-  // permutation of the n = T*k assignments
-  const int n = T * k;
-  for (int a = threadIdx.x; a < n; a += RF_THREADS) {
-    int e = idx_out[a];
-    if ((unsigned)e >= (unsigned)E) {
-      record_error(FT_DERR_EXPERT_INDEX);
-      e = -1;
-    } else {
-      atomicAdd(&s_cnt[e], 1);
-    }
-    s_idx[a] = e;
   }
-  __syncthreads();
-  // exclusive scan of the counts: each thread a run of consecutive experts
-  const int per = ceil_div(E, RF_THREADS);
-  int local = 0;
-  for (int i = 0; i < per; ++i) {
-    const int e = threadIdx.x * per + i;
-    if (e < E) local += s_cnt[e];
+  if (!last_arrival(arrivals, gridDim.y, &s_flag)) {
+    pdl_end();
+    return;
   }
-  int incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(FT_FULL_MASK, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) s_wsum[warp] = incl;
-  __syncthreads();
-  int before = 0;
-  for (int w = 0; w < warp; ++w) before += s_wsum[w];
-  int run = before + incl - local;
-  __syncthreads();                                   // every count is read before it is replaced by its offset
-  for (int i = 0; i < per; ++i) {
-    const int e = threadIdx.x * per + i;
-    if (e < E) {
-      const int c = s_cnt[e];
-      counts[e] = c;
-      offsets[e] = run;
-      s_cnt[e] = run;
-      run += c;
-    }
-  }
-  if (threadIdx.x == 0) offsets[E] = n;
-  __syncthreads();
-  for (int a = threadIdx.x; a < n; a += RF_THREADS) {
-    const int e = s_idx[a];
-    if (e < 0) continue;
-    int r = 0;
-    for (int b = 0; b < a; ++b) r += s_idx[b] == e;
-    const int pos = s_cnt[e] + r;
-    perm[pos] = a;
-    inv[a] = pos;
-  }
+  permute_block<RW_WARPS>(idx_out, T * k, E, counts, offsets, perm, inv, reinterpret_cast<int32_t*>(xs), s_wtot);
   pdl_end();
 }
 

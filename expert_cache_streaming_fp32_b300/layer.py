@@ -21,7 +21,7 @@ from typing import Optional
 
 import torch
 
-from . import (FT_TC_WIDE_ASSIGNMENTS, FT_W_BF16, FT_W_F32, FT_W_FP8E4M3, FT_W_MXFP4, FT_W_NVFP4, Cache,
+from . import (FT_ROUTE_ARRIVAL_WORDS, FT_TC_WIDE_ASSIGNMENTS, FT_W_BF16, FT_W_F32, FT_W_FP8E4M3, FT_W_MXFP4, FT_W_NVFP4, Cache,
                CpuExperts, PinnedBuffer, RegisteredBuffer, ft_combine, ft_pool_read,
                ft_expert_grouped, ft_expert_grouped_workspace, ft_expert_layout_get, ft_permute, ft_route,
                ft_route_fused, ft_router_logits)
@@ -170,6 +170,7 @@ class MoELayer:
         self.offsets = torch.empty(E + 1, **i32)
         self.perm = torch.empty(T_max * k, **i32)
         self.inv = torch.empty(T_max * k, **i32)
+        self.arrivals = torch.zeros(FT_ROUTE_ARRIVAL_WORDS, **i32)   # ft_route_fused's counters, kept zero
         self.slot_of = torch.empty(E, **i32)
         self.slot_fill = torch.empty(E, **i32)
         self.ext = torch.zeros(E, **i32)
@@ -183,7 +184,7 @@ class MoELayer:
         """Router logits, top-k and permutation (one launch for decode batches: ft_route_fused)."""
         T = x.shape[0]
         ft_route_fused(x, w_router, bias, self.cfg.top_k, self.logits[:T], self.idx[:T], self.w[:T], self.counts,
-                       self.offsets, self.perm, self.inv, stream)
+                       self.offsets, self.perm, self.inv, self.arrivals, stream)
 
     def route_unfused(self, x, w_router, bias, stream=None):
         """The same as ``route`` with the three separate kernels."""

@@ -253,37 +253,43 @@ def test_bounded_wait_gives_up_and_reports(ft):
     assert idx.cpu().tolist() == [[1, 3]]
 
 
-# ---------------------------------------------------------------- fused routing (one cluster launch)
+# ---------------------------------------------------------------- fused routing (one grid launch)
 
 @pytest.mark.parametrize("T,H,E,k,dt,zipf", [(1, 2048, 256, 8, "bf16", True), (4, 2048, 256, 8, "bf16", True),
                                              (16, 2048, 256, 8, "bf16", False), (3, 4096, 256, 6, "bf16", True),
                                              (9, 6144, 256, 8, "bf16", False), (5, 256, 16, 2, "f32", False),
                                              (16, 512, 512, 16, "bf16", False), (7, 256, 40, 3, "f32", True),
-                                             (17, 2048, 256, 8, "bf16", True), (64, 2048, 256, 8, "bf16", True)])
+                                             (17, 2048, 256, 8, "bf16", True), (64, 2048, 256, 8, "bf16", True),
+                                             (64, 4096, 64, 6, "bf16", False), (61, 6144, 128, 8, "bf16", True),
+                                             (64, 512, 512, 16, "f32", False), (65, 2048, 256, 8, "bf16", True)])
 def test_route_fused_equals_the_three_kernels_and_the_oracle(ft, T, H, E, k, dt, zipf):
     """ft_route_fused gives bit for bit the logits, routing and permutation of
-    ft_router_logits + ft_route + ft_permute (one cluster launch up to 16 tokens,
-    the three kernels above), and the oracle's routing and grouping of those logits."""
+    ft_router_logits + ft_route + ft_permute (one grid launch up to 64 tokens,
+    the three kernels above), and the oracle's routing and grouping of those
+    logits; its arrival counters are zero again after every call."""
     x = synth.normal((T, H), 1.0, 21 + T, DEV)
     wr = synth.normal((E, H), 0.02, 22 + E, DEV)
     if dt == "bf16":
         x, wr = x.to(torch.bfloat16), wr.to(torch.bfloat16)
     cfg = synth.MoEConfig("rf", H, E, k, 128, 1, synth.W_BF16, dt, seed=3, zipf_s=1.1 if zipf else 0.0)
     b = synth.zipf_bias(cfg, 0).to(DEV)
+    arrivals = torch.zeros(ft.FT_ROUTE_ARRIVAL_WORDS, dtype=torch.int32, device=DEV)
     outs = []
-    for fused in (True, False):
+    for fused in (True, True, False):          # the fused call twice: the counters are reused
         z, idx, w = _f32((T, E)), _i32((T, k)), _f32((T, k))
         counts, offsets, perm, inv = _i32(E), _i32(E + 1), _i32(max(T * k, 1)), _i32(max(T * k, 1))
         if fused:
-            ft.ft_route_fused(x, wr, b, k, z, idx, w, counts, offsets, perm, inv)
+            ft.ft_route_fused(x, wr, b, k, z, idx, w, counts, offsets, perm, inv, arrivals)
         else:
             ft.ft_router_logits(x, wr, b, z)
             ft.ft_route(z, k, idx, w)
             ft.ft_permute(idx, E, counts, offsets, perm, inv)
         torch.cuda.synchronize()
         outs.append([t.cpu().numpy() for t in (z, idx, w, counts, offsets, perm[: T * k], inv[: T * k])])
-    for a, c in zip(outs[0], outs[1]):
-        assert np.array_equal(a, c)
+        assert not arrivals.any()
+    for run in outs[1:]:
+        for a, c in zip(outs[0], run):
+            assert np.array_equal(a, c)
     z, idx, w, counts, offsets, perm, inv = outs[0]
     ref = moe.router_logits(formats.to_f64(x), formats.to_f64(wr), formats.to_f64(b))
     assert np.abs(z - ref).max() <= 2e-5 * (1 + np.abs(ref).max())
@@ -296,12 +302,77 @@ def test_route_fused_equals_the_three_kernels_and_the_oracle(ft, T, H, E, k, dt,
     assert ft.ft_get_device_error() == 0
 
 
+def test_route_fused_in_a_graph_and_on_two_streams(ft):
+    """Replays of one captured call, and two calls in flight on two streams with
+    one counter array each, give the eager results; the counters end at zero."""
+    T, H, E, k = 16, 2048, 256, 8
+    xs = [synth.normal((T, H), 1.0, 40 + i, DEV).to(torch.bfloat16) for i in range(2)]
+    wr = synth.normal((E, H), 0.02, 42, DEV).to(torch.bfloat16)
+
+    def bufs():
+        return [_f32((T, E)), _i32((T, k)), _f32((T, k)), _i32(E), _i32(E + 1), _i32(T * k), _i32(T * k),
+                torch.zeros(ft.FT_ROUTE_ARRIVAL_WORDS, dtype=torch.int32, device=DEV)]
+
+    want = []
+    for x in xs:
+        o = bufs()
+        ft.ft_route_fused(x, wr, None, k, *o)
+        torch.cuda.synchronize()
+        want.append([t.cpu() for t in o[:7]])
+    # graph replay
+    o = bufs()
+    xg = xs[0].clone()
+    g = torch.cuda.CUDAGraph()
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        with torch.cuda.graph(g, stream=st):
+            ft.ft_route_fused(xg, wr, None, k, *o, stream=st)
+    for i in (1, 0, 1):
+        xg.copy_(xs[i])
+        g.replay()
+        torch.cuda.synchronize()
+        assert all(torch.equal(a.cpu(), b) for a, b in zip(o[:7], want[i]))
+        assert not o[7].any()
+    # two streams at once
+    outs = [bufs(), bufs()]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for rep in range(20):
+        for i in range(2):
+            ft.ft_route_fused(xs[i], wr, None, k, *outs[i], stream=streams[i])
+    torch.cuda.synchronize()
+    for i in range(2):
+        assert all(torch.equal(a.cpu(), b) for a, b in zip(outs[i][:7], want[i]))
+        assert not outs[i][7].any()
+    assert ft.ft_get_device_error() == 0
+
+
+def test_route_fused_reports_counters_that_were_not_zero(ft):
+    """A nonzero arrival counter at launch is recorded as FT_DERR_TABLE (no wait, no fault)."""
+    T, H, E, k = 8, 512, 64, 4
+    x = synth.normal((T, H), 1.0, 50, DEV)
+    wr = synth.normal((E, H), 0.02, 51, DEV)
+    arrivals = torch.zeros(ft.FT_ROUTE_ARRIVAL_WORDS, dtype=torch.int32, device=DEV)
+    arrivals[1] = 1 << 20
+    assert ft.ft_get_device_error() == 0
+    o = [_f32((T, E)), _i32((T, k)), _f32((T, k)), _i32(E), _i32(E + 1), _i32(T * k), _i32(T * k)]
+    ft.ft_route_fused(x, wr, None, k, *o, arrivals)
+    torch.cuda.synchronize()
+    assert ft.ft_get_device_error() == 4        # FT_DERR_TABLE, cleared by the read
+    arrivals.zero_()
+    ft.ft_route_fused(x, wr, None, k, *o, arrivals)
+    torch.cuda.synchronize()
+    assert ft.ft_get_device_error() == 0 and not arrivals.any()
+    ri, _ = moe.route(o[0].cpu().numpy().astype(np.float64), k)
+    assert np.array_equal(o[1].cpu().numpy(), ri)
+
+
 def test_route_fused_empty_batch(ft):
     E, k = 256, 8
     counts, offsets = _i32(E), _i32(E + 1)
     x = torch.zeros(0, 2048, dtype=torch.bfloat16, device=DEV)
     wr = torch.zeros(E, 2048, dtype=torch.bfloat16, device=DEV)
     one = _i32(1)
-    ft.ft_route_fused(x, wr, None, k, _f32((1, E)), _i32((1, k)), _f32((1, k)), counts, offsets, one, one)
+    ft.ft_route_fused(x, wr, None, k, _f32((1, E)), _i32((1, k)), _f32((1, k)), counts, offsets, one, one, None)
     torch.cuda.synchronize()
     assert (counts.cpu().numpy() == 0).all() and (offsets.cpu().numpy() == 0).all()
