@@ -165,7 +165,6 @@ bs_skinny_kernel(const __grid_constant__ CUtensorMap map_w0, const __grid_consta
   using namespace sm100;
   constexpr bool MX = WT == FT_W_MXFP4;
   constexpr int BLK = MX ? 32 : 16;
-  constexpr int SPS = BS_BK / BLK;           // scale bytes per row per stage: 16 (NVFP4) or 8 (MXFP4)
   constexpr int ATOMS = MX ? 2 : 4;          // atoms per operand per stage
   const SkArgs a = bs_as_sk(ba);
   extern __shared__ __align__(1024) unsigned char smem_raw[];

@@ -170,7 +170,7 @@ FT_API int ft_router_logits(const void* x, int x_type, const void* w_router, con
   if (T == 0) return FT_OK;
   FT_REQUIRE(x && w_router && logits);
   const int RT = T >= 8 ? 8 : T >= 4 ? 4 : T >= 2 ? 2 : 1;  // rows staged per CTA
-  const size_t smem = (size_t)RT * H * sizeof(float);
+  const size_t smem = (size_t)RT * H * (x_type == FT_X_BF16 ? 2 : 4);  // rows staged in x's type
   if (smem > 227 * 1024 || ceil_div(T, RT) > 65535) return FT_EUNSUPPORTED;
   const int chunks = ceil_div(T, RT);
   const int groups = std::max(1, std::min(ceil_div(E, RL_WARPS), ceil_div(2 * sms(), chunks)));
@@ -231,8 +231,7 @@ FT_API int ft_permute(const int32_t* topk_idx, int T, int k, int E, int32_t* cou
 }
 
 // ------------------------------------------------------------------ fused routing
-// one counter for the batch and one per row chunk (at most RW_MAXT / 8 chunks)
-static_assert(1 + RW_MAXT / 8 <= FT_ROUTE_ARRIVAL_WORDS, "arrival counters");
+static_assert(FT_ROUTE_ARRIVAL_WORDS >= 1, "arrival counter");
 
 namespace {
 template <typename XT, int RT>
@@ -240,13 +239,12 @@ int launch_route_grid(const XT* x, const XT* wr, const float* bias, int T, int H
                       int32_t* idx, float* w, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
                       uint32_t* arrivals, cudaStream_t st) {
   // staged rows, and after them the last CTA's grouping tables
-  const size_t smem = std::max((size_t)RT * H * sizeof(float), (size_t)(2 + RW_WARPS) * E * sizeof(int32_t));
-  const int chunks = ceil_div(T, RT);
-  const int groups = std::max(1, std::min(ceil_div(E, RW_WARPS), ceil_div(2 * sms(), chunks)));
+  const size_t smem = std::max((size_t)RT * H * sizeof(XT), (size_t)(2 + RW_WARPS) * E * sizeof(int32_t));
+  const int groups = std::max(1, std::min(ceil_div(E, RW_WARPS), 2 * sms()));
   auto kr = E <= 256 ? route_grid_kernel<XT, RT, 8> : route_grid_kernel<XT, RT, 16>;
   if (int r = set_smem(kr, smem)) return r;
-  FT_LAUNCH(kr, dim3(groups, chunks), RW_THREADS, smem, st, x, wr, bias, T, H, E, k, z, idx, w, counts, offsets,
-            perm, inv, arrivals);
+  FT_LAUNCH(kr, groups, RW_THREADS, smem, st, x, wr, bias, T, H, E, k, z, idx, w, counts, offsets, perm, inv,
+            arrivals);
   return FT_OK;
 }
 
@@ -256,11 +254,11 @@ int route_grid_rt(const void* x, const void* wr, const float* bias, int T, int H
                   uint32_t* arrivals, cudaStream_t st) {
   const XT* xx = static_cast<const XT*>(x);
   const XT* ww = static_cast<const XT*>(wr);
-  if (T >= 8)
+  if (T > 4)
     return launch_route_grid<XT, 8>(xx, ww, bias, T, H, E, k, z, idx, w, counts, offsets, perm, inv, arrivals, st);
-  if (T >= 4)
+  if (T > 2)
     return launch_route_grid<XT, 4>(xx, ww, bias, T, H, E, k, z, idx, w, counts, offsets, perm, inv, arrivals, st);
-  if (T >= 2)
+  if (T == 2)
     return launch_route_grid<XT, 2>(xx, ww, bias, T, H, E, k, z, idx, w, counts, offsets, perm, inv, arrivals, st);
   return launch_route_grid<XT, 1>(xx, ww, bias, T, H, E, k, z, idx, w, counts, offsets, perm, inv, arrivals, st);
 }
@@ -273,8 +271,8 @@ FT_API int ft_route_fused(const void* x, int x_type, const void* w_router, const
   FT_REQUIRE(x_type == FT_X_F32 || x_type == FT_X_BF16);
   FT_REQUIRE(counts && offsets);
   if (T > 0) FT_REQUIRE(x && w_router && logits && topk_idx && topk_w && perm && inv);
-  const int RT = T >= 8 ? 8 : T >= 4 ? 4 : T >= 2 ? 2 : 1;
-  if (T == 0 || T > RW_MAXT || (size_t)RT * H * sizeof(float) > 200 * 1024) {
+  const int RT = T > 4 ? 8 : T > 2 ? 4 : T;  // rows staged by the one-launch form
+  if (T == 0 || T > RW_MAXT || (size_t)RT * H * (x_type == FT_X_BF16 ? 2 : 4) > 200 * 1024) {
     // larger batches (and the empty one): the three kernels
     if (int r = ft_router_logits(x, x_type, w_router, bias, T, H, E, logits, s)) return r;
     if (int r = ft_route(logits, T, E, k, topk_idx, topk_w, s)) return r;

@@ -32,28 +32,31 @@ __device__ __forceinline__ void load8<float>(const float* p, float (&o)[8]) {
   o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
 }
 
-// Stages token rows t0 .. t0+RT-1 of x (zeros past nrows) in shared memory as fp32.
+// Stages token rows t0 .. t0+RT-1 of x (zeros past nrows) in shared memory,
+// in x's own type (bf16 rows stay bf16: half the shared-memory reads of fp32).
+// Each thread loads its 16-byte piece of every row before storing any.
 template <typename XT, int RT>
-__device__ __forceinline__ void stage_rows(const XT* __restrict__ x, int t0, int nrows, int H, float* xs) {
-  // 8 elements (one 16-byte bf16 load or two fp32 loads) per thread step
-  for (int r = 0; r < RT; ++r) {
-    for (int h = threadIdx.x * 8; h < H; h += blockDim.x * 8) {
-      float v[8];
-      if (r < nrows) {
-        load8<XT>(x + (size_t)(t0 + r) * H + h, v);
-      } else {
+__device__ __forceinline__ void stage_rows(const XT* __restrict__ x, int t0, int nrows, int H, XT* xs) {
+  constexpr int V = 16 / (int)sizeof(XT);
+  for (int h = threadIdx.x * V; h < H; h += blockDim.x * V) {
+    uint4 v[RT];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = 0.0f;
-      }
-      *reinterpret_cast<float4*>(xs + r * H + h) = make_float4(v[0], v[1], v[2], v[3]);
-      *reinterpret_cast<float4*>(xs + r * H + h + 4) = make_float4(v[4], v[5], v[6], v[7]);
-    }
+    for (int r = 0; r < RT; ++r)
+      v[r] = r < nrows ? *reinterpret_cast<const uint4*>(x + (size_t)(t0 + r) * H + h) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int r = 0; r < RT; ++r) *reinterpret_cast<uint4*>(xs + r * H + h) = v[r];
   }
+}
+
+// Eight consecutive staged elements as fp32 (exact for both types).
+template <typename XT>
+__device__ __forceinline__ void staged8(const XT* p, float (&o)[8]) {
+  load8<XT>(p, o);
 }
 
 // Logits of the staged rows for experts e0, e0 + e_step, ... (one warp per expert).
 template <typename XT, int RT>
-__device__ __forceinline__ void logits_of_rows(const float* xs, const XT* __restrict__ wr,
+__device__ __forceinline__ void logits_of_rows(const XT* xs, const XT* __restrict__ wr,
                                                const float* __restrict__ bias, int t0, int nrows, int H, int E,
                                                int e0, int e_step, float* __restrict__ z) {
   const int lane = threadIdx.x & 31;
@@ -81,11 +84,10 @@ __device__ __forceinline__ void logits_of_rows(const float* xs, const XT* __rest
         if (k < H) {
 #pragma unroll
           for (int r = 0; r < RT; ++r) {
-            const float* xr = xs + r * H + k;
-            float4 a = *reinterpret_cast<const float4*>(xr);
-            float4 b = *reinterpret_cast<const float4*>(xr + 4);
-            acc[r] += wv[u][0] * a.x + wv[u][1] * a.y + wv[u][2] * a.z + wv[u][3] * a.w +
-                      wv[u][4] * b.x + wv[u][5] * b.y + wv[u][6] * b.z + wv[u][7] * b.w;
+            float a[8];
+            staged8<XT>(xs + r * H + k, a);
+            acc[r] += wv[u][0] * a[0] + wv[u][1] * a[1] + wv[u][2] * a[2] + wv[u][3] * a[3] +
+                      wv[u][4] * a[4] + wv[u][5] * a[5] + wv[u][6] * a[6] + wv[u][7] * a[7];
           }
         }
       }
@@ -101,7 +103,8 @@ template <typename XT, int RT>
 __global__ void __launch_bounds__(RL_WARPS * 32)
 router_logits_kernel(const XT* __restrict__ x, const XT* __restrict__ wr, const float* __restrict__ bias,
                      int T, int H, int E, float* __restrict__ z) {
-  extern __shared__ float xs[];  // [RT][H]
+  extern __shared__ __align__(16) unsigned char rl_smem[];
+  XT* xs = reinterpret_cast<XT*>(rl_smem);  // [RT][H]
   pdl_begin();
   const int t0 = blockIdx.y * RT;
   const int nrows = min(RT, T - t0);
@@ -114,75 +117,92 @@ router_logits_kernel(const XT* __restrict__ x, const XT* __restrict__ wr, const 
 
 // ====================================================================== top-k gating
 // One warp per token.  Lane l holds logits e = l, l+32, ...  Each of the k
-// rounds takes the warp-wide maximum of (value, -index) among the experts not
-// yet chosen.  Weights are a softmax over the chosen logits.
+// rounds takes, among the experts not yet chosen, the largest logit, ties to
+// the smaller expert id.  Logits are compared as order-preserving 32-bit keys
+// (-0 taken as +0, so equal logits have equal keys); a round is two warp
+// reductions: the largest key, then the smallest id holding it.  NaN logits
+// are never preferred; a round that finds only NaN left takes the smallest
+// id not yet chosen, so every id stays in range.  Weights are a softmax over
+// the chosen logits, summed in choice order.
 constexpr int RT_MAXK = 16;
 constexpr int RT_MAXE = 1024;
 
-__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
+// 0 for NaN, else a key whose unsigned order is the order of the values (> 0).
+__device__ __forceinline__ uint32_t logit_key(float v) {
+  if (v != v) return 0u;
+  const uint32_t b = __float_as_uint(v == 0.0f ? 0.0f : v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// Top-k of one token's logits z[0..E-1] by one warp; lane 0 writes idx_row and w_row.
-// The logits are read through L2: other CTAs of the same launch may have written them.
+// Top-k of one token's logits z[0..E-1] by one warp; lanes 0..k-1 write idx_row and w_row
+// (and the ids to idx_shared too, when given).  The logits are read through L2: other
+// CTAs of the same launch may have written them.
 template <int PER_LANE>
 __device__ __forceinline__ void route_token(const float* z, int E, int k, int32_t* __restrict__ idx_row,
-                                            float* __restrict__ w_row) {
+                                            float* __restrict__ w_row, int32_t* idx_shared = nullptr) {
   const int lane = threadIdx.x & 31;
   float v[PER_LANE];
+  uint32_t key[PER_LANE];
   unsigned taken = 0;
 #pragma unroll
   for (int i = 0; i < PER_LANE; ++i) {
-    int e = lane + 32 * i;
+    const int e = lane + 32 * i;
     v[i] = e < E ? __ldcg(z + e) : -INFINITY;
+    key[i] = e < E ? logit_key(v[i]) : 0u;
     if (e >= E) taken |= 1u << i;
   }
   float my_v = 0.0f;  // lane j keeps the j-th choice
   int my_i = 0;
 #pragma unroll 1
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
+    // this lane's candidate: its largest untaken key, the smaller id on ties
+    uint32_t bk = 0;
     int bi = 0x7fffffff;
+    float bv = 0.0f;
 #pragma unroll
     for (int i = 0; i < PER_LANE; ++i) {
-      int e = lane + 32 * i;
-      if (!(taken >> i & 1u) && better(v[i], e, bv, bi)) { bv = v[i]; bi = e; }
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      float ov = __shfl_xor_sync(FT_FULL_MASK, bv, o);
-      int oi = __shfl_xor_sync(FT_FULL_MASK, bi, o);
-      if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-    }
-    // NaN logits or all -inf: fall back to the lowest untaken index so the id stays in range
-    if (bi >= E) {
-      int cand = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < PER_LANE; ++i) {
-        int e = lane + 32 * i;
-        if (!(taken >> i & 1u) && e < cand) cand = e;
+      if (!(taken >> i & 1u) && key[i] > bk) {
+        bk = key[i];
+        bi = lane + 32 * i;
+        bv = v[i];
       }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) cand = min(cand, __shfl_xor_sync(FT_FULL_MASK, cand, o));
-      bi = cand;
-      bv = __ldcg(z + bi);
     }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    const uint32_t m = __reduce_max_sync(FT_FULL_MASK, bk);
+    int win;
+    float wv;
+    if (m != 0u) {
+      win = (int)__reduce_min_sync(FT_FULL_MASK, bk == m ? (uint32_t)bi : 0x7fffffffu);
+      wv = __shfl_sync(FT_FULL_MASK, bv, win & 31);
+    } else {
+      // only NaN left: the smallest id not yet chosen
+      uint32_t cand = 0x7fffffffu;
+#pragma unroll
+      for (int i = 0; i < PER_LANE; ++i)
+        if (!(taken >> i & 1u)) cand = min(cand, (uint32_t)(lane + 32 * i));
+      win = (int)__reduce_min_sync(FT_FULL_MASK, cand);
+      wv = __ldcg(z + win);
+    }
+    if ((win & 31) == lane) taken |= 1u << (win >> 5);
     if (lane == j) {
-      my_v = bv;
-      my_i = bi;
+      my_v = wv;
+      my_i = win;
     }
   }
   // softmax over the chosen logits; the sum runs in choice order
-  const float m = __shfl_sync(FT_FULL_MASK, my_v, 0);
-  const float ex = lane < k ? expf(my_v - m) : 0.0f;
-  float s = 0.0f;
-#pragma unroll 1
-  for (int j = 0; j < k; ++j) s += __shfl_sync(FT_FULL_MASK, ex, j);
-  const float inv = 1.0f / s;
+  const float mx = __shfl_sync(FT_FULL_MASK, my_v, 0);
+  const float ex = lane < k ? expf(my_v - mx) : 0.0f;
+  float part[RT_MAXK];
+#pragma unroll
+  for (int j = 0; j < RT_MAXK; ++j) part[j] = __shfl_sync(FT_FULL_MASK, ex, j);
+  float sum = 0.0f;
+#pragma unroll
+  for (int j = 0; j < RT_MAXK; ++j)
+    if (j < k) sum += part[j];
+  const float inv = 1.0f / sum;
   if (lane < k) {
     idx_row[lane] = my_i;
     w_row[lane] = ex * inv;
+    if (idx_shared) idx_shared[lane] = my_i;
   }
 }
 
@@ -205,13 +225,19 @@ route_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __r
 // lanes below; across warps a per-(warp, expert) count table is scanned in warp
 // order, continuing from the previous tiles.  Positions therefore follow the
 // assignment order a = t*k + j within each expert (stable), which makes the
-// result unique.  idx is read through L2 (it may have been written by other
-// CTAs of the same launch).  tab holds (2 + W) * E ints of shared memory.
+// result unique.  idx is in shared memory (IDX_SHARED) or global memory, read
+// through L2 (other CTAs of the same launch may have written it).  tab holds
+// (2 + W) * E ints of shared memory.
 constexpr int PM_THREADS = 1024;
 constexpr int PM_WARPS = PM_THREADS / 32;
 constexpr int PM_MAXE = 512;
 
-template <int W>
+template <int W, bool IDX_SHARED = false>
+__device__ __forceinline__ int load_id(const int32_t* idx, int a) {
+  return IDX_SHARED ? idx[a] : __ldcg(idx + a);
+}
+
+template <int W, bool IDX_SHARED = false>
 __device__ __forceinline__ void permute_block(const int32_t* idx, int n, int E, int32_t* __restrict__ counts,
                                               int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
                                               int32_t* __restrict__ inv, int32_t* tab, int32_t* warp_tot) {
@@ -225,7 +251,7 @@ __device__ __forceinline__ void permute_block(const int32_t* idx, int n, int E, 
   for (int i = tid; i < W * E; i += NT) wc[i] = 0;
   __syncthreads();
   for (int a = tid; a < n; a += NT) {
-    const int e = __ldcg(idx + a);
+    const int e = load_id<W, IDX_SHARED>(idx, a);
     if ((unsigned)e < (unsigned)E) atomicAdd(&cnt[e], 1);
     else record_error(FT_DERR_EXPERT_INDEX);
   }
@@ -272,7 +298,7 @@ __device__ __forceinline__ void permute_block(const int32_t* idx, int n, int E, 
   __syncthreads();
   for (int t0 = 0; t0 < n; t0 += NT) {
     const int a = t0 + tid;
-    int e = a < n ? __ldcg(idx + a) : -1;
+    int e = a < n ? load_id<W, IDX_SHARED>(idx, a) : -1;
     if ((unsigned)e >= (unsigned)E) e = -1;
     const unsigned peers = __match_any_sync(FT_FULL_MASK, e);
     const int rank = __popc(peers & ((1u << lane) - 1));
@@ -302,6 +328,58 @@ __device__ __forceinline__ void permute_block(const int32_t* idx, int n, int E, 
   }
 }
 
+// The same grouping for n <= 32 assignments by one warp: lane a holds the
+// expert of assignment a (anything for a >= n).  Equal experts are grouped with
+// __match_any_sync (the rank is the number of equal lanes below); the counts
+// go through cnt (E ints of shared memory), which the warp scans in place.
+__device__ __forceinline__ void permute_warp(int e_a, int n, int E, int32_t* __restrict__ counts,
+                                             int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+                                             int32_t* __restrict__ inv, int32_t* cnt) {
+  const int lane = threadIdx.x & 31;
+  for (int e = lane; e < E; e += 32) cnt[e] = 0;
+  bool valid = lane < n;
+  if (valid && (unsigned)e_a >= (unsigned)E) {
+    record_error(FT_DERR_EXPERT_INDEX);
+    valid = false;
+  }
+  const unsigned peers = __match_any_sync(FT_FULL_MASK, valid ? e_a : -1);
+  const int rank = __popc(peers & ((1u << lane) - 1));
+  __syncwarp();
+  if (valid && rank == 0) cnt[e_a] = __popc(peers);
+  __syncwarp();
+  // exclusive scan: each lane a run of consecutive experts
+  const int per = ceil_div(E, 32);
+  int local = 0;
+  for (int i = 0; i < per; ++i) {
+    const int e = lane * per + i;
+    if (e < E) local += cnt[e];
+  }
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(FT_FULL_MASK, incl, o);
+    if (lane >= o) incl += y;
+  }
+  int run = incl - local;
+  for (int i = 0; i < per; ++i) {
+    const int e = lane * per + i;
+    if (e < E) {
+      const int c = cnt[e];
+      counts[e] = c;
+      offsets[e] = run;
+      cnt[e] = run;
+      run += c;
+    }
+  }
+  if (lane == 0) offsets[E] = n;
+  __syncwarp();
+  if (valid) {
+    const int pos = cnt[e_a] + rank;
+    perm[pos] = lane;
+    inv[lane] = pos;
+  }
+}
+
 __global__ void __launch_bounds__(PM_THREADS)
 permute_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __restrict__ counts,
                int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
@@ -313,19 +391,21 @@ permute_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __restric
 }
 
 // ====================================================================== fused routing (decode batches)
-// Router logits, top-k and the permutation of a small batch (T <= RW_MAXT) in
-// one launch over the grid of router_logits_kernel (expert groups x row
-// chunks), so the router matrix is read by many SMs at once:
-//   1. each CTA computes the logits of its RT rows for its experts (the same
+// Router logits, top-k and the permutation of a small batch (T <= RW_MAXT, one
+// chunk of rows) in one launch over the grid of router_logits_kernel, so the
+// router matrix is read by many SMs at once:
+//   1. each CTA computes the logits of the rows for its experts (the same
 //      per-expert arithmetic as router_logits_kernel: bit-identical logits);
-//   2. the CTA that completes a row chunk (the last of its expert groups to
-//      arrive on the chunk's counter) routes the chunk's rows, one warp each;
-//   3. the CTA that routes the last chunk (the last arrival on the batch
-//      counter) groups all T*k assignments (permute_block).
-// Arrival counters live in a caller-owned, zero-initialised device array; the
-// last arrival on a counter puts it back to zero, so every call finds them
-// zeroed.  Nothing waits: a CTA that is not last simply exits.
-constexpr int RW_MAXT = 64;
+//   2. the CTA that arrives last on an arrival counter (after a fence) routes
+//      the rows, one warp each, and groups the T*k assignments (one warp when
+//      they fit in one, else the whole CTA).
+// The counter lives in a caller-owned, zero-initialised device word; the last
+// arrival puts it back to zero, so every call finds it zeroed.  Nothing
+// waits: a CTA that is not last simply exits.  (Larger batches are faster as
+// router_logits_kernel, route_kernel and permute_kernel: eight and more rows
+// route in parallel over several CTAs, and the 1024-thread grouping is quicker
+// than one CTA's.)
+constexpr int RW_MAXT = 8;
 constexpr int RW_WARPS = RL_WARPS;
 constexpr int RW_THREADS = RW_WARPS * 32;
 
@@ -354,33 +434,35 @@ __device__ __forceinline__ bool last_arrival(uint32_t* ctr, uint32_t n, int* s_f
 template <typename XT, int RT, int PER_LANE>
 __global__ void __launch_bounds__(RW_THREADS)
 route_grid_kernel(const XT* __restrict__ x, const XT* __restrict__ wr, const float* __restrict__ bias, int T,
-                  int H, int E, int k, float* z, int32_t* idx_out, float* w_out, int32_t* __restrict__ counts,
-                  int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
-                  uint32_t* __restrict__ arrivals) {
-  extern __shared__ float xs[];  // [RT][H] staged rows; the grouping tables of the last CTA afterwards
+                  int H, int E, int k, float* z, int32_t* __restrict__ idx_out, float* __restrict__ w_out,
+                  int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+                  int32_t* __restrict__ inv, uint32_t* __restrict__ arrivals) {
+  static_assert(RT <= RW_MAXT, "one chunk of rows");
+  extern __shared__ __align__(16) unsigned char rw_smem[];
+  XT* xs = reinterpret_cast<XT*>(rw_smem);  // [RT][H] staged rows; the grouping tables of the last CTA afterwards
   __shared__ int s_flag;
   __shared__ int32_t s_wtot[RW_WARPS];
+  __shared__ int32_t s_idx[RT * RT_MAXK];   // the batch's expert ids
   pdl_begin();
   const int warp = threadIdx.x >> 5;
-  const int chunk = blockIdx.y;
-  const int t0 = chunk * RT;
-  const int nrows = min(RT, T - t0);
-  stage_rows<XT, RT>(x, t0, nrows, H, xs);
+  const int nrows = min(RT, T);
+  stage_rows<XT, RT>(x, 0, nrows, H, xs);
   __syncthreads();
-  logits_of_rows<XT, RT>(xs, wr, bias, t0, nrows, H, E, blockIdx.x * RW_WARPS + warp, gridDim.x * RW_WARPS, z);
-  if (!last_arrival(arrivals + 1 + chunk, gridDim.x, &s_flag)) {
+  logits_of_rows<XT, RT>(xs, wr, bias, 0, nrows, H, E, blockIdx.x * RW_WARPS + warp, gridDim.x * RW_WARPS, z);
+  if (!last_arrival(arrivals, gridDim.x, &s_flag)) {
     pdl_end();
     return;
   }
-  for (int r = warp; r < nrows; r += RW_WARPS) {
-    const int t = t0 + r;
-    route_token<PER_LANE>(z + (size_t)t * E, E, k, idx_out + (size_t)t * k, w_out + (size_t)t * k);
+  for (int r = warp; r < nrows; r += RW_WARPS)
+    route_token<PER_LANE>(z + (size_t)r * E, E, k, idx_out + (size_t)r * k, w_out + (size_t)r * k, s_idx + r * k);
+  __syncthreads();
+  const int n = nrows * k;
+  int32_t* tab = reinterpret_cast<int32_t*>(rw_smem);
+  if (n <= 32) {
+    if (warp == 0) permute_warp(threadIdx.x < n ? s_idx[threadIdx.x] : -1, n, E, counts, offsets, perm, inv, tab);
+  } else {
+    permute_block<RW_WARPS, true>(s_idx, n, E, counts, offsets, perm, inv, tab, s_wtot);
   }
-  if (!last_arrival(arrivals, gridDim.y, &s_flag)) {
-    pdl_end();
-    return;
-  }
-  permute_block<RW_WARPS>(idx_out, T * k, E, counts, offsets, perm, inv, reinterpret_cast<int32_t*>(xs), s_wtot);
   pdl_end();
 }
 

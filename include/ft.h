@@ -219,18 +219,18 @@ int ft_permute(const int32_t* topk_idx, int T, int k, int E, int32_t* counts, in
 /* ------------------------------------------------------------------------
  * ft_route_fused: ft_router_logits, ft_route and ft_permute of one batch, with
  * the same arguments and results (the logits are bit-identical), for the
- * per-token routing and grouping of a decode step.  Batches of at most 64
- * tokens (with min(T, 8) * H * 4 bytes of staged rows <= 200 KiB) run as one
- * launch over the grid of ft_router_logits: each CTA computes the logits of a
- * share of the experts for a chunk of rows; the CTA that completes a chunk
- * routes its rows, and the one that routes the last chunk groups the
- * assignments.  Larger batches (and T = 0) run the three kernels.
+ * per-token routing and grouping of a decode step.  Batches of at most 8
+ * tokens (with min(T, 8) * H * (2 for bf16 x, 4 for fp32) bytes of staged
+ * rows <= 200 KiB) run as one launch over the grid of ft_router_logits: each
+ * CTA computes the logits of a share of the experts; the CTA that finishes
+ * last routes the tokens and groups the assignments.  Larger batches (and
+ * T = 0) run the three kernels, which are faster there.
  * arrivals: device uint32[FT_ROUTE_ARRIVAL_WORDS], caller-owned, all zero
- * before the first call; every call that runs the one launch leaves them zero
- * again.  One call at a time per array (calls in flight on several streams
- * need one array each).  A nonzero word at launch is recorded as
- * FT_DERR_TABLE, and that call's outputs are not valid.  Unused (may be NULL)
- * when the batch runs the three kernels.
+ * before the first call; every call leaves them zero again.  One call at a
+ * time per array (calls in flight on several streams need one array each).
+ * A nonzero word at launch is recorded as FT_DERR_TABLE, and that call's
+ * outputs are not valid.  Unused (may be NULL) when the batch runs the three
+ * kernels.
  * T >= 0, H a multiple of 8, 1 <= E <= 512, 1 <= k <= min(E, 16).
  * ---------------------------------------------------------------------- */
 #define FT_ROUTE_ARRIVAL_WORDS 16

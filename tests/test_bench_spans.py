@@ -56,16 +56,16 @@ def test_launch_count_per_step():
         n_layers, wtype = 40, bench.synth.W_BF16
 
     class Run:
-        cfg, n_waves, n_steps, batches = Cfg, 1, 256, [1, 64, 65]
+        cfg, n_waves, n_steps, batches = Cfg, 1, 256, [1, 8, 64]
         launches_per_step = bench.DecodeRun.launches_per_step
         launches_per_pass = bench.DecodeRun.launches_per_pass
 
     r = Run()
-    r.b = {1: {"split": False}, 64: {"split": True}, 65: {"split": True}}
+    r.b = {1: {"split": False}, 8: {"split": False}, 64: {"split": True}}
     assert r.launches_per_step(1) == 40 * 7       # fused route, control, fill, gather + gate/up + down, combine
-    assert r.launches_per_step(64) == 40 * 10     # fused route, a second expert call in the split form
-    assert r.launches_per_step(65) == 40 * 12     # past 64 tokens: the three routing kernels
-    assert r.launches_per_pass() == 256 * 40 * (7 + 10 + 12)
+    assert r.launches_per_step(8) == 40 * 7       # up to 8 tokens: one routing launch
+    assert r.launches_per_step(64) == 40 * 12     # the three routing kernels, a second expert call (split form)
+    assert r.launches_per_pass() == 256 * 40 * (7 + 7 + 12)
 
 
 def test_step_times_per_batch_exclude_the_reset_between_batches():

@@ -260,13 +260,15 @@ def test_bounded_wait_gives_up_and_reports(ft):
                                              (9, 6144, 256, 8, "bf16", False), (5, 256, 16, 2, "f32", False),
                                              (16, 512, 512, 16, "bf16", False), (7, 256, 40, 3, "f32", True),
                                              (17, 2048, 256, 8, "bf16", True), (64, 2048, 256, 8, "bf16", True),
-                                             (64, 4096, 64, 6, "bf16", False), (61, 6144, 128, 8, "bf16", True),
-                                             (64, 512, 512, 16, "f32", False), (65, 2048, 256, 8, "bf16", True)])
+                                             (8, 2048, 256, 8, "bf16", True), (6, 512, 512, 16, "bf16", False),
+                                             (2, 6144, 128, 8, "bf16", True), (8, 6144, 256, 8, "bf16", False),
+                                             (3, 512, 512, 16, "f32", False), (61, 6144, 128, 8, "bf16", True)])
 def test_route_fused_equals_the_three_kernels_and_the_oracle(ft, T, H, E, k, dt, zipf):
     """ft_route_fused gives bit for bit the logits, routing and permutation of
-    ft_router_logits + ft_route + ft_permute (one grid launch up to 64 tokens,
-    the three kernels above), and the oracle's routing and grouping of those
-    logits; its arrival counters are zero again after every call."""
+    ft_router_logits + ft_route + ft_permute (one grid launch up to 8 tokens,
+    the grouping by one warp up to 32 assignments, else by the CTA; the three
+    kernels above), and the oracle's routing and grouping of those logits; its
+    arrival counters are zero again after every call."""
     x = synth.normal((T, H), 1.0, 21 + T, DEV)
     wr = synth.normal((E, H), 0.02, 22 + E, DEV)
     if dt == "bf16":
@@ -305,7 +307,7 @@ def test_route_fused_equals_the_three_kernels_and_the_oracle(ft, T, H, E, k, dt,
 def test_route_fused_in_a_graph_and_on_two_streams(ft):
     """Replays of one captured call, and two calls in flight on two streams with
     one counter array each, give the eager results; the counters end at zero."""
-    T, H, E, k = 16, 2048, 256, 8
+    T, H, E, k = 8, 2048, 256, 8
     xs = [synth.normal((T, H), 1.0, 40 + i, DEV).to(torch.bfloat16) for i in range(2)]
     wr = synth.normal((E, H), 0.02, 42, DEV).to(torch.bfloat16)
 
@@ -353,7 +355,7 @@ def test_route_fused_reports_counters_that_were_not_zero(ft):
     x = synth.normal((T, H), 1.0, 50, DEV)
     wr = synth.normal((E, H), 0.02, 51, DEV)
     arrivals = torch.zeros(ft.FT_ROUTE_ARRIVAL_WORDS, dtype=torch.int32, device=DEV)
-    arrivals[1] = 1 << 20
+    arrivals[0] = 1 << 20
     assert ft.ft_get_device_error() == 0
     o = [_f32((T, E)), _i32((T, k)), _f32((T, k)), _i32(E), _i32(E + 1), _i32(T * k), _i32(T * k)]
     ft.ft_route_fused(x, wr, None, k, *o, arrivals)
