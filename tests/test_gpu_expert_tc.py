@@ -76,6 +76,8 @@ def _run(ft, x, k, I, E, perm, offsets, slot_of, pool, S, n_slots, wtype=synth.W
     (4096, 512, 16, 4, 1, 10, False),     # one token, 4 experts: gate/up K split 4 ways
     (256, 2048, 8, 2, 1, 11, False),      # one token, 2 experts: down K split 4 ways
     (512, 256, 2, 2, 100, 12, False),     # 100 rows per expert: two token chunks on the small-batch tiling
+    (256, 128, 64, 8, 250, 13, True),     # 2000 assignments over 64 experts, heavy and light
+    (512, 256, 8, 8, 255, 14, False),     # 255 rows per expert: four 64-row chunks each
 ])
 def test_tc_expert_grouped_parity(ft, H, I, E, k, T, seed, skewed):
     cfg, L, S, n_slots, pool, slot_perm, comps, x, idx = _setup(ft, H, I, E, k, T, seed, skewed)
