@@ -85,7 +85,7 @@ def parse():
                    help="decode with ft_cache_step (fill, then all experts) instead of the split form "
                         "(hits evaluated while the fill copies)")
     p.add_argument("--kernel-case", default="", choices=["", "experts_decode", "experts_prefill", "fill",
-                                                         "fill_overlap"],
+                                                         "fill_overlap", "route"],
                    help="time one expert-kernel case on a small resident pool (profiling aid; prints its own line)")
     p.add_argument("--reps", type=int, default=5)
     p.add_argument("--fp4-path", default="block_scaled", choices=["block_scaled", "expand"],
@@ -1215,6 +1215,53 @@ def fill_overlap_case(args):
                       "device_error": ft.ft_get_device_error()}))
 
 
+def route_case(args):
+    """Routing of one decode batch (T = --batches[0]) of the 40-layer BF16 stack: the 40 layers'
+    ft_route_fused calls (one launch up to 8 tokens), and the three routing kernels, each as one
+    CUDA graph over the 40 routers, with a 256 MB write between layers (so that the router rows
+    come from HBM, as in a decode step).  Prints ms per layer for both forms and for the writes
+    alone.  Holds under 1 GB on the device."""
+    import expert_cache_streaming_fp32_b300 as ft
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    cfg = synth.DECODE_BF16
+    T, H, E, k, L = int(args.batches.split(",")[0]), cfg.hidden, cfg.n_experts, cfg.top_k, cfg.n_layers
+    routers = [synth.router_weights(cfg, l, dev) for l in range(L)]
+    x = synth.AR1Trace(cfg, T, dev, tag=7).next()
+    lay = ft.MoELayer(cfg, T, dev)
+    junk = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = {}
+    for form in ("fused", "three", "writes"):
+        st = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(st):
+            lay.route(x, *routers[0], stream=st)
+            lay.route_unfused(x, *routers[0], stream=st)
+            st.synchronize()
+            with torch.cuda.graph(g, stream=st):
+                for l in range(L):
+                    junk.fill_(l)
+                    if form == "fused":
+                        lay.route(x, *routers[l], stream=st)
+                    elif form == "three":
+                        lay.route_unfused(x, *routers[l], stream=st)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        out[form] = e0.elapsed_time(e1) / args.reps / L
+    print(json.dumps({"kernel_case": "route", "config": cfg.name, "T": T, "layers": L,
+                      "ms_per_layer": {"one_launch": out["fused"] - out["writes"],
+                                       "three_kernels": out["three"] - out["writes"]},
+                      "write_ms_per_layer": out["writes"], "arrivals_zero": not bool(lay.arrivals.any()),
+                      "device_error": ft.ft_get_device_error()}))
+
+
 def kernel_case(args):
     """One layer's experts resident in a 256-record slot pool (1.6 GB); ft_expert_grouped timed alone.
 
@@ -1279,6 +1326,9 @@ def main():
         return
     if args.kernel_case == "fill_overlap":
         fill_overlap_case(args)
+        return
+    if args.kernel_case == "route":
+        route_case(args)
         return
     if args.kernel_case:
         kernel_case(args)

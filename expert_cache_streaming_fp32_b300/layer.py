@@ -36,8 +36,9 @@ from . import (FT_ROUTE_ARRIVAL_WORDS, FT_TC_WIDE_ASSIGNMENTS, FT_W_BF16, FT_W_F
 #     T=16 1364 -> 1435, T=64 4270 -> 4655;
 #   NVFP4, 43 layers, H=4096, I=2048, k=6: T=1 61.5 -> 64.3, T=4 139 -> 160;
 #   MXFP4, 4 layers, H=6144, I=2048, k=8, T=1: 2-6% more with the split form.
-# FP4 experts cost more to evaluate (the in-kernel expansion), so their hits
-# cover the extra call already at T=1.
+# (The FP4 figures were taken with the exact bf16 expansion of the weights.)  An
+# FP4 record is 2.25x to 3.2x the bytes of a bf16 one of the same hidden size, so
+# its hits cover the extra call already at T=1.
 SPLIT_MIN_ASSIGNMENTS = {FT_W_F32: 64, FT_W_BF16: 64, FT_W_FP8E4M3: 64, FT_W_NVFP4: 1, FT_W_MXFP4: 1}
 # Batches on the large-batch tensor-core tiling (prefill waves) take
 # ft_cache_step too: beside those kernels, which fill every SM, the fill's
