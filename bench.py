@@ -45,6 +45,7 @@ TRAFFIC_PER_BYTE = {"fill": (0.025e6 + 140.025e6) / 201.327e6,
                     "experts": (207.776e6 + 3.545e6 + 103.355e6 + 2.734e6) / (205.5e6 + 0.5e6 + 102.8e6)}
 CACHE_FRAC = 0.40
 ROUTE_FUSED_MAX_T = 8             # batches routed by one ft_route_fused launch
+CC_MAX_ASSIGNMENTS = 8            # FT_CC_MAX_ASSIGNMENTS: bf16 experts of one token run on the CUDA cores
 FP4_OVER_BF16 = 13.5 / 2.25       # nominal dense FP4 / bf16 tensor rates of the B300
 METRIC = "MoE-layer tokens/s (decode T=1..64, prefill 8192) and % of layer roofline"
 WORKLOAD = ("decode_bf16_40L: H=2048 E=256 top-8 I=512, bf16 weights, 40 layers, 64.4 GB pinned host pool, "
@@ -266,9 +267,13 @@ class DecodeRun:
     def launches_per_step(self, T) -> int:
         # routing (one fused launch, or router_logits + route + permute), (control, fill, expert
         # kernels) per wave, combine;
-        # bf16 experts run gather + gate/up + down on the tensor cores, other formats gate/up + down
+        # bf16 experts run gather + gate/up + down on the tensor cores (gate/up + down on the CUDA
+        # cores for one token), other formats gate/up + down
         # (the split form evaluates hits and filled experts in two expert calls)
-        n_exp = 3 if self.cfg.wtype == synth.W_BF16 else 2
+        if self.cfg.wtype == synth.W_BF16:
+            n_exp = 2 if T * self.cfg.top_k <= CC_MAX_ASSIGNMENTS else 3
+        else:
+            n_exp = 2
         if self.b[T]["split"]:
             n_exp *= 2
         n_route = 1 if T <= ROUTE_FUSED_MAX_T else 3       # ft_route_fused: one grid launch up to 8 tokens

@@ -46,6 +46,7 @@ EXPORTED = [
 ]
 FT_NOALLOC_MAX_ELEMS = 1 << 20
 FT_TC_WIDE_ASSIGNMENTS = 2048
+FT_CC_MAX_ASSIGNMENTS = 8
 FT_ROUTE_ARRIVAL_WORDS = 16
 
 

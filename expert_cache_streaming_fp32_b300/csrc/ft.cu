@@ -435,8 +435,11 @@ int make_map_fp4(CUtensorMap* m, const void* base, int K, int rows, int slots, u
 
 // The tensor-core path takes bf16, NVFP4 and MXFP4 weights (H and I multiples
 // of 128, which the record layout already requires).
+// bf16 weights at up to FT_CC_MAX_ASSIGNMENTS assignments (one decode token) are matrix-vector
+// products: the CUDA-core kernels stream them with two launches and no row gather.
 bool tc_path_applies(int wtype, int T, int k, int H, int I, int E) {
   const long long Tk = (long long)T * k;
+  if (wtype == FT_W_BF16 && Tk <= FT_CC_MAX_ASSIGNMENTS) return false;
   const bool fmt = wtype == FT_W_BF16 || tc::is_fp4(wtype);
   return fmt && H % 128 == 0 && I % 128 == 0 && E <= tc::MAX_E && Tk < (1ll << 28);
 }

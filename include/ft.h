@@ -376,8 +376,8 @@ int ft_cache_export(ft_cache* c, int32_t* key_of_slot, uint32_t* stamp, int* n_s
  * or on the slot used.
  *
  * Two execution paths, chosen by the weight format:
- *   - bf16, NVFP4 and MXFP4 weights: tcgen05 tensor cores at every batch
- *     size.  Below FT_TC_WIDE_ASSIGNMENTS assignments (T*k) the weights are the
+ *   - bf16 (above FT_CC_MAX_ASSIGNMENTS assignments), NVFP4 and MXFP4 weights:
+ *     tcgen05 tensor cores.  Below FT_TC_WIDE_ASSIGNMENTS assignments (T*k) the weights are the
  *     MMA's M side (128 weight rows) and up to 64 of an expert's token rows its
  *     N side, with the K range split when few experts are routed; from
  *     FT_TC_WIDE_ASSIGNMENTS up, 128 token rows against 128 or 256 weight rows
@@ -389,11 +389,14 @@ int ft_cache_export(ft_cache* c, int32_t* key_of_slot, uint32_t* stamp, int* n_s
  *     MXFP4 block scale above 2^15 (E8M0 byte > 142) is beyond its range: the
  *     kernel records FT_DERR_SCALE_RANGE and those outputs are wrong.  NVFP4's
  *     fp32 matrix scale multiplies the fp32 results.
- *   - fp32 and FP8 weights: CUDA cores, weights streamed once per 8-row chunk
- *     of an expert's rows and dequantised in registers; x and the intermediate
- *     silu(G)*U stay in fp32.
+ *   - fp32 and FP8 weights, and bf16 weights at T*k <= FT_CC_MAX_ASSIGNMENTS
+ *     (one decode token: each expert's product is a matrix-vector product,
+ *     which the tensor cores would only pad): CUDA cores, weights streamed
+ *     once per 8-row chunk of an expert's rows and dequantised in registers; x
+ *     and the intermediate silu(G)*U stay in fp32.
  * ---------------------------------------------------------------------- */
 #define FT_TC_WIDE_ASSIGNMENTS 2048
+#define FT_CC_MAX_ASSIGNMENTS 8
 
 /* How the tensor cores evaluate NVFP4 / MXFP4 experts, process-wide, for later
  * calls:
@@ -432,13 +435,13 @@ int ft_expert_grouped(const void* x, int x_type, int T, int k, int hidden, int i
  * synchronisation is not acceptable.  The library allocates nothing here.
  *
  * It always runs the CUDA-core kernels, for every weight format: weights
- * dequantised in registers, x and the intermediate silu(G)*U in fp32.  Its
- * results therefore differ from ft_expert_grouped's for bf16, NVFP4 and MXFP4
- * weights (which run on the tensor cores with a bf16 intermediate) within the
- * tolerance of that rounding, not bit for bit, and it is slower for them
- * except at one token (measured on B300, bf16 weights, H=2048, I=512, top-8:
- * 0.019 against 0.026 ms at one token, 0.065 against 0.041 ms at 4 tokens,
- * 0.605 against 0.075 ms at 64 tokens).
+ * dequantised in registers, x and the intermediate silu(G)*U in fp32.  Where
+ * ft_expert_grouped takes the tensor cores (bf16 weights above
+ * FT_CC_MAX_ASSIGNMENTS assignments, NVFP4 and MXFP4 weights, with a bf16 or
+ * quantised intermediate) the results therefore differ within the tolerance
+ * of that rounding, not bit for bit, and this call is slower (measured on
+ * B300, bf16 weights, H=2048, I=512, top-8: 0.065 against 0.041 ms at 4
+ * tokens, 0.605 against 0.075 ms at 64 tokens).
  *
  * The fp32 intermediate lives in one fixed device array inside the library,
  * FT_NOALLOC_MAX_ELEMS floats (4 MiB), which every GPU that loads the library

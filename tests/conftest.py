@@ -57,3 +57,14 @@ def assert_close_layer(got, ref, fro=5e-3, maxrel=2e-2):
     assert rf <= fro, f"relative Frobenius error {rf:.3e} > {fro}"
     assert mx <= maxrel * scale + 1e-30, f"max |err| {mx:.3e} > {maxrel} * max|ref| ({scale:.3e})"
     return rf, mx
+
+
+CC_MAX_ASSIGNMENTS = 8   # FT_CC_MAX_ASSIGNMENTS in include/ft.h
+
+
+def bf16_act_round(T, k):
+    """The oracle's rounding of the intermediate silu(G)*U for bf16 experts evaluated T*k
+    assignments at a time: bf16 on the tensor cores, none (fp32) on the CUDA cores, which take
+    batches of at most CC_MAX_ASSIGNMENTS assignments."""
+    from oracle import formats
+    return None if T * k <= CC_MAX_ASSIGNMENTS else formats.round_to_bf16

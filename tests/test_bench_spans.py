@@ -53,7 +53,7 @@ def test_split_step_spans():
 
 def test_launch_count_per_step():
     class Cfg:
-        n_layers, wtype = 40, bench.synth.W_BF16
+        n_layers, wtype, top_k = 40, bench.synth.W_BF16, 8
 
     class Run:
         cfg, n_waves, n_steps, batches = Cfg, 1, 256, [1, 8, 64]
@@ -62,10 +62,10 @@ def test_launch_count_per_step():
 
     r = Run()
     r.b = {1: {"split": False}, 8: {"split": False}, 64: {"split": True}}
-    assert r.launches_per_step(1) == 40 * 7       # fused route, control, fill, gather + gate/up + down, combine
-    assert r.launches_per_step(8) == 40 * 7       # up to 8 tokens: one routing launch
+    assert r.launches_per_step(1) == 40 * 6       # fused route, control, fill, gate/up + down (CUDA cores), combine
+    assert r.launches_per_step(8) == 40 * 7       # up to 8 tokens: one routing launch; gather + gate/up + down
     assert r.launches_per_step(64) == 40 * 12     # the three routing kernels, a second expert call (split form)
-    assert r.launches_per_pass() == 256 * 40 * (7 + 7 + 12)
+    assert r.launches_per_pass() == 256 * 40 * (6 + 7 + 12)
 
 
 def test_step_times_per_batch_exclude_the_reset_between_batches():

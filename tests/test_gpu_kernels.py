@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import synth
-from conftest import assert_close_layer, rel_fro
+from conftest import CC_MAX_ASSIGNMENTS, assert_close_layer, rel_fro
 from oracle import formats, moe
 
 pytestmark = pytest.mark.gpu
@@ -126,6 +126,8 @@ def _tiny_cfg(wtype, H, I, E, k, xdt="bf16", seed=7):
     (0, 256, 256, 8, 2, 37, "f32"),
     (1, 512, 256, 8, 2, 37, "bf16"),
     (1, 2048, 512, 16, 8, 64, "bf16"),
+    (1, 2048, 512, 16, 8, 1, "bf16"),       # one decode token of bf16 experts: the CUDA-core path
+    (1, 512, 256, 8, 2, 3, "bf16"),         # T*k = 6: the CUDA-core path
     (1, 768, 512, 4, 2, 200, "bf16"),       # ~100 rows per expert: many row chunks; H not a power of two
     (2, 1024, 512, 8, 2, 45, "bf16"),
     (3, 1024, 512, 8, 3, 29, "bf16"),
@@ -146,6 +148,7 @@ def test_expert_grouped_parity(ft, wtype, H, I, E, k, T, xdt):
         comps[e] = synth.expert_weights(cfg, 0, e, DEV)
         ft.pack_expert(comps[e], wtype, L, pool[slot_perm[e] * S:(slot_perm[e] + 1) * S])
     x = synth.activations(cfg, T, tag=3, device=DEV)
+    on_tc = wtype in TC_FORMATS and not (wtype == synth.W_BF16 and T * k <= CC_MAX_ASSIGNMENTS)
     idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
     counts, offsets, perm, inv = moe.permute(idx, E)
     slot_of = slot_perm.astype(np.int32).copy()
@@ -169,18 +172,17 @@ def test_expert_grouped_parity(ft, wtype, H, I, E, k, T, xdt):
             assert np.isnan(Y[rows]).all(), "rows of skipped experts must be left untouched"
             continue
         g, u, d = (formats.dequant(comps[e][m], wtype) for m in ("gate", "up", "down"))
-        # bf16 weights, and NVFP4 / MXFP4 weights at these batch sizes, run on the
-        # tensor cores, which round the intermediate to bf16
-        # bf16 weights on the tensor cores round the intermediate to bf16; NVFP4 / MXFP4 weights
-        # at small batches (H and I multiples of 256) take the block-scaled FP4 MMA, which
-        # quantises the token rows and the intermediate to the weights' format
-        x_round, act_round = None, (formats.round_to_bf16 if wtype in TC_FORMATS else None)
+        # bf16 weights on the tensor cores round the intermediate to bf16 (one-token batches of
+        # bf16 weights run on the CUDA cores, fp32 throughout); NVFP4 / MXFP4 weights at small
+        # batches (H and I multiples of 256) take the block-scaled FP4 MMA, which quantises the
+        # token rows and the intermediate to the weights' format
+        x_round, act_round = None, (formats.round_to_bf16 if on_tc else None)
         if wtype in (synth.W_NVFP4, synth.W_MXFP4) and H % 256 == 0 and I % 256 == 0:
             act_round = x_round = (formats.quant_act_nvfp4 if wtype == synth.W_NVFP4 else formats.quant_act_mxfp4)
         ref.append(moe.expert_ffn(xs[perm[rows] // k], g, u, d, act_round=act_round, x_round=x_round))
         got.append(Y[rows])
     got, ref = np.concatenate(got), np.concatenate(ref)
-    if wtype in TC_FORMATS:
+    if on_tc:
         assert_close_layer(got, ref, fro=1e-2)
         assert rel_fro(got, ref) < 2e-3
     else:

@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import synth
-from conftest import assert_close_layer
+from conftest import assert_close_layer, bf16_act_round
 from oracle import formats, moe
 from oracle.lru import LRUSim
 
@@ -169,7 +169,7 @@ def test_cache_trace_resize_split_matches_simulator(ft):
             if not C:
                 assert np.array_equal(out, out_b), f"step {step} layer {l}: output depends on the cache"
             if step % 5 == 0 or C:
-                ref = moe.moe_layer(formats.to_f64(x), ri, rw, ol.experts(l), act_round=TC_ROUND)
+                ref = moe.moe_layer(formats.to_f64(x), ri, rw, ol.experts(l), act_round=bf16_act_round(T, cfg.top_k))
                 assert_close_layer(out, ref, fro=1e-2)
     key, stamp, clock = cache.export()
     sk, ss = sim.state()
