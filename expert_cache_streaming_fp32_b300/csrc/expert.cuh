@@ -25,6 +25,7 @@ constexpr int GU_NT = EX_WARPS * GU_RPW;
 constexpr int DN_RPW = 4;       // down: output rows per warp
 constexpr int DN_NT = EX_WARPS * DN_RPW;
 constexpr int EX_UNR = 1;       // k-chunks whose loads are issued together (4 rows x 16 B per lane already in flight)
+constexpr int EX_UNR_ONE = 4;   // the same for one token row per expert (T = 1), with registers to spare
 
 // ------------------------------------------------------------------ weight formats
 // load(): the 16 bytes (and scale) a lane needs for elements k .. k+EPL-1 of a row.
@@ -248,7 +249,7 @@ __device__ __forceinline__ int find_act(const int* pref, int n, int item) {
 __device__ __forceinline__ int pow2_rows(int r) { return r <= 1 ? 1 : r <= 2 ? 2 : r <= 4 ? 4 : 8; }
 
 // ------------------------------------------------------------------ gate/up
-template <int WT, int MR>
+template <int WT, int MR, int UNR = EX_UNR>
 __device__ __forceinline__ void gateup_rows(const ExpertArgs& a, const float* xs, int xstride,
                                             const uint8_t* rec, int n_base, int p0, int rows) {
   using F = WFmt<WT>;
@@ -277,10 +278,10 @@ __device__ __forceinline__ void gateup_rows(const ExpertArgs& a, const float* xs
 #pragma unroll
   for (int i = 0; i < V; ++i) acc[i] = 0.0f;
   const int nch = ceil_div(K, CH);
-  for (int c0 = 0; c0 < nch; c0 += EX_UNR) {
-    typename F::Raw raw[EX_UNR][GU_RPW][2];
+  for (int c0 = 0; c0 < nch; c0 += UNR) {
+    typename F::Raw raw[UNR][GU_RPW][2];
 #pragma unroll
-    for (int u = 0; u < EX_UNR; ++u) {
+    for (int u = 0; u < UNR; ++u) {
       const int kk = (c0 + u) * CH + lane * EPL;
       const bool in = (c0 + u) < nch && kk < K;
 #pragma unroll
@@ -290,7 +291,7 @@ __device__ __forceinline__ void gateup_rows(const ExpertArgs& a, const float* xs
           if (in && valid[i]) raw[u][i][m] = F::load(vb[i][m], sb[i][m], kk);
     }
 #pragma unroll
-    for (int u = 0; u < EX_UNR; ++u) {
+    for (int u = 0; u < UNR; ++u) {
       const int kk = (c0 + u) * CH + lane * EPL;
       if ((c0 + u) >= nch || kk >= K) break;
 #pragma unroll
@@ -327,7 +328,9 @@ __device__ __forceinline__ void gateup_rows(const ExpertArgs& a, const float* xs
   }
 }
 
-template <int WT, typename XT>
+// ONE: every expert has one token row (T = 1): no row-count dispatch, and the registers
+// the wider row blocks would take go to more loads in flight.
+template <int WT, typename XT, bool ONE = false>
 __global__ void __launch_bounds__(EX_THREADS, 2)
 gateup_kernel(ExpertArgs a) {
   pdl_begin();
@@ -367,11 +370,17 @@ gateup_kernel(ExpertArgs a) {
     __syncthreads();
     const uint8_t* rec = a.pool + (uint64_t)a.slot_of[e] * a.S;
     const int n_base = tile * GU_NT;
-    switch (MRr) {
-      case 1: gateup_rows<WT, 1>(a, xs, xstride, rec, n_base, p0, rows); break;
-      case 2: gateup_rows<WT, 2>(a, xs, xstride, rec, n_base, p0, rows); break;
-      case 4: gateup_rows<WT, 4>(a, xs, xstride, rec, n_base, p0, rows); break;
-      default: gateup_rows<WT, 8>(a, xs, xstride, rec, n_base, p0, rows); break;
+    if (ONE) {
+      // one row at a time (a routing that repeats an expert for one token gives it more)
+      for (int r = 0; r < rows; ++r)
+        gateup_rows<WT, 1, EX_UNR_ONE>(a, xs + r * xstride, xstride, rec, n_base, p0 + r, 1);
+    } else {
+      switch (MRr) {
+        case 1: gateup_rows<WT, 1>(a, xs, xstride, rec, n_base, p0, rows); break;
+        case 2: gateup_rows<WT, 2>(a, xs, xstride, rec, n_base, p0, rows); break;
+        case 4: gateup_rows<WT, 4>(a, xs, xstride, rec, n_base, p0, rows); break;
+        default: gateup_rows<WT, 8>(a, xs, xstride, rec, n_base, p0, rows); break;
+      }
     }
     __syncthreads();
   }
@@ -379,7 +388,7 @@ gateup_kernel(ExpertArgs a) {
 }
 
 // ------------------------------------------------------------------ down
-template <int WT, int MR>
+template <int WT, int MR, int UNR = EX_UNR>
 __device__ __forceinline__ void down_rows(const ExpertArgs& a, const float* as, int astride,
                                           const uint8_t* rec, int h_base, int p0, int rows) {
   using F = WFmt<WT>;
@@ -405,10 +414,10 @@ __device__ __forceinline__ void down_rows(const ExpertArgs& a, const float* as, 
 #pragma unroll
   for (int i = 0; i < V; ++i) acc[i] = 0.0f;
   const int nch = ceil_div(K, CH);
-  for (int c0 = 0; c0 < nch; c0 += EX_UNR) {
-    typename F::Raw raw[EX_UNR][DN_RPW];
+  for (int c0 = 0; c0 < nch; c0 += UNR) {
+    typename F::Raw raw[UNR][DN_RPW];
 #pragma unroll
-    for (int u = 0; u < EX_UNR; ++u) {
+    for (int u = 0; u < UNR; ++u) {
       const int kk = (c0 + u) * CH + lane * EPL;
       const bool in = (c0 + u) < nch && kk < K;
 #pragma unroll
@@ -416,7 +425,7 @@ __device__ __forceinline__ void down_rows(const ExpertArgs& a, const float* as, 
         if (in && valid[i]) raw[u][i] = F::load(vb[i], sb[i], kk);
     }
 #pragma unroll
-    for (int u = 0; u < EX_UNR; ++u) {
+    for (int u = 0; u < UNR; ++u) {
       const int kk = (c0 + u) * CH + lane * EPL;
       if ((c0 + u) >= nch || kk >= K) break;
 #pragma unroll
@@ -445,7 +454,7 @@ __device__ __forceinline__ void down_rows(const ExpertArgs& a, const float* as, 
   }
 }
 
-template <int WT>
+template <int WT, bool ONE = false>
 __global__ void __launch_bounds__(EX_THREADS, 2)
 down_kernel(ExpertArgs a) {
   pdl_begin();
@@ -476,11 +485,16 @@ down_kernel(ExpertArgs a) {
     __syncthreads();
     const uint8_t* rec = a.pool + (uint64_t)a.slot_of[e] * a.S;
     const int h_base = tile * DN_NT;
-    switch (MRr) {
-      case 1: down_rows<WT, 1>(a, as, astride, rec, h_base, p0, rows); break;
-      case 2: down_rows<WT, 2>(a, as, astride, rec, h_base, p0, rows); break;
-      case 4: down_rows<WT, 4>(a, as, astride, rec, h_base, p0, rows); break;
-      default: down_rows<WT, 8>(a, as, astride, rec, h_base, p0, rows); break;
+    if (ONE) {
+      for (int r = 0; r < rows; ++r)
+        down_rows<WT, 1, EX_UNR_ONE>(a, as + r * astride, astride, rec, h_base, p0 + r, 1);
+    } else {
+      switch (MRr) {
+        case 1: down_rows<WT, 1>(a, as, astride, rec, h_base, p0, rows); break;
+        case 2: down_rows<WT, 2>(a, as, astride, rec, h_base, p0, rows); break;
+        case 4: down_rows<WT, 4>(a, as, astride, rec, h_base, p0, rows); break;
+        default: down_rows<WT, 8>(a, as, astride, rec, h_base, p0, rows); break;
+      }
     }
     __syncthreads();
   }

@@ -371,16 +371,18 @@ int launch_expert(const ExpertArgs& a, cudaStream_t st) {
   const size_t smem_gu = head + (size_t)EX_MR * staged_stride<EPL>(a.H) * sizeof(float);
   const size_t smem_dn = head + (size_t)EX_MR * staged_stride<EPL>(a.I) * sizeof(float);
   if (smem_gu > 227 * 1024 || smem_dn > 227 * 1024) return FT_EUNSUPPORTED;
+  // one token: every expert has one row, and the kernels keep more weight loads in flight
+  const bool one = a.T == 1;
   if (a.x_type == FT_X_BF16) {
-    auto kg = gateup_kernel<WT, __nv_bfloat16>;
+    auto kg = one ? gateup_kernel<WT, __nv_bfloat16, true> : gateup_kernel<WT, __nv_bfloat16>;
     if (int s = set_smem(kg, smem_gu)) return s;
     FT_LAUNCH(kg, occupancy_grid(kg, EX_THREADS, smem_gu), EX_THREADS, smem_gu, st, a);
   } else {
-    auto kg = gateup_kernel<WT, float>;
+    auto kg = one ? gateup_kernel<WT, float, true> : gateup_kernel<WT, float>;
     if (int s = set_smem(kg, smem_gu)) return s;
     FT_LAUNCH(kg, occupancy_grid(kg, EX_THREADS, smem_gu), EX_THREADS, smem_gu, st, a);
   }
-  auto kd = down_kernel<WT>;
+  auto kd = one ? down_kernel<WT, true> : down_kernel<WT>;
   if (int s = set_smem(kd, smem_dn)) return s;
   FT_LAUNCH(kd, occupancy_grid(kd, EX_THREADS, smem_dn), EX_THREADS, smem_dn, st, a);
   return FT_OK;
