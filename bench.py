@@ -82,6 +82,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--split-min-assignments", type=int, default=0,
                    help="smallest decode batch T*k for the split form, every format (0: the policy per format)")
+    p.add_argument("--fill-blocks", type=int, default=0,
+                   help="blocks of the decode stack's fill launch (0: the library's default)")
     p.add_argument("--no-split-fill", action="store_true",
                    help="decode with ft_cache_step (fill, then all experts) instead of the split form "
                         "(hits evaluated while the fill copies)")
@@ -240,13 +242,16 @@ class DecodeRun:
     once and replayed in every pass; its layer outputs go to a per-T device
     buffer, and its per-wave cache counters to a per-step record."""
 
-    def __init__(self, ft, cfg, pool, routers, batches, n_steps, dev, n_slots, split_min=0, e2e=False):
+    def __init__(self, ft, cfg, pool, routers, batches, n_steps, dev, n_slots, split_min=0, e2e=False,
+                 fill_blocks=0):
         self.ft, self.cfg, self.pool, self.routers = ft, cfg, pool, routers
         self.batches, self.n_steps, self.dev = list(batches), n_steps, dev
         L, E, H = cfg.n_layers, cfg.n_experts, cfg.hidden
         self.S, self.n_slots = pool.S, n_slots
         self.sp = torch.empty(n_slots * pool.S, dtype=torch.uint8, device=dev)
         self.cache = ft.Cache(L, E, pool.n_phys, n_slots, n_slots, pool.S, pool.ptr, self.sp)
+        if fill_blocks > 0:
+            self.cache.set_fill_blocks(fill_blocks)
         self.n_waves = self.cache.n_waves()
         self.fs = torch.cuda.Stream(device=dev)
         self.b = {}
@@ -1361,7 +1366,7 @@ def main():
     link = link_peak_gbs(pool.host, E * S, dev)
     n_trace = args.trace_steps
     run = DecodeRun(ft, cfg, pool, routers, batches, n_trace, dev, int(round(CACHE_FRAC * L * E)), split_min,
-                    e2e=not args.no_e2e)
+                    e2e=not args.no_e2e, fill_blocks=args.fill_blocks)
     tokens_per_pass = n_trace * sum(batches)
     log(f"pool of {n_phys} layers filled in {t_fill:.1f} s; link {link:.1f} GB/s")
     t0 = time.perf_counter()

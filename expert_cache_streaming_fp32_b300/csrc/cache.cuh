@@ -209,6 +209,19 @@ cache_control_kernel(CacheDev d, int layer, const int32_t* __restrict__ counts, 
   pdl_end();
 }
 
+// One 16-byte load from the mapped pinned host pool, read-only path, with the
+// L2 asked to fetch the whole 256-byte block around it. With 8 fill blocks the
+// fill alone saturates the link either way; beside the hits' expert call (the
+// split step) the larger requests raised 64-token decode throughput by 5% and
+// left 1- to 16-token steps unchanged.
+__device__ __forceinline__ uint4 ld_host_256(const uint4* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
 // Copies the filled experts host pool -> slots: one fixed-shape launch over a
 // device-resident (source row, destination slot) table with a device count.
 // Reads go over the host link from mapped pinned memory.
@@ -241,7 +254,7 @@ cache_fill_kernel(const uint8_t* __restrict__ host, uint8_t* __restrict__ pool, 
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int v = v0 + u * FILL_THREADS;
-        if (v < nv) t[u] = sp[v];
+        if (v < nv) t[u] = ld_host_256(sp + v);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
