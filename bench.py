@@ -41,7 +41,7 @@ BATCHES = (1, 4, 16, 64)
 # bench scales these to its own launches and labels the result as scaled.  The
 # fill's reads come over the host link, so its DRAM traffic is the writes of the
 # filled experts that reached DRAM before the launch ended.
-TRAFFIC_PER_BYTE = {"fill": (0.025e6 + 140.025e6) / 201.327e6,
+TRAFFIC_PER_BYTE = {"fill": (0.073e6 + 140.229e6) / 201.327e6,
                     "experts": (207.776e6 + 3.545e6 + 103.355e6 + 2.734e6) / (205.5e6 + 0.5e6 + 102.8e6)}
 CACHE_FRAC = 0.40
 ROUTE_FUSED_MAX_T = 8             # batches routed by one ft_route_fused launch
