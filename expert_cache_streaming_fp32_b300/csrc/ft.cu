@@ -868,15 +868,16 @@ FT_API int ft_cache_create(const ft_cache_config* cfg, ft_cache** out) {
     ft_cache_destroy(c);
     return st;
   }
-  // 16 blocks of 256 threads, 4 x 16 B reads in flight per thread (256 KiB).
+  // 32 blocks of 256 threads, 4 x 16 B reads in flight per thread (512 KiB).
   // A fill running alone holds the link's SM-copy rate (51 GB/s) from 8 blocks
   // up; reads beyond that queue in the memory system and hold up the HBM reads
   // of expert kernels running beside the fill (64-token expert calls took 1.6x
-  // as long beside 8 fill blocks, 1.8x beside 16, 3.3x beside 148).  Inside a
-  // split decode step the fill is the longer branch, and 16 blocks finish it
-  // sooner: 64-token decode of the 40-layer bf16 stack ran 8.9% faster than
-  // with 8 (measured on B300).
-  c->fill_grid = 16;
+  // as long beside 8 fill blocks, 2.6x beside 32, 3.3x beside 148).  Inside a
+  // split decode step the fill is the longer branch, and more blocks finish it
+  // sooner: 64-token decode of the 40-layer bf16 stack at 6895 / 7523 / 7821
+  // tokens/s with 8 / 16 / 32 blocks, 16-token decode within 1% (measured on
+  // B300).
+  c->fill_grid = 32;
   *out = c;
   return FT_OK;
 }

@@ -327,7 +327,7 @@ int ft_cache_step_split(ft_cache* c, int layer, const int32_t* counts, double fi
                         ft_cuda_stream s, ft_cuda_stream fill_s);
 int ft_cache_fill_join(ft_cache* c, ft_cuda_stream s);
 
-/* Thread blocks of the fill launch (default 16; 256 threads, 16 KiB of host
+/* Thread blocks of the fill launch (default 32; 256 threads, 16 KiB of host
  * reads in flight each), 1 .. 4 x the SM count; applies to later steps.  More blocks
  * keep more reads in flight over the host link; reads queued beyond what the
  * link needs also delay the device-memory reads of kernels running beside the
