@@ -42,7 +42,7 @@ EXPORTED = [
     "ft_cache_set_fill_blocks", "ft_debug_inject_failure", "ft_debug_live_resources", "ft_pool_read",
     "ft_host_register", "ft_host_unregister", "ft_cache_reset", "ft_placement_replay", "ft_cpu_create",
     "ft_cpu_destroy", "ft_cpu_experts", "ft_cpu_experts_enqueue", "ft_cpu_status", "ft_route_fused",
-    "ft_expert_set_fp4_path", "ft_debug_quant_fp4",
+    "ft_expert_set_fp4_path", "ft_debug_quant_fp4", "ft_debug_host_simd",
 ]
 FT_NOALLOC_MAX_ELEMS = 1 << 20
 FT_TC_WIDE_ASSIGNMENTS = 2048
@@ -131,6 +131,7 @@ _sigs = {
     "ft_debug_bounded_wait": (_I, [ctypes.c_int64, _P, _P]),
     "ft_debug_inject_failure": (_I, [_I, _I]),
     "ft_debug_live_resources": (_I, [ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),
+    "ft_debug_host_simd": (_I, [_I]),
     "ft_pool_read": (_I, [ctypes.c_char_p, ctypes.c_uint64, _P, ctypes.c_uint64, _I]),
     "ft_host_register": (_I, [_P, ctypes.c_uint64]),
     "ft_host_unregister": (_I, [_P]),
@@ -207,6 +208,12 @@ def ft_debug_live_resources():
     a, b = ctypes.c_int64(0), ctypes.c_int64(0)
     _check("ft_debug_live_resources", _lib.ft_debug_live_resources(ctypes.byref(a), ctypes.byref(b)))
     return a.value, b.value
+
+
+def ft_debug_host_simd(mode: int = -1) -> bool:
+    """Switches the host executor's AVX-512 FP4 form off (0) or back on (1), or only asks (-1);
+    returns whether it was on."""
+    return bool(_lib.ft_debug_host_simd(mode))
 
 
 def ft_pool_read(path: str, offset: int, dst_ptr: int, nbytes: int, threads: int = 0):

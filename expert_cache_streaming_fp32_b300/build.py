@@ -12,7 +12,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libft.so")
-SOURCES = [os.path.join(CSRC, "ft.cu")]
+SOURCES = [os.path.join(CSRC, "ft.cu"), os.path.join(CSRC, "host_simd.cpp")]
 DEPENDS = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(ROOT, "include", "ft.h")]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

@@ -104,6 +104,8 @@ FT_API int ft_debug_live_resources(int64_t* device_allocs, int64_t* streams_even
   return FT_OK;
 }
 
+FT_API int ft_debug_host_simd(int mode) { return host_simd_set(mode); }
+
 FT_API int ft_expert_layout_get(int wtype, int hidden, int inter, ft_expert_layout* out) {
   FT_REQUIRE(out);
   return expert_layout(wtype, hidden, inter, out);

@@ -15,9 +15,18 @@ from conftest import assert_close_layer, rel_fro
 from oracle import formats, moe
 
 
+@pytest.fixture(params=["simd", "portable"])
+def host_form(request, ftlib):
+    """The AVX-512 FP4 form (where this CPU has it) or the portable row decode."""
+    prev = ftlib.ft_debug_host_simd(-1)
+    ftlib.ft_debug_host_simd(1 if request.param == "simd" else 0)
+    yield request.param
+    ftlib.ft_debug_host_simd(1 if prev else 0)
+
+
 @pytest.mark.parametrize("wtype,x_dtype", [(synth.W_F32, "f32"), (synth.W_BF16, "bf16"), (synth.W_FP8, "bf16"),
                                            (synth.W_NVFP4, "bf16"), (synth.W_MXFP4, "f32")])
-def test_cpu_executor_matches_oracle(ftlib, wtype, x_dtype):
+def test_cpu_executor_matches_oracle(ftlib, host_form, wtype, x_dtype):
     ft = ftlib
     H, I, E, k, T = 256, 128, 8, 3, 6
     cfg = synth.MoEConfig(f"cpu{wtype}", H, E, k, I, 2, wtype, x_dtype, seed=60 + wtype)
@@ -67,3 +76,40 @@ def test_cpu_executor_rejects_bad_jobs(ftlib):
     with pytest.raises(ft.FTError):
         cpu.run(job)
     cpu.destroy()
+
+
+@pytest.mark.parametrize("wtype", [synth.W_NVFP4, synth.W_MXFP4])
+def test_cpu_executor_fp4_forms_agree(ftlib, wtype):
+    """The AVX-512 FP4 form against the portable row decode, on many tokens per
+    expert (more than one group of four accumulators) and several 32-element
+    groups per row: the same values up to fp32 summation order."""
+    ft = ftlib
+    if not ft.ft_debug_host_simd(-1):
+        pytest.skip("no AVX-512F on this CPU")
+    H, I, E, k, T = 384, 256, 4, 2, 11
+    cfg = synth.MoEConfig(f"forms{wtype}", H, E, k, I, 1, wtype, "bf16", seed=80 + wtype)
+    L = ft.ft_expert_layout_get(wtype, H, I)
+    S = int(L.bytes)
+    pool = torch.zeros(E * S, dtype=torch.uint8)
+    for e in range(E):
+        ft.pack_expert(synth.expert_weights(cfg, 0, e, "cpu"), wtype, L, pool[e * S:(e + 1) * S])
+    idx = torch.tensor([[0, 1]] * 9 + [[2, 0], [3, 2]], dtype=torch.int32)   # expert 0: 10 tokens
+    w = torch.rand(T, k, generator=torch.Generator().manual_seed(5))
+    ext = torch.tensor([1, 1, 1, 0], dtype=torch.int32)
+    x = synth.activations(cfg, T, tag=4)
+    outs = {}
+    cpu = ft.CpuExperts(threads=2)
+    try:
+        for on in (1, 0):
+            ft.ft_debug_host_simd(on)
+            part = torch.full((T, H), float("nan"))
+            cpu.run(cpu.job(pool.data_ptr(), S, wtype, H, I, E, 0, x, T, k, idx, w, ext, part))
+            outs[on] = part.numpy().astype(np.float64)
+    finally:
+        ft.ft_debug_host_simd(1)
+        cpu.destroy()
+    assert np.all(np.isfinite(outs[1]))
+    assert rel_fro(outs[1], outs[0]) < 1e-6
+    src = moe.ExpertSource(lambda e: synth.expert_weights(cfg, 0, e, "cpu"), wtype)
+    ref = moe.moe_layer(formats.to_f64(x), idx.numpy(), w.numpy().astype(np.float64), src, only=[0, 1, 2])
+    assert rel_fro(outs[1], ref) < 2e-5
