@@ -113,3 +113,38 @@ def test_cpu_executor_fp4_forms_agree(ftlib, wtype):
     src = moe.ExpertSource(lambda e: synth.expert_weights(cfg, 0, e, "cpu"), wtype)
     ref = moe.moe_layer(formats.to_f64(x), idx.numpy(), w.numpy().astype(np.float64), src, only=[0, 1, 2])
     assert rel_fro(outs[1], ref) < 2e-5
+
+
+_FULL_WEIGHTS = {}
+
+
+def _full_weights(cfg, e):
+    if e not in _FULL_WEIGHTS:
+        _FULL_WEIGHTS[e] = synth.expert_weights(cfg, 0, e, "cpu")
+    return _FULL_WEIGHTS[e]
+
+
+def test_cpu_executor_mxfp4_full_shape(ftlib, host_form):
+    """The MXFP4 mixed-trace expert shape (H=6144, I=2048) on the host executor, both
+    forms, two external experts of three tokens, against the oracle."""
+    ft = ftlib
+    cfg = synth.MXFP4_MIXED
+    H, I, E, k, T = cfg.hidden, cfg.inter, 4, 2, 3
+    L = ft.ft_expert_layout_get(cfg.wtype, H, I)
+    S = int(L.bytes)
+    pool = torch.zeros(E * S, dtype=torch.uint8)
+    for e in (1, 2):
+        ft.pack_expert(_full_weights(cfg, e), cfg.wtype, L, pool[e * S:(e + 1) * S])
+    idx = torch.tensor([[1, 2], [2, 0], [1, 3]], dtype=torch.int32)
+    w = torch.tensor([[0.6, 0.4], [0.7, 0.3], [0.5, 0.5]])
+    ext = torch.tensor([0, 1, 1, 0], dtype=torch.int32)
+    x = synth.activations(cfg, T, tag=7)
+    part = torch.full((T, H), float("nan"))
+    cpu = ft.CpuExperts(threads=3)
+    cpu.run(cpu.job(pool.data_ptr(), S, cfg.wtype, H, I, E, 0, x, T, k, idx, w, ext, part))
+    cpu.destroy()
+    src = moe.ExpertSource(lambda e: _full_weights(cfg, e), cfg.wtype)
+    ref = moe.moe_layer(formats.to_f64(x), idx.numpy(), w.numpy().astype(np.float64), src, only=[1, 2])
+    got = part.numpy()
+    assert_close_layer(got, ref)
+    assert rel_fro(got, ref) < 2e-5
