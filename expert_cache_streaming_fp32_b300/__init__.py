@@ -211,7 +211,7 @@ def ft_debug_live_resources():
 
 
 def ft_debug_host_simd(mode: int = -1) -> bool:
-    """Switches the host executor's AVX-512 FP4 form off (0) or back on (1), or only asks (-1);
+    """Switches the host executor's AVX-512 row form off (0) or back on (1), or only asks (-1);
     returns whether it was on."""
     return bool(_lib.ft_debug_host_simd(mode))
 

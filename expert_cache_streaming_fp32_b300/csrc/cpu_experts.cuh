@@ -36,7 +36,7 @@ struct ft_cpu {
   std::atomic<int> status{0};                     // first failed status of an enqueued job
   std::vector<std::unique_ptr<ft_cpu_job_rec>> jobs;  // enqueued jobs, alive until destroy
   // scratch of one evaluation
-  std::vector<float> X, Xs, A, Y;                 // Xs: X in pair-split order (AVX-512 FP4 form)
+  std::vector<float> X, Xs, A, Y;                 // Xs: X in pair-split order (AVX-512 form, FP4)
   std::vector<int> arow_t, arow_j, rows_of;       // per external assignment: token, slot j; per (t, j): row or -1
   std::vector<int> e_begin, e_list;               // external experts and their assignment ranges
 };
@@ -224,15 +224,19 @@ static int cpu_experts_run(ft_cpu* c, const ft_cpu_job& j) {
   constexpr int RB = 32;  // weight rows per task
   const int nE = (int)c->e_list.size();
   const int bi = (I + RB - 1) / RB, bh = (H + RB - 1) / RB;
-  if ((wt == FT_W_NVFP4 || wt == FT_W_MXFP4) && host_simd_supported()) {
-    // FP4 rows decoded in registers and dotted with every token of the expert at
-    // once (AVX-512); X and the intermediate A are kept in pair-split order, the
-    // order in which a row's codes unpack.
+  if (host_simd_supported()) {
+    // rows decoded in registers and dotted with every token of the expert at once
+    // (AVX-512); for FP4 weights X and the intermediate A are kept in pair-split
+    // order, the order in which a row's codes unpack.
     const HostTables4& tb = host_tables();
     const float* slut = wt == FT_W_MXFP4 ? tb.e8m0 : tb.e4m3;
-    const int blk = wt == FT_W_MXFP4 ? 32 : 16;
-    c->Xs.resize((size_t)T * H);
-    for (int t = 0; t < T; ++t) split_pairs32(&c->X[(size_t)t * H], H, &c->Xs[(size_t)t * H]);
+    const bool split = host_row_pair_split(wt);
+    const float* Xr = c->X.data();
+    if (split) {
+      c->Xs.resize((size_t)T * H);
+      for (int t = 0; t < T; ++t) split_pairs32(&c->X[(size_t)t * H], H, &c->Xs[(size_t)t * H]);
+      Xr = c->Xs.data();
+    }
     cpu_parallel_for(c, nE * bi, [&](int task) {
       const int e = c->e_list[task / bi], i0 = (task % bi) * RB;
       const int a0 = c->e_begin[e], n = c->e_begin[e + 1] - a0;
@@ -242,13 +246,13 @@ static int cpu_experts_run(ft_cpu* c, const ft_cpu_job& j) {
       xs.resize(n);
       g.resize(n);
       u.resize(n);
-      for (int q = 0; q < n; ++q) xs[q] = &c->Xs[(size_t)c->arow_t[a0 + q] * H];
+      for (int q = 0; q < n; ++q) xs[q] = Xr + (size_t)c->arow_t[a0 + q] * H;
       for (int i = i0; i < std::min(I, i0 + RB); ++i) {
-        const Fp4Row rg{r + L.off_val[0] + i * vrow[0], r + L.off_scale[0] + i * srow[0], slut, gscale(e, 0), H, blk};
-        const Fp4Row ru{r + L.off_val[1] + i * vrow[1], r + L.off_scale[1] + i * srow[1], slut, gscale(e, 1), H, blk};
-        fp4_rows(rg, xs.data(), n, g.data());
-        fp4_rows(ru, xs.data(), n, u.data());
-        const int pos = (i & ~31) + ((i & 1) ? 16 : 0) + ((i & 31) >> 1);   // i in pair-split order
+        const HostRow rg{wt, r + L.off_val[0] + i * vrow[0], r + L.off_scale[0] + i * srow[0], slut, gscale(e, 0), H};
+        const HostRow ru{wt, r + L.off_val[1] + i * vrow[1], r + L.off_scale[1] + i * srow[1], slut, gscale(e, 1), H};
+        host_rows(rg, xs.data(), n, g.data());
+        host_rows(ru, xs.data(), n, u.data());
+        const int pos = split ? (i & ~31) + ((i & 1) ? 16 : 0) + ((i & 31) >> 1) : i;
         for (int q = 0; q < n; ++q) c->A[(size_t)(a0 + q) * I + pos] = g[q] / (1.0f + std::exp(-g[q])) * u[q];
       }
     });
@@ -262,8 +266,8 @@ static int cpu_experts_run(ft_cpu* c, const ft_cpu_job& j) {
       y.resize(n);
       for (int q = 0; q < n; ++q) as[q] = &c->A[(size_t)(a0 + q) * I];
       for (int h = h0; h < std::min(H, h0 + RB); ++h) {
-        const Fp4Row rd{r + L.off_val[2] + h * vrow[2], r + L.off_scale[2] + h * srow[2], slut, gscale(e, 2), I, blk};
-        fp4_rows(rd, as.data(), n, y.data());
+        const HostRow rd{wt, r + L.off_val[2] + h * vrow[2], r + L.off_scale[2] + h * srow[2], slut, gscale(e, 2), I};
+        host_rows(rd, as.data(), n, y.data());
         for (int q = 0; q < n; ++q) c->Y[(size_t)(a0 + q) * H + h] = y[q];
       }
     });

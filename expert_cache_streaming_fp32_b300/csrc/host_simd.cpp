@@ -1,5 +1,5 @@
-// Host expert executor, FP4 rows: decode and dot product fused in AVX-512
-// registers.  Compiled by the host compiler (not nvcc's front end) into
+// Host expert executor: weight rows decoded and dotted with the tokens in
+// AVX-512 registers.  Compiled by the host compiler (not nvcc's front end) into
 // libft.so; every AVX-512 function carries its own target attribute and runs
 // only after host_simd_supported() said yes, so the library still loads and
 // runs on x86-64 CPUs without AVX-512 (the executor then keeps its portable
@@ -62,45 +62,108 @@ void split_pairs32(const float* x, int K, float* out) {
 }
 
 #if defined(__x86_64__)
-__attribute__((target("avx512f")))
-static void fp4_rows_avx512(const Fp4Row& r, const float* const* xs, int n, float* out) {
+namespace {
+
+#define FT_AVX512 __attribute__((target("avx512f")))
+
+// n <= 4 accumulators over the row: w16(k0) gives the 16 decoded weights at k0
+// (k0 a multiple of 16), which meet x_j[k0 .. k0+15].
+template <typename W16>
+FT_AVX512 inline void dot_rows(int K, const float* const* xs, int nj, __m512* acc, const W16& w16) {
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    const __m512 w = w16(k0);
+    for (int j = 0; j < nj; ++j) acc[j] = _mm512_fmadd_ps(w, _mm512_loadu_ps(xs[j] + k0), acc[j]);
+  }
+}
+
+// e4m3 bytes (widened to 32 bits) -> fp32: sign, exponent (bias 7) and
+// mantissa moved into place; exponent 0 is m * 2^-9; S.1111.111 is NaN.
+FT_AVX512 inline __m512 e4m3_lanes(__m512i b) {
+  const __m512i mag = _mm512_and_si512(b, _mm512_set1_epi32(0x7F));
+  const __m512i sign = _mm512_slli_epi32(_mm512_and_si512(b, _mm512_set1_epi32(0x80)), 24);
+  const __m512i normal = _mm512_add_epi32(_mm512_slli_epi32(mag, 20), _mm512_set1_epi32(120 << 23));
+  const __m512 sub = _mm512_mul_ps(_mm512_cvtepi32_ps(_mm512_and_si512(b, _mm512_set1_epi32(7))),
+                                   _mm512_set1_ps(1.0f / 512.0f));
+  __m512 v = _mm512_mask_mov_ps(_mm512_castsi512_ps(normal), _mm512_cmplt_epi32_mask(mag, _mm512_set1_epi32(8)), sub);
+  v = _mm512_castsi512_ps(_mm512_or_si512(_mm512_castps_si512(v), sign));
+  return _mm512_mask_mov_ps(v, _mm512_cmpeq_epi32_mask(mag, _mm512_set1_epi32(0x7F)), _mm512_set1_ps(NAN));
+}
+
+struct W16F32 {
+  const float* v;
+  FT_AVX512 __m512 operator()(int k0) const { return _mm512_loadu_ps(v + k0); }
+};
+
+struct W16BF16 {
+  const uint16_t* v;
+  FT_AVX512 __m512 operator()(int k0) const {
+    const __m512i w = _mm512_cvtepu16_epi32(_mm256_loadu_si256(reinterpret_cast<const __m256i*>(v + k0)));
+    return _mm512_castsi512_ps(_mm512_slli_epi32(w, 16));
+  }
+};
+
+struct W16FP8 {
+  const uint8_t* v;
+  const float* sc;  // one scale per 128 elements
+  FT_AVX512 __m512 operator()(int k0) const {
+    const __m512i b = _mm512_cvtepu8_epi32(_mm_loadu_si128(reinterpret_cast<const __m128i*>(v + k0)));
+    return _mm512_mul_ps(e4m3_lanes(b), _mm512_set1_ps(sc[k0 >> 7]));
+  }
+};
+
+FT_AVX512 void host_rows_avx512(const HostRow& r, const float* const* xs, int n, float* out) {
   alignas(64) float lut_v[16];
   for (int c = 0; c < 16; ++c) lut_v[c] = e2m1_value(c);
   const __m512 lut = _mm512_load_ps(lut_v);
   const __m512i low4 = _mm512_set1_epi32(15);
-  const int groups = r.K / 32;
   for (int j0 = 0; j0 < n; j0 += 4) {
     const int nj = n - j0 < 4 ? n - j0 : 4;
+    const float* const* x = xs + j0;
     __m512 acc[4] = {_mm512_setzero_ps(), _mm512_setzero_ps(), _mm512_setzero_ps(), _mm512_setzero_ps()};
-    for (int g = 0; g < groups; ++g) {
-      // 16 code bytes: byte b holds elements 2b (low nibble) and 2b+1 (high nibble)
-      const __m512i b = _mm512_cvtepu8_epi32(_mm_loadu_si128(reinterpret_cast<const __m128i*>(r.codes + 16 * g)));
-      __m512 ve = _mm512_permutexvar_ps(_mm512_and_si512(b, low4), lut);
-      __m512 vo = _mm512_permutexvar_ps(_mm512_srli_epi32(b, 4), lut);
-      __m512 sc;
-      if (r.block == 32) {
-        sc = _mm512_set1_ps(r.scale_lut[r.scales[g]] * r.gscale);
-      } else {
-        // two 16-element blocks: lanes 0-7 (bytes 0-7) the first, lanes 8-15 the second
-        sc = _mm512_mask_mov_ps(_mm512_set1_ps(r.scale_lut[r.scales[2 * g]] * r.gscale), (__mmask16)0xFF00,
-                                _mm512_set1_ps(r.scale_lut[r.scales[2 * g + 1]] * r.gscale));
-      }
-      ve = _mm512_mul_ps(ve, sc);
-      vo = _mm512_mul_ps(vo, sc);
-      for (int j = 0; j < nj; ++j) {
-        const float* x = xs[j0 + j] + 32 * g;
-        acc[j] = _mm512_fmadd_ps(ve, _mm512_loadu_ps(x), acc[j]);
-        acc[j] = _mm512_fmadd_ps(vo, _mm512_loadu_ps(x + 16), acc[j]);
+    switch (r.wt) {
+      case FT_W_F32:
+        dot_rows(r.K, x, nj, acc, W16F32{reinterpret_cast<const float*>(r.vals)});
+        break;
+      case FT_W_BF16:
+        dot_rows(r.K, x, nj, acc, W16BF16{reinterpret_cast<const uint16_t*>(r.vals)});
+        break;
+      case FT_W_FP8E4M3:
+        dot_rows(r.K, x, nj, acc, W16FP8{r.vals, reinterpret_cast<const float*>(r.scales)});
+        break;
+      default: {  // NVFP4, MXFP4: 32 elements (16 code bytes) per step, x in pair-split order
+        const bool mx = r.wt == FT_W_MXFP4;
+        for (int g = 0; g < r.K / 32; ++g) {
+          const __m512i b = _mm512_cvtepu8_epi32(_mm_loadu_si128(reinterpret_cast<const __m128i*>(r.vals + 16 * g)));
+          __m512 ve = _mm512_permutexvar_ps(_mm512_and_si512(b, low4), lut);   // elements 2b
+          __m512 vo = _mm512_permutexvar_ps(_mm512_srli_epi32(b, 4), lut);     // elements 2b+1
+          __m512 sc;
+          if (mx) {
+            sc = _mm512_set1_ps(r.scale_lut[r.scales[g]] * r.gscale);
+          } else {
+            // two 16-element blocks: lanes 0-7 (bytes 0-7) the first, lanes 8-15 the second
+            sc = _mm512_mask_mov_ps(_mm512_set1_ps(r.scale_lut[r.scales[2 * g]] * r.gscale), (__mmask16)0xFF00,
+                                    _mm512_set1_ps(r.scale_lut[r.scales[2 * g + 1]] * r.gscale));
+          }
+          ve = _mm512_mul_ps(ve, sc);
+          vo = _mm512_mul_ps(vo, sc);
+          for (int j = 0; j < nj; ++j) {
+            acc[j] = _mm512_fmadd_ps(ve, _mm512_loadu_ps(x[j] + 32 * g), acc[j]);
+            acc[j] = _mm512_fmadd_ps(vo, _mm512_loadu_ps(x[j] + 32 * g + 16), acc[j]);
+          }
+        }
+        break;
       }
     }
     for (int j = 0; j < nj; ++j) out[j0 + j] = _mm512_reduce_add_ps(acc[j]);
   }
 }
+
+}  // namespace
 #endif
 
-void fp4_rows(const Fp4Row& r, const float* const* xs, int n, float* out) {
+void host_rows(const HostRow& r, const float* const* xs, int n, float* out) {
 #if defined(__x86_64__)
-  fp4_rows_avx512(r, xs, n, out);
+  host_rows_avx512(r, xs, n, out);
 #else
   (void)r; (void)xs; (void)n; (void)out;
 #endif

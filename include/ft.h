@@ -111,8 +111,8 @@ int ft_debug_inject_failure(int site, int after);
  * handles (every call that fails must leave both unchanged). */
 int ft_debug_live_resources(int64_t* device_allocs, int64_t* streams_events);
 
-/* The host executor's AVX-512 form of the FP4 rows (see ft_cpu_experts):
- * mode 0 switches it off (every format then takes the portable row decode),
+/* The host executor's AVX-512 row form (see ft_cpu_experts): mode 0
+ * switches it off (every format then takes the portable row decode),
  * 1 switches it back on where the CPU has AVX-512F, any other value only asks.
  * Returns 1 if it was on before the call, 0 if not.  Process-wide; for tests
  * that compare both forms. */
@@ -533,11 +533,12 @@ int ft_stream_destroy(ft_stream* st);
  * != 0, w[t][j] * FFN_e(x[t]) from the host pool's record of (phys_layer, e),
  * and writes partial[t] = their sum over j ascending (0 where there is none).
  * Weights are decoded to fp32 row by row (every ft_wtype); x, the intermediate
- * silu(G)*U and the accumulation are fp32.  On CPUs with AVX-512F, NVFP4 and
- * MXFP4 rows are decoded in registers instead (codes through a 16-entry
- * table, one scale per block) and dotted with all of an expert's tokens at
- * once; the sums then run in another order (fp32 rounding differs, the
- * results stay deterministic).  Every pointer is host memory:
+ * silu(G)*U and the accumulation are fp32.  On CPUs with AVX-512F the rows
+ * are decoded in registers instead (FP4 codes through a 16-entry table, one
+ * scale per block; e4m3 bytes by moving their fields into place) and dotted
+ * with all of an expert's tokens at once; the weights take the same values,
+ * the sums run in another order (fp32 rounding differs, the results stay
+ * deterministic).  Every pointer is host memory:
  *   host_pool  [n_phys_layers*E][slot_bytes] records (the cache's pinned pool)
  *   x          [T][hidden] of x_type;  topk_idx, topk_w  [T][k];
  *   ext_flags  [n_experts] (ft_cache_step's external marks);  partial [T][hidden] fp32

@@ -17,7 +17,7 @@ from oracle import formats, moe
 
 @pytest.fixture(params=["simd", "portable"])
 def host_form(request, ftlib):
-    """The AVX-512 FP4 form (where this CPU has it) or the portable row decode."""
+    """The AVX-512 row form (where this CPU has it) or the portable row decode."""
     prev = ftlib.ft_debug_host_simd(-1)
     ftlib.ft_debug_host_simd(1 if request.param == "simd" else 0)
     yield request.param
@@ -78,9 +78,9 @@ def test_cpu_executor_rejects_bad_jobs(ftlib):
     cpu.destroy()
 
 
-@pytest.mark.parametrize("wtype", [synth.W_NVFP4, synth.W_MXFP4])
-def test_cpu_executor_fp4_forms_agree(ftlib, wtype):
-    """The AVX-512 FP4 form against the portable row decode, on many tokens per
+@pytest.mark.parametrize("wtype", [synth.W_F32, synth.W_BF16, synth.W_FP8, synth.W_NVFP4, synth.W_MXFP4])
+def test_cpu_executor_forms_agree(ftlib, wtype):
+    """The AVX-512 form against the portable row decode, on many tokens per
     expert (more than one group of four accumulators) and several 32-element
     groups per row: the same values up to fp32 summation order."""
     ft = ftlib
@@ -148,3 +148,53 @@ def test_cpu_executor_mxfp4_full_shape(ftlib, host_form):
     got = part.numpy()
     assert_close_layer(got, ref)
     assert rel_fro(got, ref) < 2e-5
+
+
+def test_cpu_executor_fp8_every_code(ftlib):
+    """Every finite e4m3 byte through both forms: gate row i holds byte i in
+    column p (zeros elsewhere), the up rows hold 1.0 there, the down matrix is
+    the identity and x is one-hot at p, so partial[h] = silu(e4m3(h)) with a
+    single product in every sum.  Both forms must give the same bits, and the
+    oracle's e4m3 table the same values."""
+    ft = ftlib
+    H = I = 256
+    p = 37
+    wtype = synth.W_FP8
+    L = ft.ft_expert_layout_get(wtype, H, I)
+    S = int(L.bytes)
+    rec = np.zeros(S, dtype=np.uint8)
+    codes = np.arange(256, dtype=np.uint8)
+    codes[[0x7F, 0xFF]] = 0                                   # the two NaN bytes
+    gate = np.zeros((I, H), dtype=np.uint8)
+    gate[:, p] = codes
+    up = np.zeros((I, H), dtype=np.uint8)
+    up[:, p] = 0x38                                           # e4m3 1.0
+    down = np.zeros((H, I), dtype=np.uint8)
+    down[np.arange(H), np.arange(I)] = 0x38
+    for m, mat in enumerate((gate, up, down)):
+        o = int(L.off_val[m])
+        rec[o:o + mat.size] = mat.reshape(-1)
+        ns = mat.shape[0] * (mat.shape[1] // 128)
+        so = int(L.off_scale[m])
+        rec[so:so + 4 * ns] = np.ones(ns, dtype=np.float32).view(np.uint8)
+    pool = torch.from_numpy(rec.copy())
+    x = torch.zeros(1, H, dtype=torch.bfloat16)
+    x[0, p] = 1.0
+    idx = torch.zeros(1, 1, dtype=torch.int32)
+    w = torch.ones(1, 1)
+    ext = torch.ones(1, dtype=torch.int32)
+    outs = {}
+    cpu = ft.CpuExperts(threads=2)
+    try:
+        for on in (1, 0):
+            ft.ft_debug_host_simd(on)
+            part = torch.full((1, H), float("nan"))
+            cpu.run(cpu.job(pool.data_ptr(), S, wtype, H, I, 1, 0, x, 1, 1, idx, w, ext, part))
+            outs[on] = part.numpy().copy()
+    finally:
+        ft.ft_debug_host_simd(1)
+        cpu.destroy()
+    assert np.array_equal(outs[1].view(np.uint32), outs[0].view(np.uint32))
+    g = formats.E4M3_TABLE[codes]
+    ref = g / (1.0 + np.exp(-g))
+    np.testing.assert_allclose(outs[0][0], ref, rtol=1e-6, atol=1e-30)
