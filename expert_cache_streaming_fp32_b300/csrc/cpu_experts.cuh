@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <chrono>
 #include <condition_variable>
 #include <cmath>
 #include <cstring>
@@ -26,12 +27,12 @@ struct ft_cpu {
   std::vector<std::thread> workers;
   std::mutex mu;
   std::condition_variable cv, done_cv;
-  std::function<void(int)> task;
+  const std::function<void(int)>* task = nullptr;  // the caller's, alive until busy reaches 0
   int n_tasks = 0;
   std::atomic<int> next{0};
-  int busy = 0;
-  uint64_t gen = 0;
-  bool stop = false;
+  std::atomic<int> busy{0};                         // workers still in the current generation
+  std::atomic<uint64_t> gen{0};
+  std::atomic<bool> stop{false};
   std::mutex run_mu;                              // one evaluation at a time per handle
   std::atomic<int> status{0};                     // first failed status of an enqueued job
   std::vector<std::unique_ptr<ft_cpu_job_rec>> jobs;  // enqueued jobs, alive until destroy
@@ -128,35 +129,74 @@ static inline float dot_f32(const float* a, const float* b, int n) {
 }
 
 // ------------------------------------------------------------------ thread pool
+// Every worker takes part in every generation.  Between generations a worker
+// spins on the generation counter for a while before it sleeps on the
+// condition variable, so the back-to-back loops of one job find the workers
+// awake: a sleeping worker costs a wake-up and a mutex hand-off per
+// generation.  After a short pause-loop the spin yields its core at every
+// turn, so that more threads than cores, or other threads of the process,
+// still get to run.
+constexpr int64_t CPU_SPIN_NS = 100000;
+constexpr int CPU_PAUSE_TURNS = 512;
+
+// Spins until pred() holds or CPU_SPIN_NS pass; returns pred().
+template <typename P>
+static bool cpu_spin(const P& pred) {
+  const auto t0 = std::chrono::steady_clock::now();
+  for (int i = 1;; ++i) {
+    if (pred()) return true;
+    if (i < CPU_PAUSE_TURNS) {
+#if defined(__x86_64__)
+      __builtin_ia32_pause();
+#endif
+      continue;
+    }
+    std::this_thread::yield();
+    if (std::chrono::steady_clock::now() - t0 > std::chrono::nanoseconds(CPU_SPIN_NS)) return pred();
+  }
+}
+
 static void cpu_worker(ft_cpu* c) {
   uint64_t seen = 0;
   for (;;) {
-    std::unique_lock<std::mutex> lk(c->mu);
-    c->cv.wait(lk, [&] { return c->stop || c->gen != seen; });
-    if (c->stop) return;
-    seen = c->gen;
-    lk.unlock();
-    for (int i; (i = c->next.fetch_add(1)) < c->n_tasks;) c->task(i);
-    lk.lock();
-    if (--c->busy == 0) c->done_cv.notify_all();
+    auto woken = [&] { return c->stop.load(std::memory_order_acquire) || c->gen.load(std::memory_order_acquire) != seen; };
+    if (!cpu_spin(woken)) {
+      std::unique_lock<std::mutex> lk(c->mu);
+      c->cv.wait(lk, woken);
+    }
+    if (c->stop.load(std::memory_order_acquire)) return;
+    seen = c->gen.load(std::memory_order_acquire);
+    const std::function<void(int)>& fn = *c->task;
+    for (int i; (i = c->next.fetch_add(1)) < c->n_tasks;) fn(i);
+    if (c->busy.fetch_sub(1, std::memory_order_acq_rel) == 1) {
+      std::lock_guard<std::mutex> lk(c->mu);
+      c->done_cv.notify_all();
+    }
   }
 }
 
 // Runs fn(0 .. n-1) on the pool and the calling thread; returns when all are done.
 static void cpu_parallel_for(ft_cpu* c, int n, const std::function<void(int)>& fn) {
   if (n <= 0) return;
+  if (c->workers.empty() || n == 1) {
+    for (int i = 0; i < n; ++i) fn(i);
+    return;
+  }
+  c->task = &fn;
+  c->n_tasks = n;
+  c->next.store(0, std::memory_order_relaxed);
+  c->busy.store((int)c->workers.size(), std::memory_order_relaxed);
   {
-    std::lock_guard<std::mutex> lk(c->mu);
-    c->task = fn;
-    c->n_tasks = n;
-    c->next = 0;
-    c->busy = (int)c->workers.size();
-    ++c->gen;
+    std::lock_guard<std::mutex> lk(c->mu);          // a worker between its check and its wait holds mu
+    c->gen.fetch_add(1, std::memory_order_release);
   }
   c->cv.notify_all();
   for (int i; (i = c->next.fetch_add(1)) < n;) fn(i);
-  std::unique_lock<std::mutex> lk(c->mu);
-  c->done_cv.wait(lk, [&] { return c->busy == 0; });
+  auto done = [&] { return c->busy.load(std::memory_order_acquire) == 0; };
+  if (!cpu_spin(done)) {
+    std::unique_lock<std::mutex> lk(c->mu);
+    c->done_cv.wait(lk, done);
+  }
 }
 
 // ------------------------------------------------------------------ evaluation

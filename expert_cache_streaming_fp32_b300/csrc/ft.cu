@@ -1021,7 +1021,7 @@ FT_API int ft_cpu_destroy(ft_cpu* c) {
   if (!c) return FT_OK;
   {
     std::lock_guard<std::mutex> lk(c->mu);
-    c->stop = true;
+    c->stop.store(true, std::memory_order_release);
   }
   c->cv.notify_all();
   for (auto& t : c->workers) t.join();
