@@ -198,3 +198,41 @@ def test_cpu_executor_fp8_every_code(ftlib):
     g = formats.E4M3_TABLE[codes]
     ref = g / (1.0 + np.exp(-g))
     np.testing.assert_allclose(outs[0][0], ref, rtol=1e-6, atol=1e-30)
+
+
+@pytest.mark.parametrize("threads", [1, 5, 12])
+def test_cpu_executor_pool_repeats_bitwise(ftlib, threads):
+    """The thread pool under many back-to-back and spaced jobs of different sizes
+    (loops of one task run inline, larger ones on every worker), with more
+    workers than this machine may have cores: every repeat of a job gives the
+    same bytes, and handles are created and destroyed while idle workers spin."""
+    import time
+    ft = ftlib
+    H, I, E, k = 256, 128, 6, 2
+    wtype = synth.W_BF16
+    cfg = synth.MoEConfig("pool", H, E, k, I, 1, wtype, "bf16", seed=90)
+    L = ft.ft_expert_layout_get(wtype, H, I)
+    S = int(L.bytes)
+    pool = torch.zeros(E * S, dtype=torch.uint8)
+    for e in range(E):
+        ft.pack_expert(synth.expert_weights(cfg, 0, e, "cpu"), wtype, L, pool[e * S:(e + 1) * S])
+    jobs = []
+    for T in (1, 3, 8):
+        idx = torch.tensor([[(t + j) % E for j in range(k)] for t in range(T)], dtype=torch.int32)
+        w = torch.full((T, k), 0.5)
+        ext = torch.ones(E, dtype=torch.int32)
+        jobs.append((T, idx, w, ext, synth.activations(cfg, T, tag=T)))
+    for rnd in range(3):
+        cpu = ft.CpuExperts(threads=threads)
+        first = {}
+        for it in range(40):
+            T, idx, w, ext, x = jobs[it % 3]
+            part = torch.empty(T, H)
+            cpu.run(cpu.job(pool.data_ptr(), S, wtype, H, I, E, 0, x, T, k, idx, w, ext, part))
+            if T not in first:
+                first[T] = part.clone()
+            else:
+                assert torch.equal(part, first[T])
+            if it % 10 == 9:
+                time.sleep(0.002)                 # let the workers fall asleep
+        cpu.destroy()
