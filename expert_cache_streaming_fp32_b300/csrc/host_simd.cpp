@@ -66,13 +66,21 @@ namespace {
 
 #define FT_AVX512 __attribute__((target("avx512f")))
 
-// n <= 4 accumulators over the row: w16(k0) gives the 16 decoded weights at k0
-// (k0 a multiple of 16), which meet x_j[k0 .. k0+15].
+// Accumulators per token: independent FMA chains, so that one token's sums
+// are not bound by the FMA latency.
+constexpr int NACC = 4;
+
+// n <= 4 tokens over the row: w16(k0) gives the 16 decoded weights at k0
+// (k0 a multiple of 16), which meet x_j[k0 .. k0+15]; step u of every 64
+// elements goes to accumulator u.
 template <typename W16>
-FT_AVX512 inline void dot_rows(int K, const float* const* xs, int nj, __m512* acc, const W16& w16) {
-  for (int k0 = 0; k0 < K; k0 += 16) {
-    const __m512 w = w16(k0);
-    for (int j = 0; j < nj; ++j) acc[j] = _mm512_fmadd_ps(w, _mm512_loadu_ps(xs[j] + k0), acc[j]);
+FT_AVX512 inline void dot_rows(int K, const float* const* xs, int nj, __m512 (*acc)[NACC], const W16& w16) {
+  for (int k0 = 0; k0 < K; k0 += 16 * NACC) {
+#pragma GCC unroll 4
+    for (int u = 0; u < NACC; ++u) {
+      const __m512 w = w16(k0 + 16 * u);
+      for (int j = 0; j < nj; ++j) acc[j][u] = _mm512_fmadd_ps(w, _mm512_loadu_ps(xs[j] + k0 + 16 * u), acc[j][u]);
+    }
   }
 }
 
@@ -119,7 +127,9 @@ FT_AVX512 void host_rows_avx512(const HostRow& r, const float* const* xs, int n,
   for (int j0 = 0; j0 < n; j0 += 4) {
     const int nj = n - j0 < 4 ? n - j0 : 4;
     const float* const* x = xs + j0;
-    __m512 acc[4] = {_mm512_setzero_ps(), _mm512_setzero_ps(), _mm512_setzero_ps(), _mm512_setzero_ps()};
+    __m512 acc[4][NACC];
+    for (int j = 0; j < 4; ++j)
+      for (int u = 0; u < NACC; ++u) acc[j][u] = _mm512_setzero_ps();
     switch (r.wt) {
       case FT_W_F32:
         dot_rows(r.K, x, nj, acc, W16F32{reinterpret_cast<const float*>(r.vals)});
@@ -130,31 +140,42 @@ FT_AVX512 void host_rows_avx512(const HostRow& r, const float* const* xs, int n,
       case FT_W_FP8E4M3:
         dot_rows(r.K, x, nj, acc, W16FP8{r.vals, reinterpret_cast<const float*>(r.scales)});
         break;
-      default: {  // NVFP4, MXFP4: 32 elements (16 code bytes) per step, x in pair-split order
+      default: {  // NVFP4, MXFP4: 32 elements (16 code bytes) per group, x in pair-split order
         const bool mx = r.wt == FT_W_MXFP4;
-        for (int g = 0; g < r.K / 32; ++g) {
-          const __m512i b = _mm512_cvtepu8_epi32(_mm_loadu_si128(reinterpret_cast<const __m128i*>(r.vals + 16 * g)));
-          __m512 ve = _mm512_permutexvar_ps(_mm512_and_si512(b, low4), lut);   // elements 2b
-          __m512 vo = _mm512_permutexvar_ps(_mm512_srli_epi32(b, 4), lut);     // elements 2b+1
-          __m512 sc;
-          if (mx) {
-            sc = _mm512_set1_ps(r.scale_lut[r.scales[g]] * r.gscale);
-          } else {
-            // two 16-element blocks: lanes 0-7 (bytes 0-7) the first, lanes 8-15 the second
-            sc = _mm512_mask_mov_ps(_mm512_set1_ps(r.scale_lut[r.scales[2 * g]] * r.gscale), (__mmask16)0xFF00,
-                                    _mm512_set1_ps(r.scale_lut[r.scales[2 * g + 1]] * r.gscale));
-          }
-          ve = _mm512_mul_ps(ve, sc);
-          vo = _mm512_mul_ps(vo, sc);
-          for (int j = 0; j < nj; ++j) {
-            acc[j] = _mm512_fmadd_ps(ve, _mm512_loadu_ps(x[j] + 32 * g), acc[j]);
-            acc[j] = _mm512_fmadd_ps(vo, _mm512_loadu_ps(x[j] + 32 * g + 16), acc[j]);
+        for (int g0 = 0; g0 < r.K / 32; g0 += 2) {
+#pragma GCC unroll 2
+          for (int u = 0; u < 2; ++u) {
+            const int g = g0 + u;
+            // the block scale goes into the 16-entry table once per group
+            __m512 sl;
+            if (mx) {
+              sl = _mm512_mul_ps(lut, _mm512_set1_ps(r.scale_lut[r.scales[g]] * r.gscale));
+            } else {
+              sl = lut;
+            }
+            const __m512i b = _mm512_cvtepu8_epi32(_mm_loadu_si128(reinterpret_cast<const __m128i*>(r.vals + 16 * g)));
+            __m512 ve = _mm512_permutexvar_ps(_mm512_and_si512(b, low4), sl);   // elements 2b
+            __m512 vo = _mm512_permutexvar_ps(_mm512_srli_epi32(b, 4), sl);     // elements 2b+1
+            if (!mx) {
+              // two 16-element blocks: lanes 0-7 (bytes 0-7) the first, lanes 8-15 the second
+              const __m512 sc = _mm512_mask_mov_ps(_mm512_set1_ps(r.scale_lut[r.scales[2 * g]] * r.gscale),
+                                                   (__mmask16)0xFF00,
+                                                   _mm512_set1_ps(r.scale_lut[r.scales[2 * g + 1]] * r.gscale));
+              ve = _mm512_mul_ps(ve, sc);
+              vo = _mm512_mul_ps(vo, sc);
+            }
+            for (int j = 0; j < nj; ++j) {
+              acc[j][2 * u] = _mm512_fmadd_ps(ve, _mm512_loadu_ps(x[j] + 32 * g), acc[j][2 * u]);
+              acc[j][2 * u + 1] = _mm512_fmadd_ps(vo, _mm512_loadu_ps(x[j] + 32 * g + 16), acc[j][2 * u + 1]);
+            }
           }
         }
         break;
       }
     }
-    for (int j = 0; j < nj; ++j) out[j0 + j] = _mm512_reduce_add_ps(acc[j]);
+    for (int j = 0; j < nj; ++j)
+      out[j0 + j] = _mm512_reduce_add_ps(_mm512_add_ps(_mm512_add_ps(acc[j][0], acc[j][1]),
+                                                       _mm512_add_ps(acc[j][2], acc[j][3])));
   }
 }
 
