@@ -203,9 +203,9 @@ static void cpu_parallel_for(ft_cpu* c, int n, const std::function<void(int)>& f
 static int cpu_experts_run(ft_cpu* c, const ft_cpu_job& j) {
   ft_expert_layout L;
   if (expert_layout(j.wtype, j.hidden, j.inter, &L) != FT_OK) return FT_EINVAL;
-  if (j.slot_bytes < L.bytes || !j.host_pool || !j.x || !j.topk_idx || !j.topk_w || !j.ext_flags || !j.partial)
-    return FT_EINVAL;
-  if (j.T < 0 || j.k < 1 || j.n_experts < 1 || j.phys_layer < 0) return FT_EINVAL;
+  if (j.T < 0 || j.k < 1 || j.n_experts < 1 || j.phys_layer < 0 || j.slot_bytes < L.bytes) return FT_EINVAL;
+  if (j.T == 0) return FT_OK;  // nothing is read or written
+  if (!j.host_pool || !j.x || !j.topk_idx || !j.topk_w || !j.ext_flags || !j.partial) return FT_EINVAL;
   std::lock_guard<std::mutex> run_lock(c->run_mu);
   const int T = j.T, k = j.k, H = j.hidden, I = j.inter, E = j.n_experts;
   // external assignments, grouped by expert (ascending), tokens ascending inside

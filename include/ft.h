@@ -542,6 +542,9 @@ int ft_stream_destroy(ft_stream* st);
  *   host_pool  [n_phys_layers*E][slot_bytes] records (the cache's pinned pool)
  *   x          [T][hidden] of x_type;  topk_idx, topk_w  [T][k];
  *   ext_flags  [n_experts] (ft_cache_step's external marks);  partial [T][hidden] fp32
+ * T = 0 is a no-op (the pointers may then be null).  FT_EINVAL for a null
+ * pointer otherwise, T < 0, k < 1, a shape ft_expert_layout_get refuses, or
+ * slot_bytes below the record size.
  * ---------------------------------------------------------------------- */
 typedef struct ft_cpu ft_cpu;
 typedef struct {

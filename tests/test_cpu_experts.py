@@ -236,3 +236,28 @@ def test_cpu_executor_pool_repeats_bitwise(ftlib, threads):
             if it % 10 == 9:
                 time.sleep(0.002)                 # let the workers fall asleep
         cpu.destroy()
+
+
+def test_cpu_executor_empty_jobs(ftlib, host_form):
+    """No tokens, and tokens with no external expert: nothing to evaluate, the
+    partial is all zeros (and nothing is written for T = 0)."""
+    ft = ftlib
+    H, I, E, k = 256, 128, 4, 2
+    wtype = synth.W_MXFP4
+    L = ft.ft_expert_layout_get(wtype, H, I)
+    S = int(L.bytes)
+    pool = torch.zeros(E * S, dtype=torch.uint8)
+    cpu = ft.CpuExperts(threads=3)
+    x0 = torch.zeros(0, H, dtype=torch.bfloat16)
+    i0 = torch.zeros(0, k, dtype=torch.int32)
+    p0 = torch.zeros(0, H)
+    cpu.run(cpu.job(pool.data_ptr(), S, wtype, H, I, E, 0, x0, 0, k, i0, torch.zeros(0, k),
+                    torch.ones(E, dtype=torch.int32), p0))
+    T = 5
+    x = torch.ones(T, H, dtype=torch.bfloat16)
+    idx = torch.tensor([[0, 1]] * T, dtype=torch.int32)
+    part = torch.full((T, H), float("nan"))
+    cpu.run(cpu.job(pool.data_ptr(), S, wtype, H, I, E, 0, x, T, k, idx, torch.ones(T, k),
+                    torch.tensor([0, 0, 1, 1], dtype=torch.int32), part))
+    assert torch.equal(part, torch.zeros(T, H))
+    cpu.destroy()
