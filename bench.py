@@ -88,7 +88,7 @@ def parse():
                    help="decode with ft_cache_step (fill, then all experts) instead of the split form "
                         "(hits evaluated while the fill copies)")
     p.add_argument("--kernel-case", default="", choices=["", "experts_decode", "experts_prefill", "fill",
-                                                         "fill_overlap", "route"],
+                                                         "fill_overlap", "route", "host_experts"],
                    help="time one expert-kernel case on a small resident pool (profiling aid; prints its own line)")
     p.add_argument("--reps", type=int, default=5)
     p.add_argument("--fp4-path", default="block_scaled", choices=["block_scaled", "expand"],
@@ -1225,6 +1225,82 @@ def fill_overlap_case(args):
                       "device_error": ft.ft_get_device_error()}))
 
 
+def host_records(ft, wtype, H, I, n, seed=1):
+    """n expert records of one format in ordinary host memory: seeded random bytes with
+    values and scales in range (bf16 values N(0, 0.02), e4m3 bytes below the NaN code,
+    e4m3 / E8M0 block scales near 1, NVFP4 tensor scales 0.01)."""
+    L = ft.ft_expert_layout_get(wtype, H, I)
+    S = int(L.bytes)
+    g = torch.Generator().manual_seed(seed)
+    pool = torch.randint(0, 256, (n * S,), dtype=torch.uint8, generator=g)
+    for e in range(n):
+        base = e * S
+        for m in range(3):
+            K, rows = (H, I) if m < 2 else (I, H)
+            v0, s0 = base + int(L.off_val[m]), base + int(L.off_scale[m])
+            if wtype == synth.W_BF16:
+                vals = (torch.randn(rows * K, generator=g) * 0.02).to(torch.bfloat16)
+                pool[v0:v0 + 2 * rows * K] = vals.view(torch.uint8)
+            elif wtype == synth.W_FP8:
+                pool[v0:v0 + rows * K] = torch.randint(0, 0x78, (rows * K,), dtype=torch.uint8, generator=g)
+                pool[s0:s0 + 4 * rows * (K // 128)] = torch.full((rows * (K // 128),), 0.01).view(torch.uint8)
+            elif wtype == synth.W_NVFP4:
+                ns = rows * (K // 16)
+                pool[s0:s0 + ns] = torch.randint(0x30, 0x40, (ns,), dtype=torch.uint8, generator=g)
+            elif wtype == synth.W_MXFP4:
+                ns = rows * (K // 32)
+                pool[s0:s0 + ns] = torch.randint(118, 128, (ns,), dtype=torch.uint8, generator=g)
+        if wtype == synth.W_NVFP4:
+            o = base + int(L.off_gscale)
+            pool[o:o + 12] = torch.full((3,), 0.01).view(torch.uint8)
+    return pool, S, int(L.payload_bytes)
+
+
+def host_experts_case(args):
+    """The host expert executor alone (no GPU): one token on each of 16 experts, per weight
+    format at its workload's expert shape, with the AVX-512 row form (where the CPU has it)
+    and with the portable row decode, in expert bytes per second (B_H, [Review] §2.5).
+
+    The records are seeded random bytes with in-range values and scales (host_records),
+    not the weight generator's draws, whose FP4 quantisation of 16 large experts takes
+    minutes; the executor does the same work for any in-range values."""
+    import expert_cache_streaming_fp32_b300 as ft
+    shapes = [("decode_bf16_40L", synth.W_BF16, 2048, 512), ("fp8, decode_bf16_40L shape", synth.W_FP8, 2048, 512),
+              ("nvfp4_43L", synth.W_NVFP4, 4096, 2048), ("mxfp4_mixed_4L", synth.W_MXFP4, 6144, 2048)]
+    n, k = 16, 8
+    T = n // k
+    simd = ft.ft_debug_host_simd(-1)
+    cpu = ft.CpuExperts(threads=0)
+    rows = []
+    try:
+        for name, wt, H, I in shapes:
+            pool, S, payload = host_records(ft, wt, H, I, n)
+            idx = torch.arange(n, dtype=torch.int32).reshape(T, k)
+            w = torch.full((T, k), 1.0 / k)
+            ext = torch.ones(n, dtype=torch.int32)
+            x = (torch.randn(T, H, generator=torch.Generator().manual_seed(2)) * 0.5).to(torch.bfloat16)
+            part = torch.empty(T, H)
+            job = cpu.job(pool.data_ptr(), S, wt, H, I, n, 0, x, T, k, idx, w, ext, part)
+            row = {"workload": name, "format": synth.WTYPE_NAMES[wt], "experts": n, "expert_bytes": payload}
+            for label, mode in (("simd", 1), ("portable", 0)):
+                if label == "simd" and not simd:
+                    continue
+                ft.ft_debug_host_simd(mode)
+                cpu.run(job)
+                best = float("inf")
+                for _ in range(max(10, args.reps)):
+                    t0 = time.perf_counter()
+                    cpu.run(job)
+                    best = min(best, time.perf_counter() - t0)
+                row[f"{label}_gbs"] = n * payload / best / 1e9
+                row[f"{label}_ms"] = best * 1e3
+            rows.append(row)
+    finally:
+        ft.ft_debug_host_simd(1)
+        cpu.destroy()
+    print(json.dumps({"kernel_case": "host_experts", "threads": cpu_threads(), "avx512": simd, "rows": rows}))
+
+
 def route_case(args):
     """Routing of one decode batch (T = --batches[0]) of the 40-layer BF16 stack: the 40 layers'
     ft_route_fused calls (one launch up to 8 tokens), and the three routing kernels, each as one
@@ -1339,6 +1415,9 @@ def main():
         return
     if args.kernel_case == "route":
         route_case(args)
+        return
+    if args.kernel_case == "host_experts":
+        host_experts_case(args)
         return
     if args.kernel_case:
         kernel_case(args)

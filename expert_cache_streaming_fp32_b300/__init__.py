@@ -474,8 +474,10 @@ class CpuExperts:
         """A job over host tensors (x [T, H] bf16/fp32, topk_idx/topk_w [T, k], ext_flags [E], partial [T, H] fp32)."""
         for t in (x, topk_idx, topk_w, ext_flags, partial):
             assert not t.is_cuda and t.is_contiguous()
-        return CpuJob(host_pool_ptr, slot_bytes, wtype, hidden, inter, n_experts, phys_layer, x.data_ptr(), _xtype(x),
-                      T, k, topk_idx.data_ptr(), topk_w.data_ptr(), ext_flags.data_ptr(), partial.data_ptr())
+        job = CpuJob(host_pool_ptr, slot_bytes, wtype, hidden, inter, n_experts, phys_layer, x.data_ptr(), _xtype(x),
+                     T, k, topk_idx.data_ptr(), topk_w.data_ptr(), ext_flags.data_ptr(), partial.data_ptr())
+        job._tensors = (x, topk_idx, topk_w, ext_flags, partial)   # the job's pointers stay valid while it lives
+        return job
 
     def run(self, job: CpuJob):
         _check("ft_cpu_experts", _lib.ft_cpu_experts(self.h, ctypes.byref(job)))
