@@ -467,6 +467,7 @@ class CpuExperts:
         h = _P()
         _check("ft_cpu_create", _lib.ft_cpu_create(threads, ctypes.byref(h)))
         self.h = h
+        self._enqueued = []
 
     @staticmethod
     def job(host_pool_ptr, slot_bytes, wtype, hidden, inter, n_experts, phys_layer, x, T, k, topk_idx, topk_w,
@@ -483,7 +484,10 @@ class CpuExperts:
         _check("ft_cpu_experts", _lib.ft_cpu_experts(self.h, ctypes.byref(job)))
 
     def enqueue(self, job: CpuJob, stream=None):
+        """The handle keeps the job (and runs it at every replay of a captured stream), so the
+        job and its tensors are kept here until destroy."""
         _check("ft_cpu_experts_enqueue", _lib.ft_cpu_experts_enqueue(self.h, ctypes.byref(job), _stream(stream)))
+        self._enqueued.append(job)
 
     def status(self) -> int:
         return _lib.ft_cpu_status(self.h)
@@ -492,6 +496,7 @@ class CpuExperts:
         if self.h:
             _lib.ft_cpu_destroy(self.h)
             self.h = None
+            self._enqueued = []
 
     def __del__(self):
         try:
