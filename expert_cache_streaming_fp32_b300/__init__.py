@@ -512,6 +512,7 @@ class Stream:
         h = _P()
         _check("ft_stream_create", _lib.ft_stream_create(cache.h, 1 if serialized else 0, ctypes.byref(h)))
         self.h = h
+        self.cache = cache            # the stream handle points into the cache handle
 
     def layer(self, layer, next_layer, slot_of, stream=None):
         _check("ft_stream_layer", _lib.ft_stream_layer(self.h, layer, next_layer, _ptr(slot_of), _stream(stream)))
