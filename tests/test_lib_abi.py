@@ -98,3 +98,23 @@ def test_expert_workspace_grows_with_the_batch(ftlib):
             assert w >= prev, (H, I, k, T)
             assert w % 256 == 0
             prev = w
+
+
+def test_header_compiles_as_c99_and_links(ftlib, tmp_path):
+    """include/ft.h is a C header: a C99 program that includes it and calls a host-only
+    entry point compiles with -pedantic and links against libft.so."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_ft.c"
+    src.write_text('#include "ft.h"\n'
+                   'int main(void) { return ft_qsplit(4, 50.0, 100.0) == 2 ? 0 : 1; }\n')
+    exe = tmp_path / "use_ft"
+    lib_dir = os.path.dirname(ftlib.LIB_PATH)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-L", lib_dir, "-l:libft.so", f"-Wl,-rpath,{lib_dir}", "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    assert subprocess.run([str(exe)]).returncode == 0
