@@ -709,7 +709,19 @@ def host_bandwidth(ft, cfg, pool, cpu, payload, tokens=8, reps=3):
     bh = n * payload / best / 1e9
     return {"experts": n, "bw_host_gbs": bh, "bw_fill_gbs": bp, "ratio_fill_over_host": bp / bh,
             "q_for_m": {m: ft.ft_qsplit(m, bp, bh) for m in (1, 2, 3, 4, 6, 8, 16)},
-            "threads": cpu_threads()}
+            "threads": cpu_threads(), "host_cpu": host_cpu_model(), "avx512_rows": ft.ft_debug_host_simd(-1)}
+
+
+def host_cpu_model() -> str:
+    """The host CPU's model name (/proc/cpuinfo), or "" where it cannot be read."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return ""
 
 
 def cpu_threads() -> int:
@@ -1298,7 +1310,8 @@ def host_experts_case(args):
     finally:
         ft.ft_debug_host_simd(1)
         cpu.destroy()
-    print(json.dumps({"kernel_case": "host_experts", "threads": cpu_threads(), "avx512": simd, "rows": rows}))
+    print(json.dumps({"kernel_case": "host_experts", "threads": cpu_threads(), "host_cpu": host_cpu_model(),
+                      "avx512": simd, "rows": rows}))
 
 
 def route_case(args):
