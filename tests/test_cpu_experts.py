@@ -261,3 +261,24 @@ def test_cpu_executor_empty_jobs(ftlib, host_form):
                     torch.tensor([0, 0, 1, 1], dtype=torch.int32), part))
     assert torch.equal(part, torch.zeros(T, H))
     cpu.destroy()
+
+
+def test_host_records_decode_to_finite_weights(ftlib):
+    """The host executor case's stand-in records hold in-range values and scales: the
+    executor's output over them is finite for every format."""
+    import bench
+    ft = ftlib
+    H, I, n, k = 256, 128, 4, 2
+    cpu = ft.CpuExperts(threads=2)
+    try:
+        for wt in (synth.W_BF16, synth.W_FP8, synth.W_NVFP4, synth.W_MXFP4):
+            pool, S, payload = bench.host_records(ft, wt, H, I, n)
+            assert pool.numel() == n * S and payload <= S
+            idx = torch.arange(n, dtype=torch.int32).reshape(n // k, k)
+            part = torch.full((n // k, H), float("nan"))
+            x = torch.randn(n // k, H).to(torch.bfloat16)
+            cpu.run(cpu.job(pool.data_ptr(), S, wt, H, I, n, 0, x, n // k, k, idx, torch.full((n // k, k), 0.5),
+                            torch.ones(n, dtype=torch.int32), part))
+            assert torch.isfinite(part).all() and part.abs().max() > 0
+    finally:
+        cpu.destroy()
