@@ -709,7 +709,7 @@ def host_bandwidth(ft, cfg, pool, cpu, payload, tokens=8, reps=3):
     bh = n * payload / best / 1e9
     return {"experts": n, "bw_host_gbs": bh, "bw_fill_gbs": bp, "ratio_fill_over_host": bp / bh,
             "q_for_m": {m: ft.ft_qsplit(m, bp, bh) for m in (1, 2, 3, 4, 6, 8, 16)},
-            "threads": cpu_threads(), "host_cpu": host_cpu_model(), "avx512_rows": ft.ft_debug_host_simd(-1)}
+            "threads": cpu_threads(), "host_cpu": host_cpu_model(), "host_rows_form": ft.HOST_FORMS[ft.ft_debug_host_simd(-1)]}
 
 
 def host_cpu_model() -> str:
@@ -1270,8 +1270,8 @@ def host_records(ft, wtype, H, I, n, seed=1):
 
 def host_experts_case(args):
     """The host expert executor alone (no GPU): one token on each of 16 experts, per weight
-    format at its workload's expert shape, with the AVX-512 row form (where the CPU has it)
-    and with the portable row decode, in expert bytes per second (B_H, [Review] §2.5).
+    format at its workload's expert shape, in every row form the CPU runs (AVX-512, AVX2,
+    portable), in expert bytes per second (B_H, [Review] §2.5).
 
     The records are seeded random bytes with in-range values and scales (host_records),
     not the weight generator's draws, whose FP4 quantisation of 16 large experts takes
@@ -1281,7 +1281,12 @@ def host_experts_case(args):
               ("nvfp4_43L", synth.W_NVFP4, 4096, 2048), ("mxfp4_mixed_4L", synth.W_MXFP4, 6144, 2048)]
     n, k = 16, 8
     T = n // k
-    simd = ft.ft_debug_host_simd(-1)
+    best_form = ft.ft_debug_host_simd(-1)
+    forms = []
+    for f in (2, 1, 0):
+        ft.ft_debug_host_simd(f)
+        if ft.ft_debug_host_simd(-1) == f:
+            forms.append(f)
     cpu = ft.CpuExperts(threads=0)
     rows = []
     try:
@@ -1294,24 +1299,22 @@ def host_experts_case(args):
             part = torch.empty(T, H)
             job = cpu.job(pool.data_ptr(), S, wt, H, I, n, 0, x, T, k, idx, w, ext, part)
             row = {"workload": name, "format": synth.WTYPE_NAMES[wt], "experts": n, "expert_bytes": payload}
-            for label, mode in (("simd", 1), ("portable", 0)):
-                if label == "simd" and not simd:
-                    continue
-                ft.ft_debug_host_simd(mode)
+            for f in forms:
+                ft.ft_debug_host_simd(f)
                 cpu.run(job)
                 best = float("inf")
                 for _ in range(max(10, args.reps)):
                     t0 = time.perf_counter()
                     cpu.run(job)
                     best = min(best, time.perf_counter() - t0)
-                row[f"{label}_gbs"] = n * payload / best / 1e9
-                row[f"{label}_ms"] = best * 1e3
+                row[f"{ft.HOST_FORMS[f]}_gbs"] = n * payload / best / 1e9
+                row[f"{ft.HOST_FORMS[f]}_ms"] = best * 1e3
             rows.append(row)
     finally:
-        ft.ft_debug_host_simd(1)
+        ft.ft_debug_host_simd(best_form)
         cpu.destroy()
     print(json.dumps({"kernel_case": "host_experts", "threads": cpu_threads(), "host_cpu": host_cpu_model(),
-                      "avx512": simd, "rows": rows}))
+                      "forms": [ft.HOST_FORMS[f] for f in forms], "rows": rows}))
 
 
 def route_case(args):

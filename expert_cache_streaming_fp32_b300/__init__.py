@@ -210,10 +210,13 @@ def ft_debug_live_resources():
     return a.value, b.value
 
 
-def ft_debug_host_simd(mode: int = -1) -> bool:
-    """Switches the host executor's AVX-512 row form off (0) or back on (1), or only asks (-1);
-    returns whether it was on."""
-    return bool(_lib.ft_debug_host_simd(mode))
+HOST_FORMS = ("portable", "avx2", "avx512")
+
+
+def ft_debug_host_simd(mode: int = -1) -> int:
+    """Selects the host executor's row form (0 portable, 1 AVX2, 2 AVX-512; each where the CPU
+    runs it, else the best below it), or only asks (-1); returns the form in use before."""
+    return _lib.ft_debug_host_simd(mode)
 
 
 def ft_pool_read(path: str, offset: int, dst_ptr: int, nbytes: int, threads: int = 0):

@@ -37,7 +37,7 @@ struct ft_cpu {
   std::atomic<int> status{0};                     // first failed status of an enqueued job
   std::vector<std::unique_ptr<ft_cpu_job_rec>> jobs;  // enqueued jobs, alive until destroy
   // scratch of one evaluation
-  std::vector<float> X, Xs, A, Y;                 // Xs: X in pair-split order (AVX-512 form, FP4)
+  std::vector<float> X, Xs, A, Y;                 // Xs: X in pair-split order (vector forms, FP4)
   std::vector<int> arow_t, arow_j, rows_of;       // per external assignment: token, slot j; per (t, j): row or -1
   std::vector<int> e_begin, e_list;               // external experts and their assignment ranges
 };
@@ -266,7 +266,7 @@ static int cpu_experts_run(ft_cpu* c, const ft_cpu_job& j) {
   const int bi = (I + RB - 1) / RB, bh = (H + RB - 1) / RB;
   if (host_simd_supported()) {
     // rows decoded in registers and dotted with every token of the expert at once
-    // (AVX-512); for FP4 weights X and the intermediate A are kept in pair-split
+    // (AVX-512 or AVX2); for FP4 weights X and the intermediate A are kept in pair-split
     // order, the order in which a row's codes unpack.
     const HostTables4& tb = host_tables();
     const float* slut = wt == FT_W_MXFP4 ? tb.e8m0 : tb.e4m3;

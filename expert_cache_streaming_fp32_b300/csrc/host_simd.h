@@ -1,5 +1,5 @@
-// Host expert executor: the AVX-512 form of the weight-row dot products
-// (host_simd.cpp).  Internal to libft; not part of the C ABI.
+// Host expert executor: the AVX2 and AVX-512 forms of the weight-row dot
+// products (host_simd.cpp).  Internal to libft; not part of the C ABI.
 #pragma once
 
 #include <cstdint>
@@ -8,10 +8,17 @@
 
 namespace ft {
 
-// True when the CPU has AVX-512F and the form is not switched off.
+// Forms of the row dot products: the portable decode-then-dot loop (in the
+// executor), or host_rows in AVX2+FMA or AVX-512F registers.
+enum HostSimd { HOST_PORTABLE = 0, HOST_AVX2 = 1, HOST_AVX512 = 2 };
+
+// The form in use (the best this CPU runs, unless set otherwise).
+int host_simd_form();
+// True when host_rows is to be used (the form is not the portable one).
 bool host_simd_supported();
-// mode 0 switches the AVX-512 form off, 1 back on where the CPU has it, any
-// other value only asks; returns the previous state (1 on, 0 off).
+// mode HOST_PORTABLE / HOST_AVX2 / HOST_AVX512 selects that form where the CPU
+// runs it (else the best one below it); any other value only asks.  Returns
+// the form in use before the call.
 int host_simd_set(int mode);
 
 // One weight row of K elements (K a multiple of 128) in record format wt
@@ -38,8 +45,8 @@ void split_pairs32(const float* x, int K, float* out);
 
 // out[j] = sum_k w[k] * x_j[k] for the row w and n vectors xs[j] (pair-split
 // order for the FP4 formats, natural order otherwise), each weight decoded as
-// in the portable path (value * scale).  AVX-512 only: call it only when
-// host_simd_supported().
+// in the portable path (value * scale), in the form host_simd_form() names.
+// Call it only when host_simd_supported().
 void host_rows(const HostRow& r, const float* const* xs, int n, float* out);
 
 }  // namespace ft

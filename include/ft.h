@@ -111,11 +111,11 @@ int ft_debug_inject_failure(int site, int after);
  * handles (every call that fails must leave both unchanged). */
 int ft_debug_live_resources(int64_t* device_allocs, int64_t* streams_events);
 
-/* The host executor's AVX-512 row form (see ft_cpu_experts): mode 0
- * switches it off (every format then takes the portable row decode),
- * 1 switches it back on where the CPU has AVX-512F, any other value only asks.
- * Returns 1 if it was on before the call, 0 if not.  Process-wide; for tests
- * that compare both forms. */
+/* The host executor's row form (see ft_cpu_experts): mode 0 the portable row
+ * decode, 1 AVX2 + FMA, 2 AVX-512F -- each where the CPU runs it, else the
+ * best form below it; any other value only asks.  Returns the form in use
+ * before the call (0, 1 or 2).  The default is the best form the CPU runs.
+ * Process-wide; for tests and measurements that compare the forms. */
 int ft_debug_host_simd(int mode);
 
 /* ------------------------------------------------------------------------
@@ -533,8 +533,9 @@ int ft_stream_destroy(ft_stream* st);
  * != 0, w[t][j] * FFN_e(x[t]) from the host pool's record of (phys_layer, e),
  * and writes partial[t] = their sum over j ascending (0 where there is none).
  * Weights are decoded to fp32 row by row (every ft_wtype); x, the intermediate
- * silu(G)*U and the accumulation are fp32.  On CPUs with AVX-512F the rows
- * are decoded in registers instead (FP4 codes through a 16-entry table, one
+ * silu(G)*U and the accumulation are fp32.  On x86-64 CPUs with AVX-512F, or
+ * AVX2 and FMA, the rows are decoded in registers instead (FP4 codes through a
+ * register table, one
  * scale per block; e4m3 bytes by moving their fields into place) and dotted
  * with all of an expert's tokens at once; the weights take the same values,
  * the sums run in another order (fp32 rounding differs, the results stay

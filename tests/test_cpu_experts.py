@@ -15,13 +15,27 @@ from conftest import assert_close_layer, rel_fro
 from oracle import formats, moe
 
 
-@pytest.fixture(params=["simd", "portable"])
+def available_forms(ft):
+    """The row forms this CPU runs (0 portable, 1 AVX2, 2 AVX-512)."""
+    prev = ft.ft_debug_host_simd(-1)
+    forms = []
+    for f in (0, 1, 2):
+        ft.ft_debug_host_simd(f)
+        if ft.ft_debug_host_simd(-1) == f:
+            forms.append(f)
+    ft.ft_debug_host_simd(prev)
+    return forms
+
+
+@pytest.fixture(params=[2, 1, 0], ids=["avx512", "avx2", "portable"])
 def host_form(request, ftlib):
-    """The AVX-512 row form (where this CPU has it) or the portable row decode."""
+    """One row form of the host executor; skipped where this CPU does not run it."""
+    if request.param not in available_forms(ftlib):
+        pytest.skip(f"this CPU does not run the {ftlib.HOST_FORMS[request.param]} form")
     prev = ftlib.ft_debug_host_simd(-1)
-    ftlib.ft_debug_host_simd(1 if request.param == "simd" else 0)
+    ftlib.ft_debug_host_simd(request.param)
     yield request.param
-    ftlib.ft_debug_host_simd(1 if prev else 0)
+    ftlib.ft_debug_host_simd(prev)
 
 
 @pytest.mark.parametrize("wtype,x_dtype", [(synth.W_F32, "f32"), (synth.W_BF16, "bf16"), (synth.W_FP8, "bf16"),
@@ -80,12 +94,13 @@ def test_cpu_executor_rejects_bad_jobs(ftlib):
 
 @pytest.mark.parametrize("wtype", [synth.W_F32, synth.W_BF16, synth.W_FP8, synth.W_NVFP4, synth.W_MXFP4])
 def test_cpu_executor_forms_agree(ftlib, wtype):
-    """The AVX-512 form against the portable row decode, on many tokens per
-    expert (more than one group of four accumulators) and several 32-element
+    """Every vector form this CPU runs against the portable row decode, on many
+    tokens per expert (more than one pass of tokens) and several 32-element
     groups per row: the same values up to fp32 summation order."""
     ft = ftlib
-    if not ft.ft_debug_host_simd(-1):
-        pytest.skip("no AVX-512F on this CPU")
+    forms = available_forms(ft)
+    if len(forms) < 2:
+        pytest.skip("no vector form on this CPU")
     H, I, E, k, T = 384, 256, 4, 2, 11
     cfg = synth.MoEConfig(f"forms{wtype}", H, E, k, I, 1, wtype, "bf16", seed=80 + wtype)
     L = ft.ft_expert_layout_get(wtype, H, I)
@@ -98,21 +113,23 @@ def test_cpu_executor_forms_agree(ftlib, wtype):
     ext = torch.tensor([1, 1, 1, 0], dtype=torch.int32)
     x = synth.activations(cfg, T, tag=4)
     outs = {}
+    prev = ft.ft_debug_host_simd(-1)
     cpu = ft.CpuExperts(threads=2)
     try:
-        for on in (1, 0):
-            ft.ft_debug_host_simd(on)
+        for f in forms:
+            ft.ft_debug_host_simd(f)
             part = torch.full((T, H), float("nan"))
             cpu.run(cpu.job(pool.data_ptr(), S, wtype, H, I, E, 0, x, T, k, idx, w, ext, part))
-            outs[on] = part.numpy().astype(np.float64)
+            outs[f] = part.numpy().astype(np.float64)
     finally:
-        ft.ft_debug_host_simd(1)
+        ft.ft_debug_host_simd(prev)
         cpu.destroy()
-    assert np.all(np.isfinite(outs[1]))
-    assert rel_fro(outs[1], outs[0]) < 1e-6
     src = moe.ExpertSource(lambda e: synth.expert_weights(cfg, 0, e, "cpu"), wtype)
     ref = moe.moe_layer(formats.to_f64(x), idx.numpy(), w.numpy().astype(np.float64), src, only=[0, 1, 2])
-    assert rel_fro(outs[1], ref) < 2e-5
+    for f in forms[1:]:
+        assert np.all(np.isfinite(outs[f]))
+        assert rel_fro(outs[f], outs[0]) < 1e-6, ft.HOST_FORMS[f]
+        assert rel_fro(outs[f], ref) < 2e-5, ft.HOST_FORMS[f]
 
 
 _FULL_WEIGHTS = {}
@@ -151,10 +168,10 @@ def test_cpu_executor_mxfp4_full_shape(ftlib, host_form):
 
 
 def test_cpu_executor_fp8_every_code(ftlib):
-    """Every finite e4m3 byte through both forms: gate row i holds byte i in
+    """Every finite e4m3 byte through every form: gate row i holds byte i in
     column p (zeros elsewhere), the up rows hold 1.0 there, the down matrix is
     the identity and x is one-hot at p, so partial[h] = silu(e4m3(h)) with a
-    single product in every sum.  Both forms must give the same bits, and the
+    single product in every sum.  Every form must give the same bits, and the
     oracle's e4m3 table the same values."""
     ft = ftlib
     H = I = 256
@@ -184,17 +201,20 @@ def test_cpu_executor_fp8_every_code(ftlib):
     w = torch.ones(1, 1)
     ext = torch.ones(1, dtype=torch.int32)
     outs = {}
+    forms = available_forms(ft)
+    prev = ft.ft_debug_host_simd(-1)
     cpu = ft.CpuExperts(threads=2)
     try:
-        for on in (1, 0):
-            ft.ft_debug_host_simd(on)
+        for f in forms:
+            ft.ft_debug_host_simd(f)
             part = torch.full((1, H), float("nan"))
             cpu.run(cpu.job(pool.data_ptr(), S, wtype, H, I, 1, 0, x, 1, 1, idx, w, ext, part))
-            outs[on] = part.numpy().copy()
+            outs[f] = part.numpy().copy()
     finally:
-        ft.ft_debug_host_simd(1)
+        ft.ft_debug_host_simd(prev)
         cpu.destroy()
-    assert np.array_equal(outs[1].view(np.uint32), outs[0].view(np.uint32))
+    for f in forms[1:]:
+        assert np.array_equal(outs[f].view(np.uint32), outs[0].view(np.uint32)), ft.HOST_FORMS[f]
     g = formats.E4M3_TABLE[codes]
     ref = g / (1.0 + np.exp(-g))
     np.testing.assert_allclose(outs[0][0], ref, rtol=1e-6, atol=1e-30)
