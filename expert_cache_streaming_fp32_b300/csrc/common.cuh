@@ -74,27 +74,6 @@ static inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 b
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// The same, as thread-block clusters of `cluster` CTAs along x.
-template <typename... KArgs, typename... Args>
-static inline cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                                             cudaStream_t st, int cluster, Args&&... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = (unsigned)cluster;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
-}
-
 #define FT_LAUNCH(kernel, grid, block, smem, stream, ...) \
   FT_CHECK_CUDA(::ft::launch_pdl(kernel, dim3(grid), dim3(block), (size_t)(smem), (cudaStream_t)(stream), __VA_ARGS__))
 
@@ -129,12 +108,6 @@ __device__ __forceinline__ float e8m0_to_float(uint8_t b) {
 }
 
 // ------------------------------------------------------------------ warp reductions
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(FT_FULL_MASK, v, o);
-  return v;
-}
-
 // Reduce V values (V a power of two <= 32) across the warp so that afterwards
 // lane l holds in v[0] the warp total of value index l / (32 / V).
 // Halving exchanges move half the values per step (V - 1 shuffles in total),

@@ -122,9 +122,6 @@ template <> struct WFmt<FT_W_MXFP4> {
   }
 };
 
-__host__ __device__ constexpr int fmt_epl(int wt) {
-  return wt == FT_W_F32 ? 4 : wt == FT_W_BF16 ? 8 : wt == FT_W_FP8E4M3 ? 16 : 32;
-}
 __host__ __device__ constexpr int fmt_bits(int wt) {
   return wt == FT_W_F32 ? 32 : wt == FT_W_BF16 ? 16 : wt == FT_W_FP8E4M3 ? 8 : 4;
 }

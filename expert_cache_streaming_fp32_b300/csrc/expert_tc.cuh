@@ -92,9 +92,6 @@ __host__ __device__ constexpr size_t smem_bytes(int E) {
 }
 
 // ------------------------------------------------------------------ FP4 expansion
-// bf16 bits of an E8M0 scale 2^(b - 127) (b = 0 is the bf16 subnormal 2^-127).
-__device__ __forceinline__ uint32_t e8m0_bf16_bits(uint32_t b) { return b ? (b << 7) : 0x0040u; }
-
 // Table of e4m3 byte -> bf16 bits (exact: e4m3 has 3 mantissa bits).
 __device__ __forceinline__ void fill_fp4_tables(uint16_t* lut_e4m3, int nthreads) {
   for (int i = threadIdx.x; i < 256; i += nthreads) {
